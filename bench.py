@@ -1,0 +1,336 @@
+"""Benchmark: FMM evaluation throughput (particles/s) on one B300 per rank.
+
+One step = one complete FMM evaluation (keys, sort, tree, P2M/M2M, walk, lists,
+M2L, L2L, L2P + P2P) of the default workload: N = 2^20 clustered particles
+(64 Plummer halos + 20 % background), fp32, p = 4, theta = 0.7, leaf 64 -- the
+N ~ 1e6 point of the metric. The N = 1e5 fp64 Plummer point (p = 4,
+theta = 0.7, leaf 32) is timed in the same run and reported under "also".
+
+Inputs are resident in HBM before the timed region; L2 is flushed (256 MiB
+write) between timed steps, outside the per-step CUDA events. Multi-GPU runs
+are independent replicas (the FMM here does not shard): every rank evaluates
+its own copy, the barrier + max-over-ranks timing is the only communication.
+
+``--impl reference`` times the CPU oracle (plain C, OpenMP) on a bounded
+sample of the same workload on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from body_forces_morton_b300 import workloads as W  # noqa: E402
+
+# Peaks: HBM copy bandwidth from the driver-written measurement; FP32 / FP64
+# pipe peaks derived from unit counts and the maximum SM clock (148 SMs x 128
+# FP32 lanes x 2 flop per FMA x 2.032 GHz; FP64: the nominal 1.25 TFLOP/s).
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+FP64_PEAK_TFLOPS = 1.25
+P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r^2), 3 FMA (a), 1 add (phi) ~ 19 + 1
+
+# DRAM traffic of the leaf kernel per launch, from the ncu capture committed
+# under profiles/ (bytes); keyed by the hash of the kernel source it was taken on.
+TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("k_down.cu", "expansions_gen.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "body_forces_morton_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(w, n_sample, steps=1):
+    """Oracle FMM (as it stands) on the first n_sample particles' recipe; particles/s."""
+    import oracle
+
+    g = W.generate(w, n=n_sample)
+    oracle.lib()
+    ts = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        oracle.fmm(g["pos"], g["mass"], w.p, w.theta, w.leaf, nthreads=0)
+        ts.append(time.perf_counter() - t0)
+    return n_sample / statistics.median(ts), statistics.median(ts)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = W.workload(args.workload)
+    n_sample = args.cpu_sample
+    vals = []
+    t_all = time.perf_counter()
+    for _ in range(args.warmup):
+        time_oracle(w, n_sample)
+    for _ in range(args.steps):
+        v, _ = time_oracle(w, n_sample)
+        vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": "FMM eval particles/s", "value": value, "unit": "particles/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * n_sample / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator)",
+        "config": {"workload": w.name, "n": w.n, "p": w.p, "theta": w.theta, "leaf": w.leaf},
+        "cpu_baseline": {"value": value, "unit": "particles/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"full oracle FMM (keys..P2P, fp64 expansions) on N={n_sample} particles of the "
+                                   f"{w.name} recipe, median of {args.steps}"},
+        "e2e": {"value": value, "unit": "particles/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": time.perf_counter() - t_all,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def flush_l2(buf):
+    buf.fill_(1.0)
+
+
+def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_override=None):
+    """Times `steps` evaluations; returns dict with per-step ms, stage ms, stats."""
+    n = n_override or w.n
+    g = W.generate(w, n=n)
+    tdt = torch.float32 if w.dtype == "f32" else torch.float64
+    pos = torch.from_numpy(g["pos"]).to("cuda", tdt)
+    mass = torch.from_numpy(g["mass"]).to("cuda", tdt)
+    acc = torch.empty_like(pos)
+    pot = torch.empty_like(mass)
+    plan = native.Plan(n, w.p, w.theta, w.leaf, w.dtype)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            plan.eval(pos, mass, acc, pot, stream=stream)
+        torch.cuda.synchronize()
+        step_ms, stages, launches = [], [], 0
+        stats = None
+        for _ in range(steps):
+            flush_l2(flush_buf)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            plan.eval(pos, mass, acc, pot, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
+            stats = plan.stats()
+            stages.append(stats["stage_ms"])
+            launches += stats["launches"]
+        torch.cuda.synchronize()
+    stage_avg = {k: float(np.mean([s[k] for s in stages])) for k in stages[0]}
+    return {"plan": plan, "pos": pos, "mass": mass, "g": g, "step_ms": step_ms, "stage_ms": stage_avg,
+            "stats": stats, "launches": launches, "n": n}
+
+
+def bench_e2e(plan, g, steps, torch):
+    pos_h = torch.from_numpy(g["pos"]).pin_memory()
+    mass_h = torch.from_numpy(g["mass"]).pin_memory()
+    acc_h = torch.empty_like(pos_h).pin_memory()
+    pot_h = torch.empty_like(mass_h).pin_memory()
+    plan.eval_host(pos_h, mass_h, acc_h, pot_h)
+    ts = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        plan.eval_host(pos_h, mass_h, acc_h, pot_h)
+        ts.append(time.perf_counter() - t0)
+    h2d = pos_h.numel() * pos_h.element_size() + mass_h.numel() * mass_h.element_size()
+    d2h = acc_h.numel() * acc_h.element_size() + pot_h.numel() * pot_h.element_size()
+    return plan.n / statistics.median(ts), h2d, d2h
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from body_forces_morton_b300 import native
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    stream = torch.cuda.Stream()
+    flush_buf = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MiB > 126 MB L2
+    w = W.workload(args.workload)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+
+    sampler = ClockSampler(local_rank)
+    barrier()
+    sampler.start()
+    t_wall = time.perf_counter()
+    res = bench_workload(w, args.steps, args.warmup, torch, native, stream, flush_buf)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    total_ms = float(np.sum(res["step_ms"]))
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * res["n"] / (ms_per_step / 1e3)
+
+    # secondary point: N = 1e5 fp64 Plummer
+    also = {}
+    if not args.no_also:
+        w3 = W.WORKLOADS[3]
+        r3 = bench_workload(w3, max(3, args.steps // 2), args.warmup, torch, native, stream, flush_buf)
+        ms3 = float(np.mean(r3["step_ms"]))
+        also[w3.name] = {"value": r3["n"] / (ms3 / 1e3), "unit": "particles/s", "ms_per_step": ms3,
+                         "stage_ms": r3["stage_ms"], "dtype": "f64", "p": w3.p, "theta": w3.theta, "leaf": w3.leaf,
+                         "m2l_roofline": m2l_roofline(r3, w3)}
+        r3["plan"].close()
+
+    e2e_val, h2d, d2h = bench_e2e(res["plan"], res["g"], max(3, args.steps // 2), torch)
+    st = res["stats"]
+    leaf_ms = res["stage_ms"]["leaf"]
+    pairs = st["n_p2p_interactions"] - res["n"]  # zero-separation self pairs are skipped
+    achieved = P2P_FLOPS_PER_PAIR * pairs / (leaf_ms / 1e3) / 1e12
+    peak = FP32_PEAK_TFLOPS if w.dtype == "f32" else FP64_PEAK_TFLOPS
+    src_hash = kernel_source_hash()
+    traffic = TRAFFIC.get((w.name, src_hash))
+    line = {
+        "metric": "FMM eval particles/s", "value": value, "unit": "particles/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator)",
+        "config": {"workload": w.name, "n": res["n"], "p": w.p, "theta": w.theta, "leaf": w.leaf,
+                   "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "stage_ms": res["stage_ms"],
+        "counts": {k: st[k] for k in ("n_nodes", "n_leaves", "depth", "n_m2l", "n_p2p", "n_p2p_interactions",
+                                      "walk_pairs")},
+        "roofline": {"kernel": "k_leaf (L2P + P2P)", "bound": "alu", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_note": "derived: 148 SM x 128 FP32 lanes x 2 x 2.032 GHz" if w.dtype == "f32"
+                     else "nominal FP64 1.25 TFLOP/s",
+                     "flops_note": f"{P2P_FLOPS_PER_PAIR} flop per particle pair, {pairs} pairs per launch",
+                     "traffic": traffic},
+        "m2l_roofline": m2l_roofline(res, w),
+        "e2e": {"value": e2e_val, "unit": "particles/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": res["launches"],
+        "clocks": clocks,
+        "also": also,
+        "wall_s": t_wall,
+        "kernel_src": src_hash,
+    }
+    if rank == 0 and not args.no_cpu:
+        v, t = time_oracle(w, args.cpu_sample)
+        line["cpu_baseline"] = {"value": v, "unit": "particles/s", "cores": cpu_cores(), "kind": "oracle",
+                                "sample": f"full oracle FMM on N={args.cpu_sample} particles of the {w.name} "
+                                          f"recipe ({t:.1f} s)"}
+    res["plan"].close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def m2l_roofline(res, w):
+    """Algorithmic M2L flops: 2 * C(p+6,6) (contraction) + ~10 * C(p+3,3) (derivative build) per pair."""
+    from math import comb
+
+    per_pair = 2 * comb(w.p + 6, 6) + 10 * comb(w.p + 3, 3)
+    ms = res["stage_ms"]["m2l"]
+    achieved = per_pair * res["stats"]["n_m2l"] / (ms / 1e3) / 1e12
+    peak = FP32_PEAK_TFLOPS if w.dtype == "f32" else FP64_PEAK_TFLOPS
+    return {"kernel": "k_m2l", "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "flops_per_pair": per_pair, "pairs": res["stats"]["n_m2l"]}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="clustered_2p20_f32")
+    ap.add_argument("--cpu-sample", type=int, default=1 << 17)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--no-also", action="store_true", help="skip the secondary N=1e5 fp64 point")
+    args = ap.parse_args()
+    rank, world, local_rank = env_rank()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

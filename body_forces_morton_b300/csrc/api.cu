@@ -1,0 +1,541 @@
+// C ABI of the FMM library: plan life cycle, the evaluation pipeline, the
+// kick-drift-kick step, statistics and inspection exports.
+//
+// An evaluation runs in two phases on the caller's stream:
+//   phase 1  root box, keys, radix sort (+ gather), octree levels;
+//            then one read-back of the small status block (node count, depth)
+//   phase 2  upward pass, dual-tree walk (2 * depth + 1 generations), lists,
+//            M2L, L2L (depth + 1 levels), L2P + P2P + scatter;
+//            then one read-back of the status block.
+// Capacities of the node, frontier and pair buffers are estimates; a kernel
+// that would exceed one skips the write and sets a bit in the status word, and
+// the evaluation is repeated with larger buffers.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/fmm.h"
+#include "plan.h"
+
+using namespace bfm;
+
+struct fmm_plan {
+    Plan P;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+void set_err(const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+}
+
+#define CUDA_TRY(call)                                                                         \
+    do {                                                                                       \
+        cudaError_t e_ = (call);                                                               \
+        if (e_ != cudaSuccess) {                                                               \
+            set_err("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
+            return e_ == cudaErrorMemoryAllocation ? FMM_ERR_OOM : FMM_ERR_CUDA;               \
+        }                                                                                      \
+    } while (0)
+
+template <class X> cudaError_t dalloc(X *&p, size_t count)
+{
+    p = nullptr;
+    if (count == 0) count = 1;
+    return cudaMalloc((void **)&p, count * sizeof(X));
+}
+
+void dfree(void *p)
+{
+    if (p) cudaFree(p);
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+        else prev = -1;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+constexpr int RS_TILE = 4096;
+
+void free_nodes(Plan &P)
+{
+    int **ints[] = {&P.node_first, &P.node_count, &P.node_child0, &P.node_nchild, &P.node_parent,
+                    &P.node_level, &P.node_done,  &P.m2l_cnt,     &P.p2p_cnt,     &P.m2l_off,
+                    &P.p2p_off,    &P.long_seg};
+    for (int **q : ints) { dfree(*q); *q = nullptr; }
+    void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L};
+    for (void **q : vs) { dfree(*q); *q = nullptr; }
+    dfree(P.flags);
+    P.flags = nullptr;
+}
+
+void free_lists(Plan &P)
+{
+    dfree(P.frontier[0]); dfree(P.frontier[1]);
+    dfree(P.m2l_pairs); dfree(P.p2p_pairs); dfree(P.m2l_src); dfree(P.p2p_src);
+    P.frontier[0] = P.frontier[1] = nullptr;
+    P.m2l_pairs = P.p2p_pairs = nullptr;
+    P.m2l_src = P.p2p_src = nullptr;
+}
+
+fmm_status alloc_nodes(Plan &P, int64_t cap)
+{
+    free_nodes(P);
+    P.cap_nodes = cap;
+    const size_t c = (size_t)cap, e = (size_t)P.esize;
+    CUDA_TRY(dalloc(P.node_first, c));
+    CUDA_TRY(dalloc(P.node_count, c));
+    CUDA_TRY(dalloc(P.node_child0, c));
+    CUDA_TRY(dalloc(P.node_nchild, c));
+    CUDA_TRY(dalloc(P.node_parent, c));
+    CUDA_TRY(dalloc(P.node_level, c));
+    CUDA_TRY(dalloc(P.node_done, c));
+    CUDA_TRY(dalloc(P.m2l_cnt, c));
+    CUDA_TRY(dalloc(P.p2p_cnt, c));
+    CUDA_TRY(dalloc(P.m2l_off, c + 1));
+    CUDA_TRY(dalloc(P.p2p_off, c + 1));
+    CUDA_TRY(dalloc(P.long_seg, 2 * c));
+    CUDA_TRY(cudaMalloc(&P.node_lo, 3 * c * e));
+    CUDA_TRY(cudaMalloc(&P.node_hi, 3 * c * e));
+    CUDA_TRY(cudaMalloc(&P.node_c, 4 * c * e));
+    CUDA_TRY(cudaMalloc(&P.node_l, 4 * c * e));
+    CUDA_TRY(cudaMalloc(&P.M, (size_t)P.ncp * c * e));
+    CUDA_TRY(cudaMalloc(&P.Lm2l, (size_t)P.ncp * c * e));
+    CUDA_TRY(cudaMalloc(&P.L, (size_t)P.ncp * c * e));
+    CUDA_TRY(cudaMemset(P.m2l_cnt, 0, c * sizeof(int)));
+    CUDA_TRY(cudaMemset(P.p2p_cnt, 0, c * sizeof(int)));
+    const int64_t tiles_sort = (P.n + RS_TILE - 1) / RS_TILE;
+    P.cap_flags = std::max<int64_t>({tiles_sort * 256, cap / 32 + 64, 2 * (cap / 1024) + 64});
+    CUDA_TRY(dalloc(P.flags, (size_t)P.cap_flags));
+    CUDA_TRY(cudaMemset(P.flags, 0, (size_t)P.cap_flags * sizeof(unsigned long long)));
+    P.epoch = 0;
+    return FMM_OK;
+}
+
+fmm_status alloc_lists(Plan &P, int64_t cap_frontier, int64_t cap_m2l, int64_t cap_p2p)
+{
+    free_lists(P);
+    P.cap_frontier = cap_frontier;
+    P.cap_m2l = cap_m2l;
+    P.cap_p2p = cap_p2p;
+    CUDA_TRY(dalloc(P.frontier[0], (size_t)cap_frontier));
+    CUDA_TRY(dalloc(P.frontier[1], (size_t)cap_frontier));
+    CUDA_TRY(dalloc(P.m2l_pairs, (size_t)cap_m2l));
+    CUDA_TRY(dalloc(P.p2p_pairs, (size_t)cap_p2p));
+    CUDA_TRY(dalloc(P.m2l_src, 2 * (size_t)cap_m2l));
+    CUDA_TRY(dalloc(P.p2p_src, 2 * (size_t)cap_p2p));
+    return FMM_OK;
+}
+
+void destroy_plan(Plan &P)
+{
+    free_nodes(P);
+    free_lists(P);
+    dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
+    dfree(P.xyzm); dfree(P.div); dfree(P.scratch); dfree(P.ctr);
+    dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
+    if (P.ctr_host) cudaFreeHost(P.ctr_host);
+    for (int i = 0; i < kNumEvents; ++i)
+        if (P.ev[i]) cudaEventDestroy(P.ev[i]);
+}
+
+int64_t clamp_cap(double v) { return (int64_t)std::min(v, 2.0e9); }
+
+// Node-count and list estimates; the evaluation grows them when exceeded.
+int64_t node_estimate(const Plan &P) { return std::max<int64_t>(4096, 6 * P.n / P.leaf + 1024); }
+
+void record(Plan &P, int k, cudaStream_t s) { cudaEventRecord(P.ev[k], s); }
+
+const char *error_bits(unsigned e)
+{
+    static thread_local char buf[160];
+    snprintf(buf, sizeof(buf), "%s%s%s%s%s%s%s%s", e & ERR_NONFINITE ? "nonfinite " : "", e & ERR_NODES ? "nodes " : "",
+             e & ERR_FRONTIER ? "frontier " : "", e & ERR_M2L_CAP ? "m2l " : "", e & ERR_P2P_CAP ? "p2p " : "",
+             e & ERR_SPIN ? "spin-limit " : "", e & ERR_BOUNDS ? "bounds " : "", e & ERR_WALK ? "walk " : "");
+    return buf;
+}
+
+fmm_status sync_counters(Plan &P, cudaStream_t s)
+{
+    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(cudaMemcpyAsync(P.ctr_host, P.ctr, sizeof(DevCounters), cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    return FMM_OK;
+}
+
+fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, void *pot, cudaStream_t s)
+{
+    if (!pos || !mass || !acc) {
+        set_err("fmm_eval: pos, mass and acc_out must be non-NULL device pointers");
+        return FMM_ERR_INVALID_ARG;
+    }
+    P.retries = 0;
+    for (int attempt = 0; attempt < 8; ++attempt) {
+        P.slot = 0;
+        P.launches = 0;
+        if (P.epoch > (1u << 24) - 512) {
+            CUDA_TRY(cudaMemsetAsync(P.flags, 0, (size_t)P.cap_flags * sizeof(unsigned long long), s));
+            P.epoch = 0;
+        }
+        // ---- phase 1
+        record(P, 0, s);
+        CUDA_TRY(cudaMemsetAsync(P.ctr, 0, sizeof(DevCounters), s));
+        P.launches += launch_keys(P, pos, s);
+        record(P, 1, s);
+        P.launches += launch_sort(P, pos, mass, s);
+        record(P, 2, s);
+        P.launches += launch_tree(P, s);
+        record(P, 3, s);
+        fmm_status st = sync_counters(P, s);
+        if (st) return st;
+        const DevCounters &h = *P.ctr_host;
+        if (h.error & ERR_NONFINITE) {
+            set_err("fmm_eval: a position is not finite");
+            return FMM_ERR_NONFINITE;
+        }
+        if (h.error & ERR_NODES) {
+            st = alloc_nodes(P, 2 * P.cap_nodes);
+            if (st) return st;
+            P.retries++;
+            continue;
+        }
+        if (h.error) {
+            set_err("fmm_eval: device check failed in the tree build: %s", error_bits(h.error));
+            return FMM_ERR_INTERNAL;
+        }
+        int depth = 0;
+        for (int l = 0; l <= kMaxLevel; ++l)
+            if (h.level_off[l + 1] > h.level_off[l]) depth = l;
+        P.depth = depth;
+        P.n_nodes = h.level_off[depth + 1];
+        // ---- phase 2
+        record(P, 4, s);
+        CUDA_TRY(cudaMemsetAsync(P.node_done, 0, (size_t)P.n_nodes * sizeof(int), s));
+        CUDA_TRY(cudaMemsetAsync(P.m2l_cnt, 0, (size_t)P.n_nodes * sizeof(int), s));
+        CUDA_TRY(cudaMemsetAsync(P.p2p_cnt, 0, (size_t)P.n_nodes * sizeof(int), s));
+        P.launches += launch_upward(P, s);
+        record(P, 5, s);
+        P.launches += launch_walk(P, depth, s);
+        record(P, 6, s);
+        P.launches += launch_lists(P, s);
+        record(P, 7, s);
+        P.launches += launch_m2l(P, s);
+        record(P, 8, s);
+        P.launches += launch_l2l(P, depth, s);
+        record(P, 9, s);
+        P.launches += launch_leaf(P, acc, pot, s);
+        record(P, 10, s);
+        st = sync_counters(P, s);
+        if (st) return st;
+        const unsigned cap_bits = ERR_FRONTIER | ERR_M2L_CAP | ERR_P2P_CAP;
+        if (h.error & cap_bits) {
+            int64_t cf = P.cap_frontier, cm = P.cap_m2l, cp = P.cap_p2p;
+            if (h.error & ERR_FRONTIER) cf = clamp_cap(std::max(2.0 * cf, 1.5 * h.frontier_max));
+            if (h.error & ERR_M2L_CAP) cm = clamp_cap(std::max(2.0 * cm, 1.3 * h.n_m2l_pairs));
+            if (h.error & ERR_P2P_CAP) cp = clamp_cap(std::max(2.0 * cp, 1.3 * h.n_p2p_pairs));
+            st = alloc_lists(P, cf, cm, cp);
+            if (st) return st;
+            P.retries++;
+            continue;
+        }
+        if (h.error) {
+            set_err("fmm_eval: device check failed: %s", error_bits(h.error));
+            return FMM_ERR_INTERNAL;
+        }
+        if (h.frontier_cnt[(2 * depth + 1) % 3] != 0) {
+            set_err("fmm_eval: dual-tree walk did not finish in %d generations", 2 * depth + 1);
+            return FMM_ERR_INTERNAL;
+        }
+        P.n_m2l = 2ll * h.n_m2l_pairs;
+        P.walk_pairs = h.walk_pairs;
+        P.p2p_inter = h.p2p_interactions;
+        P.have_eval = true;
+        return FMM_OK;
+    }
+    set_err("fmm_eval: interaction buffers still overflow after %d regrowths", P.retries);
+    return FMM_ERR_CAPACITY;
+}
+
+}  // namespace
+
+unsigned bfm::Plan::next_epoch()
+{
+    epoch = (epoch + 1) & 0xffffffu;
+    if (epoch == 0) epoch = 1;
+    return epoch;
+}
+
+extern "C" {
+
+fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dtype)
+{
+    g_err.clear();
+    if (n < 1 || n > (int64_t(1) << 30)) { set_err("fmm_plan_create: n must be in [1, 2^30]"); return nullptr; }
+    if (p < 0 || p > kMaxP) { set_err("fmm_plan_create: p must be in [0, 8]"); return nullptr; }
+    if (!(theta > 0.0) || theta > 1.0) { set_err("fmm_plan_create: theta must be in (0, 1]"); return nullptr; }
+    if (leaf < 1) { set_err("fmm_plan_create: leaf must be >= 1"); return nullptr; }
+    if (dtype != FMM_F32 && dtype != FMM_F64) { set_err("fmm_plan_create: unknown dtype"); return nullptr; }
+    fmm_plan *h = new (std::nothrow) fmm_plan();
+    if (!h) { set_err("fmm_plan_create: out of host memory"); return nullptr; }
+    Plan &P = h->P;
+    P.n = n; P.p = p; P.theta = theta; P.leaf = leaf; P.dtype = (int)dtype;
+    P.esize = dtype == FMM_F32 ? 4 : 8;
+    P.nc = (p + 1) * (p + 2) * (p + 3) / 6;
+    P.ncp = (P.nc + 3) / 4 * 4;
+    auto fail = [&](fmm_status) -> fmm_plan * {
+        destroy_plan(P);
+        delete h;
+        return nullptr;
+    };
+    auto ok = [&](cudaError_t e, const char *what) {
+        if (e != cudaSuccess) set_err("fmm_plan_create: %s: %s", what, cudaGetErrorString(e));
+        return e == cudaSuccess;
+    };
+    if (!ok(cudaGetDevice(&P.device), "cudaGetDevice")) return fail(FMM_ERR_CUDA);
+    if (!ok(cudaDeviceGetAttribute(&P.num_sms, cudaDevAttrMultiProcessorCount, P.device), "SM count"))
+        return fail(FMM_ERR_CUDA);
+    const size_t nn = (size_t)n, e = (size_t)P.esize;
+    if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
+        !ok(dalloc(P.idx[0], nn), "perm") || !ok(dalloc(P.idx[1], nn), "perm") ||
+        !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(dalloc(P.div, nn), "divergence") ||
+        !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
+        !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
+        return fail(FMM_ERR_OOM);
+    for (int i = 0; i < kNumEvents; ++i)
+        if (!ok(cudaEventCreate(&P.ev[i]), "events")) return fail(FMM_ERR_CUDA);
+    const int64_t cap = node_estimate(P);
+    if (alloc_nodes(P, cap) != FMM_OK) return fail(FMM_ERR_OOM);
+    if (alloc_lists(P, clamp_cap(8.0 * cap), clamp_cap(48.0 * cap), clamp_cap(12.0 * cap)) != FMM_OK)
+        return fail(FMM_ERR_OOM);
+    return h;
+}
+
+fmm_status fmm_eval(fmm_plan *plan, const void *pos, const void *mass, void *acc_out, void *pot_out, void *stream)
+{
+    g_err.clear();
+    if (!plan) { set_err("fmm_eval: NULL plan"); return FMM_ERR_INVALID_ARG; }
+    DeviceGuard g(plan->P.device);
+    plan->P.cache_valid = false;
+    return eval_device(plan->P, pos, mass, acc_out, pot_out, (cudaStream_t)stream);
+}
+
+fmm_status fmm_eval_host(fmm_plan *plan, const void *pos, const void *mass, void *acc_out, void *pot_out,
+                         void *stream)
+{
+    g_err.clear();
+    if (!plan || !pos || !mass || !acc_out) {
+        set_err("fmm_eval_host: plan, pos, mass and acc_out must be non-NULL");
+        return FMM_ERR_INVALID_ARG;
+    }
+    Plan &P = plan->P;
+    DeviceGuard g(P.device);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t e = (size_t)P.esize, n = (size_t)P.n;
+    if (!P.h_pos) {
+        CUDA_TRY(cudaMalloc(&P.h_pos, 3 * n * e));
+        CUDA_TRY(cudaMalloc(&P.h_mass, n * e));
+        CUDA_TRY(cudaMalloc(&P.h_acc, 3 * n * e));
+        CUDA_TRY(cudaMalloc(&P.h_pot, n * e));
+    }
+    P.cache_valid = false;
+    CUDA_TRY(cudaMemcpyAsync(P.h_pos, pos, 3 * n * e, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(P.h_mass, mass, n * e, cudaMemcpyHostToDevice, s));
+    fmm_status st = eval_device(P, P.h_pos, P.h_mass, P.h_acc, pot_out ? P.h_pot : nullptr, s);
+    if (st) return st;
+    CUDA_TRY(cudaMemcpyAsync(acc_out, P.h_acc, 3 * n * e, cudaMemcpyDeviceToHost, s));
+    if (pot_out) CUDA_TRY(cudaMemcpyAsync(pot_out, P.h_pot, n * e, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    return FMM_OK;
+}
+
+fmm_status fmm_kdk_step(fmm_plan *plan, void *pos, void *vel, const void *mass, double dt, void *stream)
+{
+    g_err.clear();
+    if (!plan || !pos || !vel || !mass) {
+        set_err("fmm_kdk_step: plan, pos, vel and mass must be non-NULL");
+        return FMM_ERR_INVALID_ARG;
+    }
+    Plan &P = plan->P;
+    DeviceGuard g(P.device);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!P.acc_cache) CUDA_TRY(cudaMalloc(&P.acc_cache, 3 * (size_t)P.n * P.esize));
+    const bool cached = P.cache_valid && P.cache_pos == pos && P.cache_vel == vel && P.cache_mass == mass;
+    P.cache_valid = false;
+    int kdk_launches = 0;
+    if (!cached) {
+        fmm_status st = eval_device(P, pos, mass, P.acc_cache, nullptr, s);
+        if (st) return st;
+        kdk_launches += P.launches;
+    }
+    kdk_launches += launch_kick(P, vel, P.acc_cache, 0.5 * dt, s);
+    kdk_launches += launch_drift(P, pos, vel, dt, s);
+    fmm_status st = eval_device(P, pos, mass, P.acc_cache, nullptr, s);
+    if (st) return st;
+    kdk_launches += P.launches;
+    kdk_launches += launch_kick(P, vel, P.acc_cache, 0.5 * dt, s);
+    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(cudaStreamSynchronize(s));
+    P.launches = kdk_launches;
+    P.cache_valid = true;
+    P.cache_pos = pos;
+    P.cache_vel = vel;
+    P.cache_mass = mass;
+    return FMM_OK;
+}
+
+void fmm_kdk_reset(fmm_plan *plan)
+{
+    if (plan) plan->P.cache_valid = false;
+}
+
+void fmm_destroy(fmm_plan *plan)
+{
+    if (!plan) return;
+    DeviceGuard g(plan->P.device);
+    cudaDeviceSynchronize();
+    destroy_plan(plan->P);
+    delete plan;
+}
+
+const char *fmm_last_error(void) { return g_err.c_str(); }
+
+fmm_status fmm_plan_stats(const fmm_plan *plan, fmm_stats *out)
+{
+    g_err.clear();
+    if (!plan || !out) { set_err("fmm_plan_stats: NULL argument"); return FMM_ERR_INVALID_ARG; }
+    const Plan &P = plan->P;
+    memset(out, 0, sizeof(*out));
+    out->n = P.n;
+    out->p = P.p;
+    if (!P.have_eval) return FMM_OK;
+    DeviceGuard g(P.device);
+    const DevCounters &h = *P.ctr_host;
+    out->n_nodes = P.n_nodes;
+    out->depth = P.depth;
+    out->n_m2l = P.n_m2l;
+    out->n_p2p_interactions = P.p2p_inter;
+    out->walk_pairs = P.walk_pairs;
+    out->launches = P.launches;
+    out->retries = P.retries;
+    // every leaf has exactly one self pair, counted once in the directed lists
+    int64_t leaves = 0;
+    {
+        std::vector<int> nch((size_t)P.n_nodes);
+        if (cudaMemcpy(nch.data(), P.node_nchild, nch.size() * sizeof(int), cudaMemcpyDeviceToHost) == cudaSuccess)
+            for (int v : nch) leaves += v == 0;
+    }
+    out->n_leaves = leaves;
+    out->n_p2p = 2ll * h.n_p2p_pairs - leaves;
+    static const int a[FMM_N_STAGES] = {0, 1, 2, 4, 5, 6, 7, 8, 9};
+    static const int b[FMM_N_STAGES] = {1, 2, 3, 5, 6, 7, 8, 9, 10};
+    for (int k = 0; k < FMM_N_STAGES; ++k) {
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, P.ev[a[k]], P.ev[b[k]]);
+        out->stage_ms[k] = ms;
+    }
+    float tot = 0.f;
+    cudaEventElapsedTime(&tot, P.ev[0], P.ev[10]);
+    out->total_ms = tot;
+    return FMM_OK;
+}
+
+int64_t fmm_plan_export_size(const fmm_plan *plan, int what)
+{
+    if (!plan) return -1;
+    const Plan &P = plan->P;
+    const int64_t nn = P.have_eval ? P.n_nodes : 0, e = P.esize;
+    switch (what) {
+    case FMM_EXPORT_KEYS: return 8 * P.n;
+    case FMM_EXPORT_PERM: return 4 * P.n;
+    case FMM_EXPORT_NODE_FIRST: case FMM_EXPORT_NODE_COUNT: case FMM_EXPORT_NODE_CHILD0:
+    case FMM_EXPORT_NODE_NCHILD: case FMM_EXPORT_NODE_PARENT: case FMM_EXPORT_NODE_LEVEL: return 4 * nn;
+    case FMM_EXPORT_LEVEL_OFF: return 4 * (kMaxLevel + 2);
+    case FMM_EXPORT_NODE_LO: case FMM_EXPORT_NODE_HI: case FMM_EXPORT_NODE_CENTRE: case FMM_EXPORT_NODE_HALF:
+        return 3 * e * nn;
+    case FMM_EXPORT_MULTIPOLE: case FMM_EXPORT_LOCAL_M2L: case FMM_EXPORT_LOCAL: return (int64_t)P.nc * e * nn;
+    case FMM_EXPORT_M2L_OFF: case FMM_EXPORT_P2P_OFF: return 4 * (nn + 1);
+    case FMM_EXPORT_M2L_SRC: case FMM_EXPORT_P2P_SRC: {
+        if (!P.have_eval) return 0;
+        int total = 0;
+        const int *off = what == FMM_EXPORT_M2L_SRC ? P.m2l_off : P.p2p_off;
+        if (cudaMemcpy(&total, off + nn, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+        return 4 * (int64_t)total;
+    }
+    default: return -1;
+    }
+}
+
+fmm_status fmm_plan_export(const fmm_plan *plan, int what, void *dst, int64_t bytes)
+{
+    g_err.clear();
+    const int64_t need = fmm_plan_export_size(plan, what);
+    if (!plan || !dst || need < 0 || bytes < need) {
+        set_err("fmm_plan_export: bad plan, selector or buffer size (need %lld bytes)", (long long)need);
+        return FMM_ERR_INVALID_ARG;
+    }
+    const Plan &P = plan->P;
+    DeviceGuard g(P.device);
+    CUDA_TRY(cudaDeviceSynchronize());
+    const int64_t nn = P.n_nodes, e = P.esize;
+    auto copy = [&](const void *src) -> fmm_status {
+        CUDA_TRY(cudaMemcpy(dst, src, (size_t)need, cudaMemcpyDeviceToHost));
+        return FMM_OK;
+    };
+    switch (what) {
+    case FMM_EXPORT_KEYS: return copy(P.keys[0]);
+    case FMM_EXPORT_PERM: return copy(P.idx[0]);
+    case FMM_EXPORT_NODE_FIRST: return copy(P.node_first);
+    case FMM_EXPORT_NODE_COUNT: return copy(P.node_count);
+    case FMM_EXPORT_NODE_CHILD0: return copy(P.node_child0);
+    case FMM_EXPORT_NODE_NCHILD: return copy(P.node_nchild);
+    case FMM_EXPORT_NODE_PARENT: return copy(P.node_parent);
+    case FMM_EXPORT_NODE_LEVEL: return copy(P.node_level);
+    case FMM_EXPORT_LEVEL_OFF: memcpy(dst, P.ctr_host->level_off, (size_t)need); return FMM_OK;
+    case FMM_EXPORT_NODE_LO: return copy(P.node_lo);
+    case FMM_EXPORT_NODE_HI: return copy(P.node_hi);
+    case FMM_EXPORT_M2L_OFF: return copy(P.m2l_off);
+    case FMM_EXPORT_P2P_OFF: return copy(P.p2p_off);
+    case FMM_EXPORT_M2L_SRC: return copy(P.m2l_src);
+    case FMM_EXPORT_P2P_SRC: return copy(P.p2p_src);
+    case FMM_EXPORT_NODE_CENTRE: case FMM_EXPORT_NODE_HALF: {
+        std::vector<char> tmp((size_t)(4 * e * nn));
+        CUDA_TRY(cudaMemcpy(tmp.data(), what == FMM_EXPORT_NODE_CENTRE ? P.node_c : P.node_l, tmp.size(),
+                            cudaMemcpyDeviceToHost));
+        for (int64_t a = 0; a < nn; ++a) memcpy((char *)dst + 3 * e * a, tmp.data() + 4 * e * a, (size_t)(3 * e));
+        return FMM_OK;
+    }
+    case FMM_EXPORT_MULTIPOLE: case FMM_EXPORT_LOCAL_M2L: case FMM_EXPORT_LOCAL: {
+        const void *src = what == FMM_EXPORT_MULTIPOLE ? P.M : (what == FMM_EXPORT_LOCAL_M2L ? P.Lm2l : P.L);
+        std::vector<char> tmp((size_t)(P.ncp * e * nn));
+        CUDA_TRY(cudaMemcpy(tmp.data(), src, tmp.size(), cudaMemcpyDeviceToHost));
+        for (int64_t a = 0; a < nn; ++a)
+            memcpy((char *)dst + P.nc * e * a, tmp.data() + P.ncp * e * a, (size_t)(P.nc * e));
+        return FMM_OK;
+    }
+    default: break;
+    }
+    set_err("fmm_plan_export: unknown selector %d", what);
+    return FMM_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

@@ -1,0 +1,180 @@
+// Shared device utilities of the FMM library: vector types, exactly rounded
+// scalar operations for the geometry, the device status word, a decoupled
+// look-back chained scan and warp helpers.
+#pragma once
+
+#include <cuda/atomic>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bfm {
+
+constexpr int kMaxLevel = 21;        // Morton keys carry 21 bits per axis
+constexpr int kMaxP = 8;
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---- device status word bits (ORed by kernels, read by the host) ----------
+enum : unsigned {
+    ERR_NONFINITE = 1u << 0,  // a NaN / Inf position
+    ERR_NODES = 1u << 1,      // node capacity exceeded
+    ERR_FRONTIER = 1u << 2,   // walk frontier capacity exceeded
+    ERR_M2L_CAP = 1u << 3,    // M2L pair capacity exceeded
+    ERR_P2P_CAP = 1u << 4,    // P2P pair capacity exceeded
+    ERR_SPIN = 1u << 5,       // a bounded wait gave up
+    ERR_BOUNDS = 1u << 6,     // an index check failed (skipped access)
+    ERR_WALK = 1u << 7,       // walk did not terminate in the expected iterations
+};
+
+// ---- per-evaluation device counters (zeroed at the start of every evaluation)
+struct DevCounters {
+    unsigned error;
+    int n_nodes;
+    int depth;
+    int bbox_done;
+    int level_off[kMaxLevel + 3];
+    double box[4];                 // root box min corner (x, y, z) and side, in the plan's dtype widened
+    unsigned hist[8][256];         // radix digit histograms, one row per pass
+    unsigned tile_ctr[96];         // one ticket counter per chained-scan use
+    int frontier_cnt[3];           // walk frontier sizes (cycled)
+    int frontier_max;
+    int n_m2l_pairs;
+    int n_p2p_pairs;
+    long long walk_pairs;
+    long long p2p_interactions;
+    int n_long;                    // list segments too long for the warp sort
+    int pad;
+};
+
+// ---- vector types ---------------------------------------------------------
+struct __align__(32) dbl4 { double x, y, z, w; };
+template <class T> struct V4;
+template <> struct V4<float> { using type = float4; };
+template <> struct V4<double> { using type = dbl4; };
+template <class T> using vec4 = typename V4<T>::type;
+
+template <class T> __device__ __forceinline__ vec4<T> make4(T x, T y, T z, T w)
+{
+    vec4<T> v;
+    v.x = x; v.y = y; v.z = z; v.w = w;
+    return v;
+}
+
+// ---- exactly rounded scalar ops (never contracted into FMA) ----------------
+__device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
+__device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
+__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
+__device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
+__device__ __forceinline__ double div_rn(double a, double b) { return __ddiv_rn(a, b); }
+
+// |v|^2 as ((x*x + y*y) + z*z), every step rounded
+template <class T> __device__ __forceinline__ T norm2_rn(T x, T y, T z)
+{
+    return add_rn(add_rn(mul_rn(x, x), mul_rn(y, y)), mul_rn(z, z));
+}
+
+// ---- loads that bypass L1 (data written by other blocks of the same kernel)
+template <class T> __device__ __forceinline__ T ld_cg(const T *p) { return __ldcg(p); }
+__device__ __forceinline__ dbl4 ld_cg(const dbl4 *p)
+{
+    const double2 *q = reinterpret_cast<const double2 *>(p);
+    double2 a = __ldcg(q), b = __ldcg(q + 1);
+    dbl4 r;
+    r.x = a.x; r.y = a.y; r.z = b.x; r.w = b.y;
+    return r;
+}
+
+__device__ __forceinline__ void set_error(DevCounters *c, unsigned bit) { atomicOr(&c->error, bit); }
+
+// ---- chained scan with decoupled look-back ---------------------------------
+// Flag word: [63:40] epoch, [39:38] state (1 = aggregate, 2 = inclusive prefix), [37:0] value.
+constexpr unsigned long long kFlagValueMask = (1ull << 38) - 1;
+constexpr unsigned kSpinLimit = 1u << 22;
+
+__device__ __forceinline__ unsigned long long flag_pack(unsigned epoch, unsigned state, unsigned long long v)
+{
+    return ((unsigned long long)(epoch & 0xffffffu) << 40) | ((unsigned long long)state << 38) | (v & kFlagValueMask);
+}
+
+__device__ __forceinline__ void flag_store(unsigned long long *p, unsigned long long v)
+{
+    cuda::atomic_ref<unsigned long long, cuda::thread_scope_device> r(*p);
+    r.store(v, cuda::memory_order_release);
+}
+
+__device__ __forceinline__ unsigned long long flag_load(unsigned long long *p)
+{
+    cuda::atomic_ref<unsigned long long, cuda::thread_scope_device> r(*p);
+    return r.load(cuda::memory_order_acquire);
+}
+
+// Exclusive prefix of `aggregate` over the tiles before `tile` in one chained
+// scan. flags[t * stride] is tile t's word. Called by one thread per scanned
+// quantity. Every tile with a lower index was taken earlier from the same ticket
+// counter, so it is running or done and the wait ends; the spin is bounded all the
+// same and reports ERR_SPIN (returning a partial prefix) if it ever gives up.
+__device__ __forceinline__ unsigned long long chained_exclusive(unsigned long long *flags, int stride, int tile,
+                                                                unsigned long long aggregate, unsigned epoch,
+                                                                DevCounters *ctr)
+{
+    if (tile == 0) {
+        flag_store(flags, flag_pack(epoch, 2, aggregate));
+        return 0;
+    }
+    flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 1, aggregate));
+    unsigned long long excl = 0;
+    int t = tile - 1;
+    unsigned spins = 0;
+    const unsigned long long ep = (unsigned long long)(epoch & 0xffffffu);
+    while (t >= 0) {
+        unsigned long long f = flag_load(flags + (size_t)t * stride);
+        unsigned state = (unsigned)((f >> 38) & 3u);
+        if ((f >> 40) != ep || state == 0) {
+            if (++spins > kSpinLimit) {
+                set_error(ctr, ERR_SPIN);
+                break;
+            }
+            continue;
+        }
+        excl += f & kFlagValueMask;
+        if (state == 2) break;
+        --t;
+    }
+    flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 2, excl + aggregate));
+    return excl;
+}
+
+// ---- warp helpers ------------------------------------------------------------
+__device__ __forceinline__ unsigned lanemask_lt()
+{
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+template <class T> __device__ __forceinline__ T warp_sum_xor(T v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// inclusive scan over the warp of an int
+__device__ __forceinline__ int warp_incl_scan(int v)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+template <class T> __device__ __forceinline__ T pos_inf();
+template <> __device__ __forceinline__ float pos_inf<float>() { return __int_as_float(0x7f800000); }
+template <> __device__ __forceinline__ double pos_inf<double>() { return __longlong_as_double(0x7ff0000000000000ll); }
+
+}  // namespace bfm

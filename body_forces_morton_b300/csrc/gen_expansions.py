@@ -1,0 +1,244 @@
+"""Emit ``expansions_gen.cuh``: fully unrolled Cartesian expansion operators.
+
+For every order P in 0..8 this writes a specialisation ``Exp<P>`` with device
+functions templated on the real type (float / double):
+
+  p2m  M_n  += m s^n / n!                                  (JZ-FMM moment eqs.)
+  m2m  Mp_n += sum_{k<=n} Mc_k d^{n-k} / (n-k)!              (upward translation)
+  m2l  L_k  += -sum_{|n|<=P-|k|} (-1)^{|n|} M_n D^{n+k}(R)   (M2L eqs.), with
+       D^n = d^n(1/r) from the recurrence
+       l r^2 D^n = -(2l-1) sum_i n_i R_i D^{n-e_i} - (l-1) sum_i n_i(n_i-1) D^{n-2e_i}
+  l2l  Lc_k += sum_{j>=k} Lp_j e^{j-k} / (j-k)!               (downward translation)
+  l2p  phi = sum_k L_k x^k/k!,  a = -sum_k L_{k+e_a} x^k/k!   (Taylor eq.)
+
+Every index is a compile-time constant, so the coefficient arrays of the
+callers live in registers. Coefficient order: graded by total degree; within
+a degree the x exponent descends, then the y exponent.
+
+Run ``python gen_expansions.py`` to regenerate; the output is committed.
+"""
+from __future__ import annotations
+
+import os
+from math import factorial
+
+MAXP = 8
+
+
+def ncoef(p):
+    return (p + 1) * (p + 2) * (p + 3) // 6
+
+
+def idx(n):
+    nx, ny, nz = n
+    d = nx + ny + nz
+    t = d - nx
+    return d * (d + 1) * (d + 2) // 6 + t * (t + 1) // 2 + (t - ny)
+
+
+def table(p):
+    out = []
+    for d in range(p + 1):
+        for nx in range(d, -1, -1):
+            for ny in range(d - nx, -1, -1):
+                out.append((nx, ny, d - nx - ny))
+    assert [idx(n) for n in out] == list(range(len(out)))
+    return out
+
+
+def lit(v):
+    """A real literal converted to T at compile time."""
+    return f"T({float(v)!r})"
+
+
+AX = "xyz"
+
+
+def mono_recurrence(p, src, var, name, first=None):
+    """Lines computing name[n] = (first) * var^n / n! for |n| <= p.
+
+    ``var`` is a prefix: the scaled coordinates var{axis}{k} = var_axis / k
+    must be defined by the caller for k = 1..p.
+    """
+    lines = []
+    mi = table(p)
+    lines.append(f"T {name}[{len(mi)}];")
+    lines.append(f"{name}[0] = {first if first else 'T(1)'};")
+    for n in mi[1:]:
+        i = 0 if n[0] > 0 else (1 if n[1] > 0 else 2)
+        m = list(n)
+        m[i] -= 1
+        lines.append(f"{name}[{idx(n)}] = {name}[{idx(tuple(m))}] * {var}{AX[i]}{n[i]};")
+    return lines
+
+
+def scaled_coords(p, var, x, y, z):
+    lines = []
+    if p == 0:
+        return lines
+    for a, c in zip(AX, (x, y, z)):
+        lines.append(f"const T {var}{a}1 = {c};")
+        for k in range(2, p + 1):
+            lines.append(f"const T {var}{a}{k} = {c} * {lit(1.0 / k)};")
+    return lines
+
+
+def gen_p2m(p):
+    b = ["template <class T> static __device__ __forceinline__ void p2m(T sx, T sy, T sz, T m, T* M) {"]
+    if p == 0:
+        b.append("  (void)sx; (void)sy; (void)sz;")
+    b += ["  " + l for l in scaled_coords(p, "s", "sx", "sy", "sz")]
+    b += ["  " + l for l in mono_recurrence(p, None, "s", "t", first="m")]
+    for n in table(p):
+        b.append(f"  M[{idx(n)}] += t[{idx(n)}];")
+    b.append("}")
+    return b
+
+
+def gen_m2m(p):
+    b = ["template <class T> static __device__ __forceinline__ void m2m(const T* Mc, T dx, T dy, T dz, T* Mp) {"]
+    if p == 0:
+        b.append("  (void)dx; (void)dy; (void)dz;")
+    if p > 0:
+        b += ["  " + l for l in scaled_coords(p, "d", "dx", "dy", "dz")]
+        b += ["  " + l for l in mono_recurrence(p, None, "d", "u")]
+    for n in table(p):
+        terms = []
+        for k in table(p):
+            if k[0] <= n[0] and k[1] <= n[1] and k[2] <= n[2]:
+                q = (n[0] - k[0], n[1] - k[1], n[2] - k[2])
+                if q == (0, 0, 0):
+                    terms.append(f"Mc[{idx(k)}]")
+                else:
+                    terms.append(f"Mc[{idx(k)}] * u[{idx(q)}]")
+        b.append(f"  Mp[{idx(n)}] += " + " + ".join(terms) + ";")
+    b.append("}")
+    return b
+
+
+def gen_derivs(p):
+    """Lines building D[ncoef(p)] from rx, ry, rz (1/r derivative tensor)."""
+    mi = table(p)
+    L = [f"T D[{len(mi)}];",
+         "const T r2 = rx * rx + ry * ry + rz * rz;",
+         "D[0] = rsqrt_t(r2);"]
+    if p == 0:
+        return L
+    L.append("const T ir2 = D[0] * D[0];")
+    L.append("const T ax = rx * ir2, ay = ry * ir2, az = rz * ir2;")
+    for a in AX:
+        for k in range(2, p + 1):
+            L.append(f"const T a{a}{k} = a{a} * {lit(k)};")
+    for l in range(2, p + 1):
+        L.append(f"const T c2_{l} = ir2 * {lit(-(l - 1) / l)};")
+    for n in mi[1:]:
+        l = sum(n)
+        s1 = []
+        s2 = []
+        for i in range(3):
+            if n[i] >= 1:
+                m = list(n)
+                m[i] -= 1
+                coef = f"a{AX[i]}" if n[i] == 1 else f"a{AX[i]}{n[i]}"
+                s1.append(f"{coef} * D[{idx(tuple(m))}]")
+            if n[i] >= 2:
+                m = list(n)
+                m[i] -= 2
+                s2.append(f"{lit(n[i] * (n[i] - 1))} * D[{idx(tuple(m))}]")
+        c1 = lit(-(2 * l - 1) / l)
+        expr = f"{c1} * ({' + '.join(s1)})"
+        if s2:
+            expr += f" + c2_{l} * ({' + '.join(s2)})"
+        L.append(f"D[{idx(n)}] = {expr};")
+    return L
+
+
+def gen_m2l(p):
+    b = ["template <class T> static __device__ __forceinline__ void m2l(const T* M, T rx, T ry, T rz, T* L) {"]
+    b += ["  " + l for l in gen_derivs(p)]
+    mi = table(p)
+    for k in mi:
+        lk = sum(k)
+        for n in mi:
+            ln = sum(n)
+            if ln + lk > p:
+                continue
+            j = idx((n[0] + k[0], n[1] + k[1], n[2] + k[2]))
+            op = "+=" if ln % 2 == 1 else "-="
+            b.append(f"  L[{idx(k)}] {op} M[{idx(n)}] * D[{j}];")
+    b.append("}")
+    return b
+
+
+def gen_l2l(p):
+    b = ["template <class T> static __device__ __forceinline__ void l2l(const T* Lp, T ex, T ey, T ez, T* Lc) {"]
+    if p == 0:
+        b.append("  (void)ex; (void)ey; (void)ez;")
+    if p > 0:
+        b += ["  " + l for l in scaled_coords(p, "e", "ex", "ey", "ez")]
+        b += ["  " + l for l in mono_recurrence(p, None, "e", "u")]
+    mi = table(p)
+    for k in mi:
+        terms = []
+        for j in mi:
+            if j[0] >= k[0] and j[1] >= k[1] and j[2] >= k[2]:
+                q = (j[0] - k[0], j[1] - k[1], j[2] - k[2])
+                terms.append(f"Lp[{idx(j)}]" if q == (0, 0, 0) else f"Lp[{idx(j)}] * u[{idx(q)}]")
+        b.append(f"  Lc[{idx(k)}] += " + " + ".join(terms) + ";")
+    b.append("}")
+    return b
+
+
+def gen_l2p(p):
+    b = ["template <class T> static __device__ __forceinline__ void l2p(const T* L, T dx, T dy, T dz,",
+         "                                                        T& phi, T& ax, T& ay, T& az) {"]
+    if p > 0:
+        b += ["  " + l for l in scaled_coords(p, "x", "dx", "dy", "dz")]
+        b += ["  " + l for l in mono_recurrence(p, None, "x", "u")]
+    else:
+        b.append("  (void)dx; (void)dy; (void)dz;")
+        b.append("  T u[1]; u[0] = T(1);")
+    mi = table(p)
+    b.append("  T f = T(0), gx = T(0), gy = T(0), gz = T(0);")
+    for k in mi:
+        b.append(f"  f += L[{idx(k)}] * u[{idx(k)}];")
+        if sum(k) < p:
+            for a, g in zip(range(3), ("gx", "gy", "gz")):
+                q = list(k)
+                q[a] += 1
+                b.append(f"  {g} += L[{idx(tuple(q))}] * u[{idx(k)}];")
+    b.append("  phi += f; ax -= gx; ay -= gy; az -= gz;")
+    b.append("}")
+    return b
+
+
+def main():
+    out = ["// Generated by gen_expansions.py -- do not edit by hand.",
+           "// Unrolled Cartesian expansion operators for orders 0..8 (see the generator's docstring).",
+           "#pragma once",
+           "",
+           "namespace bfm {",
+           "",
+           "#ifndef BFM_HOST_SHIM",
+           "__device__ __forceinline__ float rsqrt_t(float x) { return rsqrtf(x); }",
+           "__device__ __forceinline__ double rsqrt_t(double x) { return rsqrt(x); }",
+           "#endif",
+           "",
+           "template <int P> struct Exp;",
+           ""]
+    for p in range(MAXP + 1):
+        out.append(f"template <> struct Exp<{p}> {{")
+        out.append(f"  static constexpr int NC = {ncoef(p)};")
+        for gen in (gen_p2m, gen_m2m, gen_m2l, gen_l2l, gen_l2p):
+            out += ["  " + l for l in gen(p)]
+        out.append("};")
+        out.append("")
+    out.append("}  // namespace bfm")
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "expansions_gen.cuh")
+    with open(path, "w") as f:
+        f.write("\n".join(out) + "\n")
+    print(path, sum(1 for _ in out), "lines")
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,291 @@
+// Root box, Morton keys and the stable LSD radix sort of (key, index) pairs.
+//
+// JZ-FMM page, "Why this works well on GPUs": particles are sorted so that
+// neighbours sit next to each other; sorting and tree construction stay on the
+// GPU. Keys interleave 21 bits per axis of the root cube (x highest within each
+// 3-bit digit); the quantisation q = min(floor(((x - lo) / side) * 2^21), 2^21 - 1)
+// is evaluated step by step in the plan's precision without contraction, so the
+// keys are exactly those of any other implementation doing the same steps.
+//
+// Radix sort: 8 passes of 8 bits. Each pass is one kernel: a block takes a
+// 4096-key tile from a ticket counter, ranks its keys per digit with warp
+// match_any (stable within the tile), and finds the tile's output offset per
+// digit with a decoupled look-back over the earlier tiles. The last pass also
+// gathers (x, y, z, m) into sorted order.
+#include "plan.h"
+
+namespace bfm {
+
+namespace {
+
+constexpr int kBoxThreads = 256;
+constexpr int RS_THREADS = 256;
+constexpr int RS_WARPS = RS_THREADS / 32;
+constexpr int RS_ITEMS = 16;
+constexpr int RS_TILE = RS_THREADS * RS_ITEMS;
+
+__device__ __forceinline__ uint64_t spread3(uint32_t v)
+{
+    uint64_t x = v & 0x1fffffu;
+    x = (x | (x << 32)) & 0x1f00000000ffffull;
+    x = (x | (x << 16)) & 0x1f0000ff0000ffull;
+    x = (x | (x << 8)) & 0x100f00f00f00f00full;
+    x = (x | (x << 4)) & 0x10c30c30c30c30c3ull;
+    x = (x | (x << 2)) & 0x1249249249249249ull;
+    return x;
+}
+
+template <class T> __device__ __forceinline__ bool finite_t(T v) { return isfinite(v); }
+template <class T> __device__ __forceinline__ T tmin(T a, T b) { return b < a ? b : a; }
+template <class T> __device__ __forceinline__ T tmax(T a, T b) { return b > a ? b : a; }
+
+// Root box: per-block min/max, the last block to finish reduces the partials.
+template <class T>
+__global__ __launch_bounds__(kBoxThreads) void k_bbox(const T *__restrict__ pos, int n, T *__restrict__ partial,
+                                                      DevCounters *ctr)
+{
+    T lo[3], hi[3];
+    for (int a = 0; a < 3; ++a) { lo[a] = pos_inf<T>(); hi[a] = -pos_inf<T>(); }
+    bool bad = false;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        for (int a = 0; a < 3; ++a) {
+            T v = pos[3 * (int64_t)i + a];
+            bad |= !finite_t(v);
+            lo[a] = tmin(lo[a], v);
+            hi[a] = tmax(hi[a], v);
+        }
+    }
+    if (__any_sync(kFull, bad) && (threadIdx.x & 31) == 0) set_error(ctr, ERR_NONFINITE);
+    for (int o = 16; o > 0; o >>= 1)
+        for (int a = 0; a < 3; ++a) {
+            lo[a] = tmin(lo[a], __shfl_xor_sync(kFull, lo[a], o));
+            hi[a] = tmax(hi[a], __shfl_xor_sync(kFull, hi[a], o));
+        }
+    __shared__ T s[kBoxThreads / 32][6];
+    __shared__ bool s_last;
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0)
+        for (int a = 0; a < 3; ++a) { s[w][a] = lo[a]; s[w][3 + a] = hi[a]; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int k = 1; k < kBoxThreads / 32; ++k)
+            for (int a = 0; a < 3; ++a) {
+                s[0][a] = tmin(s[0][a], s[k][a]);
+                s[0][3 + a] = tmax(s[0][3 + a], s[k][3 + a]);
+            }
+        for (int a = 0; a < 6; ++a) partial[6 * blockIdx.x + a] = s[0][a];
+        __threadfence();
+        s_last = atomicAdd(&ctr->bbox_done, 1) == (int)gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!s_last || threadIdx.x != 0) return;
+    __threadfence();
+    T r[6];
+    for (int a = 0; a < 3; ++a) { r[a] = pos_inf<T>(); r[3 + a] = -pos_inf<T>(); }
+    for (int b = 0; b < (int)gridDim.x; ++b)
+        for (int a = 0; a < 3; ++a) {
+            r[a] = tmin(r[a], ld_cg(partial + 6 * b + a));
+            r[3 + a] = tmax(r[3 + a], ld_cg(partial + 6 * b + 3 + a));
+        }
+    T side = sub_rn(r[3], r[0]);
+    for (int a = 1; a < 3; ++a) {
+        T e = sub_rn(r[3 + a], r[a]);
+        if (e > side) side = e;
+    }
+    if (!(side > T(0))) side = T(1);
+    for (int a = 0; a < 3; ++a) ctr->box[a] = (double)r[a];
+    ctr->box[3] = (double)side;
+}
+
+template <class T> __device__ __forceinline__ uint32_t quantise(T x, T lo, T side)
+{
+    T u = mul_rn(div_rn(sub_rn(x, lo), side), T(2097152.0));
+    T f = floor(u);
+    uint32_t q = (uint32_t)f;
+    return q > 2097151u ? 2097151u : q;
+}
+
+// Keys in the caller's order plus the digit histograms of all 8 passes.
+template <class T>
+__global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, uint64_t *__restrict__ keys,
+                                              DevCounters *ctr)
+{
+    __shared__ unsigned h[8][256];
+    for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const T lo0 = (T)ctr->box[0], lo1 = (T)ctr->box[1], lo2 = (T)ctr->box[2], side = (T)ctr->box[3];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const T *q = pos + 3 * (int64_t)i;
+        uint64_t k = (spread3(quantise(q[0], lo0, side)) << 2) | (spread3(quantise(q[1], lo1, side)) << 1) |
+                     spread3(quantise(q[2], lo2, side));
+        keys[i] = k;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) atomicAdd(&h[r][(k >> (8 * r)) & 255u], 1u);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) {
+        unsigned v = (&h[0][0])[i];
+        if (v) atomicAdd(&ctr->hist[0][0] + i, v);
+    }
+}
+
+template <class T, bool FIRST, bool LAST>
+__global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__restrict__ kin,
+                                                           const uint32_t *__restrict__ vin,
+                                                           uint64_t *__restrict__ kout, uint32_t *__restrict__ vout,
+                                                           int n, int pass, unsigned long long *flags, unsigned epoch,
+                                                           int slot, DevCounters *ctr, const T *__restrict__ pos,
+                                                           const T *__restrict__ mass, vec4<T> *__restrict__ xyzm)
+{
+    __shared__ unsigned s_hist[RS_WARPS][256];
+    __shared__ unsigned s_base[256];
+    __shared__ unsigned s_wsum[RS_WARPS];
+    __shared__ int s_tile;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < RS_WARPS * 256; i += RS_THREADS) (&s_hist[0][0])[i] = 0;
+    if (tid == 0) s_tile = (int)atomicAdd(&ctr->tile_ctr[slot], 1u);
+    __syncthreads();
+    const int tile = s_tile;
+    const int shift = 8 * pass;
+    const int64_t start = (int64_t)tile * RS_TILE + warp * (32 * RS_ITEMS);
+    uint64_t k[RS_ITEMS];
+    uint32_t v[RS_ITEMS];
+    unsigned rank[RS_ITEMS];
+#pragma unroll
+    for (int j = 0; j < RS_ITEMS; ++j) {
+        int64_t i = start + j * 32 + lane;
+        bool valid = i < n;
+        k[j] = valid ? kin[i] : ~0ull;
+        v[j] = valid ? (FIRST ? (uint32_t)i : vin[i]) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < RS_ITEMS; ++j) {
+        const bool valid = start + j * 32 + lane < n;
+        const unsigned d = valid ? (unsigned)((k[j] >> shift) & 255u) : 256u;
+        const unsigned peers = __match_any_sync(kFull, d);
+        const int leader = __ffs(peers) - 1;
+        unsigned mine = (lane == leader && valid) ? s_hist[warp][d] : 0u;
+        const unsigned b = __shfl_sync(kFull, mine, leader);
+        rank[j] = b + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (lane == leader && valid) s_hist[warp][d] = b + __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // per digit: warp offsets within the tile, tile total, look-back, global base
+    {
+        const int d = tid;
+        unsigned tot = 0;
+#pragma unroll
+        for (int w = 0; w < RS_WARPS; ++w) {
+            unsigned c = s_hist[w][d];
+            s_hist[w][d] = tot;
+            tot += c;
+        }
+        unsigned long long excl = chained_exclusive(flags + d, 256, tile, tot, epoch, ctr);
+        // exclusive scan over digits of this pass's global histogram
+        unsigned g = ctr->hist[pass][d];
+        unsigned incl = g;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            unsigned t = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        unsigned wbase = 0;
+        for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
+        s_base[d] = wbase + incl - g + (unsigned)excl;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < RS_ITEMS; ++j) {
+        const int64_t i = start + j * 32 + lane;
+        if (i < n) {
+            const unsigned d = (unsigned)((k[j] >> shift) & 255u);
+            const unsigned out = s_base[d] + s_hist[warp][d] + rank[j];
+            if (out < (unsigned)n) {
+                kout[out] = k[j];
+                vout[out] = v[j];
+                if (LAST) {
+                    const T *q = pos + 3 * (int64_t)v[j];
+                    xyzm[out] = make4<T>(q[0], q[1], q[2], mass[v[j]]);
+                }
+            } else {
+                set_error(ctr, ERR_BOUNDS);
+            }
+        }
+    }
+}
+
+// Divergence level of consecutive sorted keys: the first tree level at which
+// keys[i-1] and keys[i] fall in different cells (22 when equal). Also sets up
+// the root node.
+__global__ void k_diverge(const uint64_t *__restrict__ keys, int n, uint8_t *__restrict__ div, int *first,
+                          int *count, int *child0, int *nchild, int *parent, int *level, DevCounters *ctr)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        if (i == 0) {
+            div[0] = 0;
+            first[0] = 0; count[0] = n; child0[0] = -1; nchild[0] = 0; parent[0] = -1; level[0] = 0;
+            ctr->level_off[0] = 0;
+            ctr->level_off[1] = 1;
+        } else {
+            uint64_t x = keys[i - 1] ^ keys[i];
+            div[i] = x ? (uint8_t)(21 - (63 - __clzll((long long)x)) / 3) : (uint8_t)22;
+        }
+    }
+}
+
+template <class T>
+int launch_keys_t(Plan &P, const void *pos, cudaStream_t s)
+{
+    const int nb = P.num_sms * 4;
+    k_bbox<T><<<nb, kBoxThreads, 0, s>>>((const T *)pos, (int)P.n, (T *)P.scratch, P.ctr);
+    k_keys<T><<<P.num_sms * 8, 256, 0, s>>>((const T *)pos, (int)P.n, P.keys[0], P.ctr);
+    return 2;
+}
+
+template <class T>
+int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
+{
+    const int n = (int)P.n;
+    const int tiles = (n + RS_TILE - 1) / RS_TILE;
+    int launches = 0;
+    for (int pass = 0; pass < 8; ++pass) {
+        const int src = pass & 1, dst = src ^ 1;
+        const int slot = P.next_slot();
+        const unsigned ep = P.next_epoch();
+        if (pass == 0)
+            k_radix_pass<T, true, false><<<tiles, RS_THREADS, 0, s>>>(P.keys[src], nullptr, P.keys[dst], P.idx[dst], n,
+                                                                     pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
+                                                                     nullptr);
+        else if (pass == 7)
+            k_radix_pass<T, false, true><<<tiles, RS_THREADS, 0, s>>>(
+                P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, (const T *)pos,
+                (const T *)mass, (vec4<T> *)P.xyzm);
+        else
+            k_radix_pass<T, false, false><<<tiles, RS_THREADS, 0, s>>>(P.keys[src], P.idx[src], P.keys[dst],
+                                                                      P.idx[dst], n, pass, P.flags, ep, slot, P.ctr,
+                                                                      nullptr, nullptr, nullptr);
+        ++launches;
+    }
+    // after 8 passes the sorted data is back in buffer 0
+    k_diverge<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], n, P.div, P.node_first, P.node_count, P.node_child0,
+                                           P.node_nchild, P.node_parent, P.node_level, P.ctr);
+    return launches + 1;
+}
+
+}  // namespace
+
+int launch_keys(Plan &P, const void *pos, cudaStream_t s)
+{
+    return P.dtype == 0 ? launch_keys_t<float>(P, pos, s) : launch_keys_t<double>(P, pos, s);
+}
+
+int launch_sort(Plan &P, const void *pos, const void *mass, cudaStream_t s)
+{
+    return P.dtype == 0 ? launch_sort_t<float>(P, pos, mass, s) : launch_sort_t<double>(P, pos, mass, s);
+}
+
+}  // namespace bfm

@@ -1,0 +1,177 @@
+// Upward pass: node boxes, centres, half-widths, P2M at the leaves and M2M to
+// the parents, in one kernel.
+//
+// JZ-FMM page, "Combining near and far interactions", stage 1: calculate the
+// moments of the leaves, then translate and combine the children's moments
+// around their parent centres. Moments M_n = sum m s^n / n! about the centre
+// c = (lo + hi) / 2 of the node's tight box; l = (hi - lo) / 2 is the per-axis
+// half-width of the opening criterion.
+//
+// One warp per leaf. When a warp finishes a node it takes a ticket on the
+// parent; the warp holding the parent's last ticket goes on with the parent
+// (all its children are complete), so no warp ever waits. Sums are reduced in
+// a fixed butterfly order, so the result does not depend on which warp gets there.
+#include "expansions_gen.cuh"
+#include "plan.h"
+
+namespace bfm {
+
+namespace {
+
+template <class T> __device__ __forceinline__ T tmin(T a, T b) { return b < a ? b : a; }
+template <class T> __device__ __forceinline__ T tmax(T a, T b) { return b > a ? b : a; }
+
+template <class T>
+__device__ __forceinline__ void store_geometry(int a, const T lo[3], const T hi[3], T *__restrict__ node_lo,
+                                               T *__restrict__ node_hi, vec4<T> *__restrict__ nc,
+                                               vec4<T> *__restrict__ nl, T c[3])
+{
+    T l[3];
+    for (int k = 0; k < 3; ++k) {
+        c[k] = mul_rn(add_rn(lo[k], hi[k]), T(0.5));
+        l[k] = mul_rn(sub_rn(hi[k], lo[k]), T(0.5));
+    }
+    if ((threadIdx.x & 31) == 0) {
+        for (int k = 0; k < 3; ++k) {
+            node_lo[3 * a + k] = lo[k];
+            node_hi[3 * a + k] = hi[k];
+        }
+        nc[a] = make4<T>(c[0], c[1], c[2], norm2_rn(l[0], l[1], l[2]));
+        nl[a] = make4<T>(l[0], l[1], l[2], T(0));
+    }
+}
+
+template <class T, int P>
+__device__ __forceinline__ void store_coeffs(T *__restrict__ dst, const T (&v)[Exp<P>::NC])
+{
+    if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+        for (int k = 0; k < Exp<P>::NC; ++k) dst[k] = v[k];
+    }
+}
+
+template <class T, int P>
+__global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__restrict__ xyzm,
+                                                const int *__restrict__ first, const int *__restrict__ count,
+                                                const int *__restrict__ child0, const int *__restrict__ nchild,
+                                                const int *__restrict__ parent, int *done, T *node_lo, T *node_hi,
+                                                vec4<T> *nc, vec4<T> *nl, T *M, int ncp)
+{
+    constexpr int NC = Exp<P>::NC;
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
+        if (nchild[a] != 0) continue;
+        // ---- leaf: box, centre, P2M
+        const int f = first[a], c = count[a];
+        T lo[3], hi[3], cen[3];
+        for (int k = 0; k < 3; ++k) { lo[k] = pos_inf<T>(); hi[k] = -pos_inf<T>(); }
+        for (int i = f + lane; i < f + c; i += 32) {
+            vec4<T> q = xyzm[i];
+            lo[0] = tmin(lo[0], q.x); hi[0] = tmax(hi[0], q.x);
+            lo[1] = tmin(lo[1], q.y); hi[1] = tmax(hi[1], q.y);
+            lo[2] = tmin(lo[2], q.z); hi[2] = tmax(hi[2], q.z);
+        }
+        for (int o = 16; o > 0; o >>= 1)
+            for (int k = 0; k < 3; ++k) {
+                lo[k] = tmin(lo[k], __shfl_xor_sync(kFull, lo[k], o));
+                hi[k] = tmax(hi[k], __shfl_xor_sync(kFull, hi[k], o));
+            }
+        store_geometry<T>(a, lo, hi, node_lo, node_hi, nc, nl, cen);
+        {
+            T m[NC];
+#pragma unroll
+            for (int k = 0; k < NC; ++k) m[k] = T(0);
+            for (int i = f + lane; i < f + c; i += 32) {
+                vec4<T> q = xyzm[i];
+                Exp<P>::template p2m<T>(q.x - cen[0], q.y - cen[1], q.z - cen[2], q.w, m);
+            }
+#pragma unroll
+            for (int k = 0; k < NC; ++k) m[k] = warp_sum_xor(m[k]);
+            store_coeffs<T, P>(M + (size_t)a * ncp, m);
+        }
+        // ---- climb while this warp completes the parent's last child
+        int cur = a;
+        for (;;) {
+            __threadfence();
+            const int par = parent[cur];
+            if (par < 0) break;
+            int ticket = 0;
+            if (lane == 0) ticket = atomicAdd(&done[par], 1);
+            ticket = __shfl_sync(kFull, ticket, 0);
+            if (ticket != nchild[par] - 1) break;
+            __threadfence();
+            const int c0 = child0[par], nch = nchild[par];
+            for (int k = 0; k < 3; ++k) { lo[k] = pos_inf<T>(); hi[k] = -pos_inf<T>(); }
+            if (lane < nch) {
+                for (int k = 0; k < 3; ++k) {
+                    lo[k] = ld_cg(node_lo + 3 * (c0 + lane) + k);
+                    hi[k] = ld_cg(node_hi + 3 * (c0 + lane) + k);
+                }
+            }
+            for (int o = 16; o > 0; o >>= 1)
+                for (int k = 0; k < 3; ++k) {
+                    lo[k] = tmin(lo[k], __shfl_xor_sync(kFull, lo[k], o));
+                    hi[k] = tmax(hi[k], __shfl_xor_sync(kFull, hi[k], o));
+                }
+            store_geometry<T>(par, lo, hi, node_lo, node_hi, nc, nl, cen);
+            T m[NC];
+#pragma unroll
+            for (int k = 0; k < NC; ++k) m[k] = T(0);
+            if (lane < nch) {
+                const int ch = c0 + lane;
+                T mc[NC];
+#pragma unroll
+                for (int k = 0; k < NC; ++k) mc[k] = ld_cg(M + (size_t)ch * ncp + k);
+                vec4<T> cc = ld_cg(nc + ch);
+                Exp<P>::template m2m<T>(mc, cc.x - cen[0], cc.y - cen[1], cc.z - cen[2], m);
+            }
+            // children sit in lanes 0..7: butterfly over groups of 8 lanes
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                T v = m[k];
+                v += __shfl_xor_sync(kFull, v, 4);
+                v += __shfl_xor_sync(kFull, v, 2);
+                v += __shfl_xor_sync(kFull, v, 1);
+                m[k] = v;
+            }
+            store_coeffs<T, P>(M + (size_t)par * ncp, m);
+            cur = par;
+        }
+    }
+}
+
+template <class T, int P>
+int launch_upward_tp(Plan &P_, cudaStream_t s)
+{
+    k_upward<T, P><<<P_.num_sms * 8, 256, 0, s>>>((int)P_.n_nodes, (const vec4<T> *)P_.xyzm, P_.node_first,
+                                                  P_.node_count, P_.node_child0, P_.node_nchild, P_.node_parent,
+                                                  P_.node_done, (T *)P_.node_lo, (T *)P_.node_hi,
+                                                  (vec4<T> *)P_.node_c, (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp);
+    return 1;
+}
+
+template <class T>
+int launch_upward_t(Plan &P, cudaStream_t s)
+{
+    switch (P.p) {
+    case 0: return launch_upward_tp<T, 0>(P, s);
+    case 1: return launch_upward_tp<T, 1>(P, s);
+    case 2: return launch_upward_tp<T, 2>(P, s);
+    case 3: return launch_upward_tp<T, 3>(P, s);
+    case 4: return launch_upward_tp<T, 4>(P, s);
+    case 5: return launch_upward_tp<T, 5>(P, s);
+    case 6: return launch_upward_tp<T, 6>(P, s);
+    case 7: return launch_upward_tp<T, 7>(P, s);
+    default: return launch_upward_tp<T, 8>(P, s);
+    }
+}
+
+}  // namespace
+
+int launch_upward(Plan &P, cudaStream_t s)
+{
+    return P.dtype == 0 ? launch_upward_t<float>(P, s) : launch_upward_t<double>(P, s);
+}
+
+}  // namespace bfm

@@ -1,0 +1,366 @@
+// Dual-tree walk and the interaction lists.
+//
+// JZ-FMM page, "Combining near and far interactions", stage 2: accept
+// well-separated node pairs for multipole-to-local translations and refine the
+// rest; the opening-criterion eq. accepts (A, B), A != B, when
+// |l_A + l_B| < theta |c_A - c_B|, here evaluated squared, operation by
+// operation in the plan's precision. The traversal is the symmetric one:
+//   (A, A): a leaf gives P2P(A <- A); otherwise every child pair (C_i, C_j), i <= j;
+//   (A, B) accepted: M2L both ways;
+//   (A, B) both leaves: P2P both ways;
+//   otherwise split the node with the larger |l| (the lower index on a tie),
+//   never a leaf, and visit (child, other).
+// The set of pairs this produces does not depend on the visiting order, so
+// the walk runs breadth first: one kernel per frontier generation, appending
+// through warp-aggregated atomics.
+//
+// Lists: per-receiver counts (taken during the walk) -> exclusive scan (one
+// kernel, decoupled look-back) -> atomic fill -> every receiver's segment sorted
+// ascending by source, which makes the order, and with it every later sum,
+// independent of the atomics.
+#include "plan.h"
+
+namespace bfm {
+
+namespace {
+
+constexpr int WK_THREADS = 256;
+constexpr int SEG_WARP_MAX = 1024;     // segments up to this length sort in a warp
+constexpr int CS_THREADS = 256, CS_ITEMS = 4, CS_TILE = CS_THREADS * CS_ITEMS;
+
+__global__ void k_walk_init(int2 *f0, DevCounters *ctr)
+{
+    f0[0] = make_int2(0, 0);
+    ctr->frontier_cnt[0] = 1;
+    ctr->frontier_cnt[1] = 0;
+    ctr->frontier_cnt[2] = 0;
+    ctr->frontier_max = 1;
+}
+
+template <class T>
+__global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__restrict__ fin, int2 *__restrict__ fout,
+                                                          int cap_frontier, const int *__restrict__ nchild,
+                                                          const int *__restrict__ child0,
+                                                          const int *__restrict__ count,
+                                                          const vec4<T> *__restrict__ nc,
+                                                          const vec4<T> *__restrict__ nl, T th2, int2 *m2l_pairs,
+                                                          int cap_m2l, int2 *p2p_pairs, int cap_p2p, int *m2l_cnt,
+                                                          int *p2p_cnt, DevCounters *ctr)
+{
+    const int nin = ctr->frontier_cnt[it % 3];
+    int *cnt_out = &ctr->frontier_cnt[(it + 1) % 3];
+    if (blockIdx.x == 0 && threadIdx.x == 0) ctr->frontier_cnt[(it + 2) % 3] = 0;
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int nread = nin < cap_frontier ? nin : cap_frontier;
+    for (int base = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; base < nread; base += nwarps * 32) {
+        const int i = base + lane;
+        const bool valid = i < nread;
+        int A = 0, B = 0, kids = 0, split = -1, other = 0;
+        bool m2l = false, p2p = false;
+        long long inter = 0;
+        if (valid) {
+            int2 pr = fin[i];
+            A = pr.x;
+            B = pr.y;
+            const int nA = nchild[A];
+            if (A == B) {
+                if (nA == 0) {
+                    p2p = true;
+                    inter = (long long)count[A] * count[A];
+                } else {
+                    kids = nA * (nA + 1) / 2;
+                    split = A;
+                }
+            } else {
+                const int nB = nchild[B];
+                const vec4<T> cA = nc[A], cB = nc[B], lA = nl[A], lB = nl[B];
+                const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
+                const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
+                if (s2 < mul_rn(th2, r2)) {
+                    m2l = true;
+                } else if (nA == 0 && nB == 0) {
+                    p2p = true;
+                    inter = 2ll * count[A] * count[B];
+                } else {
+                    const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
+                    split = splitA ? A : B;
+                    other = splitA ? B : A;
+                    kids = splitA ? nA : nB;
+                }
+            }
+        }
+        // ---- M2L pair
+        {
+            const unsigned m = __ballot_sync(kFull, m2l);
+            if (m) {
+                int b0 = 0;
+                if (lane == 0) b0 = atomicAdd(&ctr->n_m2l_pairs, __popc(m));
+                b0 = __shfl_sync(kFull, b0, 0);
+                if (m2l) {
+                    const int slot = b0 + __popc(m & lanemask_lt());
+                    if (slot < cap_m2l) {
+                        m2l_pairs[slot] = make_int2(A, B);
+                        atomicAdd(&m2l_cnt[A], 1);
+                        atomicAdd(&m2l_cnt[B], 1);
+                    } else {
+                        set_error(ctr, ERR_M2L_CAP);
+                    }
+                }
+            }
+        }
+        // ---- P2P pair
+        {
+            const unsigned m = __ballot_sync(kFull, p2p);
+            if (m) {
+                int b0 = 0;
+                if (lane == 0) b0 = atomicAdd(&ctr->n_p2p_pairs, __popc(m));
+                b0 = __shfl_sync(kFull, b0, 0);
+                if (p2p) {
+                    const int slot = b0 + __popc(m & lanemask_lt());
+                    if (slot < cap_p2p) {
+                        p2p_pairs[slot] = make_int2(A, B);
+                        atomicAdd(&p2p_cnt[A], 1);
+                        if (A != B) atomicAdd(&p2p_cnt[B], 1);
+                    } else {
+                        set_error(ctr, ERR_P2P_CAP);
+                    }
+                }
+                long long s = inter;
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+                if (lane == 0) atomicAdd((unsigned long long *)&ctr->p2p_interactions, (unsigned long long)s);
+            }
+        }
+        // ---- next frontier
+        {
+            const int incl = warp_incl_scan(kids);
+            const int tot = __shfl_sync(kFull, incl, 31);
+            const unsigned vm = __ballot_sync(kFull, valid);
+            if (lane == 0) atomicAdd((unsigned long long *)&ctr->walk_pairs, (unsigned long long)__popc(vm));
+            if (tot) {
+                int b0 = 0;
+                if (lane == 0) {
+                    b0 = atomicAdd(cnt_out, tot);
+                    atomicMax(&ctr->frontier_max, b0 + tot);
+                }
+                b0 = __shfl_sync(kFull, b0, 0);
+                int o = b0 + incl - kids;
+                if (kids) {
+                    const int c0 = child0[split];
+                    if (A == B) {
+                        const int nA = nchild[A];
+                        for (int x = 0; x < nA; ++x)
+                            for (int y = x; y < nA; ++y, ++o) {
+                                if (o < cap_frontier) fout[o] = make_int2(c0 + x, c0 + y);
+                                else set_error(ctr, ERR_FRONTIER);
+                            }
+                    } else {
+                        for (int x = 0; x < kids; ++x, ++o) {
+                            const int C = c0 + x;
+                            if (o < cap_frontier) fout[o] = C < other ? make_int2(C, other) : make_int2(other, C);
+                            else set_error(ctr, ERR_FRONTIER);
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Exclusive scan of the per-receiver counts into CSR offsets (both lists at once).
+__global__ __launch_bounds__(CS_THREADS) void k_csr_scan(int n_nodes, const int *__restrict__ m2l_cnt,
+                                                         const int *__restrict__ p2p_cnt, int *__restrict__ m2l_off,
+                                                         int *__restrict__ p2p_off, unsigned long long *flags,
+                                                         unsigned epoch, int slot, DevCounters *ctr)
+{
+    __shared__ int s_tile;
+    __shared__ int s_w[2][CS_THREADS / 32];
+    __shared__ long long s_ex[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ntiles = (n_nodes + CS_TILE - 1) / CS_TILE;
+    for (;;) {
+        if (tid == 0) s_tile = (int)atomicAdd(&ctr->tile_ctr[slot], 1u);
+        __syncthreads();
+        const int tile = s_tile;
+        if (tile >= ntiles) break;
+        const int i0 = tile * CS_TILE + tid * CS_ITEMS;
+        int a[CS_ITEMS], b[CS_ITEMS], sa = 0, sb = 0;
+#pragma unroll
+        for (int k = 0; k < CS_ITEMS; ++k) {
+            const int i = i0 + k;
+            a[k] = i < n_nodes ? m2l_cnt[i] : 0;
+            b[k] = i < n_nodes ? p2p_cnt[i] : 0;
+            sa += a[k];
+            sb += b[k];
+        }
+        const int ia = warp_incl_scan(sa), ib = warp_incl_scan(sb);
+        if (lane == 31) { s_w[0][warp] = ia; s_w[1][warp] = ib; }
+        __syncthreads();
+        if (tid < 2) {
+            int tot = 0;
+            for (int w = 0; w < CS_THREADS / 32; ++w) tot += s_w[tid][w];
+            s_ex[tid] = (long long)chained_exclusive(flags + tid, 2, tile, (unsigned long long)tot, epoch, ctr);
+            if (tile == ntiles - 1) (tid == 0 ? m2l_off : p2p_off)[n_nodes] = (int)(s_ex[tid] + tot);
+        }
+        __syncthreads();
+        int wa = 0, wb = 0;
+        for (int w = 0; w < warp; ++w) { wa += s_w[0][w]; wb += s_w[1][w]; }
+        int ra = (int)s_ex[0] + wa + ia - sa, rb = (int)s_ex[1] + wb + ib - sb;
+#pragma unroll
+        for (int k = 0; k < CS_ITEMS; ++k) {
+            const int i = i0 + k;
+            if (i < n_nodes) {
+                m2l_off[i] = ra;
+                p2p_off[i] = rb;
+            }
+            ra += a[k];
+            rb += b[k];
+        }
+        __syncthreads();
+    }
+}
+
+// Scatter the unordered pairs into their receivers' segments. The counts are
+// used as countdown cursors and end at zero, ready for the next evaluation.
+__global__ void k_csr_fill(const int2 *__restrict__ m2l_pairs, int cap_m2l, const int2 *__restrict__ p2p_pairs,
+                           int cap_p2p, int *m2l_cnt, int *p2p_cnt, const int *__restrict__ m2l_off,
+                           const int *__restrict__ p2p_off, int *__restrict__ m2l_src, int *__restrict__ p2p_src,
+                           const DevCounters *ctr)
+{
+    const int nm = min(ctr->n_m2l_pairs, cap_m2l), np = min(ctr->n_p2p_pairs, cap_p2p);
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nm + np; i += gridDim.x * blockDim.x) {
+        if (i < nm) {
+            const int2 pr = m2l_pairs[i];
+            m2l_src[m2l_off[pr.x] + atomicSub(&m2l_cnt[pr.x], 1) - 1] = pr.y;
+            m2l_src[m2l_off[pr.y] + atomicSub(&m2l_cnt[pr.y], 1) - 1] = pr.x;
+        } else {
+            const int2 pr = p2p_pairs[i - nm];
+            p2p_src[p2p_off[pr.x] + atomicSub(&p2p_cnt[pr.x], 1) - 1] = pr.y;
+            if (pr.x != pr.y) p2p_src[p2p_off[pr.y] + atomicSub(&p2p_cnt[pr.y], 1) - 1] = pr.x;
+        }
+    }
+}
+
+// Ascending bitonic network for any length: every merge starts with the
+// mirrored compare, so padding at the top (+inf) never has to move.
+__device__ __forceinline__ void cmpswap(int *v, int i, int j)
+{
+    const int a = v[i], b = v[j];
+    if (b < a) { v[i] = b; v[j] = a; }
+}
+
+// One warp per receiver; segments longer than SEG_WARP_MAX go to a second pass.
+__global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restrict__ m2l_off, int *m2l_src,
+                                                 const int *__restrict__ p2p_off, int *p2p_src, int *long_seg,
+                                                 DevCounters *ctr)
+{
+    __shared__ int buf[8][SEG_WARP_MAX];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int *v = buf[w];
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int job = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; job < 2 * n_nodes; job += nwarps) {
+        const int a = job >> 1;
+        const bool isp = job & 1;
+        const int beg = isp ? p2p_off[a] : m2l_off[a];
+        const int len = (isp ? p2p_off[a + 1] : m2l_off[a + 1]) - beg;
+        int *src = (isp ? p2p_src : m2l_src) + beg;
+        if (len <= 1) continue;
+        if (len > SEG_WARP_MAX) {
+            if (lane == 0) long_seg[atomicAdd(&ctr->n_long, 1)] = job;
+            continue;
+        }
+        int S = 2;
+        while (S < len) S <<= 1;
+        for (int i = lane; i < S; i += 32) v[i] = i < len ? src[i] : 0x7fffffff;
+        __syncwarp();
+        for (int k = 2; k <= S; k <<= 1) {
+            for (int i = lane; i < S / 2; i += 32) {
+                const int h = k >> 1, blk = i / h, pos = i % h;
+                cmpswap(v, blk * k + pos, blk * k + k - 1 - pos);
+            }
+            __syncwarp();
+            for (int j = k >> 2; j >= 1; j >>= 1) {
+                for (int i = lane; i < S / 2; i += 32) {
+                    const int blk = i / j, pos = i % j;
+                    cmpswap(v, blk * 2 * j + pos, blk * 2 * j + pos + j);
+                }
+                __syncwarp();
+            }
+        }
+        for (int i = lane; i < len; i += 32) src[i] = v[i];
+        __syncwarp();
+    }
+}
+
+// Long segments: one block each, the same network on global memory (indices at
+// or beyond the length stand for +inf and are never touched).
+__global__ __launch_bounds__(1024) void k_segsort_long(const int *__restrict__ m2l_off, int *m2l_src,
+                                                       const int *__restrict__ p2p_off, int *p2p_src,
+                                                       const int *__restrict__ long_seg, const DevCounters *ctr)
+{
+    const int nlong = ctr->n_long;
+    for (int t = blockIdx.x; t < nlong; t += gridDim.x) {
+        const int job = long_seg[t];
+        const int a = job >> 1;
+        const bool isp = job & 1;
+        const int beg = isp ? p2p_off[a] : m2l_off[a];
+        const int len = (isp ? p2p_off[a + 1] : m2l_off[a + 1]) - beg;
+        int *v = (isp ? p2p_src : m2l_src) + beg;
+        int S = 2;
+        while (S < len) S <<= 1;
+        for (int k = 2; k <= S; k <<= 1) {
+            for (int i = threadIdx.x; i < S / 2; i += blockDim.x) {
+                const int h = k >> 1, blk = i / h, pos = i % h;
+                const int x = blk * k + pos, y = blk * k + k - 1 - pos;
+                if (y < len) cmpswap(v, x, y);
+            }
+            __syncthreads();
+            for (int j = k >> 2; j >= 1; j >>= 1) {
+                for (int i = threadIdx.x; i < S / 2; i += blockDim.x) {
+                    const int blk = i / j, pos = i % j;
+                    const int x = blk * 2 * j + pos, y = x + j;
+                    if (y < len) cmpswap(v, x, y);
+                }
+                __syncthreads();
+            }
+        }
+    }
+}
+
+template <class T>
+int launch_walk_t(Plan &P, int depth, cudaStream_t s)
+{
+    const T th2 = (T)(P.theta * P.theta);
+    k_walk_init<<<1, 1, 0, s>>>(P.frontier[0], P.ctr);
+    const int iters = 2 * depth + 1;
+    for (int it = 0; it < iters; ++it) {
+        k_walk_iter<T><<<P.num_sms * 8, WK_THREADS, 0, s>>>(
+            it, P.frontier[it & 1], P.frontier[(it + 1) & 1], (int)P.cap_frontier, P.node_nchild, P.node_child0,
+            P.node_count, (const vec4<T> *)P.node_c, (const vec4<T> *)P.node_l, th2, P.m2l_pairs, (int)P.cap_m2l,
+            P.p2p_pairs, (int)P.cap_p2p, P.m2l_cnt, P.p2p_cnt, P.ctr);
+    }
+    return iters + 1;
+}
+
+}  // namespace
+
+int launch_walk(Plan &P, int depth, cudaStream_t s)
+{
+    return P.dtype == 0 ? launch_walk_t<float>(P, depth, s) : launch_walk_t<double>(P, depth, s);
+}
+
+int launch_lists(Plan &P, cudaStream_t s)
+{
+    const int nn = (int)P.n_nodes;
+    const int slot = P.next_slot();
+    const unsigned ep = P.next_epoch();
+    k_csr_scan<<<P.num_sms * 4, CS_THREADS, 0, s>>>(nn, P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off, P.flags, ep, slot,
+                                                    P.ctr);
+    k_csr_fill<<<P.num_sms * 8, 256, 0, s>>>(P.m2l_pairs, (int)P.cap_m2l, P.p2p_pairs, (int)P.cap_p2p, P.m2l_cnt,
+                                             P.p2p_cnt, P.m2l_off, P.p2p_off, P.m2l_src, P.p2p_src, P.ctr);
+    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(nn, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
+    k_segsort_long<<<P.num_sms, 1024, 0, s>>>(P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
+    return 4;
+}
+
+}  // namespace bfm

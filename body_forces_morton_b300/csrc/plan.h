@@ -1,0 +1,102 @@
+// Host-side plan of the FMM library: device buffers, capacities and the
+// launchers each kernel file provides.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace bfm {
+
+constexpr int kNumEvents = 12;
+
+struct Plan {
+    // parameters
+    int64_t n = 0;
+    int p = 4;
+    int nc = 35;        // coefficients per expansion
+    int ncp = 36;       // padded row stride (multiple of 4 elements)
+    double theta = 0.7;
+    int leaf = 32;
+    int dtype = 0;      // 0 f32, 1 f64
+    int esize = 4;      // bytes per real
+    int device = 0;
+    int num_sms = 148;
+
+    // capacities
+    int64_t cap_nodes = 0, cap_frontier = 0, cap_m2l = 0, cap_p2p = 0, cap_flags = 0;
+
+    // particle buffers
+    uint64_t *keys[2] = {nullptr, nullptr};
+    uint32_t *idx[2] = {nullptr, nullptr};
+    void *xyzm = nullptr;          // sorted particles, vec4<T> (x, y, z, m)
+    uint8_t *div = nullptr;        // divergence level of consecutive sorted keys
+
+    // node buffers
+    int *node_first = nullptr, *node_count = nullptr, *node_child0 = nullptr, *node_nchild = nullptr;
+    int *node_parent = nullptr, *node_level = nullptr, *node_done = nullptr;
+    void *node_lo = nullptr, *node_hi = nullptr;  // T[3] per node
+    void *node_c = nullptr, *node_l = nullptr;    // vec4<T>: (cx, cy, cz, |l|^2), (lx, ly, lz, 0)
+    void *M = nullptr, *Lm2l = nullptr, *L = nullptr;  // T[ncp] per node
+
+    // walk and lists
+    int2 *frontier[2] = {nullptr, nullptr};
+    int2 *m2l_pairs = nullptr, *p2p_pairs = nullptr;
+    int *m2l_cnt = nullptr, *p2p_cnt = nullptr;    // per receiver counts (also fill cursors)
+    int *m2l_off = nullptr, *p2p_off = nullptr;    // CSR offsets [cap_nodes + 1]
+    int *m2l_src = nullptr, *p2p_src = nullptr;    // CSR sources [2 * cap]
+    int *long_seg = nullptr;                       // receivers whose lists are too long for the warp sort
+
+    void *scratch = nullptr;       // 64 KiB for small per-block partials
+
+    // chained-scan flags
+    unsigned long long *flags = nullptr;
+    unsigned epoch = 0;
+    int slot = 0;                  // next ticket counter
+
+    // status
+    DevCounters *ctr = nullptr;      // device
+    DevCounters *ctr_host = nullptr; // pinned mirror
+
+    // host-buffer staging (fmm_eval_host), allocated on first use
+    void *h_pos = nullptr, *h_mass = nullptr, *h_acc = nullptr, *h_pot = nullptr;
+
+    // KDK acceleration cache, caller's order
+    void *acc_cache = nullptr;
+    bool cache_valid = false;
+    const void *cache_pos = nullptr, *cache_vel = nullptr, *cache_mass = nullptr;
+
+    // timing and stats of the last evaluation
+    cudaEvent_t ev[kNumEvents] = {};
+    int ev_stage[kNumEvents] = {};
+    int n_ev = 0;
+    int launches = 0;
+    int retries = 0;
+    int depth = 0;
+    int64_t n_nodes = 0, n_leaves = 0, n_m2l = 0, n_p2p = 0, p2p_inter = 0, walk_pairs = 0;
+    bool have_eval = false;
+    double stage_ms[16] = {};
+    double total_ms = 0;
+
+    unsigned next_epoch();
+    int next_slot() { return slot++; }
+};
+
+// ---- launchers (one per kernel file) ----------------------------------------
+// Each returns the number of kernels it launched.
+int launch_keys(Plan &P, const void *pos, cudaStream_t s);
+int launch_sort(Plan &P, const void *pos, const void *mass, cudaStream_t s);
+int launch_tree(Plan &P, cudaStream_t s);
+int launch_upward(Plan &P, cudaStream_t s);
+int launch_walk(Plan &P, int depth, cudaStream_t s);
+int launch_lists(Plan &P, cudaStream_t s);
+int launch_m2l(Plan &P, cudaStream_t s);
+int launch_l2l(Plan &P, int depth, cudaStream_t s);
+int launch_leaf(Plan &P, void *acc, void *pot, cudaStream_t s);
+int launch_kick(Plan &P, void *vel, const void *acc, double h, cudaStream_t s);
+int launch_drift(Plan &P, void *pos, const void *vel, double dt, cudaStream_t s);
+
+inline int grid_for(const Plan &P, int per_sm = 8) { return P.num_sms * per_sm; }
+
+}  // namespace bfm

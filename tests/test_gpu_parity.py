@@ -1,0 +1,174 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: keys, sort permutation, tree, node boxes and interaction lists
+bit-exact; expansion coefficients per stage; accelerations within a per-particle
+L2 relative error (floored at 1e-3 of the median) of 1e-10 in fp64 and 1e-4 in
+fp32, potentials likewise.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from body_forces_morton_b300 import workloads as W
+from gpu_helpers import (ALL_STRUCT, TOL_ACC, accel_error, assert_structure_equal, coeff_error, gpu_eval,
+                         pot_error)
+
+pytestmark = pytest.mark.gpu
+
+COEFF_TOL = {"f64": 1e-10, "f32": 2e-4}
+
+
+def full_parity(pos, mass, p, theta, leaf, check_coeffs=True):
+    dt = "f32" if pos.dtype == np.float32 else "f64"
+    ex_names = ALL_STRUCT + (("multipole", "local_m2l", "local") if check_coeffs else ())
+    acc, pot, ex, st = gpu_eval(pos, mass, p, theta, leaf, exports=ex_names)
+    r = oracle.fmm(pos, mass, p, theta, leaf)
+    assert_structure_equal(ex, r)
+    nn = len(r.first)
+    nc = oracle.ncoef(p)
+    if check_coeffs:
+        assert coeff_error(ex["multipole"].reshape(nn, nc), r.M, p) < COEFF_TOL[dt], "P2P/M2M moments"
+        assert coeff_error(ex["local_m2l"].reshape(nn, nc), r.Lm2l, p) < COEFF_TOL[dt], "M2L locals"
+        assert coeff_error(ex["local"].reshape(nn, nc), r.L, p) < COEFF_TOL[dt], "L2L locals"
+    e = accel_error(acc.astype(np.float64), r.acc)
+    ep = pot_error(pot.astype(np.float64), r.pot)
+    assert e.max() <= TOL_ACC[dt], f"max acc error {e.max():.3e}"
+    assert ep.max() <= TOL_ACC[dt], f"max pot error {ep.max():.3e}"
+    assert st["n_nodes"] == nn and st["n_m2l"] == len(r.m2l_src) and st["n_p2p"] == len(r.p2p_src)
+    assert st["n_p2p_interactions"] == r.n_p2p_interactions
+    return e, r, st
+
+
+@pytest.mark.parametrize("cfg", [1, 2])
+def test_small_configs_full_parity(cfg):
+    w = W.WORKLOADS[cfg]
+    g = W.generate(w)
+    full_parity(g["pos"], g["mass"], w.p, w.theta, w.leaf)
+
+
+def test_plummer_reduced_f64():
+    w = W.WORKLOADS[3]
+    g = W.generate(w, n=30000)
+    full_parity(g["pos"], g["mass"], w.p, w.theta, w.leaf)
+
+
+@pytest.mark.parametrize("n", [65536, 100003])
+def test_clustered_f32(n):
+    w = W.WORKLOADS[4]
+    g = W.generate(w, n=n)
+    full_parity(g["pos"], g["mass"], w.p, w.theta, w.leaf)
+
+
+def test_kdk_config_params_f32():
+    w = W.WORKLOADS[5]
+    g = W.generate(w, n=70000)
+    full_parity(g["pos"], g["mass"], w.p, w.theta, w.leaf)
+
+
+@pytest.mark.parametrize("p", range(0, 9))
+def test_every_order_f64(p):
+    g = W.generate(W.WORKLOADS[2], n=3000)
+    full_parity(g["pos"], g["mass"], p, 0.5, 16)
+
+
+@pytest.mark.parametrize("p", [2, 5, 6])
+def test_orders_f32(p):
+    g = W.generate(W.WORKLOADS[4], n=20000)
+    full_parity(g["pos"], g["mass"], p, 0.6, 32)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 33, 4095, 4097, 10007])
+@pytest.mark.parametrize("dt", ["f64", "f32"])
+@pytest.mark.parametrize("leaf", [1, 8])
+def test_ragged_sizes(n, dt, leaf):
+    g = W.generate(W.WORKLOADS[1], n=n, dtype=dt)
+    if n == 1:
+        acc, pot, ex, st = gpu_eval(g["pos"], g["mass"], 4, 0.7, leaf)
+        assert np.all(acc == 0) and np.all(pot == 0) and st["n_nodes"] == 1
+        return
+    full_parity(g["pos"], g["mass"], 4, 0.7, leaf)
+
+
+@pytest.mark.parametrize("theta", [0.05, 0.3, 1.0])
+def test_opening_angles(theta):
+    g = W.generate(W.WORKLOADS[2], n=5000)
+    full_parity(g["pos"], g["mass"], 3, theta, 8)
+
+
+def test_coincident_particles_and_depth_limit():
+    """Coincident points: a depth-21 leaf holding more than `leaf` particles."""
+    rng = np.random.default_rng(0)
+    pos = np.vstack([np.full((100, 3), 0.5), rng.random((400, 3))])
+    mass = np.full(500, 1.0 / 500)
+    e, r, st = full_parity(pos, mass, 4, 0.7, 8)
+    assert r.depth == 21 and st["depth"] == 21
+
+
+def test_tiny_theta_equals_direct_sum():
+    g = W.generate(W.WORKLOADS[2], n=4000)
+    acc, pot, _, _ = gpu_eval(g["pos"], g["mass"], 4, 1e-6, 16)
+    acc_d, pot_d = oracle.direct_sum(g["pos"], g["mass"])
+    assert accel_error(acc, acc_d).max() < 1e-12
+    assert pot_error(pot, pot_d).max() < 1e-12
+
+
+def test_deterministic_bitwise():
+    g = W.generate(W.WORKLOADS[4], n=50000)
+    a1, p1, _, _ = gpu_eval(g["pos"], g["mass"], 4, 0.7, 64)
+    a2, p2, _, _ = gpu_eval(g["pos"], g["mass"], 4, 0.7, 64, repeat=3)
+    assert np.array_equal(a1, a2) and np.array_equal(p1, p2)
+
+
+def test_plan_reuse_and_pot_optional():
+    import torch
+
+    from body_forces_morton_b300 import native
+
+    g1 = W.generate(W.WORKLOADS[1], n=5000)
+    g2 = W.generate(W.WORKLOADS[2], n=5000)
+    with native.Plan(5000, 4, 0.7, 32, "f64") as pl:
+        a1, _, _, _ = gpu_eval(g1["pos"], g1["mass"], 4, 0.7, 32, plan=pl)
+        a2, _, _, _ = gpu_eval(g2["pos"], g2["mass"], 4, 0.7, 32, plan=pl, want_pot=False)
+        a1b, _, _, _ = gpu_eval(g1["pos"], g1["mass"], 4, 0.7, 32, plan=pl)
+    assert np.array_equal(a1, a1b)
+    r2 = oracle.fmm(g2["pos"], g2["mass"], 4, 0.7, 32)
+    assert accel_error(a2, r2.acc).max() <= 1e-10
+
+
+def test_eval_host_matches_device():
+    from body_forces_morton_b300 import native
+
+    g = W.generate(W.WORKLOADS[4], n=40000)
+    acc_d, pot_d, _, _ = gpu_eval(g["pos"], g["mass"], 4, 0.7, 64)
+    acc_h = np.empty_like(g["pos"])
+    pot_h = np.empty_like(g["mass"])
+    with native.Plan(40000, 4, 0.7, 64, "f32") as pl:
+        pl.eval_host(g["pos"], g["mass"], acc_h, pot_h)
+    assert np.array_equal(acc_h, acc_d) and np.array_equal(pot_h, pot_d)
+
+
+def test_error_paths():
+    import torch
+
+    from body_forces_morton_b300 import native
+
+    with pytest.raises(native.FmmError):
+        native.Plan(0, 4, 0.7, 32, "f64")
+    with pytest.raises(native.FmmError):
+        native.Plan(10, 9, 0.7, 32, "f64")
+    with pytest.raises(native.FmmError):
+        native.Plan(10, 4, 1.5, 32, "f64")
+    with native.Plan(100, 4, 0.7, 8, "f64") as pl:
+        pos = torch.rand(100, 3, dtype=torch.float64, device="cuda")
+        pos[17, 1] = float("nan")
+        mass = torch.full((100,), 0.01, dtype=torch.float64, device="cuda")
+        acc = torch.empty_like(pos)
+        with pytest.raises(native.FmmError) as ei:
+            pl.eval(pos, mass, acc)
+        assert ei.value.status == 5
+        with pytest.raises(native.FmmError) as ei:
+            native.fmm_eval(pl.handle, pos, None, acc)
+        assert ei.value.status == 1
+        pos[17, 1] = 0.5
+        pl.eval(pos, mass, acc)  # the plan stays usable after an error
+        assert torch.isfinite(acc).all()
