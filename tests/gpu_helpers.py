@@ -57,19 +57,32 @@ def assert_structure_equal(ex, r):
     assert np.array_equal(ex["p2p_src"], r.p2p_src), "P2P lists differ"
 
 
-def coeff_error(got, ref, p):
-    """Max over nodes and degrees of |got - ref| / max|ref| within that node and degree."""
+def _weights(r, p):
+    """|l|^|n| / n! per node and coefficient (l = the node's half-width vector)."""
     import oracle
+    from math import factorial
 
     mi = oracle.multi_indices(p)
-    deg = mi.sum(axis=1)
-    worst = 0.0
-    for d in range(p + 1):
-        cols = deg == d
-        scale = np.abs(ref[:, cols]).max(axis=1, keepdims=True)
-        scale = np.where(scale > 0, scale, 1.0)
-        worst = max(worst, float(np.max(np.abs(got[:, cols] - ref[:, cols]) / scale)))
-    return worst
+    fact = np.array([factorial(a) * factorial(b) * factorial(c) for a, b, c in mi], dtype=np.float64)
+    ln = np.linalg.norm(r.half, axis=1)
+    return ln[:, None] ** mi.sum(axis=1)[None, :] / fact[None, :]
+
+
+def moment_error(got, r, p):
+    """max |dM_n| / (M_0 |l|^|n| / n!): the moments' own bound on the node's box."""
+    scale = np.abs(r.M[:, :1]) * _weights(r, p) + 1e-300
+    return float(np.max(np.abs(got - r.M) / scale))
+
+
+def local_error(got, ref, r, p):
+    """Per node sum_k |dL_k| w_k / sum_k |L_k| w_k with w_k = |l|^|k| / k!: the
+    relative size of the polynomial difference on the node's box."""
+    w = _weights(r, p)
+    den = np.sum(np.abs(ref) * w, axis=1)
+    num = np.sum(np.abs(got - ref) * w, axis=1)
+    ok = den > 0
+    assert np.all(num[~ok] == 0)
+    return float(np.max(num[ok] / den[ok])) if ok.any() else 0.0
 
 
 def accel_error(acc, ref):

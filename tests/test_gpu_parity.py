@@ -10,12 +10,12 @@ import pytest
 
 import oracle
 from body_forces_morton_b300 import workloads as W
-from gpu_helpers import (ALL_STRUCT, TOL_ACC, accel_error, assert_structure_equal, coeff_error, gpu_eval,
-                         pot_error)
+from gpu_helpers import (ALL_STRUCT, TOL_ACC, accel_error, assert_structure_equal, gpu_eval, local_error,
+                         moment_error, pot_error)
 
 pytestmark = pytest.mark.gpu
 
-COEFF_TOL = {"f64": 1e-10, "f32": 2e-4}
+COEFF_TOL = {"f64": 1e-11, "f32": 5e-4}
 
 
 def full_parity(pos, mass, p, theta, leaf, check_coeffs=True):
@@ -27,11 +27,16 @@ def full_parity(pos, mass, p, theta, leaf, check_coeffs=True):
     nn = len(r.first)
     nc = oracle.ncoef(p)
     if check_coeffs:
-        assert coeff_error(ex["multipole"].reshape(nn, nc), r.M, p) < COEFF_TOL[dt], "P2P/M2M moments"
-        assert coeff_error(ex["local_m2l"].reshape(nn, nc), r.Lm2l, p) < COEFF_TOL[dt], "M2L locals"
-        assert coeff_error(ex["local"].reshape(nn, nc), r.L, p) < COEFF_TOL[dt], "L2L locals"
+        em = moment_error(ex["multipole"].reshape(nn, nc).astype(np.float64), r, p)
+        el2 = local_error(ex["local_m2l"].reshape(nn, nc).astype(np.float64), r.Lm2l, r, p)
+        el = local_error(ex["local"].reshape(nn, nc).astype(np.float64), r.L, r, p)
+        print(f"N={len(mass)} {dt} p={p}: moments {em:.2e} m2l {el2:.2e} local {el:.2e}")
+        assert em < COEFF_TOL[dt], f"P2M/M2M moments {em:.3e}"
+        assert el2 < COEFF_TOL[dt], f"M2L locals {el2:.3e}"
+        assert el < COEFF_TOL[dt], f"L2L locals {el:.3e}"
     e = accel_error(acc.astype(np.float64), r.acc)
     ep = pot_error(pot.astype(np.float64), r.pot)
+    print(f"  acc error max {e.max():.2e} p99 {np.percentile(e, 99):.2e}; pot max {ep.max():.2e}")
     assert e.max() <= TOL_ACC[dt], f"max acc error {e.max():.3e}"
     assert ep.max() <= TOL_ACC[dt], f"max pot error {ep.max():.3e}"
     assert st["n_nodes"] == nn and st["n_m2l"] == len(r.m2l_src) and st["n_p2p"] == len(r.p2p_src)
