@@ -78,14 +78,31 @@ __global__ __launch_bounds__(kBoxThreads) void k_bbox(const T *__restrict__ pos,
         s_last = atomicAdd(&ctr->bbox_done, 1) == (int)gridDim.x - 1;
     }
     __syncthreads();
-    if (!s_last || threadIdx.x != 0) return;
+    if (!s_last) return;
+    // last block: reduce the per-block partials with all its threads
     __threadfence();
-    T r[6];
-    for (int a = 0; a < 3; ++a) { r[a] = pos_inf<T>(); r[3 + a] = -pos_inf<T>(); }
-    for (int b = 0; b < (int)gridDim.x; ++b)
+    for (int a = 0; a < 3; ++a) { lo[a] = pos_inf<T>(); hi[a] = -pos_inf<T>(); }
+    for (int b = threadIdx.x; b < (int)gridDim.x; b += blockDim.x)
         for (int a = 0; a < 3; ++a) {
-            r[a] = tmin(r[a], ld_cg(partial + 6 * b + a));
-            r[3 + a] = tmax(r[3 + a], ld_cg(partial + 6 * b + 3 + a));
+            lo[a] = tmin(lo[a], ld_cg(partial + 6 * b + a));
+            hi[a] = tmax(hi[a], ld_cg(partial + 6 * b + 3 + a));
+        }
+    for (int o = 16; o > 0; o >>= 1)
+        for (int a = 0; a < 3; ++a) {
+            lo[a] = tmin(lo[a], __shfl_xor_sync(kFull, lo[a], o));
+            hi[a] = tmax(hi[a], __shfl_xor_sync(kFull, hi[a], o));
+        }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0)
+        for (int a = 0; a < 3; ++a) { s[w][a] = lo[a]; s[w][3 + a] = hi[a]; }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    T r[6];
+    for (int a = 0; a < 6; ++a) r[a] = s[0][a];
+    for (int k = 1; k < kBoxThreads / 32; ++k)
+        for (int a = 0; a < 3; ++a) {
+            r[a] = tmin(r[a], s[k][a]);
+            r[3 + a] = tmax(r[3 + a], s[k][3 + a]);
         }
     T side = sub_rn(r[3], r[0]);
     for (int a = 1; a < 3; ++a) {

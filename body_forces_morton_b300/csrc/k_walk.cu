@@ -37,6 +37,27 @@ __global__ void k_walk_init(int2 *f0, DevCounters *ctr)
     ctr->frontier_max = 1;
 }
 
+// Block-wide exclusive scan of one int per thread; returns the block total.
+__device__ __forceinline__ int block_excl_scan(int v, int &excl, int *s_warp)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int incl = warp_incl_scan(v);
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int base = 0, tot = 0;
+    for (int w = 0; w < WK_THREADS / 32; ++w) {
+        const int t = s_warp[w];
+        base += w < warp ? t : 0;
+        tot += t;
+    }
+    excl = base + incl - v;
+    __syncthreads();
+    return tot;
+}
+
+// One generation of the walk: every frontier pair is decided and its outputs
+// (an M2L pair, a P2P pair or child pairs) are appended; a block reserves the
+// space of a whole 256-pair tile with one atomic per output list.
 template <class T>
 __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__restrict__ fin, int2 *__restrict__ fout,
                                                           int cap_frontier, const int *__restrict__ nchild,
@@ -47,27 +68,29 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
                                                           int cap_m2l, int2 *p2p_pairs, int cap_p2p, int *m2l_cnt,
                                                           int *p2p_cnt, DevCounters *ctr)
 {
+    __shared__ int s_warp[WK_THREADS / 32];
+    __shared__ int s_base[3];
     const int nin = ctr->frontier_cnt[it % 3];
     int *cnt_out = &ctr->frontier_cnt[(it + 1) % 3];
     if (blockIdx.x == 0 && threadIdx.x == 0) ctr->frontier_cnt[(it + 2) % 3] = 0;
-    const int lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int nread = nin < cap_frontier ? nin : cap_frontier;
-    for (int base = ((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; base < nread; base += nwarps * 32) {
-        const int i = base + lane;
+    long long inter_sum = 0;
+    int visited = 0, kids_max = 0;
+    for (int base = blockIdx.x * WK_THREADS; base < nread; base += gridDim.x * WK_THREADS) {
+        const int i = base + threadIdx.x;
         const bool valid = i < nread;
         int A = 0, B = 0, kids = 0, split = -1, other = 0;
-        bool m2l = false, p2p = false;
-        long long inter = 0;
+        int m2l = 0, p2p = 0;
         if (valid) {
-            int2 pr = fin[i];
+            ++visited;
+            const int2 pr = fin[i];
             A = pr.x;
             B = pr.y;
             const int nA = nchild[A];
             if (A == B) {
                 if (nA == 0) {
-                    p2p = true;
-                    inter = (long long)count[A] * count[A];
+                    p2p = 1;
+                    inter_sum += (long long)count[A] * count[A];
                 } else {
                     kids = nA * (nA + 1) / 2;
                     split = A;
@@ -78,10 +101,10 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
                 const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
                 const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
                 if (s2 < mul_rn(th2, r2)) {
-                    m2l = true;
+                    m2l = 1;
                 } else if (nA == 0 && nB == 0) {
-                    p2p = true;
-                    inter = 2ll * count[A] * count[B];
+                    p2p = 1;
+                    inter_sum += 2ll * count[A] * count[B];
                 } else {
                     const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
                     split = splitA ? A : B;
@@ -90,81 +113,67 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
                 }
             }
         }
-        // ---- M2L pair
-        {
-            const unsigned m = __ballot_sync(kFull, m2l);
-            if (m) {
-                int b0 = 0;
-                if (lane == 0) b0 = atomicAdd(&ctr->n_m2l_pairs, __popc(m));
-                b0 = __shfl_sync(kFull, b0, 0);
-                if (m2l) {
-                    const int slot = b0 + __popc(m & lanemask_lt());
-                    if (slot < cap_m2l) {
-                        m2l_pairs[slot] = make_int2(A, B);
-                        atomicAdd(&m2l_cnt[A], 1);
-                        atomicAdd(&m2l_cnt[B], 1);
-                    } else {
-                        set_error(ctr, ERR_M2L_CAP);
+        int ex_m, ex_p, ex_k;
+        const int tot_m = block_excl_scan(m2l, ex_m, s_warp);
+        const int tot_p = block_excl_scan(p2p, ex_p, s_warp);
+        const int tot_k = block_excl_scan(kids, ex_k, s_warp);
+        if (threadIdx.x == 0) {
+            s_base[0] = tot_m ? atomicAdd(&ctr->n_m2l_pairs, tot_m) : 0;
+            s_base[1] = tot_p ? atomicAdd(&ctr->n_p2p_pairs, tot_p) : 0;
+            s_base[2] = tot_k ? atomicAdd(cnt_out, tot_k) : 0;
+            kids_max = max(kids_max, s_base[2] + tot_k);
+        }
+        __syncthreads();
+        if (m2l) {
+            const int slot = s_base[0] + ex_m;
+            if (slot < cap_m2l) {
+                m2l_pairs[slot] = make_int2(A, B);
+                atomicAdd(&m2l_cnt[A], 1);
+                atomicAdd(&m2l_cnt[B], 1);
+            } else {
+                set_error(ctr, ERR_M2L_CAP);
+            }
+        }
+        if (p2p) {
+            const int slot = s_base[1] + ex_p;
+            if (slot < cap_p2p) {
+                p2p_pairs[slot] = make_int2(A, B);
+                atomicAdd(&p2p_cnt[A], 1);
+                if (A != B) atomicAdd(&p2p_cnt[B], 1);
+            } else {
+                set_error(ctr, ERR_P2P_CAP);
+            }
+        }
+        if (kids) {
+            int o = s_base[2] + ex_k;
+            const int c0 = child0[split];
+            if (A == B) {
+                const int nA = nchild[A];
+                for (int x = 0; x < nA; ++x)
+                    for (int y = x; y < nA; ++y, ++o) {
+                        if (o < cap_frontier) fout[o] = make_int2(c0 + x, c0 + y);
+                        else set_error(ctr, ERR_FRONTIER);
                     }
+            } else {
+                for (int x = 0; x < kids; ++x, ++o) {
+                    const int C = c0 + x;
+                    if (o < cap_frontier) fout[o] = C < other ? make_int2(C, other) : make_int2(other, C);
+                    else set_error(ctr, ERR_FRONTIER);
                 }
             }
         }
-        // ---- P2P pair
-        {
-            const unsigned m = __ballot_sync(kFull, p2p);
-            if (m) {
-                int b0 = 0;
-                if (lane == 0) b0 = atomicAdd(&ctr->n_p2p_pairs, __popc(m));
-                b0 = __shfl_sync(kFull, b0, 0);
-                if (p2p) {
-                    const int slot = b0 + __popc(m & lanemask_lt());
-                    if (slot < cap_p2p) {
-                        p2p_pairs[slot] = make_int2(A, B);
-                        atomicAdd(&p2p_cnt[A], 1);
-                        if (A != B) atomicAdd(&p2p_cnt[B], 1);
-                    } else {
-                        set_error(ctr, ERR_P2P_CAP);
-                    }
-                }
-                long long s = inter;
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-                if (lane == 0) atomicAdd((unsigned long long *)&ctr->p2p_interactions, (unsigned long long)s);
-            }
-        }
-        // ---- next frontier
-        {
-            const int incl = warp_incl_scan(kids);
-            const int tot = __shfl_sync(kFull, incl, 31);
-            const unsigned vm = __ballot_sync(kFull, valid);
-            if (lane == 0) atomicAdd((unsigned long long *)&ctr->walk_pairs, (unsigned long long)__popc(vm));
-            if (tot) {
-                int b0 = 0;
-                if (lane == 0) {
-                    b0 = atomicAdd(cnt_out, tot);
-                    atomicMax(&ctr->frontier_max, b0 + tot);
-                }
-                b0 = __shfl_sync(kFull, b0, 0);
-                int o = b0 + incl - kids;
-                if (kids) {
-                    const int c0 = child0[split];
-                    if (A == B) {
-                        const int nA = nchild[A];
-                        for (int x = 0; x < nA; ++x)
-                            for (int y = x; y < nA; ++y, ++o) {
-                                if (o < cap_frontier) fout[o] = make_int2(c0 + x, c0 + y);
-                                else set_error(ctr, ERR_FRONTIER);
-                            }
-                    } else {
-                        for (int x = 0; x < kids; ++x, ++o) {
-                            const int C = c0 + x;
-                            if (o < cap_frontier) fout[o] = C < other ? make_int2(C, other) : make_int2(other, C);
-                            else set_error(ctr, ERR_FRONTIER);
-                        }
-                    }
-                }
-            }
-        }
+        __syncthreads();
     }
+    // per-block statistics, one atomic each
+    for (int o = 16; o > 0; o >>= 1) {
+        inter_sum += __shfl_xor_sync(kFull, inter_sum, o);
+        visited += __shfl_xor_sync(kFull, visited, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (inter_sum) atomicAdd((unsigned long long *)&ctr->p2p_interactions, (unsigned long long)inter_sum);
+        if (visited) atomicAdd((unsigned long long *)&ctr->walk_pairs, (unsigned long long)visited);
+    }
+    if (threadIdx.x == 0 && kids_max) atomicMax(&ctr->frontier_max, kids_max);
 }
 
 // Exclusive scan of the per-receiver counts into CSR offsets (both lists at once).
@@ -273,16 +282,18 @@ __global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restr
         while (S < len) S <<= 1;
         for (int i = lane; i < S; i += 32) v[i] = i < len ? src[i] : 0x7fffffff;
         __syncwarp();
-        for (int k = 2; k <= S; k <<= 1) {
+        for (int lk = 1; (1 << lk) <= S; ++lk) {
+            const int k = 1 << lk;
             for (int i = lane; i < S / 2; i += 32) {
-                const int h = k >> 1, blk = i / h, pos = i % h;
+                const int blk = i >> (lk - 1), pos = i & ((k >> 1) - 1);
                 cmpswap(v, blk * k + pos, blk * k + k - 1 - pos);
             }
             __syncwarp();
-            for (int j = k >> 2; j >= 1; j >>= 1) {
+            for (int lj = lk - 2; lj >= 0; --lj) {
+                const int j = 1 << lj;
                 for (int i = lane; i < S / 2; i += 32) {
-                    const int blk = i / j, pos = i % j;
-                    cmpswap(v, blk * 2 * j + pos, blk * 2 * j + pos + j);
+                    const int blk = i >> lj, pos = i & (j - 1);
+                    cmpswap(v, (blk << (lj + 1)) + pos, (blk << (lj + 1)) + pos + j);
                 }
                 __syncwarp();
             }
@@ -308,17 +319,19 @@ __global__ __launch_bounds__(1024) void k_segsort_long(const int *__restrict__ m
         int *v = (isp ? p2p_src : m2l_src) + beg;
         int S = 2;
         while (S < len) S <<= 1;
-        for (int k = 2; k <= S; k <<= 1) {
+        for (int lk = 1; (1 << lk) <= S; ++lk) {
+            const int k = 1 << lk;
             for (int i = threadIdx.x; i < S / 2; i += blockDim.x) {
-                const int h = k >> 1, blk = i / h, pos = i % h;
+                const int blk = i >> (lk - 1), pos = i & ((k >> 1) - 1);
                 const int x = blk * k + pos, y = blk * k + k - 1 - pos;
                 if (y < len) cmpswap(v, x, y);
             }
             __syncthreads();
-            for (int j = k >> 2; j >= 1; j >>= 1) {
+            for (int lj = lk - 2; lj >= 0; --lj) {
+                const int j = 1 << lj;
                 for (int i = threadIdx.x; i < S / 2; i += blockDim.x) {
-                    const int blk = i / j, pos = i % j;
-                    const int x = blk * 2 * j + pos, y = x + j;
+                    const int blk = i >> lj, pos = i & (j - 1);
+                    const int x = (blk << (lj + 1)) + pos, y = x + j;
                     if (y < len) cmpswap(v, x, y);
                 }
                 __syncthreads();
