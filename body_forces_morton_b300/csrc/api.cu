@@ -81,12 +81,14 @@ void free_nodes(Plan &P)
 {
     int **ints[] = {&P.node_first, &P.node_count, &P.node_child0, &P.node_nchild, &P.node_parent,
                     &P.node_level, &P.node_done,  &P.m2l_cnt,     &P.p2p_cnt,     &P.m2l_off,
-                    &P.p2p_off,    &P.long_seg};
+                    &P.p2p_off,    &P.long_seg,    &P.order};
     for (int **q : ints) { dfree(*q); *q = nullptr; }
     void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L};
     for (void **q : vs) { dfree(*q); *q = nullptr; }
     dfree(P.flags);
     P.flags = nullptr;
+    dfree(P.order_key);
+    P.order_key = nullptr;
 }
 
 void free_lists(Plan &P)
@@ -115,6 +117,8 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
     CUDA_TRY(dalloc(P.m2l_off, c + 1));
     CUDA_TRY(dalloc(P.p2p_off, c + 1));
     CUDA_TRY(dalloc(P.long_seg, 2 * c));
+    CUDA_TRY(dalloc(P.order, 2 * c));
+    CUDA_TRY(dalloc(P.order_key, 2 * c));
     CUDA_TRY(cudaMalloc(&P.node_lo, 3 * c * e));
     CUDA_TRY(cudaMalloc(&P.node_hi, 3 * c * e));
     CUDA_TRY(cudaMalloc(&P.node_c, 4 * c * e));
@@ -152,7 +156,7 @@ void destroy_plan(Plan &P)
     free_nodes(P);
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
-    dfree(P.xyzm); dfree(P.div); dfree(P.scratch); dfree(P.ctr);
+    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.scratch); dfree(P.ctr);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     if (P.ctr_host) cudaFreeHost(P.ctr_host);
     for (int i = 0; i < kNumEvents; ++i)
@@ -317,7 +321,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     const size_t nn = (size_t)n, e = (size_t)P.esize;
     if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
         !ok(dalloc(P.idx[0], nn), "perm") || !ok(dalloc(P.idx[1], nn), "perm") ||
-        !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(dalloc(P.div, nn), "divergence") ||
+        !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);

@@ -43,6 +43,9 @@ struct DevCounters {
     long long p2p_interactions;
     int n_long;                    // list segments too long for the warp sort
     int pad;
+    int order_cnt[2][64];          // work buckets (0: P2P receivers, 1: M2L receivers)
+    int order_cur[2][64];
+    int work_ctr[4];               // dynamic work counters
 };
 
 // ---- vector types ---------------------------------------------------------
@@ -171,6 +174,43 @@ __device__ __forceinline__ int warp_incl_scan(int v)
         if (lane >= o) v += t;
     }
     return v;
+}
+
+// Sum v over the 32 lanes and write the NC sums to dst: three halving steps
+// (offsets 16, 8, 4) leave each lane NR/8 partial sums of its own coefficient
+// block, two butterfly steps (2, 1) finish them. Fixed order, so reproducible.
+template <class T, int NR, int NC>
+__device__ __forceinline__ void reduce_store(T (&v)[NR], int lane, T *__restrict__ dst)
+{
+    constexpr int H1 = NR / 2, H2 = NR / 4, H3 = NR / 8;
+    T a[H1], b[H2], c[H3];
+    const bool u4 = lane & 16, u3 = lane & 8, u2 = lane & 4;
+#pragma unroll
+    for (int i = 0; i < H1; ++i) {
+        const T send = u4 ? v[i] : v[i + H1], keep = u4 ? v[i + H1] : v[i];
+        a[i] = keep + __shfl_xor_sync(kFull, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < H2; ++i) {
+        const T send = u3 ? a[i] : a[i + H2], keep = u3 ? a[i + H2] : a[i];
+        b[i] = keep + __shfl_xor_sync(kFull, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < H3; ++i) {
+        const T send = u2 ? b[i] : b[i + H3], keep = u2 ? b[i + H3] : b[i];
+        c[i] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+#pragma unroll
+    for (int i = 0; i < H3; ++i) {
+        c[i] += __shfl_xor_sync(kFull, c[i], 2);
+        c[i] += __shfl_xor_sync(kFull, c[i], 1);
+    }
+    if ((lane & 3) == 0) {
+        const int base = (u4 ? H1 : 0) + (u3 ? H2 : 0) + (u2 ? H3 : 0);
+#pragma unroll
+        for (int i = 0; i < H3; ++i)
+            if (base + i < NC) dst[base + i] = c[i];
+    }
 }
 
 template <class T> __device__ __forceinline__ T pos_inf();

@@ -7,11 +7,12 @@
 // (direct gravity eq.: Phi_i += -G m_j / r, a_i += G m_j (x_j - x_i) / r^3,
 // skipping zero separations, i.e. the particle itself).
 //
-// Leaf kernel: one warp per receiving leaf. The particles of its source leaves
-// are staged through shared memory (32 list entries and up to a chunk of
-// particles at a time) and read back as warp-wide broadcasts; the lane mapping
-// keeps all 32 lanes busy for small leaves by splitting the sources. Results
-// are written straight to the caller's particle order.
+// Leaves: a small L2P kernel evaluates the local expansions at the particles;
+// the P2P kernel (one warp per receiving leaf) stages the particles of the
+// source leaves through shared memory (32 list entries and up to a chunk of
+// particles at a time), reads them back as broadcasts, keeps all lanes busy for
+// small leaves by splitting the sources, adds the far field and writes straight
+// to the caller's particle order.
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -46,13 +47,17 @@ __global__ __launch_bounds__(256) void k_l2l(int level, const DevCounters *__res
     }
 }
 
-template <class T>
+// One source particle s acting on a receiver at (x, y, z). The self leaf may
+// hold the receiver itself (zero separation), which MASKED skips; between two
+// different leaves the separation is never zero (equal positions share a key
+// and so a leaf), so the main loop runs unmasked.
+template <class T, bool MASKED>
 __device__ __forceinline__ void p2p_one(const vec4<T> &s, T x, T y, T z, T &phi, T &ax, T &ay, T &az)
 {
     const T dx = s.x - x, dy = s.y - y, dz = s.z - z;
     const T r2 = dx * dx + dy * dy + dz * dz;
     T rinv = rsqrt_t(r2);
-    rinv = r2 > T(0) ? rinv : T(0);  // zero separation: the particle itself (or an exact duplicate)
+    if (MASKED) rinv = r2 > T(0) ? rinv : T(0);
     const T mr = s.w * rinv;
     const T mr3 = mr * rinv * rinv;
     ax += mr3 * dx;
@@ -61,14 +66,37 @@ __device__ __forceinline__ void p2p_one(const vec4<T> &s, T x, T y, T z, T &phi,
     phi -= mr;
 }
 
-constexpr int LF_WARPS = 4;                            // warps per block of the leaf kernel
+// L2P: the complete local expansion of every leaf at its particles, into `far`
+// (sorted order, (phi, ax, ay, az)); the P2P kernel adds the near field.
+template <class T, int P>
+__global__ __launch_bounds__(256) void k_l2p(int n_nodes, const int *__restrict__ first, const int *__restrict__ count,
+                                             const int *__restrict__ nchild, const vec4<T> *__restrict__ xyzm,
+                                             const vec4<T> *__restrict__ nc, const T *__restrict__ L, int ncp,
+                                             vec4<T> *__restrict__ far)
+{
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
+        if (nchild[a] != 0) continue;
+        const int f = first[a], c = count[a];
+        const vec4<T> ca = nc[a];
+        const T *La = L + (size_t)a * ncp;
+        for (int i = f + lane; i < f + c; i += 32) {
+            const vec4<T> q = xyzm[i];
+            T phi = T(0), ax = T(0), ay = T(0), az = T(0);
+            Exp<P>::template l2p<T>(La, q.x - ca.x, q.y - ca.y, q.z - ca.z, phi, ax, ay, az);
+            far[i] = make4<T>(phi, ax, ay, az);
+        }
+    }
+}
+
+constexpr int LF_WARPS = 4;                            // warps per block of the P2P kernel
 template <class T> struct LeafChunk { static constexpr int value = 256; };   // staged source particles per warp
 template <> struct LeafChunk<double> { static constexpr int value = 128; };
 
-// Stage up to CH particles of the concatenated source leaves [g0, g0 + CH) of
-// the current group of (at most 32) list entries into shared memory.
-// Lane i holds the group's i-th leaf: first particle fb, count cb, exclusive
-// prefix ex of the counts.
+// Stage particles [g0, g0 + CH) of the concatenation of the current group's
+// source leaves into shared memory. Lane i holds the group's i-th leaf: first
+// particle fb and exclusive prefix ex of the counts (ascending over the lanes).
 template <class T, int CH>
 __device__ __forceinline__ int stage_sources(vec4<T> *buf, const vec4<T> *__restrict__ xyzm, int fb, int ex,
                                              int tot, int g0, int lane)
@@ -77,8 +105,7 @@ __device__ __forceinline__ int stage_sources(vec4<T> *buf, const vec4<T> *__rest
     for (int k0 = 0; k0 < n_here; k0 += 32) {  // warp-uniform: every lane takes part in the shuffles
         const int k = k0 + lane;
         const int g = g0 + k;
-        // the leaf holding particle g of the group: last lane with ex <= g (ex ascends over the lanes)
-        int lo = 0;
+        int lo = 0;  // last lane whose leaf starts at or before g
 #pragma unroll
         for (int step = 16; step > 0; step >>= 1) {
             const int exm = __shfl_sync(kFull, ex, lo + step);
@@ -91,133 +118,159 @@ __device__ __forceinline__ int stage_sources(vec4<T> *buf, const vec4<T> *__rest
     return n_here;
 }
 
-// L2P + P2P for one receiver leaf per warp.
-//  count <= 32: lane = (r, q), r < 2^k >= count the receiver, q one of 32 / 2^k
-//               source strides; the strides are summed by a fixed butterfly.
-//  count > 32:  each lane takes receivers lane and lane + 32 of a 64-particle
-//               round, so every staged source feeds two interactions.
-template <class T, int P>
-__global__ __launch_bounds__(LF_WARPS * 32) void k_leaf(int n_nodes, const int *__restrict__ first,
-                                                        const int *__restrict__ count,
-                                                        const int *__restrict__ nchild,
-                                                        const vec4<T> *__restrict__ xyzm,
-                                                        const uint32_t *__restrict__ perm,
-                                                        const vec4<T> *__restrict__ nc, const T *__restrict__ L,
-                                                        int ncp, const int *__restrict__ off,
-                                                        const int *__restrict__ src, T *__restrict__ acc,
-                                                        T *__restrict__ pot)
+// Interactions of the staged sources buf[q], buf[q+S], ... with K receivers.
+template <class T, bool MASKED, int K>
+__device__ __forceinline__ void p2p_span(const vec4<T> *buf, int n_here, int q, int S, const vec4<T> (&p)[K],
+                                         T (&acc)[K][4])
+{
+    int j = q;
+    for (; j + S < n_here; j += 2 * S) {
+        const vec4<T> s0 = buf[j], s1 = buf[j + S];
+#pragma unroll
+        for (int k = 0; k < K; ++k) p2p_one<T, MASKED>(s0, p[k].x, p[k].y, p[k].z, acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+#pragma unroll
+        for (int k = 0; k < K; ++k) p2p_one<T, MASKED>(s1, p[k].x, p[k].y, p[k].z, acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+    }
+    if (j < n_here) {
+        const vec4<T> s0 = buf[j];
+#pragma unroll
+        for (int k = 0; k < K; ++k) p2p_one<T, MASKED>(s0, p[k].x, p[k].y, p[k].z, acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+    }
+}
+
+// One round of up to 32 K receivers [r0, r0 + cr) of leaf a. Lane = q R + rp
+// (rp < R = ceil(cr / K), q < S = 32 / R) holds receivers rp + k R, k < K, and
+// walks the staged sources from offset q with stride S. Lanes at or beyond
+// R S only stage. The S partial sums of a receiver are added in order of q
+// through shared memory, so the result is reproducible.
+template <class T, int K>
+__device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, int beg, int end,
+                                          const int *__restrict__ first, const int *__restrict__ count,
+                                          const vec4<T> *__restrict__ xyzm, const uint32_t *__restrict__ perm,
+                                          const vec4<T> *__restrict__ far, const int *__restrict__ src,
+                                          T *__restrict__ acc_out, T *__restrict__ pot_out, vec4<T> *buf,
+                                          T (*red)[4], int lane)
+{
+    constexpr int CH = LeafChunk<T>::value;
+    const int R = (cr + K - 1) / K, S = 32 / R;
+    const int rp = lane % R, q = lane / R;
+    const bool worker = q < S;
+    vec4<T> p[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int rr = rp + k * R;
+        p[k] = xyzm[f + r0 + (rr < cr ? rr : 0)];
+    }
+    T acc[K][4];
+#pragma unroll
+    for (int k = 0; k < K; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = T(0);
+    const int qq = worker ? q : (1 << 30);  // idle lanes start past every chunk
+    // the leaf's own particles (zero separations possible)
+    for (int g0 = 0; g0 < c; g0 += CH) {
+        const int n_here = min(CH, c - g0);
+        __syncwarp();
+        for (int k = lane; k < n_here; k += 32) buf[k] = xyzm[f + g0 + k];
+        __syncwarp();
+        p2p_span<T, true, K>(buf, n_here, qq, S, p, acc);
+    }
+    // every other source leaf, 32 list entries at a time
+    for (int lb = beg; lb < end; lb += 32) {
+        const int e = lb + lane;
+        int fb = 0, cb = 0;
+        if (e < end) {
+            const int b = src[e];
+            if (b != a) {
+                fb = first[b];
+                cb = count[b];
+            }
+        }
+        const int incl = warp_incl_scan(cb);
+        const int tot = __shfl_sync(kFull, incl, 31);
+        const int ex = incl - cb;
+        for (int g0 = 0; g0 < tot; g0 += CH) {
+            __syncwarp();
+            const int n_here = stage_sources<T, CH>(buf, xyzm, fb, ex, tot, g0, lane);
+            __syncwarp();
+            p2p_span<T, false, K>(buf, n_here, qq, S, p, acc);
+        }
+    }
+    // sum the S strides of each receiver in order of q
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        __syncwarp();
+        red[lane][0] = acc[k][0];
+        red[lane][1] = acc[k][1];
+        red[lane][2] = acc[k][2];
+        red[lane][3] = acc[k][3];
+        __syncwarp();
+        const int rr = rp + k * R;
+        if (q == 0 && rr < cr) {
+            T t[4] = {red[rp][0], red[rp][1], red[rp][2], red[rp][3]};
+            for (int qs = 1; qs < S; ++qs)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) t[v] += red[qs * R + rp][v];
+            const int i = f + r0 + rr;
+            const vec4<T> fa = far[i];
+            const uint32_t o = perm[i];
+            acc_out[3 * (size_t)o] = fa.y + t[1];
+            acc_out[3 * (size_t)o + 1] = fa.z + t[2];
+            acc_out[3 * (size_t)o + 2] = fa.w + t[3];
+            if (pot_out) pot_out[o] = fa.x + t[0];
+        }
+    }
+}
+
+// P2P for one receiving leaf per warp (leaves taken from a shared counter in
+// decreasing order of work), plus the far field from `far`, scattered to the
+// caller's order. The receivers per lane K (1, 2 or 4) are
+// chosen per leaf to keep the most lanes doing useful interactions; the
+// leaf's own particles are a separate masked pass, the rest runs unmasked.
+template <class T>
+__global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__restrict__ cst, const int *__restrict__ order,
+                                                       DevCounters *ctr, const int *__restrict__ first,
+                                                       const int *__restrict__ count,
+                                                       const int *__restrict__ nchild,
+                                                       const vec4<T> *__restrict__ xyzm,
+                                                       const uint32_t *__restrict__ perm,
+                                                       const vec4<T> *__restrict__ far, const int *__restrict__ off,
+                                                       const int *__restrict__ src, T *__restrict__ acc_out,
+                                                       T *__restrict__ pot_out)
 {
     constexpr int CH = LeafChunk<T>::value;
     __shared__ vec4<T> s_src[LF_WARPS][CH];
+    __shared__ T s_red[LF_WARPS][32][4];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    vec4<T> *buf = s_src[w];
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
-        if (nchild[a] != 0) continue;
+    int n_work = 0;
+    for (int b = 1; b < 64; ++b) n_work += cst->order_cnt[0][b];
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[0], 1);
+        t = __shfl_sync(kFull, t, 0);
+        if (t >= n_work) break;
+        const int a = order[t];
         const int f = first[a], c = count[a];
-        const vec4<T> ca = nc[a];
         const int beg = off[a], end = off[a + 1];
-        const T *La = L + (size_t)a * ncp;
-        if (c <= 32) {
-            int lg = 0;
-            while ((1 << lg) < c) ++lg;
-            const int r = lane & ((1 << lg) - 1), q = lane >> lg, S = 32 >> lg;
-            const bool active = r < c;
-            const vec4<T> pi = xyzm[f + (active ? r : 0)];
-            T phi = T(0), ax = T(0), ay = T(0), az = T(0);
-            for (int lb = beg; lb < end; lb += 32) {
-                const int e = lb + lane;
-                int fb = 0, cb = 0;
-                if (e < end) {
-                    const int b = src[e];
-                    fb = first[b];
-                    cb = count[b];
-                }
-                const int incl = warp_incl_scan(cb);
-                const int tot = __shfl_sync(kFull, incl, 31);
-                const int ex = incl - cb;
-                for (int g0 = 0; g0 < tot; g0 += CH) {
-                    __syncwarp();
-                    const int n_here = stage_sources<T, CH>(buf, xyzm, fb, ex, tot, g0, lane);
-                    __syncwarp();
-                    int j = q;
-                    for (; j + 3 * S < n_here; j += 4 * S) {
-                        p2p_one<T>(buf[j], pi.x, pi.y, pi.z, phi, ax, ay, az);
-                        p2p_one<T>(buf[j + S], pi.x, pi.y, pi.z, phi, ax, ay, az);
-                        p2p_one<T>(buf[j + 2 * S], pi.x, pi.y, pi.z, phi, ax, ay, az);
-                        p2p_one<T>(buf[j + 3 * S], pi.x, pi.y, pi.z, phi, ax, ay, az);
-                    }
-                    for (; j < n_here; j += S) p2p_one<T>(buf[j], pi.x, pi.y, pi.z, phi, ax, ay, az);
-                }
+        for (int r0 = 0; r0 < c; r0 += 128) {
+            const int cr = min(128, c - r0);
+            // useful fraction of the lane-interactions with K receivers per lane is cr S / (32 K),
+            // S = 32 / ceil(cr / K); ties go to the larger K (fewer shared loads per interaction)
+            int best = 4, best_num = -1;
+#pragma unroll
+            for (int K = 1; K <= 4; K <<= 1) {
+                const int R = (cr + K - 1) / K;
+                if (R > 32) continue;
+                const int num = cr * (32 / R) * (4 / K);
+                if (num >= best_num) { best_num = num; best = K; }
             }
-            // sum the source strides: lanes with the same r, fixed order
-            for (int o = 1 << lg; o < 32; o <<= 1) {
-                phi += __shfl_xor_sync(kFull, phi, o);
-                ax += __shfl_xor_sync(kFull, ax, o);
-                ay += __shfl_xor_sync(kFull, ay, o);
-                az += __shfl_xor_sync(kFull, az, o);
-            }
-            if (active && q == 0) {
-                Exp<P>::template l2p<T>(La, pi.x - ca.x, pi.y - ca.y, pi.z - ca.z, phi, ax, ay, az);
-                const uint32_t o = perm[f + r];
-                acc[3 * (size_t)o] = ax;
-                acc[3 * (size_t)o + 1] = ay;
-                acc[3 * (size_t)o + 2] = az;
-                if (pot) pot[o] = phi;
-            }
-        } else {
-            for (int r0 = 0; r0 < c; r0 += 64) {
-                const bool act0 = r0 + lane < c, act1 = r0 + 32 + lane < c;
-                const vec4<T> p0 = xyzm[f + r0 + (act0 ? lane : 0)];
-                const vec4<T> p1 = xyzm[f + r0 + (act1 ? 32 + lane : 0)];
-                T phi0 = T(0), ax0 = T(0), ay0 = T(0), az0 = T(0);
-                T phi1 = T(0), ax1 = T(0), ay1 = T(0), az1 = T(0);
-                for (int lb = beg; lb < end; lb += 32) {
-                    const int e = lb + lane;
-                    int fb = 0, cb = 0;
-                    if (e < end) {
-                        const int b = src[e];
-                        fb = first[b];
-                        cb = count[b];
-                    }
-                    const int incl = warp_incl_scan(cb);
-                    const int tot = __shfl_sync(kFull, incl, 31);
-                    const int ex = incl - cb;
-                    for (int g0 = 0; g0 < tot; g0 += CH) {
-                        __syncwarp();
-                        const int n_here = stage_sources<T, CH>(buf, xyzm, fb, ex, tot, g0, lane);
-                        __syncwarp();
-                        int j = 0;
-                        for (; j + 1 < n_here; j += 2) {
-                            const vec4<T> s0 = buf[j], s1 = buf[j + 1];
-                            p2p_one<T>(s0, p0.x, p0.y, p0.z, phi0, ax0, ay0, az0);
-                            p2p_one<T>(s0, p1.x, p1.y, p1.z, phi1, ax1, ay1, az1);
-                            p2p_one<T>(s1, p0.x, p0.y, p0.z, phi0, ax0, ay0, az0);
-                            p2p_one<T>(s1, p1.x, p1.y, p1.z, phi1, ax1, ay1, az1);
-                        }
-                        if (j < n_here) {
-                            p2p_one<T>(buf[j], p0.x, p0.y, p0.z, phi0, ax0, ay0, az0);
-                            p2p_one<T>(buf[j], p1.x, p1.y, p1.z, phi1, ax1, ay1, az1);
-                        }
-                    }
-                }
-                if (act0) {
-                    Exp<P>::template l2p<T>(La, p0.x - ca.x, p0.y - ca.y, p0.z - ca.z, phi0, ax0, ay0, az0);
-                    const uint32_t o = perm[f + r0 + lane];
-                    acc[3 * (size_t)o] = ax0;
-                    acc[3 * (size_t)o + 1] = ay0;
-                    acc[3 * (size_t)o + 2] = az0;
-                    if (pot) pot[o] = phi0;
-                }
-                if (act1) {
-                    Exp<P>::template l2p<T>(La, p1.x - ca.x, p1.y - ca.y, p1.z - ca.z, phi1, ax1, ay1, az1);
-                    const uint32_t o = perm[f + r0 + 32 + lane];
-                    acc[3 * (size_t)o] = ax1;
-                    acc[3 * (size_t)o + 1] = ay1;
-                    acc[3 * (size_t)o + 2] = az1;
-                    if (pot) pot[o] = phi1;
-                }
-            }
+            if (best == 1)
+                p2p_round<T, 1>(a, f, c, r0, cr, beg, end, first, count, xyzm, perm, far, src, acc_out, pot_out,
+                                s_src[w], s_red[w], lane);
+            else if (best == 2)
+                p2p_round<T, 2>(a, f, c, r0, cr, beg, end, first, count, xyzm, perm, far, src, acc_out, pot_out,
+                                s_src[w], s_red[w], lane);
+            else
+                p2p_round<T, 4>(a, f, c, r0, cr, beg, end, first, count, xyzm, perm, far, src, acc_out, pot_out,
+                                s_src[w], s_red[w], lane);
         }
     }
 }
@@ -234,10 +287,14 @@ int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 template <class T, int P>
 int launch_leaf_tp(Plan &P_, void *acc, void *pot, cudaStream_t s)
 {
-    k_leaf<T, P><<<P_.num_sms * 16, LF_WARPS * 32, 0, s>>>((int)P_.n_nodes, P_.node_first, P_.node_count, P_.node_nchild,
-                                                (const vec4<T> *)P_.xyzm, P_.idx[0], (const vec4<T> *)P_.node_c,
-                                                (const T *)P_.L, P_.ncp, P_.p2p_off, P_.p2p_src, (T *)acc, (T *)pot);
-    return 1;
+    k_l2p<T, P><<<P_.num_sms * 8, 256, 0, s>>>((int)P_.n_nodes, P_.node_first, P_.node_count, P_.node_nchild,
+                                               (const vec4<T> *)P_.xyzm, (const vec4<T> *)P_.node_c,
+                                               (const T *)P_.L, P_.ncp, (vec4<T> *)P_.far);
+    k_p2p<T><<<P_.num_sms * 16, LF_WARPS * 32, 0, s>>>(P_.ctr, P_.order, P_.ctr, P_.node_first, P_.node_count,
+                                                       P_.node_nchild, (const vec4<T> *)P_.xyzm, P_.idx[0],
+                                                       (const vec4<T> *)P_.far, P_.p2p_off, P_.p2p_src, (T *)acc,
+                                                       (T *)pot);
+    return 2;
 }
 
 #define BFM_DISPATCH_P(fn, T, ...)                        \

@@ -8,9 +8,12 @@
 // the source particles; the derivative tensor is built on chip for every pair
 // (no per-pair operator data in memory).
 //
-// One warp per receiver; lane j takes the receiver's sources j, j+32, ... in
+// One warp per receiver, receivers taken from a shared counter in decreasing
+// order of list length; lane j takes the receiver's sources j, j+32, ... in
 // list order (ascending source index) and keeps a private partial L in
-// registers; a fixed butterfly sums the lanes, so the result is reproducible.
+// registers. The multipoles of each round of 32 sources are staged through
+// shared memory with coalesced 16-byte loads; a fixed reduction sums the
+// lanes, so the result is reproducible.
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -18,46 +21,82 @@ namespace bfm {
 
 namespace {
 
+constexpr int M2L_WARPS = 4;
+
+template <class T> struct Vec16;
+template <> struct Vec16<float> { using type = float4; static constexpr int n = 4; };
+template <> struct Vec16<double> { using type = double2; static constexpr int n = 2; };
+
+template <class T, int P> struct M2LShape {
+    static constexpr int NC = Exp<P>::NC;
+    static constexpr int NCP = (NC + 3) / 4 * 4;      // row stride of M in global memory
+    static constexpr int STR = NCP + 1;               // odd row stride in shared memory
+    static constexpr int V = Vec16<T>::n;             // elements per 16-byte load
+    static constexpr int NV = NCP / V;
+    static constexpr int NR = (NC + 7) / 8 * 8;       // accumulators, padded for the halving reduction
+    static constexpr size_t smem = sizeof(T) * M2L_WARPS * 32 * STR;
+};
+
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_m2l(int n_nodes, const int *__restrict__ off, const int *__restrict__ src,
-                                             const vec4<T> *__restrict__ nc, const T *__restrict__ M, int ncp,
-                                             T *__restrict__ Lout)
+__global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(int n_nodes, const int *__restrict__ order,
+                                                        const int *__restrict__ off,
+                                                        const int *__restrict__ src, const vec4<T> *__restrict__ nc,
+                                                        const T *__restrict__ M, T *__restrict__ Lout,
+                                                        DevCounters *ctr)
 {
-    constexpr int NC = Exp<P>::NC;
-    const int lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
+    using S = M2LShape<T, P>;
+    using V16 = typename Vec16<T>::type;
+    extern __shared__ __align__(16) unsigned char m2l_smem[];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    T *rows = reinterpret_cast<T *>(m2l_smem) + (size_t)w * 32 * S::STR;
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[1], 1);
+        t = __shfl_sync(kFull, t, 0);
+        if (t >= n_nodes) break;
+        const int a = order[t];
         const int beg = off[a], end = off[a + 1];
         const vec4<T> ca = nc[a];
-        T L[NC];
+        T L[S::NR];
 #pragma unroll
-        for (int k = 0; k < NC; ++k) L[k] = T(0);
-        for (int q = beg + lane; q < end; q += 32) {
-            const int b = src[q];
-            const vec4<T> cb = nc[b];
-            T mb[NC];
-            const T *row = M + (size_t)b * ncp;
+        for (int k = 0; k < S::NR; ++k) L[k] = T(0);
+        for (int q0 = beg; q0 < end; q0 += 32) {
+            const int q = q0 + lane;
+            const bool valid = q < end;
+            const int b = valid ? src[q] : 0;
+            const int nsrc = min(32, end - q0);
+            __syncwarp();
+            // stage the multipole rows of this round's sources (16-byte loads, one row per source)
+            for (int t0 = 0; t0 < nsrc * S::NV; t0 += 32) {
+                const int t = t0 + lane;
+                const int row = t / S::NV, col = t - row * S::NV;
+                const int bb = __shfl_sync(kFull, b, row & 31);
+                if (t < nsrc * S::NV) {
+                    const V16 x = __ldg(reinterpret_cast<const V16 *>(M + (size_t)bb * S::NCP) + col);
+                    const T *xs = reinterpret_cast<const T *>(&x);
 #pragma unroll
-            for (int k = 0; k < NC; ++k) mb[k] = __ldg(row + k);
-            Exp<P>::template m2l<T>(mb, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
+                    for (int i = 0; i < S::V; ++i) rows[row * S::STR + col * S::V + i] = xs[i];
+                }
+            }
+            __syncwarp();
+            if (valid) {
+                const vec4<T> cb = nc[b];
+                Exp<P>::template m2l<T>(rows + lane * S::STR, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
+            }
         }
-        if (end - beg > 0) {
-#pragma unroll
-            for (int k = 0; k < NC; ++k) L[k] = warp_sum_xor(L[k]);
-        }
-        if (lane == 0) {
-            T *dst = Lout + (size_t)a * ncp;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) dst[k] = L[k];
-        }
+        reduce_store<T, S::NR, S::NC>(L, lane, Lout + (size_t)a * S::NCP);
     }
 }
 
 template <class T, int P>
 int launch_m2l_tp(Plan &P_, cudaStream_t s)
 {
-    k_m2l<T, P><<<P_.num_sms * 8, 256, 0, s>>>((int)P_.n_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
-                                               (const T *)P_.M, P_.ncp, (T *)P_.Lm2l);
+    using S = M2LShape<T, P>;
+    static_assert(S::NCP % S::V == 0, "row stride must be a whole number of 16-byte loads");
+    cudaFuncSetAttribute(k_m2l<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::smem);
+    k_m2l<T, P><<<P_.num_sms * 16, M2L_WARPS * 32, S::smem, s>>>(
+        (int)P_.n_nodes, P_.order + P_.n_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
+        (const T *)P_.M, (T *)P_.Lm2l, P_.ctr);
     return 1;
 }
 

@@ -41,14 +41,7 @@ __device__ __forceinline__ void store_geometry(int a, const T lo[3], const T hi[
     }
 }
 
-template <class T, int P>
-__device__ __forceinline__ void store_coeffs(T *__restrict__ dst, const T (&v)[Exp<P>::NC])
-{
-    if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-        for (int k = 0; k < Exp<P>::NC; ++k) dst[k] = v[k];
-    }
-}
+template <int NC> struct Padded { static constexpr int value = (NC + 7) / 8 * 8; };
 
 template <class T, int P>
 __global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__restrict__ xyzm,
@@ -58,6 +51,7 @@ __global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__re
                                                 vec4<T> *nc, vec4<T> *nl, T *M, int ncp)
 {
     constexpr int NC = Exp<P>::NC;
+    constexpr int NR = Padded<NC>::value;
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
@@ -79,21 +73,22 @@ __global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__re
             }
         store_geometry<T>(a, lo, hi, node_lo, node_hi, nc, nl, cen);
         {
-            T m[NC];
+            T m[NR];
 #pragma unroll
-            for (int k = 0; k < NC; ++k) m[k] = T(0);
+            for (int k = 0; k < NR; ++k) m[k] = T(0);
             for (int i = f + lane; i < f + c; i += 32) {
                 vec4<T> q = xyzm[i];
                 Exp<P>::template p2m<T>(q.x - cen[0], q.y - cen[1], q.z - cen[2], q.w, m);
             }
-#pragma unroll
-            for (int k = 0; k < NC; ++k) m[k] = warp_sum_xor(m[k]);
-            store_coeffs<T, P>(M + (size_t)a * ncp, m);
+            reduce_store<T, NR, NC>(m, lane, M + (size_t)a * ncp);
         }
         // ---- climb while this warp completes the parent's last child
         int cur = a;
         for (;;) {
+            // every lane's stores of this node (geometry by lane 0, moment blocks by lanes 0, 4, ...)
+            // are visible before lane 0 takes the parent's ticket
             __threadfence();
+            __syncwarp();
             const int par = parent[cur];
             if (par < 0) break;
             int ticket = 0;
@@ -115,9 +110,9 @@ __global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__re
                     hi[k] = tmax(hi[k], __shfl_xor_sync(kFull, hi[k], o));
                 }
             store_geometry<T>(par, lo, hi, node_lo, node_hi, nc, nl, cen);
-            T m[NC];
+            T m[NR];
 #pragma unroll
-            for (int k = 0; k < NC; ++k) m[k] = T(0);
+            for (int k = 0; k < NR; ++k) m[k] = T(0);
             if (lane < nch) {
                 const int ch = c0 + lane;
                 T mc[NC];
@@ -126,16 +121,8 @@ __global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__re
                 vec4<T> cc = ld_cg(nc + ch);
                 Exp<P>::template m2m<T>(mc, cc.x - cen[0], cc.y - cen[1], cc.z - cen[2], m);
             }
-            // children sit in lanes 0..7: butterfly over groups of 8 lanes
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                T v = m[k];
-                v += __shfl_xor_sync(kFull, v, 4);
-                v += __shfl_xor_sync(kFull, v, 2);
-                v += __shfl_xor_sync(kFull, v, 1);
-                m[k] = v;
-            }
-            store_coeffs<T, P>(M + (size_t)par * ncp, m);
+            // children sit in lanes 0..7, the other lanes hold zeros
+            reduce_store<T, NR, NC>(m, lane, M + (size_t)par * ncp);
             cur = par;
         }
     }

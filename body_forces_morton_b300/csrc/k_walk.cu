@@ -37,24 +37,6 @@ __global__ void k_walk_init(int2 *f0, DevCounters *ctr)
     ctr->frontier_max = 1;
 }
 
-// Block-wide exclusive scan of one int per thread; returns the block total.
-__device__ __forceinline__ int block_excl_scan(int v, int &excl, int *s_warp)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int incl = warp_incl_scan(v);
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    int base = 0, tot = 0;
-    for (int w = 0; w < WK_THREADS / 32; ++w) {
-        const int t = s_warp[w];
-        base += w < warp ? t : 0;
-        tot += t;
-    }
-    excl = base + incl - v;
-    __syncthreads();
-    return tot;
-}
-
 // One generation of the walk: every frontier pair is decided and its outputs
 // (an M2L pair, a P2P pair or child pairs) are appended; a block reserves the
 // space of a whole 256-pair tile with one atomic per output list.
@@ -68,7 +50,7 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
                                                           int cap_m2l, int2 *p2p_pairs, int cap_p2p, int *m2l_cnt,
                                                           int *p2p_cnt, DevCounters *ctr)
 {
-    __shared__ int s_warp[WK_THREADS / 32];
+    __shared__ int s_wtot[3][WK_THREADS / 32];
     __shared__ int s_base[3];
     const int nin = ctr->frontier_cnt[it % 3];
     int *cnt_out = &ctr->frontier_cnt[(it + 1) % 3];
@@ -113,19 +95,34 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
                 }
             }
         }
-        int ex_m, ex_p, ex_k;
-        const int tot_m = block_excl_scan(m2l, ex_m, s_warp);
-        const int tot_p = block_excl_scan(p2p, ex_p, s_warp);
-        const int tot_k = block_excl_scan(kids, ex_k, s_warp);
-        if (threadIdx.x == 0) {
-            s_base[0] = tot_m ? atomicAdd(&ctr->n_m2l_pairs, tot_m) : 0;
-            s_base[1] = tot_p ? atomicAdd(&ctr->n_p2p_pairs, tot_p) : 0;
-            s_base[2] = tot_k ? atomicAdd(cnt_out, tot_k) : 0;
-            kids_max = max(kids_max, s_base[2] + tot_k);
+        // warp-level scans, then one exchange of the warp totals per tile
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int im = warp_incl_scan(m2l), ip = warp_incl_scan(p2p), ik = warp_incl_scan(kids);
+        if (lane == 31) {
+            s_wtot[0][warp] = im;
+            s_wtot[1][warp] = ip;
+            s_wtot[2][warp] = ik;
         }
         __syncthreads();
+        if (threadIdx.x < 3) {
+            const int list = threadIdx.x;
+            int run = 0;
+            for (int w2 = 0; w2 < WK_THREADS / 32; ++w2) {
+                const int t = s_wtot[list][w2];
+                s_wtot[list][w2] = run;
+                run += t;
+            }
+            int *ctrp = list == 0 ? &ctr->n_m2l_pairs : (list == 1 ? &ctr->n_p2p_pairs : cnt_out);
+            const int b0 = run ? atomicAdd(ctrp, run) : 0;
+            s_base[list] = b0;
+            if (list == 2) kids_max = max(kids_max, b0 + run);
+        }
+        __syncthreads();
+        const int ex_m = s_base[0] + s_wtot[0][warp] + im - m2l;
+        const int ex_p = s_base[1] + s_wtot[1][warp] + ip - p2p;
+        const int ex_k = s_base[2] + s_wtot[2][warp] + ik - kids;
         if (m2l) {
-            const int slot = s_base[0] + ex_m;
+            const int slot = ex_m;
             if (slot < cap_m2l) {
                 m2l_pairs[slot] = make_int2(A, B);
                 atomicAdd(&m2l_cnt[A], 1);
@@ -135,7 +132,7 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
             }
         }
         if (p2p) {
-            const int slot = s_base[1] + ex_p;
+            const int slot = ex_p;
             if (slot < cap_p2p) {
                 p2p_pairs[slot] = make_int2(A, B);
                 atomicAdd(&p2p_cnt[A], 1);
@@ -145,7 +142,7 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
             }
         }
         if (kids) {
-            int o = s_base[2] + ex_k;
+            int o = ex_k;
             const int c0 = child0[split];
             if (A == B) {
                 const int nA = nchild[A];
@@ -173,7 +170,7 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
         if (inter_sum) atomicAdd((unsigned long long *)&ctr->p2p_interactions, (unsigned long long)inter_sum);
         if (visited) atomicAdd((unsigned long long *)&ctr->walk_pairs, (unsigned long long)visited);
     }
-    if (threadIdx.x == 0 && kids_max) atomicMax(&ctr->frontier_max, kids_max);
+    if (threadIdx.x == 2 && kids_max) atomicMax(&ctr->frontier_max, kids_max);
 }
 
 // Exclusive scan of the per-receiver counts into CSR offsets (both lists at once).
@@ -258,14 +255,90 @@ __device__ __forceinline__ void cmpswap(int *v, int i, int j)
     if (b < a) { v[i] = b; v[j] = a; }
 }
 
-// One warp per receiver; segments longer than SEG_WARP_MAX go to a second pass.
+// Warp-wide ascending bitonic sort of 32 NR keys, key e = 32 j + lane in v[j]:
+// the flip-first network of cmpswap above. The flip partner of e is e ^ (k-1),
+// the half-cleaner partner e ^ d; partners in another lane come by shuffle,
+// partners in the same lane (distance >= 32) are registers. New values are
+// always computed from old ones.
+template <int NR>
+__device__ __forceinline__ void warp_sort(int (&v)[NR])
+{
+    constexpr int LOGN = 5 + (NR == 1 ? 0 : NR == 2 ? 1 : NR == 4 ? 2 : 3);
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int lk = 1; lk <= LOGN; ++lk) {
+        const int k = 1 << lk;
+        if (k <= 32) {
+#pragma unroll
+            for (int j = 0; j < NR; ++j) {
+                const int other = __shfl_xor_sync(kFull, v[j], k - 1);
+                const bool lower = (lane & (k >> 1)) == 0;
+                v[j] = lower ? min(v[j], other) : max(v[j], other);
+            }
+        } else {
+            const int jm = (k >> 5) - 1;
+            int nv[NR];
+#pragma unroll
+            for (int j = 0; j < NR; ++j) {
+                const int other = __shfl_xor_sync(kFull, v[j ^ jm], 31);
+                const bool lower = (j & (k >> 6)) == 0;
+                nv[j] = lower ? min(v[j], other) : max(v[j], other);
+            }
+#pragma unroll
+            for (int j = 0; j < NR; ++j) v[j] = nv[j];
+        }
+#pragma unroll
+        for (int lj = lk - 2; lj >= 0; --lj) {
+            const int d = 1 << lj;
+            if (d >= 32) {
+                const int dj = d >> 5;
+#pragma unroll
+                for (int j = 0; j < NR; ++j) {
+                    if ((j & dj) == 0) {
+                        const int a = v[j], b = v[j + dj];
+                        v[j] = min(a, b);
+                        v[j + dj] = max(a, b);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < NR; ++j) {
+                    const int other = __shfl_xor_sync(kFull, v[j], d);
+                    const bool lower = (lane & d) == 0;
+                    v[j] = lower ? min(v[j], other) : max(v[j], other);
+                }
+            }
+        }
+    }
+}
+
+template <int NR>
+__device__ __forceinline__ void sort_list_regs(int *src, int len)
+{
+    const int lane = threadIdx.x & 31;
+    int v[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        const int e = j * 32 + lane;
+        v[j] = e < len ? src[e] : 0x7fffffff;
+    }
+    warp_sort<NR>(v);
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        const int e = j * 32 + lane;
+        if (e < len) src[e] = v[j];
+    }
+}
+
+// One warp per receiver list; lists up to 256 sort in registers, up to
+// SEG_WARP_MAX in shared memory, longer ones go to a second pass.
 __global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restrict__ m2l_off, int *m2l_src,
                                                  const int *__restrict__ p2p_off, int *p2p_src, int *long_seg,
                                                  DevCounters *ctr)
 {
     __shared__ int buf[8][SEG_WARP_MAX];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int *v = buf[w];
+    int *sv = buf[w];
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int job = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; job < 2 * n_nodes; job += nwarps) {
         const int a = job >> 1;
@@ -274,31 +347,35 @@ __global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restr
         const int len = (isp ? p2p_off[a + 1] : m2l_off[a + 1]) - beg;
         int *src = (isp ? p2p_src : m2l_src) + beg;
         if (len <= 1) continue;
+        if (len <= 32) { sort_list_regs<1>(src, len); continue; }
+        if (len <= 64) { sort_list_regs<2>(src, len); continue; }
+        if (len <= 128) { sort_list_regs<4>(src, len); continue; }
+        if (len <= 256) { sort_list_regs<8>(src, len); continue; }
         if (len > SEG_WARP_MAX) {
             if (lane == 0) long_seg[atomicAdd(&ctr->n_long, 1)] = job;
             continue;
         }
         int S = 2;
         while (S < len) S <<= 1;
-        for (int i = lane; i < S; i += 32) v[i] = i < len ? src[i] : 0x7fffffff;
+        for (int i = lane; i < S; i += 32) sv[i] = i < len ? src[i] : 0x7fffffff;
         __syncwarp();
         for (int lk = 1; (1 << lk) <= S; ++lk) {
             const int k = 1 << lk;
             for (int i = lane; i < S / 2; i += 32) {
                 const int blk = i >> (lk - 1), pos = i & ((k >> 1) - 1);
-                cmpswap(v, blk * k + pos, blk * k + k - 1 - pos);
+                cmpswap(sv, blk * k + pos, blk * k + k - 1 - pos);
             }
             __syncwarp();
             for (int lj = lk - 2; lj >= 0; --lj) {
                 const int j = 1 << lj;
                 for (int i = lane; i < S / 2; i += 32) {
                     const int blk = i >> lj, pos = i & (j - 1);
-                    cmpswap(v, (blk << (lj + 1)) + pos, (blk << (lj + 1)) + pos + j);
+                    cmpswap(sv, (blk << (lj + 1)) + pos, (blk << (lj + 1)) + pos + j);
                 }
                 __syncwarp();
             }
         }
-        for (int i = lane; i < len; i += 32) src[i] = v[i];
+        for (int i = lane; i < len; i += 32) src[i] = sv[i];
         __syncwarp();
     }
 }
@@ -340,6 +417,59 @@ __global__ __launch_bounds__(1024) void k_segsort_long(const int *__restrict__ m
     }
 }
 
+// Work order of the receivers, heaviest first: bucket b = floor(log2(work)) + 1
+// (0 for no work), buckets taken in decreasing b. P2P work of a leaf is
+// count * (sum of its source leaves' counts); M2L work of a node is its list
+// length. The order decides only which warp takes which receiver, never a result.
+__global__ __launch_bounds__(256) void k_order_count(int n_nodes, const int *__restrict__ count,
+                                                     const int *__restrict__ nchild, const int *__restrict__ m2l_off,
+                                                     const int *__restrict__ p2p_off, const int *__restrict__ p2p_src,
+                                                     uint8_t *__restrict__ key, DevCounters *ctr)
+{
+    const int lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
+        long long work = 0;
+        if (nchild[a] == 0) {
+            const int beg = p2p_off[a], end = p2p_off[a + 1];
+            long long s = 0;
+            for (int e = beg + lane; e < end; e += 32) s += count[p2p_src[e]];
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            work = s * count[a];
+        }
+        if (lane == 0) {
+            const int kp = work > 0 ? 64 - __clzll(work) : 0;
+            const int len = m2l_off[a + 1] - m2l_off[a];
+            const int km = len > 0 ? 32 - __clz(len) : 0;
+            key[a] = (uint8_t)kp;
+            key[n_nodes + a] = (uint8_t)km;
+            if (kp) atomicAdd(&ctr->order_cnt[0][kp], 1);
+            atomicAdd(&ctr->order_cnt[1][km], 1);
+        }
+    }
+}
+
+__global__ __launch_bounds__(256) void k_order_scatter(int n_nodes, const uint8_t *__restrict__ key, int *order,
+                                                       DevCounters *ctr)
+{
+    __shared__ int base[2][64];
+    const int tid = (int)threadIdx.x;
+    if (tid < 2) {
+        const int lowest = tid == 0 ? 1 : 0;  // P2P skips bucket 0 (no work); M2L keeps it, last
+        int run = 0;
+        for (int b = 63; b >= lowest; --b) {
+            base[tid][b] = run;
+            run += ctr->order_cnt[tid][b];
+        }
+    }
+    __syncthreads();
+    for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n_nodes; a += gridDim.x * blockDim.x) {
+        const int kp = key[a], km = key[n_nodes + a];
+        if (kp) order[base[0][kp] + atomicAdd(&ctr->order_cur[0][kp], 1)] = a;
+        order[n_nodes + base[1][km] + atomicAdd(&ctr->order_cur[1][km], 1)] = a;
+    }
+}
+
 template <class T>
 int launch_walk_t(Plan &P, int depth, cudaStream_t s)
 {
@@ -373,7 +503,10 @@ int launch_lists(Plan &P, cudaStream_t s)
                                              P.p2p_cnt, P.m2l_off, P.p2p_off, P.m2l_src, P.p2p_src, P.ctr);
     k_segsort<<<P.num_sms * 8, 256, 0, s>>>(nn, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
     k_segsort_long<<<P.num_sms, 1024, 0, s>>>(P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
-    return 4;
+    k_order_count<<<P.num_sms * 8, 256, 0, s>>>(nn, P.node_count, P.node_nchild, P.m2l_off, P.p2p_off, P.p2p_src,
+                                               P.order_key, P.ctr);
+    k_order_scatter<<<P.num_sms * 4, 256, 0, s>>>(nn, P.order_key, P.order, P.ctr);
+    return 6;
 }
 
 }  // namespace bfm

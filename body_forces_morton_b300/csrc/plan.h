@@ -31,6 +31,7 @@ struct Plan {
     uint64_t *keys[2] = {nullptr, nullptr};
     uint32_t *idx[2] = {nullptr, nullptr};
     void *xyzm = nullptr;          // sorted particles, vec4<T> (x, y, z, m)
+    void *far = nullptr;           // far field at the sorted particles, vec4<T> (phi, ax, ay, az)
     uint8_t *div = nullptr;        // divergence level of consecutive sorted keys
 
     // node buffers
@@ -47,6 +48,8 @@ struct Plan {
     int *m2l_off = nullptr, *p2p_off = nullptr;    // CSR offsets [cap_nodes + 1]
     int *m2l_src = nullptr, *p2p_src = nullptr;    // CSR sources [2 * cap]
     int *long_seg = nullptr;                       // receivers whose lists are too long for the warp sort
+    int *order = nullptr;                          // [2][cap_nodes] receivers by decreasing work (P2P, M2L)
+    uint8_t *order_key = nullptr;                  // [2][cap_nodes] work bucket of every node
 
     void *scratch = nullptr;       // 64 KiB for small per-block partials
 
