@@ -86,7 +86,9 @@ def lib():
         L.fmm_plan_export_size.argtypes = [vp, i32]
         L.fmm_plan_export_size.restype = i64
         L.fmm_plan_export.argtypes = [vp, i32, vp, i64]
-        for f in ("fmm_eval", "fmm_eval_host", "fmm_kdk_step", "fmm_plan_stats", "fmm_plan_export"):
+        L.fmm_morton_keys_noalloc.argtypes = [vp, i64, i32, vp, vp, vp]
+        for f in ("fmm_eval", "fmm_eval_host", "fmm_kdk_step", "fmm_plan_stats", "fmm_plan_export",
+                  "fmm_morton_keys_noalloc"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -142,6 +144,14 @@ def fmm_eval_host(plan, pos, mass, acc_out, pot_out=None, stream=None):
 
 def fmm_kdk_step(plan, pos, vel, mass, dt: float, stream=None):
     _check(lib().fmm_kdk_step(plan, _ptr(pos), _ptr(vel), _ptr(mass), float(dt), _stream(stream)))
+
+
+def fmm_morton_keys_noalloc(pos, n: int, dtype: int, keys_out, box_out=None, stream=None):
+    """Root box and Morton keys of n <= 2^21 particles with no device allocation."""
+    st = lib().fmm_morton_keys_noalloc(_ptr(pos), int(n), int(dtype), _ptr(keys_out), _ptr(box_out),
+                                       _stream(stream))
+    if st != 0:
+        raise FmmError(st, "fmm_morton_keys_noalloc failed")
 
 
 def fmm_kdk_reset(plan):

@@ -193,6 +193,34 @@ enum {
 int64_t fmm_plan_export_size(const fmm_plan *plan, int what);
 fmm_status fmm_plan_export(const fmm_plan *plan, int what, void *dst, int64_t bytes);
 
+/*
+ * Root box and Morton keys without any device allocation (the pages have no
+ * counterpart; this is a library convenience).
+ *
+ * For callers that cannot allocate device memory when they need the keys: code
+ * inside a stream capture, code working within a fixed memory budget handed out
+ * by its own allocator, or a real-time loop that must not take the driver's
+ * allocation locks. It needs no plan: the caller passes pos [n x 3] (device,
+ * `dtype` reals) and keys_out [n] (device, uint64, written in the caller's
+ * particle order) and optionally box_out [4] (device doubles: the root cube's
+ * lower corner x, y, z and its side). The keys are the same as the plan path's
+ * (21-bit quantisation against the root cube, x highest in each 3-bit digit).
+ *
+ * Scratch: a fixed 48 KiB array in the library's device image (one partial box
+ * per 2048 particles, for at most 1024 blocks), held by every GPU that loads
+ * the library until the process exits. Hence n must be in [1, 2^21]; larger n
+ * (or NULL pos/keys_out, or an unknown dtype) returns FMM_ERR_INVALID_ARG
+ * without touching the GPU. The first call on a device looks the array's
+ * device address up (once per device, with that device current); make that
+ * first call before any stream capture. Every call clears the words that must
+ * start at zero; calls that overlap on the GPU (two streams, or two host
+ * threads on one device) share the array and race. The call blocks until the
+ * keys are written and returns FMM_ERR_NONFINITE if a coordinate is NaN or
+ * infinite. It calls no allocating routine.
+ */
+fmm_status fmm_morton_keys_noalloc(const void *pos, int64_t n, fmm_dtype dtype, uint64_t *keys_out,
+                                   double *box_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
