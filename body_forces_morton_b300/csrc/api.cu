@@ -407,6 +407,49 @@ fmm_status fmm_kdk_step(fmm_plan *plan, void *pos, void *vel, const void *mass, 
     return FMM_OK;
 }
 
+fmm_status fmm_kdk_step_lattice(fmm_plan *plan, void *pos, void *vel, const void *mass, double dt, int pos_exp,
+                                int vel_exp, void *stream)
+{
+    g_err.clear();
+    if (!plan || !pos || !vel || !mass) {
+        set_err("fmm_kdk_step_lattice: plan, pos, vel and mass must be non-NULL");
+        return FMM_ERR_INVALID_ARG;
+    }
+    Plan &P = plan->P;
+    if (pos_exp < -1000 || pos_exp > 100 || vel_exp < -1000 || vel_exp > 100) {
+        set_err("fmm_kdk_step_lattice: lattice exponents out of range");
+        return FMM_ERR_INVALID_ARG;
+    }
+    DeviceGuard g(P.device);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!P.acc_cache) CUDA_TRY(cudaMalloc(&P.acc_cache, 3 * (size_t)P.n * P.esize));
+    const bool cached = P.cache_valid && P.cache_pos == pos && P.cache_vel == vel && P.cache_mass == mass;
+    P.cache_valid = false;
+    int launches = 0;
+    // put the state on its lattices (a no-op once it lies there): x += 0, v += 0 rounded
+    launches += launch_lattice_axpy(P, pos, nullptr, 0.0, pos_exp, pos_exp, s);
+    launches += launch_lattice_axpy(P, vel, nullptr, 0.0, vel_exp, vel_exp, s);
+    if (!cached) {
+        fmm_status st = eval_device(P, pos, mass, P.acc_cache, nullptr, s);
+        if (st) return st;
+        launches += P.launches;
+    }
+    launches += launch_lattice_axpy(P, vel, P.acc_cache, 0.5 * dt, vel_exp, vel_exp, s);
+    launches += launch_lattice_axpy(P, pos, vel, dt, pos_exp, pos_exp, s);
+    fmm_status st = eval_device(P, pos, mass, P.acc_cache, nullptr, s);
+    if (st) return st;
+    launches += P.launches;
+    launches += launch_lattice_axpy(P, vel, P.acc_cache, 0.5 * dt, vel_exp, vel_exp, s);
+    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(cudaStreamSynchronize(s));
+    P.launches = launches;
+    P.cache_valid = true;
+    P.cache_pos = pos;
+    P.cache_vel = vel;
+    P.cache_mass = mass;
+    return FMM_OK;
+}
+
 void fmm_kdk_reset(fmm_plan *plan)
 {
     if (plan) plan->P.cache_valid = false;

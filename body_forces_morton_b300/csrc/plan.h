@@ -99,6 +99,7 @@ int launch_l2l(Plan &P, int depth, cudaStream_t s);
 int launch_leaf(Plan &P, void *acc, void *pot, cudaStream_t s);
 int launch_kick(Plan &P, void *vel, const void *acc, double h, cudaStream_t s);
 int launch_drift(Plan &P, void *pos, const void *vel, double dt, cudaStream_t s);
+int launch_lattice_axpy(Plan &P, void *y, const void *x, double h, int e_y, int e_inc, cudaStream_t s);
 
 inline int grid_for(const Plan &P, int per_sm = 8) { return P.num_sms * per_sm; }
 

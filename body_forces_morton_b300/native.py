@@ -76,6 +76,7 @@ def lib():
         L.fmm_eval.argtypes = [vp, vp, vp, vp, vp, vp]
         L.fmm_eval_host.argtypes = [vp, vp, vp, vp, vp, vp]
         L.fmm_kdk_step.argtypes = [vp, vp, vp, vp, dbl, vp]
+        L.fmm_kdk_step_lattice.argtypes = [vp, vp, vp, vp, dbl, i32, i32, vp]
         L.fmm_kdk_reset.argtypes = [vp]
         L.fmm_kdk_reset.restype = None
         L.fmm_destroy.argtypes = [vp]
@@ -87,7 +88,7 @@ def lib():
         L.fmm_plan_export_size.restype = i64
         L.fmm_plan_export.argtypes = [vp, i32, vp, i64]
         L.fmm_morton_keys_noalloc.argtypes = [vp, i64, i32, vp, vp, vp]
-        for f in ("fmm_eval", "fmm_eval_host", "fmm_kdk_step", "fmm_plan_stats", "fmm_plan_export",
+        for f in ("fmm_eval", "fmm_eval_host", "fmm_kdk_step", "fmm_kdk_step_lattice", "fmm_plan_stats", "fmm_plan_export",
                   "fmm_morton_keys_noalloc"):
             getattr(L, f).restype = i32
         _lib = L
@@ -144,6 +145,11 @@ def fmm_eval_host(plan, pos, mass, acc_out, pot_out=None, stream=None):
 
 def fmm_kdk_step(plan, pos, vel, mass, dt: float, stream=None):
     _check(lib().fmm_kdk_step(plan, _ptr(pos), _ptr(vel), _ptr(mass), float(dt), _stream(stream)))
+
+
+def fmm_kdk_step_lattice(plan, pos, vel, mass, dt: float, pos_exp: int, vel_exp: int, stream=None):
+    _check(lib().fmm_kdk_step_lattice(plan, _ptr(pos), _ptr(vel), _ptr(mass), float(dt), int(pos_exp), int(vel_exp),
+                                      _stream(stream)))
 
 
 def fmm_morton_keys_noalloc(pos, n: int, dtype: int, keys_out, box_out=None, stream=None):
@@ -205,6 +211,9 @@ class Plan:
 
     def kdk_step(self, pos, vel, mass, dt, stream=None):
         fmm_kdk_step(self.handle, pos, vel, mass, dt, stream)
+
+    def kdk_step_lattice(self, pos, vel, mass, dt, pos_exp=-40, vel_exp=-40, stream=None):
+        fmm_kdk_step_lattice(self.handle, pos, vel, mass, dt, pos_exp, vel_exp, stream)
 
     def kdk_reset(self):
         fmm_kdk_reset(self.handle)

@@ -133,6 +133,21 @@ fmm_status fmm_eval_host(fmm_plan *plan, const void *pos, const void *mass, void
  */
 fmm_status fmm_kdk_step(fmm_plan *plan, void *pos, void *vel, const void *mass, double dt, void *stream);
 
+/*
+ * The same step on an integer lattice (JZ-FMM page, "Why reversibility
+ * matters"): positions live on the lattice 2^pos_exp Z, velocities on
+ * 2^vel_exp Z, and every kick and drift increment is rounded to its lattice
+ * (round half to even, so the increment of -dt is exactly minus that of dt).
+ * The force stays floating point and is reproduced bit for bit at a revisited
+ * state, so a step with -dt undoes a step with dt exactly, whatever the
+ * dynamics. pos and vel are first rounded to their lattices (a no-op once they
+ * lie there). The values must stay below 2^(mantissa bits) lattice units
+ * (|x| < 2^(53 + pos_exp) in fp64) for the sums to be exact. Shares the
+ * acceleration cache of fmm_kdk_step.
+ */
+fmm_status fmm_kdk_step_lattice(fmm_plan *plan, void *pos, void *vel, const void *mass, double dt, int pos_exp,
+                                int vel_exp, void *stream);
+
 /* Drop the cached acceleration of fmm_kdk_step (the next step evaluates it afresh). */
 void fmm_kdk_reset(fmm_plan *plan);
 

@@ -47,8 +47,9 @@ def lib():
         L.orc_fmm.argtypes = [i32, i64, vp, vp, i32, dbl, i32, vp, i32, i32, C.POINTER(_Result)]
         L.orc_result_free.argtypes = [C.POINTER(_Result)]
         L.orc_kdk_step.argtypes = [i64, vp, vp, vp, vp, dbl, i32, dbl, i32, i32]
+        L.orc_kdk_lattice_step.argtypes = [i64, vp, vp, vp, vp, dbl, i32, i32, i32, dbl, i32, i32]
         for f in ("orc_direct_sum", "orc_derivs", "orc_p2m", "orc_m2m", "orc_m2l", "orc_l2l",
-                  "orc_l2p", "orc_keys", "orc_fmm", "orc_kdk_step"):
+                  "orc_l2p", "orc_keys", "orc_fmm", "orc_kdk_step", "orc_kdk_lattice_step"):
             getattr(L, f).restype = i32
         L.orc_result_free.restype = None
         _lib = L
@@ -298,3 +299,13 @@ def kdk_step(pos, vel, mass, acc, dt: float, p: int, theta: float, leaf: int, nt
             raise TypeError("kdk_step works on C-contiguous float64 arrays")
     _check(lib().orc_kdk_step(len(mass), _ptr(pos), _ptr(vel), _ptr(mass), _ptr(acc), float(dt), p,
                               float(theta), leaf, nthreads), "kdk_step")
+
+
+def kdk_lattice_step(pos, vel, mass, acc, dt: float, pos_exp: int, vel_exp: int, p: int, theta: float, leaf: int,
+                     nthreads: int = 0):
+    """One lattice kick-drift-kick step in place (fp64); see orc_kdk_lattice_step."""
+    for a in (pos, vel, mass, acc):
+        if a.dtype != np.float64 or not a.flags.c_contiguous:
+            raise TypeError("kdk_lattice_step works on C-contiguous float64 arrays")
+    _check(lib().orc_kdk_lattice_step(len(mass), _ptr(pos), _ptr(vel), _ptr(mass), _ptr(acc), float(dt), pos_exp,
+                                      vel_exp, p, float(theta), leaf, nthreads), "kdk_lattice_step")

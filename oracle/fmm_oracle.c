@@ -859,3 +859,33 @@ int orc_kdk_step(int64_t n, double *pos, double *vel, const double *mass, double
     for (int64_t i = 0; i < 3 * n; ++i) vel[i] += acc[i] * (0.5 * dt);
     return ORC_OK;
 }
+
+/*
+ * Kick-drift-kick on an integer lattice (JZ-FMM page, "Why reversibility
+ * matters": positions and velocities live on a lattice, the force stays
+ * floating point, reversing an update subtracts the same increment).
+ * Lattice spacings are 2^pos_exp and 2^vel_exp; every increment is rounded to
+ * its lattice (round half to even, symmetric in the sign of dt), so a step
+ * with -dt undoes a step with dt exactly when the force at a revisited state
+ * is reproduced bit for bit. pos and vel are first rounded to their lattices
+ * (a no-op once they lie on them). `acc` holds a(x) on entry, a(x_new) on exit.
+ */
+static double to_lattice(double y, double inv_spacing, double spacing) { return nearbyint(y * inv_spacing) * spacing; }
+
+int orc_kdk_lattice_step(int64_t n, double *pos, double *vel, const double *mass, double *acc, double dt,
+                         int pos_exp, int vel_exp, int p, double theta, int leaf, int nthreads)
+{
+    const double dx = ldexp(1.0, pos_exp), idx = ldexp(1.0, -pos_exp);
+    const double dv = ldexp(1.0, vel_exp), idv = ldexp(1.0, -vel_exp);
+    const double h = 0.5 * dt;
+    for (int64_t i = 0; i < 3 * n; ++i) { pos[i] = to_lattice(pos[i], idx, dx); vel[i] = to_lattice(vel[i], idv, dv); }
+    for (int64_t i = 0; i < 3 * n; ++i) vel[i] += to_lattice(acc[i] * h, idv, dv);
+    for (int64_t i = 0; i < 3 * n; ++i) pos[i] += to_lattice(vel[i] * dt, idx, dx);
+    orc_result r;
+    int st = orc_fmm(ORC_DTYPE_F64, n, pos, mass, p, theta, leaf, NULL, 0, nthreads, &r);
+    if (st) return st;
+    memcpy(acc, r.acc, sizeof(double) * 3 * (size_t)n);
+    orc_result_free(&r);
+    for (int64_t i = 0; i < 3 * n; ++i) vel[i] += to_lattice(acc[i] * h, idv, dv);
+    return ORC_OK;
+}
