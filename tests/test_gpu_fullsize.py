@@ -1,0 +1,74 @@
+"""Full-size parity: the workloads at their own sizes, in the configuration the
+benchmark times.
+
+* config 3 (Plummer, N = 1e5, fp64): tree and lists bit-exact, every
+  particle's acceleration against the full oracle FMM, and the p x theta sweep
+  against the direct sum on the first 1000 particles (error falls with p and
+  as theta shrinks);
+* config 4 (clustered, N = 2^20, fp32) and config 5 (clustered, N = 2^22,
+  fp32, p 3, theta 0.6): tree and lists bit-exact, accelerations of a seeded
+  sample of particles against the oracle evaluated on that sample only.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from body_forces_morton_b300 import workloads as W
+from gpu_helpers import ALL_STRUCT, TOL_ACC, accel_error, assert_structure_equal, gpu_eval, pot_error
+
+pytestmark = pytest.mark.gpu
+
+
+def sampled_parity(w, n_sample=3000):
+    g = W.generate(w)
+    acc, pot, ex, st = gpu_eval(g["pos"], g["mass"], w.p, w.theta, w.leaf, exports=ALL_STRUCT)
+    r_tree = oracle.fmm(g["pos"], g["mass"], w.p, w.theta, w.leaf, tree_only=True)
+    assert_structure_equal(ex, r_tree)
+    mask = np.zeros(w.n, bool)
+    mask[np.random.default_rng(w.seed).choice(w.n, n_sample, replace=False)] = True
+    r = oracle.fmm(g["pos"], g["mass"], w.p, w.theta, w.leaf, eval_mask=mask)
+    e = accel_error(acc[mask].astype(np.float64), r.acc[mask])
+    ep = pot_error(pot[mask].astype(np.float64), r.pot[mask])
+    print(f"{w.name}: sampled acc error max {e.max():.2e} p99 {np.percentile(e, 99):.2e}, pot {ep.max():.2e}; "
+          f"nodes {st['n_nodes']} depth {st['depth']} m2l {st['n_m2l']} p2p pairs {st['n_p2p_interactions']}")
+    assert e.max() <= TOL_ACC[w.dtype] and ep.max() <= TOL_ACC[w.dtype]
+
+
+def test_config3_full_parity_fp64():
+    w = W.WORKLOADS[3]
+    g = W.generate(w)
+    acc, pot, ex, st = gpu_eval(g["pos"], g["mass"], w.p, w.theta, w.leaf, exports=ALL_STRUCT)
+    r = oracle.fmm(g["pos"], g["mass"], w.p, w.theta, w.leaf)
+    assert_structure_equal(ex, r)
+    e = accel_error(acc, r.acc)
+    ep = pot_error(pot, r.pot)
+    print(f"config 3 full: acc error max {e.max():.2e}, pot {ep.max():.2e}")
+    assert e.max() <= 1e-10 and ep.max() <= 1e-10
+
+
+def test_config3_sweep_against_direct_sum():
+    """Error vs the direct sum on the first 1000 particles over p and theta."""
+    w = W.WORKLOADS[3]
+    g = W.generate(w)
+    tgt = np.arange(1000)
+    acc_d, pot_d = oracle.direct_sum(g["pos"], g["mass"], targets=tgt)
+    rms, mx = {}, {}
+    for theta in (0.4, 0.5, 0.7):
+        for p in (2, 3, 4, 5, 6):
+            acc, _, _, _ = gpu_eval(g["pos"], g["mass"], p, theta, w.leaf, want_pot=False)
+            e = accel_error(acc[tgt], acc_d[tgt])
+            rms[p, theta] = float(np.sqrt(np.mean(e ** 2)))
+            mx[p, theta] = float(e.max())
+            print(f"p={p} theta={theta}: max {mx[p, theta]:.3e} p99 {np.percentile(e, 99):.3e} rms {rms[p, theta]:.3e}")
+    for theta in (0.4, 0.5, 0.7):
+        assert all(rms[p + 1, theta] < rms[p, theta] for p in (2, 3, 4, 5))
+    for p in (2, 3, 4, 5, 6):
+        assert rms[p, 0.4] < rms[p, 0.5] < rms[p, 0.7]
+
+
+def test_config4_sampled_parity_fp32():
+    sampled_parity(W.WORKLOADS[4])
+
+
+def test_config5_sampled_parity_fp32():
+    sampled_parity(W.WORKLOADS[5])
