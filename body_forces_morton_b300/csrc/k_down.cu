@@ -13,6 +13,8 @@
 // particles at a time), reads them back as broadcasts, keeps all lanes busy for
 // small leaves by splitting the sources, adds the far field and writes straight
 // to the caller's particle order.
+#include <type_traits>
+
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -138,6 +140,121 @@ __device__ __forceinline__ void p2p_span(const vec4<T> *buf, int n_here, int q, 
     }
 }
 
+// ---- fp32: two sources per instruction with the packed f32x2 arithmetic of
+// sm_100-family GPUs (one instruction issues the operation for both halves).
+// Staged sources are stored pair-interleaved, (x_j, x_j+1, y_j, y_j+1, z_j,
+// z_j+1, m_j, m_j+1) per pair, so two 16-byte shared loads give four packed
+// operands; an odd tail is padded with a massless particle far away.
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2_pack(float a, float b)
+{
+    f2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b)
+{
+    f2_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c)
+{
+    f2_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ void put_pair_layout(float *fb, int k, float x, float y, float z, float m)
+{
+    const int base = (k >> 1) * 8 + (k & 1);
+    fb[base] = x;
+    fb[base + 2] = y;
+    fb[base + 4] = z;
+    fb[base + 6] = m;
+}
+
+// Two sources (packed SX, SY, SZ, SM) acting on one receiver (packed broadcast
+// X, Y, Z); A = (phi, ax, ay, az), each the even-source and odd-source halves.
+__device__ __forceinline__ void p2p_two(f2_t SX, f2_t SY, f2_t SZ, f2_t SM, f2_t X, f2_t Y, f2_t Z, f2_t (&A)[4])
+{
+    const f2_t dx = f2_sub(SX, X), dy = f2_sub(SY, Y), dz = f2_sub(SZ, Z);
+    f2_t r2 = f2_mul(dx, dx);
+    r2 = f2_fma(dy, dy, r2);
+    r2 = f2_fma(dz, dz, r2);
+    float ra, rb;
+    f2_unpack(r2, ra, rb);
+    const f2_t ri = f2_pack(rsqrtf(ra), rsqrtf(rb));
+    const f2_t mr = f2_mul(SM, ri);
+    const f2_t mr3 = f2_mul(mr, f2_mul(ri, ri));
+    A[1] = f2_fma(mr3, dx, A[1]);
+    A[2] = f2_fma(mr3, dy, A[2]);
+    A[3] = f2_fma(mr3, dz, A[3]);
+    A[0] = f2_sub(A[0], mr);
+}
+
+template <int CH>
+__device__ __forceinline__ int stage_sources_pairs(float *fb, const float4 *__restrict__ xyzm, int lf, int ex,
+                                                   int tot, int g0, int lane)
+{
+    const int n_here = min(CH, tot - g0);
+    for (int k0 = 0; k0 < n_here; k0 += 32) {
+        const int k = k0 + lane;
+        const int g = g0 + k;
+        int lo = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {
+            const int exm = __shfl_sync(kFull, ex, lo + step);
+            lo = exm <= g ? lo + step : lo;
+        }
+        const int f = __shfl_sync(kFull, lf, lo);
+        const int e = __shfl_sync(kFull, ex, lo);
+        if (k < n_here) {
+            const float4 v = xyzm[f + (g - e)];
+            put_pair_layout(fb, k, v.x, v.y, v.z, v.w);
+        }
+    }
+    if ((n_here & 1) && lane == 0) put_pair_layout(fb, n_here, 1e18f, 1e18f, 1e18f, 0.0f);
+    return (n_here + 1) >> 1;
+}
+
+template <int K>
+__device__ __forceinline__ void p2p_span_pairs(const float *fb, int npairs, int q, int S, const f2_t (&X)[K],
+                                               const f2_t (&Y)[K], const f2_t (&Z)[K], f2_t (&A)[K][4])
+{
+    const ulonglong2 *pb = reinterpret_cast<const ulonglong2 *>(fb);
+    int j = q;
+    for (; j + S < npairs; j += 2 * S) {
+        const ulonglong2 a0 = pb[2 * j], b0 = pb[2 * j + 1];
+        const ulonglong2 a1 = pb[2 * (j + S)], b1 = pb[2 * (j + S) + 1];
+#pragma unroll
+        for (int k = 0; k < K; ++k) p2p_two(a0.x, a0.y, b0.x, b0.y, X[k], Y[k], Z[k], A[k]);
+#pragma unroll
+        for (int k = 0; k < K; ++k) p2p_two(a1.x, a1.y, b1.x, b1.y, X[k], Y[k], Z[k], A[k]);
+    }
+    if (j < npairs) {
+        const ulonglong2 a0 = pb[2 * j], b0 = pb[2 * j + 1];
+#pragma unroll
+        for (int k = 0; k < K; ++k) p2p_two(a0.x, a0.y, b0.x, b0.y, X[k], Y[k], Z[k], A[k]);
+    }
+}
+
 // One round of up to 32 K receivers [r0, r0 + cr) of leaf a. Lane = q R + rp
 // (rp < R = ceil(cr / K), q < S = 32 / R) holds receivers rp + k R, k < K, and
 // walks the staged sources from offset q with stride S. Lanes at or beyond
@@ -174,24 +291,64 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
         p2p_span<T, true, K>(buf, n_here, qq, S, p, acc);
     }
     // every other source leaf, 32 list entries at a time
-    for (int lb = beg; lb < end; lb += 32) {
-        const int e = lb + lane;
-        int fb = 0, cb = 0;
-        if (e < end) {
-            const int b = src[e];
-            if (b != a) {
-                fb = first[b];
-                cb = count[b];
+    if constexpr (std::is_same<T, float>::value) {
+        f2_t X[K], Y[K], Z[K], A[K][4];
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            X[k] = f2_pack(p[k].x, p[k].x);
+            Y[k] = f2_pack(p[k].y, p[k].y);
+            Z[k] = f2_pack(p[k].z, p[k].z);
+            A[k][0] = A[k][1] = A[k][2] = A[k][3] = f2_pack(0.0f, 0.0f);
+        }
+        float *fbuf = reinterpret_cast<float *>(buf);
+        for (int lb = beg; lb < end; lb += 32) {
+            const int e = lb + lane;
+            int fb = 0, cb = 0;
+            if (e < end) {
+                const int b = src[e];
+                if (b != a) {
+                    fb = first[b];
+                    cb = count[b];
+                }
+            }
+            const int incl = warp_incl_scan(cb);
+            const int tot = __shfl_sync(kFull, incl, 31);
+            const int ex = incl - cb;
+            for (int g0 = 0; g0 < tot; g0 += CH) {
+                __syncwarp();
+                const int npairs = stage_sources_pairs<CH>(fbuf, xyzm, fb, ex, tot, g0, lane);
+                __syncwarp();
+                p2p_span_pairs<K>(fbuf, npairs, qq, S, X, Y, Z, A);
             }
         }
-        const int incl = warp_incl_scan(cb);
-        const int tot = __shfl_sync(kFull, incl, 31);
-        const int ex = incl - cb;
-        for (int g0 = 0; g0 < tot; g0 += CH) {
-            __syncwarp();
-            const int n_here = stage_sources<T, CH>(buf, xyzm, fb, ex, tot, g0, lane);
-            __syncwarp();
-            p2p_span<T, false, K>(buf, n_here, qq, S, p, acc);
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                float lo, hi;
+                f2_unpack(A[k][v], lo, hi);
+                acc[k][v] += lo + hi;
+            }
+    } else {
+        for (int lb = beg; lb < end; lb += 32) {
+            const int e = lb + lane;
+            int fb = 0, cb = 0;
+            if (e < end) {
+                const int b = src[e];
+                if (b != a) {
+                    fb = first[b];
+                    cb = count[b];
+                }
+            }
+            const int incl = warp_incl_scan(cb);
+            const int tot = __shfl_sync(kFull, incl, 31);
+            const int ex = incl - cb;
+            for (int g0 = 0; g0 < tot; g0 += CH) {
+                __syncwarp();
+                const int n_here = stage_sources<T, CH>(buf, xyzm, fb, ex, tot, g0, lane);
+                __syncwarp();
+                p2p_span<T, false, K>(buf, n_here, qq, S, p, acc);
+            }
         }
     }
     // sum the S strides of each receiver in order of q
