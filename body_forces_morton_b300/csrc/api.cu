@@ -139,6 +139,10 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
 fmm_status alloc_lists(Plan &P, int64_t cap_frontier, int64_t cap_m2l, int64_t cap_p2p)
 {
     free_lists(P);
+    auto round_up = [](int64_t v) { return (v + kShards - 1) / kShards * kShards; };
+    cap_frontier = round_up(cap_frontier);
+    cap_m2l = round_up(cap_m2l);
+    cap_p2p = round_up(cap_p2p);
     P.cap_frontier = cap_frontier;
     P.cap_m2l = cap_m2l;
     P.cap_p2p = cap_p2p;
@@ -253,10 +257,16 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         if (st) return st;
         const unsigned cap_bits = ERR_FRONTIER | ERR_M2L_CAP | ERR_P2P_CAP;
         if (h.error & cap_bits) {
+            // sharded lists: grow to 1.5x the fullest shard (or double), times the shard count
             int64_t cf = P.cap_frontier, cm = P.cap_m2l, cp = P.cap_p2p;
-            if (h.error & ERR_FRONTIER) cf = clamp_cap(std::max(2.0 * cf, 1.5 * h.frontier_max));
-            if (h.error & ERR_M2L_CAP) cm = clamp_cap(std::max(2.0 * cm, 1.3 * h.n_m2l_pairs));
-            if (h.error & ERR_P2P_CAP) cp = clamp_cap(std::max(2.0 * cp, 1.3 * h.n_p2p_pairs));
+            int mmax = 0, pmax = 0;
+            for (int s2 = 0; s2 < kShards; ++s2) {
+                mmax = std::max(mmax, h.n_m2l_pairs[s2]);
+                pmax = std::max(pmax, h.n_p2p_pairs[s2]);
+            }
+            if (h.error & ERR_FRONTIER) cf = clamp_cap(std::max(2.0 * cf, 1.5 * kShards * (double)h.frontier_max));
+            if (h.error & ERR_M2L_CAP) cm = clamp_cap(std::max(2.0 * cm, 1.5 * kShards * (double)mmax));
+            if (h.error & ERR_P2P_CAP) cp = clamp_cap(std::max(2.0 * cp, 1.5 * kShards * (double)pmax));
             st = alloc_lists(P, cf, cm, cp);
             if (st) return st;
             P.retries++;
@@ -266,11 +276,18 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
             set_err("fmm_eval: device check failed: %s", error_bits(h.error));
             return FMM_ERR_INTERNAL;
         }
-        if (h.frontier_cnt[(2 * depth + 1) % 3] != 0) {
+        int64_t left = 0, m2l_pairs = 0, p2p_pairs = 0;
+        for (int s2 = 0; s2 < kShards; ++s2) {
+            left += h.frontier_cnt[(2 * depth + 1) % 3][s2];
+            m2l_pairs += h.n_m2l_pairs[s2];
+            p2p_pairs += h.n_p2p_pairs[s2];
+        }
+        if (left != 0) {
             set_err("fmm_eval: dual-tree walk did not finish in %d generations", 2 * depth + 1);
             return FMM_ERR_INTERNAL;
         }
-        P.n_m2l = 2ll * h.n_m2l_pairs;
+        P.n_m2l = 2 * m2l_pairs;
+        P.n_p2p_pairs = p2p_pairs;
         P.walk_pairs = h.walk_pairs;
         P.p2p_inter = h.p2p_interactions;
         P.have_eval = true;
@@ -476,7 +493,6 @@ fmm_status fmm_plan_stats(const fmm_plan *plan, fmm_stats *out)
     out->p = P.p;
     if (!P.have_eval) return FMM_OK;
     DeviceGuard g(P.device);
-    const DevCounters &h = *P.ctr_host;
     out->n_nodes = P.n_nodes;
     out->depth = P.depth;
     out->n_m2l = P.n_m2l;
@@ -492,7 +508,7 @@ fmm_status fmm_plan_stats(const fmm_plan *plan, fmm_stats *out)
             for (int v : nch) leaves += v == 0;
     }
     out->n_leaves = leaves;
-    out->n_p2p = 2ll * h.n_p2p_pairs - leaves;
+    out->n_p2p = 2 * P.n_p2p_pairs - leaves;
     static const int a[FMM_N_STAGES] = {0, 1, 2, 4, 5, 6, 7, 8, 9};
     static const int b[FMM_N_STAGES] = {1, 2, 3, 5, 6, 7, 8, 9, 10};
     for (int k = 0; k < FMM_N_STAGES; ++k) {

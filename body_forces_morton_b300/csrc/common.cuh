@@ -12,6 +12,7 @@ namespace bfm {
 constexpr int kMaxLevel = 21;        // Morton keys carry 21 bits per axis
 constexpr int kMaxP = 8;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kShards = 64;          // the walk's outputs are split into this many independently counted shards
 
 // ---- device status word bits (ORed by kernels, read by the host) ----------
 enum : unsigned {
@@ -35,10 +36,10 @@ struct DevCounters {
     double box[4];                 // root box min corner (x, y, z) and side, in the plan's dtype widened
     unsigned hist[8][256];         // radix digit histograms, one row per pass
     unsigned tile_ctr[96];         // one ticket counter per chained-scan use
-    int frontier_cnt[3];           // walk frontier sizes (cycled)
-    int frontier_max;
-    int n_m2l_pairs;
-    int n_p2p_pairs;
+    int frontier_cnt[3][64];       // walk frontier sizes per shard (cycled over 3 generations)
+    int frontier_max;              // largest shard fill seen by the walk
+    int n_m2l_pairs[64];           // unordered M2L pairs per shard
+    int n_p2p_pairs[64];           // unordered P2P pairs per shard (self pairs included)
     long long walk_pairs;
     long long p2p_interactions;
     int n_long;                    // list segments too long for the warp sort
@@ -146,6 +147,55 @@ __device__ __forceinline__ unsigned long long chained_exclusive(unsigned long lo
         --t;
     }
     flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 2, excl + aggregate));
+    return excl;
+}
+
+// The same exclusive prefix computed by a whole warp (every lane calls it, lane
+// 0's `aggregate` counts): each round reads 32 predecessors' flags at once and
+// adds them up to the nearest inclusive prefix, so the look-back takes one
+// round per 32 tiles without an inclusive prefix. Returns the prefix to every
+// lane. Bounded like chained_exclusive.
+__device__ __forceinline__ unsigned long long chained_exclusive_warp(unsigned long long *flags, int stride, int tile,
+                                                                     unsigned long long aggregate, unsigned epoch,
+                                                                     DevCounters *ctr)
+{
+    const int lane = threadIdx.x & 31;
+    if (tile == 0) {
+        if (lane == 0) flag_store(flags, flag_pack(epoch, 2, aggregate));
+        return 0;
+    }
+    if (lane == 0) flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 1, aggregate));
+    const unsigned long long ep = (unsigned long long)(epoch & 0xffffffu);
+    unsigned long long excl = 0;
+    int t = tile - 1;
+    unsigned spins = 0;
+    for (;;) {
+        const int idx = t - lane;
+        unsigned state = 2;  // before tile 0: an inclusive prefix of 0
+        unsigned long long v = 0;
+        if (idx >= 0) {
+            const unsigned long long f = flag_load(flags + (size_t)idx * stride);
+            state = (f >> 40) == ep ? (unsigned)((f >> 38) & 3u) : 0u;
+            v = f & kFlagValueMask;
+        }
+        const unsigned incl_mask = __ballot_sync(kFull, state == 2);
+        const unsigned wait_mask = __ballot_sync(kFull, state == 0);
+        const int stop = incl_mask ? __ffs(incl_mask) - 1 : 31;   // lanes 0..stop are needed
+        const unsigned need = stop == 31 ? kFull : ((2u << stop) - 1u);
+        if (wait_mask & need) {
+            if (++spins > kSpinLimit) {
+                if (lane == 0) set_error(ctr, ERR_SPIN);
+                break;
+            }
+            continue;
+        }
+        unsigned long long s = lane <= stop ? v : 0ull;
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+        excl += s;
+        if (incl_mask) break;
+        t -= 32;
+    }
+    if (lane == 0) flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 2, excl + aggregate));
     return excl;
 }
 

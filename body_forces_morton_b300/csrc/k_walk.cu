@@ -12,7 +12,7 @@
 //   never a leaf, and visit (child, other).
 // The set of pairs this produces does not depend on the visiting order, so
 // the walk runs breadth first: one kernel per frontier generation, appending
-// through warp-aggregated atomics.
+// through warp-aggregated atomics on sharded output lists.
 //
 // Lists: per-receiver counts (taken during the walk) -> exclusive scan (one
 // kernel, decoupled look-back) -> atomic fill -> every receiver's segment sorted
@@ -31,146 +31,185 @@ constexpr int CS_THREADS = 256, CS_ITEMS = 4, CS_TILE = CS_THREADS * CS_ITEMS;
 __global__ void k_walk_init(int2 *f0, DevCounters *ctr)
 {
     f0[0] = make_int2(0, 0);
-    ctr->frontier_cnt[0] = 1;
-    ctr->frontier_cnt[1] = 0;
-    ctr->frontier_cnt[2] = 0;
+    ctr->frontier_cnt[0][0] = 1;
     ctr->frontier_max = 1;
 }
 
+// Prefix over the shards of a sharded list (each shard's count clamped to its
+// capacity) into s_pre[0 .. kShards]; called by a whole block of >= 64 threads.
+// The 64 counts are read in parallel and scanned by two warps.
+__device__ __forceinline__ void shard_prefix(const int *cnt, int cap_s, int *s_pre)
+{
+    __shared__ int s_half;
+    const int t = threadIdx.x, lane = t & 31;
+    int v = 0, incl = 0;
+    if (t < kShards) {
+        v = min(cnt[t], cap_s);
+        incl = warp_incl_scan(v);
+        if (t == 31) s_half = incl;
+    }
+    __syncthreads();
+    if (t < kShards) {
+        const int add = t >= 32 ? s_half : 0;
+        s_pre[t] = add + incl - v;
+        if (t == kShards - 1) s_pre[kShards] = add + incl;
+    }
+    (void)lane;
+    __syncthreads();
+}
+
+// Storage address of element g of a sharded list (s_pre from shard_prefix).
+__device__ __forceinline__ size_t shard_addr(const int *s_pre, int g, int cap_s)
+{
+    int lo = 0;
+#pragma unroll
+    for (int step = kShards / 2; step > 0; step >>= 1)
+        if (s_pre[lo + step] <= g) lo += step;
+    return (size_t)lo * cap_s + (g - s_pre[lo]);
+}
+
 // One generation of the walk: every frontier pair is decided and its outputs
-// (an M2L pair, a P2P pair or child pairs) are appended; a block reserves the
-// space of a whole 256-pair tile with one atomic per output list.
+// (an M2L pair, a P2P pair or child pairs) are appended. Each output list is
+// split into kShards shards with their own counters; a warp appends to the
+// shard of its index with one atomic per list, so no block-wide barrier and
+// no single hot counter is involved.
 template <class T>
 __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__restrict__ fin, int2 *__restrict__ fout,
-                                                          int cap_frontier, const int *__restrict__ nchild,
+                                                          int capf_s, const int *__restrict__ nchild,
                                                           const int *__restrict__ child0,
                                                           const int *__restrict__ count,
                                                           const vec4<T> *__restrict__ nc,
                                                           const vec4<T> *__restrict__ nl, T th2, int2 *m2l_pairs,
-                                                          int cap_m2l, int2 *p2p_pairs, int cap_p2p, int *m2l_cnt,
+                                                          int capm_s, int2 *p2p_pairs, int capp_s, int *m2l_cnt,
                                                           int *p2p_cnt, DevCounters *ctr)
 {
-    __shared__ int s_wtot[3][WK_THREADS / 32];
-    __shared__ int s_base[3];
-    const int nin = ctr->frontier_cnt[it % 3];
-    int *cnt_out = &ctr->frontier_cnt[(it + 1) % 3];
-    if (blockIdx.x == 0 && threadIdx.x == 0) ctr->frontier_cnt[(it + 2) % 3] = 0;
-    const int nread = nin < cap_frontier ? nin : cap_frontier;
+    __shared__ int s_pre[kShards + 1];
+    int *cnt_in = ctr->frontier_cnt[it % 3];
+    int *cnt_out = ctr->frontier_cnt[(it + 1) % 3];
+    if (blockIdx.x == 0 && threadIdx.x < kShards) ctr->frontier_cnt[(it + 2) % 3][threadIdx.x] = 0;
+    shard_prefix(cnt_in, capf_s, s_pre);
+    const int nread = s_pre[kShards];
+    const int lane = threadIdx.x & 31;
+    const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int shard = gwarp % kShards;
     long long inter_sum = 0;
-    int visited = 0, kids_max = 0;
-    for (int base = blockIdx.x * WK_THREADS; base < nread; base += gridDim.x * WK_THREADS) {
-        const int i = base + threadIdx.x;
-        const bool valid = i < nread;
-        int A = 0, B = 0, kids = 0, split = -1, other = 0;
-        int m2l = 0, p2p = 0;
-        if (valid) {
+    int visited = 0, fill_max = 0;
+    constexpr int U = 4;  // pairs per lane per chunk: their loads overlap, one atomic per list per 128 pairs
+    for (int base = gwarp * 32 * U; base < nread; base += nwarps * 32 * U) {
+        int A[U], B[U], kids[U], split[U], other[U], m2l[U], p2p[U];
+        int2 pr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + u * 32 + lane;
+            pr[u] = i < nread ? fin[shard_addr(s_pre, i, capf_s)] : make_int2(-1, -1);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            A[u] = pr[u].x;
+            B[u] = pr[u].y;
+            kids[u] = 0;
+            split[u] = -1;
+            other[u] = 0;
+            m2l[u] = 0;
+            p2p[u] = 0;
+            if (A[u] < 0) continue;
             ++visited;
-            const int2 pr = fin[i];
-            A = pr.x;
-            B = pr.y;
-            const int nA = nchild[A];
-            if (A == B) {
+            const int nA = nchild[A[u]];
+            if (A[u] == B[u]) {
                 if (nA == 0) {
-                    p2p = 1;
-                    inter_sum += (long long)count[A] * count[A];
+                    p2p[u] = 1;
+                    inter_sum += (long long)count[A[u]] * count[A[u]];
                 } else {
-                    kids = nA * (nA + 1) / 2;
-                    split = A;
+                    kids[u] = nA * (nA + 1) / 2;
+                    split[u] = A[u];
                 }
             } else {
-                const int nB = nchild[B];
-                const vec4<T> cA = nc[A], cB = nc[B], lA = nl[A], lB = nl[B];
+                const int nB = nchild[B[u]];
+                const vec4<T> cA = nc[A[u]], cB = nc[B[u]], lA = nl[A[u]], lB = nl[B[u]];
                 const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
                 const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
                 if (s2 < mul_rn(th2, r2)) {
-                    m2l = 1;
+                    m2l[u] = 1;
                 } else if (nA == 0 && nB == 0) {
-                    p2p = 1;
-                    inter_sum += 2ll * count[A] * count[B];
+                    p2p[u] = 1;
+                    inter_sum += 2ll * count[A[u]] * count[B[u]];
                 } else {
                     const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
-                    split = splitA ? A : B;
-                    other = splitA ? B : A;
-                    kids = splitA ? nA : nB;
+                    split[u] = splitA ? A[u] : B[u];
+                    other[u] = splitA ? B[u] : A[u];
+                    kids[u] = splitA ? nA : nB;
                 }
             }
         }
-        // warp-level scans, then one exchange of the warp totals per tile
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        const int im = warp_incl_scan(m2l), ip = warp_incl_scan(p2p), ik = warp_incl_scan(kids);
-        if (lane == 31) {
-            s_wtot[0][warp] = im;
-            s_wtot[1][warp] = ip;
-            s_wtot[2][warp] = ik;
+        int sm = 0, sp = 0, sk = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) { sm += m2l[u]; sp += p2p[u]; sk += kids[u]; }
+        const int im = warp_incl_scan(sm), ip = warp_incl_scan(sp), ik = warp_incl_scan(sk);
+        const int tm = __shfl_sync(kFull, im, 31), tp = __shfl_sync(kFull, ip, 31), tk = __shfl_sync(kFull, ik, 31);
+        int bm = 0, bp = 0, bk = 0;
+        if (lane == 0) {
+            if (tm) bm = atomicAdd(&ctr->n_m2l_pairs[shard], tm);
+            if (tp) bp = atomicAdd(&ctr->n_p2p_pairs[shard], tp);
+            if (tk) bk = atomicAdd(&cnt_out[shard], tk);
         }
-        __syncthreads();
-        if (threadIdx.x < 3) {
-            const int list = threadIdx.x;
-            int run = 0;
-            for (int w2 = 0; w2 < WK_THREADS / 32; ++w2) {
-                const int t = s_wtot[list][w2];
-                s_wtot[list][w2] = run;
-                run += t;
+        bm = __shfl_sync(kFull, bm, 0) + im - sm;
+        bp = __shfl_sync(kFull, bp, 0) + ip - sp;
+        bk = __shfl_sync(kFull, bk, 0);
+        fill_max = max(fill_max, bk + tk);
+        int o = bk + ik - sk;
+        int2 *dst = fout + (size_t)shard * capf_s;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (m2l[u]) {
+                if (bm < capm_s) {
+                    m2l_pairs[(size_t)shard * capm_s + bm] = make_int2(A[u], B[u]);
+                    atomicAdd(&m2l_cnt[A[u]], 1);
+                    atomicAdd(&m2l_cnt[B[u]], 1);
+                } else {
+                    set_error(ctr, ERR_M2L_CAP);
+                }
+                ++bm;
             }
-            int *ctrp = list == 0 ? &ctr->n_m2l_pairs : (list == 1 ? &ctr->n_p2p_pairs : cnt_out);
-            const int b0 = run ? atomicAdd(ctrp, run) : 0;
-            s_base[list] = b0;
-            if (list == 2) kids_max = max(kids_max, b0 + run);
-        }
-        __syncthreads();
-        const int ex_m = s_base[0] + s_wtot[0][warp] + im - m2l;
-        const int ex_p = s_base[1] + s_wtot[1][warp] + ip - p2p;
-        const int ex_k = s_base[2] + s_wtot[2][warp] + ik - kids;
-        if (m2l) {
-            const int slot = ex_m;
-            if (slot < cap_m2l) {
-                m2l_pairs[slot] = make_int2(A, B);
-                atomicAdd(&m2l_cnt[A], 1);
-                atomicAdd(&m2l_cnt[B], 1);
-            } else {
-                set_error(ctr, ERR_M2L_CAP);
+            if (p2p[u]) {
+                if (bp < capp_s) {
+                    p2p_pairs[(size_t)shard * capp_s + bp] = make_int2(A[u], B[u]);
+                    atomicAdd(&p2p_cnt[A[u]], 1);
+                    if (A[u] != B[u]) atomicAdd(&p2p_cnt[B[u]], 1);
+                } else {
+                    set_error(ctr, ERR_P2P_CAP);
+                }
+                ++bp;
             }
-        }
-        if (p2p) {
-            const int slot = ex_p;
-            if (slot < cap_p2p) {
-                p2p_pairs[slot] = make_int2(A, B);
-                atomicAdd(&p2p_cnt[A], 1);
-                if (A != B) atomicAdd(&p2p_cnt[B], 1);
-            } else {
-                set_error(ctr, ERR_P2P_CAP);
-            }
-        }
-        if (kids) {
-            int o = ex_k;
-            const int c0 = child0[split];
-            if (A == B) {
-                const int nA = nchild[A];
-                for (int x = 0; x < nA; ++x)
-                    for (int y = x; y < nA; ++y, ++o) {
-                        if (o < cap_frontier) fout[o] = make_int2(c0 + x, c0 + y);
+            if (kids[u]) {
+                const int c0 = child0[split[u]];
+                if (A[u] == B[u]) {
+                    const int nA = nchild[A[u]];
+                    for (int x = 0; x < nA; ++x)
+                        for (int y = x; y < nA; ++y, ++o) {
+                            if (o < capf_s) dst[o] = make_int2(c0 + x, c0 + y);
+                            else set_error(ctr, ERR_FRONTIER);
+                        }
+                } else {
+                    for (int x = 0; x < kids[u]; ++x, ++o) {
+                        const int C = c0 + x;
+                        if (o < capf_s) dst[o] = C < other[u] ? make_int2(C, other[u]) : make_int2(other[u], C);
                         else set_error(ctr, ERR_FRONTIER);
                     }
-            } else {
-                for (int x = 0; x < kids; ++x, ++o) {
-                    const int C = c0 + x;
-                    if (o < cap_frontier) fout[o] = C < other ? make_int2(C, other) : make_int2(other, C);
-                    else set_error(ctr, ERR_FRONTIER);
                 }
             }
         }
-        __syncthreads();
     }
-    // per-block statistics, one atomic each
+    // per-warp statistics, one atomic each
     for (int o = 16; o > 0; o >>= 1) {
         inter_sum += __shfl_xor_sync(kFull, inter_sum, o);
         visited += __shfl_xor_sync(kFull, visited, o);
     }
-    if ((threadIdx.x & 31) == 0) {
+    if (lane == 0) {
         if (inter_sum) atomicAdd((unsigned long long *)&ctr->p2p_interactions, (unsigned long long)inter_sum);
         if (visited) atomicAdd((unsigned long long *)&ctr->walk_pairs, (unsigned long long)visited);
+        if (fill_max) atomicMax(&ctr->frontier_max, fill_max);
     }
-    if (threadIdx.x == 2 && kids_max) atomicMax(&ctr->frontier_max, kids_max);
 }
 
 // Exclusive scan of the per-receiver counts into CSR offsets (both lists at once).
@@ -202,11 +241,15 @@ __global__ __launch_bounds__(CS_THREADS) void k_csr_scan(int n_nodes, const int 
         const int ia = warp_incl_scan(sa), ib = warp_incl_scan(sb);
         if (lane == 31) { s_w[0][warp] = ia; s_w[1][warp] = ib; }
         __syncthreads();
-        if (tid < 2) {
+        if (warp < 2) {
             int tot = 0;
-            for (int w = 0; w < CS_THREADS / 32; ++w) tot += s_w[tid][w];
-            s_ex[tid] = (long long)chained_exclusive(flags + tid, 2, tile, (unsigned long long)tot, epoch, ctr);
-            if (tile == ntiles - 1) (tid == 0 ? m2l_off : p2p_off)[n_nodes] = (int)(s_ex[tid] + tot);
+            for (int w = 0; w < CS_THREADS / 32; ++w) tot += s_w[warp][w];
+            const long long ex = (long long)chained_exclusive_warp(flags + warp, 2, tile, (unsigned long long)tot,
+                                                                   epoch, ctr);
+            if (lane == 0) {
+                s_ex[warp] = ex;
+                if (tile == ntiles - 1) (warp == 0 ? m2l_off : p2p_off)[n_nodes] = (int)(ex + tot);
+            }
         }
         __syncthreads();
         int wa = 0, wb = 0;
@@ -228,19 +271,22 @@ __global__ __launch_bounds__(CS_THREADS) void k_csr_scan(int n_nodes, const int 
 
 // Scatter the unordered pairs into their receivers' segments. The counts are
 // used as countdown cursors and end at zero, ready for the next evaluation.
-__global__ void k_csr_fill(const int2 *__restrict__ m2l_pairs, int cap_m2l, const int2 *__restrict__ p2p_pairs,
-                           int cap_p2p, int *m2l_cnt, int *p2p_cnt, const int *__restrict__ m2l_off,
+__global__ void k_csr_fill(const int2 *__restrict__ m2l_pairs, int capm_s, const int2 *__restrict__ p2p_pairs,
+                           int capp_s, int *m2l_cnt, int *p2p_cnt, const int *__restrict__ m2l_off,
                            const int *__restrict__ p2p_off, int *__restrict__ m2l_src, int *__restrict__ p2p_src,
                            const DevCounters *ctr)
 {
-    const int nm = min(ctr->n_m2l_pairs, cap_m2l), np = min(ctr->n_p2p_pairs, cap_p2p);
+    __shared__ int pm[kShards + 1], pp[kShards + 1];
+    shard_prefix(ctr->n_m2l_pairs, capm_s, pm);
+    shard_prefix(ctr->n_p2p_pairs, capp_s, pp);
+    const int nm = pm[kShards], np = pp[kShards];
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nm + np; i += gridDim.x * blockDim.x) {
         if (i < nm) {
-            const int2 pr = m2l_pairs[i];
+            const int2 pr = m2l_pairs[shard_addr(pm, i, capm_s)];
             m2l_src[m2l_off[pr.x] + atomicSub(&m2l_cnt[pr.x], 1) - 1] = pr.y;
             m2l_src[m2l_off[pr.y] + atomicSub(&m2l_cnt[pr.y], 1) - 1] = pr.x;
         } else {
-            const int2 pr = p2p_pairs[i - nm];
+            const int2 pr = p2p_pairs[shard_addr(pp, i - nm, capp_s)];
             p2p_src[p2p_off[pr.x] + atomicSub(&p2p_cnt[pr.x], 1) - 1] = pr.y;
             if (pr.x != pr.y) p2p_src[p2p_off[pr.y] + atomicSub(&p2p_cnt[pr.y], 1) - 1] = pr.x;
         }
@@ -334,6 +380,7 @@ __device__ __forceinline__ void sort_list_regs(int *src, int len)
 // SEG_WARP_MAX in shared memory, longer ones go to a second pass.
 __global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restrict__ m2l_off, int *m2l_src,
                                                  const int *__restrict__ p2p_off, int *p2p_src, int *long_seg,
+                                                 const int *__restrict__ count, uint8_t *__restrict__ key,
                                                  DevCounters *ctr)
 {
     __shared__ int buf[8][SEG_WARP_MAX];
@@ -346,6 +393,24 @@ __global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restr
         const int beg = isp ? p2p_off[a] : m2l_off[a];
         const int len = (isp ? p2p_off[a + 1] : m2l_off[a + 1]) - beg;
         int *src = (isp ? p2p_src : m2l_src) + beg;
+        // work bucket of this receiver (see k_order_scatter): P2P work = count * sum of the
+        // source leaves' counts, M2L work = list length; bucket floor(log2(work)) + 1, 0 for none
+        {
+            int k;
+            if (isp) {
+                long long s = 0;
+                for (int e = lane; e < len; e += 32) s += count[src[e]];
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+                const long long work = s * count[a];
+                k = work > 0 ? 64 - __clzll(work) : 0;
+            } else {
+                k = len > 0 ? 32 - __clz(len) : 0;
+            }
+            if (lane == 0) {
+                key[(isp ? 0 : n_nodes) + a] = (uint8_t)k;
+                if (k || !isp) atomicAdd(&ctr->order_cnt[isp ? 0 : 1][k], 1);
+            }
+        }
         if (len <= 1) continue;
         if (len <= 32) { sort_list_regs<1>(src, len); continue; }
         if (len <= 64) { sort_list_regs<2>(src, len); continue; }
@@ -418,41 +483,15 @@ __global__ __launch_bounds__(1024) void k_segsort_long(const int *__restrict__ m
 }
 
 // Work order of the receivers, heaviest first: bucket b = floor(log2(work)) + 1
-// (0 for no work), buckets taken in decreasing b. P2P work of a leaf is
-// count * (sum of its source leaves' counts); M2L work of a node is its list
-// length. The order decides only which warp takes which receiver, never a result.
-__global__ __launch_bounds__(256) void k_order_count(int n_nodes, const int *__restrict__ count,
-                                                     const int *__restrict__ nchild, const int *__restrict__ m2l_off,
-                                                     const int *__restrict__ p2p_off, const int *__restrict__ p2p_src,
-                                                     uint8_t *__restrict__ key, DevCounters *ctr)
-{
-    const int lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
-        long long work = 0;
-        if (nchild[a] == 0) {
-            const int beg = p2p_off[a], end = p2p_off[a + 1];
-            long long s = 0;
-            for (int e = beg + lane; e < end; e += 32) s += count[p2p_src[e]];
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-            work = s * count[a];
-        }
-        if (lane == 0) {
-            const int kp = work > 0 ? 64 - __clzll(work) : 0;
-            const int len = m2l_off[a + 1] - m2l_off[a];
-            const int km = len > 0 ? 32 - __clz(len) : 0;
-            key[a] = (uint8_t)kp;
-            key[n_nodes + a] = (uint8_t)km;
-            if (kp) atomicAdd(&ctr->order_cnt[0][kp], 1);
-            atomicAdd(&ctr->order_cnt[1][km], 1);
-        }
-    }
-}
-
+// (0 for no work), buckets taken in decreasing b (keys written by k_segsort).
+// The order decides only which warp takes which receiver, never a result, so
+// positions inside a bucket may come in any order: a block counts its nodes
+// per bucket in shared memory and reserves their places with one atomic per
+// bucket.
 __global__ __launch_bounds__(256) void k_order_scatter(int n_nodes, const uint8_t *__restrict__ key, int *order,
                                                        DevCounters *ctr)
 {
-    __shared__ int base[2][64];
+    __shared__ int base[2][64], s_cnt[2][64], s_pos[2][64];
     const int tid = (int)threadIdx.x;
     if (tid < 2) {
         const int lowest = tid == 0 ? 1 : 0;  // P2P skips bucket 0 (no work); M2L keeps it, last
@@ -462,11 +501,29 @@ __global__ __launch_bounds__(256) void k_order_scatter(int n_nodes, const uint8_
             run += ctr->order_cnt[tid][b];
         }
     }
-    __syncthreads();
-    for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n_nodes; a += gridDim.x * blockDim.x) {
-        const int kp = key[a], km = key[n_nodes + a];
-        if (kp) order[base[0][kp] + atomicAdd(&ctr->order_cur[0][kp], 1)] = a;
-        order[n_nodes + base[1][km] + atomicAdd(&ctr->order_cur[1][km], 1)] = a;
+    for (int a0 = blockIdx.x * blockDim.x; a0 < n_nodes; a0 += gridDim.x * blockDim.x) {
+        if (tid < 128) (&s_cnt[0][0])[tid] = 0;
+        __syncthreads();
+        const int a = a0 + tid;
+        int kp = 0, km = 0, rp = -1, rm = -1;
+        if (a < n_nodes) {
+            kp = key[a];
+            km = key[n_nodes + a];
+            if (kp) rp = atomicAdd(&s_cnt[0][kp], 1);
+            rm = atomicAdd(&s_cnt[1][km], 1);
+        }
+        __syncthreads();
+        if (tid < 128) {
+            const int list = tid >> 6, b = tid & 63;
+            const int c = s_cnt[list][b];
+            s_pos[list][b] = c ? base[list][b] + atomicAdd(&ctr->order_cur[list][b], c) : 0;
+        }
+        __syncthreads();
+        if (a < n_nodes) {
+            if (kp) order[s_pos[0][kp] + rp] = a;
+            order[n_nodes + s_pos[1][km] + rm] = a;
+        }
+        __syncthreads();
     }
 }
 
@@ -478,9 +535,9 @@ int launch_walk_t(Plan &P, int depth, cudaStream_t s)
     const int iters = 2 * depth + 1;
     for (int it = 0; it < iters; ++it) {
         k_walk_iter<T><<<P.num_sms * 8, WK_THREADS, 0, s>>>(
-            it, P.frontier[it & 1], P.frontier[(it + 1) & 1], (int)P.cap_frontier, P.node_nchild, P.node_child0,
-            P.node_count, (const vec4<T> *)P.node_c, (const vec4<T> *)P.node_l, th2, P.m2l_pairs, (int)P.cap_m2l,
-            P.p2p_pairs, (int)P.cap_p2p, P.m2l_cnt, P.p2p_cnt, P.ctr);
+            it, P.frontier[it & 1], P.frontier[(it + 1) & 1], (int)(P.cap_frontier / kShards), P.node_nchild,
+            P.node_child0, P.node_count, (const vec4<T> *)P.node_c, (const vec4<T> *)P.node_l, th2, P.m2l_pairs,
+            (int)(P.cap_m2l / kShards), P.p2p_pairs, (int)(P.cap_p2p / kShards), P.m2l_cnt, P.p2p_cnt, P.ctr);
     }
     return iters + 1;
 }
@@ -499,14 +556,14 @@ int launch_lists(Plan &P, cudaStream_t s)
     const unsigned ep = P.next_epoch();
     k_csr_scan<<<P.num_sms * 4, CS_THREADS, 0, s>>>(nn, P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off, P.flags, ep, slot,
                                                     P.ctr);
-    k_csr_fill<<<P.num_sms * 8, 256, 0, s>>>(P.m2l_pairs, (int)P.cap_m2l, P.p2p_pairs, (int)P.cap_p2p, P.m2l_cnt,
-                                             P.p2p_cnt, P.m2l_off, P.p2p_off, P.m2l_src, P.p2p_src, P.ctr);
-    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(nn, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
+    k_csr_fill<<<P.num_sms * 8, 256, 0, s>>>(P.m2l_pairs, (int)(P.cap_m2l / kShards), P.p2p_pairs,
+                                             (int)(P.cap_p2p / kShards), P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off,
+                                             P.m2l_src, P.p2p_src, P.ctr);
+    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(nn, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
+                                            P.node_count, P.order_key, P.ctr);
     k_segsort_long<<<P.num_sms, 1024, 0, s>>>(P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
-    k_order_count<<<P.num_sms * 8, 256, 0, s>>>(nn, P.node_count, P.node_nchild, P.m2l_off, P.p2p_off, P.p2p_src,
-                                               P.order_key, P.ctr);
     k_order_scatter<<<P.num_sms * 4, 256, 0, s>>>(nn, P.order_key, P.order, P.ctr);
-    return 6;
+    return 5;
 }
 
 }  // namespace bfm

@@ -77,7 +77,7 @@ struct Plan {
     int launches = 0;
     int retries = 0;
     int depth = 0;
-    int64_t n_nodes = 0, n_leaves = 0, n_m2l = 0, n_p2p = 0, p2p_inter = 0, walk_pairs = 0;
+    int64_t n_nodes = 0, n_leaves = 0, n_m2l = 0, n_p2p = 0, n_p2p_pairs = 0, p2p_inter = 0, walk_pairs = 0;
     bool have_eval = false;
     double stage_ms[16] = {};
     double total_ms = 0;
