@@ -70,9 +70,9 @@ __device__ __forceinline__ size_t shard_addr(const int *s_pre, int g, int cap_s)
 
 // One generation of the walk: every frontier pair is decided and its outputs
 // (an M2L pair, a P2P pair or child pairs) are appended. Each output list is
-// split into kShards shards with their own counters; a warp appends to the
-// shard of its index with one atomic per list, so no block-wide barrier and
-// no single hot counter is involved.
+// split into kShards shards with their own counters; a block reserves the
+// space of a whole 256-pair tile in the shard of its index with one atomic per
+// list, so no single counter is hot.
 template <class T>
 __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__restrict__ fin, int2 *__restrict__ fout,
                                                           int capf_s, const int *__restrict__ nchild,
@@ -90,115 +90,109 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
     shard_prefix(cnt_in, capf_s, s_pre);
     const int nread = s_pre[kShards];
     const int lane = threadIdx.x & 31;
-    const int gwarp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    const int shard = gwarp % kShards;
+    __shared__ int s_wtot[3][WK_THREADS / 32];
+    __shared__ int s_base[3];
     long long inter_sum = 0;
     int visited = 0, fill_max = 0;
-    constexpr int U = 4;  // pairs per lane per chunk: their loads overlap, one atomic per list per 128 pairs
-    for (int base = gwarp * 32 * U; base < nread; base += nwarps * 32 * U) {
-        int A[U], B[U], kids[U], split[U], other[U], m2l[U], p2p[U];
-        int2 pr[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = base + u * 32 + lane;
-            pr[u] = i < nread ? fin[shard_addr(s_pre, i, capf_s)] : make_int2(-1, -1);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            A[u] = pr[u].x;
-            B[u] = pr[u].y;
-            kids[u] = 0;
-            split[u] = -1;
-            other[u] = 0;
-            m2l[u] = 0;
-            p2p[u] = 0;
-            if (A[u] < 0) continue;
+    const int warp = threadIdx.x >> 5;
+    const int bshard = blockIdx.x % kShards;
+    for (int base = blockIdx.x * WK_THREADS; base < nread; base += gridDim.x * WK_THREADS) {
+        const int i = base + threadIdx.x;
+        int A = -1, B = -1, kids = 0, split = -1, other = 0, m2l = 0, p2p = 0;
+        if (i < nread) {
+            const int2 pr = fin[shard_addr(s_pre, i, capf_s)];
+            A = pr.x;
+            B = pr.y;
             ++visited;
-            const int nA = nchild[A[u]];
-            if (A[u] == B[u]) {
+            const int nA = nchild[A];
+            if (A == B) {
                 if (nA == 0) {
-                    p2p[u] = 1;
-                    inter_sum += (long long)count[A[u]] * count[A[u]];
+                    p2p = 1;
+                    inter_sum += (long long)count[A] * count[A];
                 } else {
-                    kids[u] = nA * (nA + 1) / 2;
-                    split[u] = A[u];
+                    kids = nA * (nA + 1) / 2;
+                    split = A;
                 }
             } else {
-                const int nB = nchild[B[u]];
-                const vec4<T> cA = nc[A[u]], cB = nc[B[u]], lA = nl[A[u]], lB = nl[B[u]];
+                const int nB = nchild[B];
+                const vec4<T> cA = nc[A], cB = nc[B], lA = nl[A], lB = nl[B];
                 const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
                 const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
                 if (s2 < mul_rn(th2, r2)) {
-                    m2l[u] = 1;
+                    m2l = 1;
                 } else if (nA == 0 && nB == 0) {
-                    p2p[u] = 1;
-                    inter_sum += 2ll * count[A[u]] * count[B[u]];
+                    p2p = 1;
+                    inter_sum += 2ll * count[A] * count[B];
                 } else {
                     const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
-                    split[u] = splitA ? A[u] : B[u];
-                    other[u] = splitA ? B[u] : A[u];
-                    kids[u] = splitA ? nA : nB;
+                    split = splitA ? A : B;
+                    other = splitA ? B : A;
+                    kids = splitA ? nA : nB;
                 }
             }
         }
-        int sm = 0, sp = 0, sk = 0;
-#pragma unroll
-        for (int u = 0; u < U; ++u) { sm += m2l[u]; sp += p2p[u]; sk += kids[u]; }
-        const int im = warp_incl_scan(sm), ip = warp_incl_scan(sp), ik = warp_incl_scan(sk);
-        const int tm = __shfl_sync(kFull, im, 31), tp = __shfl_sync(kFull, ip, 31), tk = __shfl_sync(kFull, ik, 31);
-        int bm = 0, bp = 0, bk = 0;
-        if (lane == 0) {
-            if (tm) bm = atomicAdd(&ctr->n_m2l_pairs[shard], tm);
-            if (tp) bp = atomicAdd(&ctr->n_p2p_pairs[shard], tp);
-            if (tk) bk = atomicAdd(&cnt_out[shard], tk);
+        // warp scans, then one exchange of the warp totals and one atomic per list per tile
+        const int im = warp_incl_scan(m2l), ip = warp_incl_scan(p2p), ik = warp_incl_scan(kids);
+        if (lane == 31) {
+            s_wtot[0][warp] = im;
+            s_wtot[1][warp] = ip;
+            s_wtot[2][warp] = ik;
         }
-        bm = __shfl_sync(kFull, bm, 0) + im - sm;
-        bp = __shfl_sync(kFull, bp, 0) + ip - sp;
-        bk = __shfl_sync(kFull, bk, 0);
-        fill_max = max(fill_max, bk + tk);
-        int o = bk + ik - sk;
-        int2 *dst = fout + (size_t)shard * capf_s;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (m2l[u]) {
-                if (bm < capm_s) {
-                    m2l_pairs[(size_t)shard * capm_s + bm] = make_int2(A[u], B[u]);
-                    atomicAdd(&m2l_cnt[A[u]], 1);
-                    atomicAdd(&m2l_cnt[B[u]], 1);
-                } else {
-                    set_error(ctr, ERR_M2L_CAP);
-                }
-                ++bm;
+        __syncthreads();
+        if (threadIdx.x < 3) {
+            const int list = threadIdx.x;
+            int run = 0;
+            for (int w2 = 0; w2 < WK_THREADS / 32; ++w2) {
+                const int t = s_wtot[list][w2];
+                s_wtot[list][w2] = run;
+                run += t;
             }
-            if (p2p[u]) {
-                if (bp < capp_s) {
-                    p2p_pairs[(size_t)shard * capp_s + bp] = make_int2(A[u], B[u]);
-                    atomicAdd(&p2p_cnt[A[u]], 1);
-                    if (A[u] != B[u]) atomicAdd(&p2p_cnt[B[u]], 1);
-                } else {
-                    set_error(ctr, ERR_P2P_CAP);
-                }
-                ++bp;
+            int *ctrp = list == 0 ? &ctr->n_m2l_pairs[bshard] : (list == 1 ? &ctr->n_p2p_pairs[bshard] : &cnt_out[bshard]);
+            const int b0 = run ? atomicAdd(ctrp, run) : 0;
+            s_base[list] = b0;
+            if (list == 2) fill_max = max(fill_max, b0 + run);
+        }
+        __syncthreads();
+        if (m2l) {
+            const int slot = s_base[0] + s_wtot[0][warp] + im - 1;
+            if (slot < capm_s) {
+                m2l_pairs[(size_t)bshard * capm_s + slot] = make_int2(A, B);
+                atomicAdd(&m2l_cnt[A], 1);
+                atomicAdd(&m2l_cnt[B], 1);
+            } else {
+                set_error(ctr, ERR_M2L_CAP);
             }
-            if (kids[u]) {
-                const int c0 = child0[split[u]];
-                if (A[u] == B[u]) {
-                    const int nA = nchild[A[u]];
-                    for (int x = 0; x < nA; ++x)
-                        for (int y = x; y < nA; ++y, ++o) {
-                            if (o < capf_s) dst[o] = make_int2(c0 + x, c0 + y);
-                            else set_error(ctr, ERR_FRONTIER);
-                        }
-                } else {
-                    for (int x = 0; x < kids[u]; ++x, ++o) {
-                        const int C = c0 + x;
-                        if (o < capf_s) dst[o] = C < other[u] ? make_int2(C, other[u]) : make_int2(other[u], C);
+        }
+        if (p2p) {
+            const int slot = s_base[1] + s_wtot[1][warp] + ip - 1;
+            if (slot < capp_s) {
+                p2p_pairs[(size_t)bshard * capp_s + slot] = make_int2(A, B);
+                atomicAdd(&p2p_cnt[A], 1);
+                if (A != B) atomicAdd(&p2p_cnt[B], 1);
+            } else {
+                set_error(ctr, ERR_P2P_CAP);
+            }
+        }
+        if (kids) {
+            int o = s_base[2] + s_wtot[2][warp] + ik - kids;
+            int2 *dst = fout + (size_t)bshard * capf_s;
+            const int c0 = child0[split];
+            if (A == B) {
+                const int nA = nchild[A];
+                for (int x = 0; x < nA; ++x)
+                    for (int y = x; y < nA; ++y, ++o) {
+                        if (o < capf_s) dst[o] = make_int2(c0 + x, c0 + y);
                         else set_error(ctr, ERR_FRONTIER);
                     }
+            } else {
+                for (int x = 0; x < kids; ++x, ++o) {
+                    const int C = c0 + x;
+                    if (o < capf_s) dst[o] = C < other ? make_int2(C, other) : make_int2(other, C);
+                    else set_error(ctr, ERR_FRONTIER);
                 }
             }
         }
+        __syncthreads();
     }
     // per-warp statistics, one atomic each
     for (int o = 16; o > 0; o >>= 1) {
@@ -208,8 +202,8 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__
     if (lane == 0) {
         if (inter_sum) atomicAdd((unsigned long long *)&ctr->p2p_interactions, (unsigned long long)inter_sum);
         if (visited) atomicAdd((unsigned long long *)&ctr->walk_pairs, (unsigned long long)visited);
-        if (fill_max) atomicMax(&ctr->frontier_max, fill_max);
     }
+    if (threadIdx.x == 2 && fill_max) atomicMax(&ctr->frontier_max, fill_max);
 }
 
 // Exclusive scan of the per-receiver counts into CSR offsets (both lists at once).
