@@ -162,6 +162,44 @@ def flush_l2(buf):
     buf.fill_(1.0)
 
 
+def aggregate_over_ranks(local_ms: float, n_local: int, world: int, dist=None, device=None):
+    """Whole-job throughput of independent replicas: every rank timed its own
+    evaluations; the job takes as long as the slowest rank (max over ranks), and
+    all ranks' particles count. Returns (value particles/s, max ms)."""
+    total = float(local_ms)
+    if dist is not None and world > 1:
+        import torch
+
+        t = torch.tensor([total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    return world * n_local / (total / 1e3), total
+
+
+def bench_kdk(w, steps, warmup, torch, native, stream):
+    """Particles/s per kick-drift-kick step (one force evaluation per step, the
+    step's first kick reuses the cached acceleration)."""
+    g = W.generate(w)
+    tdt = torch.float32 if w.dtype == "f32" else torch.float64
+    pos = torch.from_numpy(g["pos"]).to("cuda", tdt)
+    vel = torch.from_numpy(g["vel"]).to("cuda", tdt)
+    mass = torch.from_numpy(g["mass"]).to("cuda", tdt)
+    with native.Plan(w.n, w.p, w.theta, w.leaf, w.dtype) as plan, torch.cuda.stream(stream):
+        for _ in range(warmup):
+            plan.kdk_step(pos, vel, mass, 1e-3, stream=stream)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            plan.kdk_step(pos, vel, mass, 1e-3, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+    return {"value": w.n / (ms / 1e3), "unit": "particles/s per KDK step", "ms_per_step": ms, "dtype": w.dtype,
+            "p": w.p, "theta": w.theta, "leaf": w.leaf, "n": w.n}
+
+
 def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_override=None):
     """Times `steps` evaluations; returns dict with per-step ms, stage ms, stats."""
     n = n_override or w.n
@@ -239,13 +277,9 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
-    total_ms = float(np.sum(res["step_ms"]))
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * res["n"] / (ms_per_step / 1e3)
+    value, total_ms = aggregate_over_ranks(float(np.sum(res["step_ms"])) / args.steps, res["n"], world, dist,
+                                           device="cuda")
+    ms_per_step = total_ms
 
     # secondary point: N = 1e5 fp64 Plummer
     also = {}
@@ -257,6 +291,8 @@ def run_ours(args, rank, world, local_rank):
                          "stage_ms": r3["stage_ms"], "dtype": "f64", "p": w3.p, "theta": w3.theta, "leaf": w3.leaf,
                          "m2l_roofline": m2l_roofline(r3, w3)}
         r3["plan"].close()
+        w5 = W.WORKLOADS[5]
+        also[w5.name] = bench_kdk(w5, max(3, args.steps // 2), args.warmup, torch, native, stream)
 
     e2e = None
     if not args.no_e2e:
@@ -294,10 +330,10 @@ def run_ours(args, rank, world, local_rank):
         "kernel_src": src_hash,
     }
     if rank == 0 and not args.no_cpu:
-        v, t = time_oracle(w, args.cpu_sample)
+        v, t = time_oracle(w, args.cpu_sample, steps=3)
         line["cpu_baseline"] = {"value": v, "unit": "particles/s", "cores": cpu_cores(), "kind": "oracle",
-                                "sample": f"full oracle FMM on N={args.cpu_sample} particles of the {w.name} "
-                                          f"recipe ({t:.1f} s)"}
+                                "sample": f"full oracle FMM (fp64 expansions, OpenMP) on N={args.cpu_sample} "
+                                          f"particles of the {w.name} recipe, median of 3 runs ({t:.1f} s each)"}
     res["plan"].close()
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -316,6 +317,15 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     if (!(theta > 0.0) || theta > 1.0) { set_err("fmm_plan_create: theta must be in (0, 1]"); return nullptr; }
     if (leaf < 1) { set_err("fmm_plan_create: leaf must be >= 1"); return nullptr; }
     if (dtype != FMM_F32 && dtype != FMM_F64) { set_err("fmm_plan_create: unknown dtype"); return nullptr; }
+    // Host-side fault injection for tests (no GPU fault is ever provoked):
+    //   BFM_FMM_FAULT=alloc     creation fails as if a device allocation had failed;
+    //   BFM_FMM_FAULT=capacity  buffers start minimal, so evaluations exercise the regrowth path.
+    const char *fault = getenv("BFM_FMM_FAULT");
+    if (fault && strcmp(fault, "alloc") == 0) {
+        set_err("fmm_plan_create: device allocation failed (injected by BFM_FMM_FAULT=alloc)");
+        return nullptr;
+    }
+    const bool minimal = fault && strcmp(fault, "capacity") == 0;
     fmm_plan *h = new (std::nothrow) fmm_plan();
     if (!h) { set_err("fmm_plan_create: out of host memory"); return nullptr; }
     Plan &P = h->P;
@@ -344,9 +354,10 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         return fail(FMM_ERR_OOM);
     for (int i = 0; i < kNumEvents; ++i)
         if (!ok(cudaEventCreate(&P.ev[i]), "events")) return fail(FMM_ERR_CUDA);
-    const int64_t cap = node_estimate(P);
+    const int64_t cap = minimal ? 1024 : node_estimate(P);
     if (alloc_nodes(P, cap) != FMM_OK) return fail(FMM_ERR_OOM);
-    if (alloc_lists(P, clamp_cap(8.0 * cap), clamp_cap(48.0 * cap), clamp_cap(12.0 * cap)) != FMM_OK)
+    const double lf = minimal ? 1.0 / 16 : 1.0;
+    if (alloc_lists(P, clamp_cap(8.0 * lf * cap), clamp_cap(48.0 * lf * cap), clamp_cap(12.0 * lf * cap)) != FMM_OK)
         return fail(FMM_ERR_OOM);
     return h;
 }
