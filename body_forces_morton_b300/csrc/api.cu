@@ -161,7 +161,7 @@ void destroy_plan(Plan &P)
     free_nodes(P);
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
-    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.scratch); dfree(P.ctr);
+    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.rel); dfree(P.scratch); dfree(P.ctr);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     if (P.ctr_host) cudaFreeHost(P.ctr_host);
     for (int i = 0; i < kNumEvents; ++i)
@@ -349,6 +349,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
         !ok(dalloc(P.idx[0], nn), "perm") || !ok(dalloc(P.idx[1], nn), "perm") ||
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
+        (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);

@@ -447,11 +447,15 @@ int launch_leaf_tp(Plan &P_, void *acc, void *pot, cudaStream_t s)
     k_l2p<T, P><<<P_.num_sms * 8, 256, 0, s>>>((int)P_.n_nodes, P_.node_first, P_.node_count, P_.node_nchild,
                                                (const vec4<T> *)P_.xyzm, (const vec4<T> *)P_.node_c,
                                                (const T *)P_.L, P_.ncp, (vec4<T> *)P_.far);
-    k_p2p<T><<<P_.num_sms * 16, LF_WARPS * 32, 0, s>>>(P_.ctr, P_.order, P_.ctr, P_.node_first, P_.node_count,
-                                                       P_.node_nchild, (const vec4<T> *)P_.xyzm, P_.idx[0],
-                                                       (const vec4<T> *)P_.far, P_.p2p_off, P_.p2p_src, (T *)acc,
-                                                       (T *)pot);
-    return 2;
+    if constexpr (sizeof(T) == 8) {
+        return 1 + launch_p2p_df(P_, acc, pot, s);
+    } else {
+        k_p2p<T><<<P_.num_sms * 16, LF_WARPS * 32, 0, s>>>(P_.ctr, P_.order, P_.ctr, P_.node_first, P_.node_count,
+                                                           P_.node_nchild, (const vec4<T> *)P_.xyzm, P_.idx[0],
+                                                           (const vec4<T> *)P_.far, P_.p2p_off, P_.p2p_src,
+                                                           (T *)acc, (T *)pot);
+        return 2;
+    }
 }
 
 #define BFM_DISPATCH_P(fn, T, ...)                        \

@@ -33,6 +33,7 @@ struct Plan {
     void *xyzm = nullptr;          // sorted particles, vec4<T> (x, y, z, m)
     void *far = nullptr;           // far field at the sorted particles, vec4<T> (phi, ax, ay, az)
     uint8_t *div = nullptr;        // divergence level of consecutive sorted keys
+    void *rel = nullptr;           // fp64 plans: leaf-relative particles as double-float float4 [2][N]
 
     // node buffers
     int *node_first = nullptr, *node_count = nullptr, *node_child0 = nullptr, *node_nchild = nullptr;
@@ -97,6 +98,7 @@ int launch_lists(Plan &P, cudaStream_t s);
 int launch_m2l(Plan &P, cudaStream_t s);
 int launch_l2l(Plan &P, int depth, cudaStream_t s);
 int launch_leaf(Plan &P, void *acc, void *pot, cudaStream_t s);
+int launch_p2p_df(Plan &P, void *acc, void *pot, cudaStream_t s);
 int launch_kick(Plan &P, void *vel, const void *acc, double h, cudaStream_t s);
 int launch_drift(Plan &P, void *pos, const void *vel, double dt, cudaStream_t s);
 int launch_lattice_axpy(Plan &P, void *y, const void *x, double h, int e_y, int e_inc, cudaStream_t s);

@@ -177,3 +177,31 @@ def test_error_paths():
         pos[17, 1] = 0.5
         pl.eval(pos, mass, acc)  # the plan stays usable after an error
         assert torch.isfinite(acc).all()
+
+
+@pytest.mark.parametrize("scale,shift,mscale", [(1e-12, 0.0, 1.0), (1e9, 0.0, 1e-20), (1.0, 1e6, 1e25),
+                                                (3e-30, 7e-29, 1e-3)])
+def test_fp64_units_extreme_scales(scale, shift, mscale):
+    """The fp64 near field runs in power-of-two units of the root box and the
+    total mass; far from unit scales the result still matches the oracle."""
+    g = W.generate(W.WORKLOADS[2], n=3000)
+    full_parity(g["pos"] * scale + shift, g["mass"] * mscale, 4, 0.7, 32, check_coeffs=False)
+
+
+@pytest.mark.parametrize("same_leaf", [False, True])
+def test_fp64_close_pair(same_leaf):
+    """Two particles 8e-15 apart (below 2^-42 of the box, where the near field
+    switches to its wide-range form): across the root's midplane, so in
+    different leaves, or inside one leaf."""
+    rng = np.random.default_rng(3)
+    pos = rng.random((600, 3))
+    pos[2], pos[3] = 0.0, 1.0                     # root cube [0, 1]^3 exactly
+    x0 = 0.5 if not same_leaf else 0.3
+    pos[0] = [x0 - 4e-15, 0.3, 0.3]
+    pos[1] = [x0 + 4e-15, 0.3, 0.3]
+    mass = np.full(600, 1.0 / 600)
+    e, r, _ = full_parity(pos, mass, 4, 0.7, 8, check_coeffs=False)
+    leaf_of = np.empty(600, int)
+    for a in np.flatnonzero(r.nchild == 0):
+        leaf_of[r.perm[r.first[a]:r.first[a] + r.count[a]]] = a
+    assert (leaf_of[0] == leaf_of[1]) == same_leaf
