@@ -84,7 +84,7 @@ void free_nodes(Plan &P)
                     &P.node_level, &P.node_done,  &P.m2l_cnt,     &P.p2p_cnt,     &P.m2l_off,
                     &P.p2p_off,    &P.long_seg,    &P.order};
     for (int **q : ints) { dfree(*q); *q = nullptr; }
-    void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L};
+    void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L, &P.Mdf};
     for (void **q : vs) { dfree(*q); *q = nullptr; }
     dfree(P.flags);
     P.flags = nullptr;
@@ -127,6 +127,7 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
     CUDA_TRY(cudaMalloc(&P.M, (size_t)P.ncp * c * e));
     CUDA_TRY(cudaMalloc(&P.Lm2l, (size_t)P.ncp * c * e));
     CUDA_TRY(cudaMalloc(&P.L, (size_t)P.ncp * c * e));
+    if (P.dtype == 1 && P.p <= kMaxPDf) CUDA_TRY(cudaMalloc(&P.Mdf, (size_t)P.ncp * c * 2 * sizeof(float)));
     CUDA_TRY(cudaMemset(P.m2l_cnt, 0, c * sizeof(int)));
     CUDA_TRY(cudaMemset(P.p2p_cnt, 0, c * sizeof(int)));
     const int64_t tiles_sort = (P.n + RS_TILE - 1) / RS_TILE;

@@ -226,11 +226,13 @@ __device__ __forceinline__ int warp_incl_scan(int v)
     return v;
 }
 
-// Sum v over the 32 lanes and write the NC sums to dst: three halving steps
-// (offsets 16, 8, 4) leave each lane NR/8 partial sums of its own coefficient
-// block, two butterfly steps (2, 1) finish them. Fixed order, so reproducible.
-template <class T, int NR, int NC>
-__device__ __forceinline__ void reduce_store(T (&v)[NR], int lane, T *__restrict__ dst)
+// Sum v over the 32 lanes and hand the NC sums to store(k, sum): three halving
+// steps (offsets 16, 8, 4) leave each lane NR/8 partial sums of its own
+// coefficient block, two butterfly steps (2, 1) finish them; lane 4 j then
+// stores its block. Fixed order, so reproducible, and the same lane always
+// stores the same k.
+template <class T, int NR, int NC, class F>
+__device__ __forceinline__ void reduce_apply(T (&v)[NR], int lane, F &&store)
 {
     constexpr int H1 = NR / 2, H2 = NR / 4, H3 = NR / 8;
     T a[H1], b[H2], c[H3];
@@ -259,8 +261,14 @@ __device__ __forceinline__ void reduce_store(T (&v)[NR], int lane, T *__restrict
         const int base = (u4 ? H1 : 0) + (u3 ? H2 : 0) + (u2 ? H3 : 0);
 #pragma unroll
         for (int i = 0; i < H3; ++i)
-            if (base + i < NC) dst[base + i] = c[i];
+            if (base + i < NC) store(base + i, c[i]);
     }
+}
+
+template <class T, int NR, int NC>
+__device__ __forceinline__ void reduce_store(T (&v)[NR], int lane, T *__restrict__ dst)
+{
+    reduce_apply<T, NR, NC>(v, lane, [dst](int k, const T &x) { dst[k] = x; });
 }
 
 template <class T> __device__ __forceinline__ T pos_inf();

@@ -15,6 +15,12 @@ Every index is a compile-time constant, so the coefficient arrays of the
 callers live in registers. Coefficient order: graded by total degree; within
 a degree the x exponent descends, then the y exponent.
 
+It also writes ``expansions_df_gen.cuh``: ``ExpDF<P>::m2l`` for P <= 4, the
+same M2L with every value a double-float (dfloat.cuh): the derivative
+recurrence in double-word operations (constants split into fp32 pairs at
+generation time, exact ones applied with the cheaper forms), the contraction
+as lazily normalised product accumulations.
+
 Run ``python gen_expansions.py`` to regenerate; the output is committed.
 """
 from __future__ import annotations
@@ -212,6 +218,114 @@ def gen_l2p(p):
     return b
 
 
+MAXP_DF = 4
+
+
+def _f32(c):
+    import struct
+    return struct.unpack("f", struct.pack("f", c))[0]
+
+
+def df_cmul(x, c):
+    """Double-float x times the real constant c."""
+    from math import frexp
+    if c == 1:
+        return x
+    if c == -1:
+        return f"df_neg({x})"
+    if frexp(abs(c))[0] == 0.5:
+        return f"df_scale({x}, {c!r}f)"
+    if _f32(c) == c:
+        return f"df_mulf({x}, {c!r}f)"
+    h = _f32(c)
+    lo = _f32(c - h)
+    return f"df_mul({x}, df_make({h!r}f, {lo!r}f))"
+
+
+def df_sum(terms):
+    acc = terms[0]
+    for t in terms[1:]:
+        acc = f"df_add({acc}, {t})"
+    return acc
+
+
+def gen_derivs_df(p):
+    """Lines building df D[ncoef(p)] from df rx, ry, rz."""
+    mi = table(p)
+    L = [f"df D[{len(mi)}];",
+         "const df r2 = df_add(df_add(df_sqr(rx), df_sqr(ry)), df_sqr(rz));",
+         "D[0] = df_rsqrt(r2);"]
+    if p == 0:
+        return L
+    L.append("const df ir2 = df_sqr(D[0]);")
+    L.append("const df ax = df_mul(rx, ir2), ay = df_mul(ry, ir2), az = df_mul(rz, ir2);")
+    for a in AX:
+        for k in range(2, p + 1):
+            L.append(f"const df a{a}{k} = {df_cmul('a' + a, float(k))};")
+    for l in range(2, p + 1):
+        L.append(f"const df c2_{l} = {df_cmul('ir2', -(l - 1) / l)};")
+    for n in mi[1:]:
+        l = sum(n)
+        s1 = []
+        s2 = []
+        for i in range(3):
+            if n[i] >= 1:
+                m = list(n)
+                m[i] -= 1
+                coef = f"a{AX[i]}" if n[i] == 1 else f"a{AX[i]}{n[i]}"
+                s1.append(f"df_mul({coef}, D[{idx(tuple(m))}])")
+            if n[i] >= 2:
+                m = list(n)
+                m[i] -= 2
+                s2.append(df_cmul(f"D[{idx(tuple(m))}]", float(n[i] * (n[i] - 1))))
+        expr = df_cmul(df_sum(s1), -(2 * l - 1) / l)
+        if s2:
+            expr = f"df_add({expr}, df_mul(c2_{l}, {df_sum(s2)}))"
+        L.append(f"D[{idx(n)}] = {expr};")
+    return L
+
+
+def gen_m2l_df(p):
+    b = ["static __device__ __forceinline__ void m2l(const df* M, df rx, df ry, df rz, dacc* L) {"]
+    b += ["  " + l for l in gen_derivs_df(p)]
+    mi = table(p)
+    for k in mi:
+        lk = sum(k)
+        for n in mi:
+            ln = sum(n)
+            if ln + lk > p:
+                continue
+            j = idx((n[0] + k[0], n[1] + k[1], n[2] + k[2]))
+            mn = f"M[{idx(n)}]" if ln % 2 == 1 else f"df_neg(M[{idx(n)}])"
+            b.append(f"  mac(L[{idx(k)}], {mn}, D[{j}]);")
+    b.append("}")
+    return b
+
+
+def main_df():
+    out = ["// Generated by gen_expansions.py -- do not edit by hand.",
+           "// Double-float M2L for orders 0..4 (see the generator's docstring).",
+           "#pragma once",
+           "",
+           '#include "dfloat.cuh"',
+           "",
+           "namespace bfm {",
+           "",
+           "template <int P> struct ExpDF;",
+           ""]
+    for p in range(MAXP_DF + 1):
+        out.append(f"template <> struct ExpDF<{p}> {{")
+        out.append(f"  static constexpr int NC = {ncoef(p)};")
+        out += ["  " + l for l in gen_m2l_df(p)]
+        out.append("};")
+        out.append("")
+    out.append("}  // namespace bfm")
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "expansions_df_gen.cuh")
+    with open(path, "w") as f:
+        f.write("\n".join(out) + "\n")
+    print(path, len(out), "lines")
+
+
 def main():
     out = ["// Generated by gen_expansions.py -- do not edit by hand.",
            "// Unrolled Cartesian expansion operators for orders 0..8 (see the generator's docstring).",
@@ -238,6 +352,7 @@ def main():
     with open(path, "w") as f:
         f.write("\n".join(out) + "\n")
     print(path, sum(1 for _ in out), "lines")
+    main_df()
 
 
 if __name__ == "__main__":

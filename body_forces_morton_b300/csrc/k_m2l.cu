@@ -120,7 +120,8 @@ int launch_m2l_t(Plan &P, cudaStream_t s)
 
 int launch_m2l(Plan &P, cudaStream_t s)
 {
-    return P.dtype == 0 ? launch_m2l_t<float>(P, s) : launch_m2l_t<double>(P, s);
+    if (P.dtype == 0) return launch_m2l_t<float>(P, s);
+    return P.p <= kMaxPDf ? launch_m2l_df(P, s) : launch_m2l_t<double>(P, s);
 }
 
 }  // namespace bfm

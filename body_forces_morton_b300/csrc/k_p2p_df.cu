@@ -12,88 +12,12 @@
 // receiver i in A is (delta + s_j) - s_i with delta = c_B - c_A: every value is
 // of the size of a leaf, so the separation keeps ~48 bits relative to the leaf
 // size rather than to |x|. Sums run in a fixed order (reproducible).
-//
-// Arithmetic (Dekker / Knuth error-free transformations): two_sum, two_prod via
-// FMA, and the "sloppy" double-word addition (error ~2^-48 of the operands'
-// magnitude); the reciprocal square root is an fp32 seed refined by one
-// Newton step evaluated in double-word precision.
+#include "dfloat.cuh"
 #include "plan.h"
 
 namespace bfm {
 
 namespace {
-
-struct df { float h, l; };
-
-__device__ __forceinline__ df df_from(double v)
-{
-    df r;
-    r.h = __double2float_rn(v);
-    r.l = __double2float_rn(v - (double)r.h);
-    return r;
-}
-
-__device__ __forceinline__ df fast_two_sum(float a, float b)
-{
-    df r;
-    r.h = __fadd_rn(a, b);
-    r.l = __fsub_rn(b, __fsub_rn(r.h, a));
-    return r;
-}
-
-__device__ __forceinline__ df two_sum(float a, float b)
-{
-    df r;
-    r.h = __fadd_rn(a, b);
-    const float bb = __fsub_rn(r.h, a);
-    r.l = __fadd_rn(__fsub_rn(a, __fsub_rn(r.h, bb)), __fsub_rn(b, bb));
-    return r;
-}
-
-__device__ __forceinline__ df df_add(df x, df y)
-{
-    df s = two_sum(x.h, y.h);
-    const float e = __fadd_rn(s.l, __fadd_rn(x.l, y.l));
-    return fast_two_sum(s.h, e);
-}
-
-__device__ __forceinline__ df df_sub(df x, df y)
-{
-    y.h = -y.h;
-    y.l = -y.l;
-    return df_add(x, y);
-}
-
-__device__ __forceinline__ df df_mul(df x, df y)
-{
-    const float p = __fmul_rn(x.h, y.h);
-    float e = __fmaf_rn(x.h, y.h, -p);
-    e = __fmaf_rn(x.h, y.l, e);
-    e = __fmaf_rn(x.l, y.h, e);
-    return fast_two_sum(p, e);
-}
-
-__device__ __forceinline__ df df_sqr(df x)
-{
-    const float p = __fmul_rn(x.h, x.h);
-    float e = __fmaf_rn(x.h, x.h, -p);
-    e = __fmaf_rn(__fadd_rn(x.h, x.h), x.l, e);
-    return fast_two_sum(p, e);
-}
-
-// 1 / sqrt(r) for r > 0: y0 = rsqrtf(r.h), y = y0 + y0 (1 - r y0^2) / 2 with the
-// residual 1 - r y0^2 formed in double-word precision (it is ~2^-23, so its own
-// fp32 rounding is far below the result's precision).
-__device__ __forceinline__ df df_rsqrt(df r)
-{
-    const float y0 = rsqrtf(r.h);
-    df y2;
-    y2.h = __fmul_rn(y0, y0);
-    y2.l = __fmaf_rn(y0, y0, -y2.h);
-    const df ry2 = df_mul(r, y2);
-    const float resid = __fsub_rn(__fsub_rn(1.0f, ry2.h), ry2.l);
-    return fast_two_sum(y0, __fmul_rn(__fmul_rn(y0, 0.5f), resid));
-}
 
 // a staged source: position offset from the receiving leaf's centre and mass
 struct SrcDF { df x, y, z, m; };
@@ -149,21 +73,11 @@ __device__ __forceinline__ void p2p_df_one(const SrcDF &s, int j, const df &xi, 
 constexpr int DF_WARPS = 4;
 constexpr int DF_CH = 128;  // staged source particles per warp
 
-// Power-of-two units of the double-word arithmetic: lengths in 2^ex with
-// 2^(ex-1) <= the root's largest half-width < 2^ex, masses in 2^em with the
-// total mass (the root's monopole) below 2^em. Scaled offsets and centre
-// differences stay below 2 and masses at most 1, so fp32's exponent range
-// holds every intermediate of a pair separated by more than 2^-42 of the box.
-// The scalings are exact; acc = acc' 2^(em - 2 ex), phi = phi' 2^(em - ex).
-__device__ __forceinline__ void df_units(const dbl4 *__restrict__ nl, const double *__restrict__ M, int &ex, int &em)
-{
-    const dbl4 l = nl[0];
-    frexp(fmax(fmax(l.x, l.y), l.z), &ex);
-    frexp(M[0], &em);
-}
-
-// Scaled offsets of every particle from its leaf's centre, split into double
-// words: rel[i] = (sx.h, sy.h, sz.h, m.h) and rel[N + i] = (sx.l, sy.l, sz.l, m.l).
+// Scaled offsets of every particle from its leaf's centre (units of df_units:
+// scaled offsets and centre differences stay below 2 and masses at most 1, so
+// fp32's exponent range holds every intermediate of a pair separated by more
+// than 2^-42 of the box; acc = acc' 2^(em - 2 ex), phi = phi' 2^(em - ex)), split
+// into double words: rel[i] = (sx.h, sy.h, sz.h, m.h) and rel[N + i] = (sx.l, sy.l, sz.l, m.l).
 __global__ __launch_bounds__(256) void k_leaf_offsets(int n_nodes, int n, const int *__restrict__ first,
                                                       const int *__restrict__ count, const int *__restrict__ nchild,
                                                       const dbl4 *__restrict__ xyzm, const dbl4 *__restrict__ nc,
@@ -234,9 +148,9 @@ __device__ __forceinline__ int stage_df(float4 *buf, int *sidx, const float4 *__
             const int j = f + (g - e);
             const float4 h = rel[j], l = rel[n + j];
             SrcDF s;
-            s.x = df_add(d[0], df{h.x, l.x});
-            s.y = df_add(d[1], df{h.y, l.y});
-            s.z = df_add(d[2], df{h.z, l.z});
+            s.x = df_add(d[0], df_make(h.x, l.x));
+            s.y = df_add(d[1], df_make(h.y, l.y));
+            s.z = df_add(d[2], df_make(h.z, l.z));
             s.m = {h.w, l.w};
             put_src(buf, k, s);
             sidx[k] = j;
@@ -286,11 +200,11 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
         const int rr = rp + k * R;
         ri[k] = f + r0 + (rr < cr ? rr : 0);
         const float4 h = rel[ri[k]], l = rel[n + ri[k]];
-        rx[k] = df{h.x, l.x};
-        ry[k] = df{h.y, l.y};
-        rz[k] = df{h.z, l.z};
+        rx[k] = df_make(h.x, l.x);
+        ry[k] = df_make(h.y, l.y);
+        rz[k] = df_make(h.z, l.z);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) acc[k][v] = df{0.0f, 0.0f};
+        for (int v = 0; v < 4; ++v) acc[k][v] = df_make(0.0f, 0.0f);
     }
     const dbl4 ca = nc[a];
     const float ext_a = ext_scaled(ca, cx.ex);
@@ -302,10 +216,10 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
         for (int k = lane; k < n_here; k += 32) {
             const float4 h = rel[f + g0 + k], l = rel[n + f + g0 + k];
             SrcDF s;
-            s.x = df{h.x, l.x};
-            s.y = df{h.y, l.y};
-            s.z = df{h.z, l.z};
-            s.m = df{h.w, l.w};
+            s.x = df_make(h.x, l.x);
+            s.y = df_make(h.y, l.y);
+            s.z = df_make(h.z, l.z);
+            s.m = df_make(h.w, l.w);
             put_src(buf, k, s);
             sidx[k] = f + g0 + k;
         }
@@ -316,7 +230,7 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
         const int e = lb + lane;
         int lf = 0, cb = 0;
         float eb = 0.0f;  // |delta| + |l_B|: bound on |delta + s_j|
-        df dxl = {0.0f, 0.0f}, dyl = dxl, dzl = dxl;
+        df dxl = df_make(0.0f, 0.0f), dyl = dxl, dzl = dxl;
         if (e < end) {
             const int b = src[e];
             if (b != a) {

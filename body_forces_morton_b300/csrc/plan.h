@@ -41,6 +41,7 @@ struct Plan {
     void *node_lo = nullptr, *node_hi = nullptr;  // T[3] per node
     void *node_c = nullptr, *node_l = nullptr;    // vec4<T>: (cx, cy, cz, |l|^2), (lx, ly, lz, 0)
     void *M = nullptr, *Lm2l = nullptr, *L = nullptr;  // T[ncp] per node
+    void *Mdf = nullptr;           // fp64 plans: moments as double-float pairs in level units, [ncp] per node
 
     // walk and lists
     int2 *frontier[2] = {nullptr, nullptr};
@@ -96,6 +97,8 @@ int launch_upward(Plan &P, cudaStream_t s);
 int launch_walk(Plan &P, int depth, cudaStream_t s);
 int launch_lists(Plan &P, cudaStream_t s);
 int launch_m2l(Plan &P, cudaStream_t s);
+int launch_m2l_df(Plan &P, cudaStream_t s);  // fp64 plans, p <= kMaxPDf
+constexpr int kMaxPDf = 4;
 int launch_l2l(Plan &P, int depth, cudaStream_t s);
 int launch_leaf(Plan &P, void *acc, void *pot, cudaStream_t s);
 int launch_p2p_df(Plan &P, void *acc, void *pot, cudaStream_t s);

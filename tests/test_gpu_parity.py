@@ -205,3 +205,36 @@ def test_fp64_close_pair(same_leaf):
     for a in np.flatnonzero(r.nchild == 0):
         leaf_of[r.perm[r.first[a]:r.first[a] + r.count[a]]] = a
     assert (leaf_of[0] == leaf_of[1]) == same_leaf
+
+
+def _df_wide_pairs(r):
+    """M2L pairs outside the ranges of the fp64 path's double-word units
+    (level gap above 8, or |R / h_A|^2 outside [2^-30, 2^30] with
+    h_A = 2^(ex - level_A), 2^(ex-1) <= the root's largest half-width < 2^ex)."""
+    ex = np.frexp(r.half[0].max())[1]
+    n = 0
+    for a in range(r.n_nodes):
+        src = r.m2l_list(a)
+        if len(src) == 0:
+            continue
+        rs = (r.centre[a] - r.centre[src]) * 2.0 ** -(ex - int(r.level[a]))
+        r2 = (rs.astype(np.float32).astype(np.float64) ** 2).sum(axis=1)
+        dl = np.abs(int(r.level[a]) - r.level[src])
+        n += int(((dl > 8) | (r2 < 2.0 ** -30) | (r2 > 2.0 ** 30)).sum())
+    return n
+
+
+def test_fp64_m2l_wide_pairs():
+    """Two dense clumps 1e-9 apart on either side of the root's midplane: their
+    nodes meet in M2L at a separation far below their cells' size, which the
+    fp64 M2L evaluates in its fp64 pass; coefficients and accelerations must
+    still match the oracle."""
+    rng = np.random.default_rng(11)
+    bg = rng.random((500, 3))
+    bg[0], bg[1] = 0.0, 1.0
+    c1 = np.array([0.5 - 5e-10, 0.3, 0.3]) + 1e-12 * rng.standard_normal((40, 3))
+    c2 = np.array([0.5 + 5e-10, 0.3, 0.3]) + 1e-12 * rng.standard_normal((40, 3))
+    pos = np.vstack([bg, c1, c2])
+    mass = rng.uniform(0.5, 1.5, len(pos)) / len(pos)
+    e, r, _ = full_parity(pos, mass, 4, 0.7, 8, check_coeffs=True)
+    assert _df_wide_pairs(r) > 0
