@@ -253,7 +253,9 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         record(P, 8, s);
         P.launches += launch_l2l(P, depth, s);
         record(P, 9, s);
-        P.launches += launch_leaf(P, acc, pot, s);
+        P.launches += launch_l2p(P, s);
+        record(P, 11, s);
+        P.launches += launch_p2p(P, acc, pot, s);
         record(P, 10, s);
         st = sync_counters(P, s);
         if (st) return st;
@@ -522,8 +524,8 @@ fmm_status fmm_plan_stats(const fmm_plan *plan, fmm_stats *out)
     }
     out->n_leaves = leaves;
     out->n_p2p = 2 * P.n_p2p_pairs - leaves;
-    static const int a[FMM_N_STAGES] = {0, 1, 2, 4, 5, 6, 7, 8, 9};
-    static const int b[FMM_N_STAGES] = {1, 2, 3, 5, 6, 7, 8, 9, 10};
+    static const int a[FMM_N_STAGES] = {0, 1, 2, 4, 5, 6, 7, 8, 9, 11};
+    static const int b[FMM_N_STAGES] = {1, 2, 3, 5, 6, 7, 8, 9, 11, 10};
     for (int k = 0; k < FMM_N_STAGES; ++k) {
         float ms = 0.f;
         cudaEventElapsedTime(&ms, P.ev[a[k]], P.ev[b[k]]);

@@ -93,12 +93,14 @@ __device__ __forceinline__ df df_sqr(df x)
     return fast_two_sum(p, e);
 }
 
-// 1 / sqrt(r) for r > 0: y0 = rsqrtf(r.h), then one Newton step
-// y = y0 + y0 (1 - r y0^2) / 2 with the residual formed in double-word
+// 1 / sqrt(r) for normal r > 0 (callers keep r.h >= 2^-84): y0 from the
+// special-function unit's approximate reciprocal square root, then one Newton
+// step y = y0 + y0 (1 - r y0^2) / 2 with the residual formed in double-word
 // precision (it is ~2^-23, so its own fp32 rounding is far below 2^-48).
 __device__ __forceinline__ df df_rsqrt(df r)
 {
-    const float y0 = rsqrtf(r.h);
+    float y0;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y0) : "f"(r.h));
     df y2;
     y2.h = __fmul_rn(y0, y0);
     y2.l = __fmaf_rn(y0, y0, -y2.h);

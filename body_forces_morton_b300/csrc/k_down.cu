@@ -190,6 +190,17 @@ __device__ __forceinline__ void put_pair_layout(float *fb, int k, float x, float
     fb[base + 6] = m;
 }
 
+// Reciprocal square root with subnormal inputs flushed to zero: the bare
+// special-function instruction. r^2 of two distinct fp32 particles is subnormal
+// only for separations below 1.1e-19, which fp32 inputs of this code never
+// reach (such a pair would get an infinite force).
+__device__ __forceinline__ float rsqrt_ftz(float x)
+{
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Two sources (packed SX, SY, SZ, SM) acting on one receiver (packed broadcast
 // X, Y, Z); A = (phi, ax, ay, az), each the even-source and odd-source halves.
 __device__ __forceinline__ void p2p_two(f2_t SX, f2_t SY, f2_t SZ, f2_t SM, f2_t X, f2_t Y, f2_t Z, f2_t (&A)[4])
@@ -200,7 +211,7 @@ __device__ __forceinline__ void p2p_two(f2_t SX, f2_t SY, f2_t SZ, f2_t SM, f2_t
     r2 = f2_fma(dz, dz, r2);
     float ra, rb;
     f2_unpack(r2, ra, rb);
-    const f2_t ri = f2_pack(rsqrtf(ra), rsqrtf(rb));
+    const f2_t ri = f2_pack(rsqrt_ftz(ra), rsqrt_ftz(rb));
     const f2_t mr = f2_mul(SM, ri);
     const f2_t mr3 = f2_mul(mr, f2_mul(ri, ri));
     A[1] = f2_fma(mr3, dx, A[1]);
@@ -442,20 +453,12 @@ int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 }
 
 template <class T, int P>
-int launch_leaf_tp(Plan &P_, void *acc, void *pot, cudaStream_t s)
+int launch_l2p_tp(Plan &P_, cudaStream_t s)
 {
     k_l2p<T, P><<<P_.num_sms * 8, 256, 0, s>>>((int)P_.n_nodes, P_.node_first, P_.node_count, P_.node_nchild,
                                                (const vec4<T> *)P_.xyzm, (const vec4<T> *)P_.node_c,
                                                (const T *)P_.L, P_.ncp, (vec4<T> *)P_.far);
-    if constexpr (sizeof(T) == 8) {
-        return 1 + launch_p2p_df(P_, acc, pot, s);
-    } else {
-        k_p2p<T><<<P_.num_sms * 16, LF_WARPS * 32, 0, s>>>(P_.ctr, P_.order, P_.ctr, P_.node_first, P_.node_count,
-                                                           P_.node_nchild, (const vec4<T> *)P_.xyzm, P_.idx[0],
-                                                           (const vec4<T> *)P_.far, P_.p2p_off, P_.p2p_src,
-                                                           (T *)acc, (T *)pot);
-        return 2;
-    }
+    return 1;
 }
 
 #define BFM_DISPATCH_P(fn, T, ...)                        \
@@ -472,10 +475,7 @@ int launch_leaf_tp(Plan &P_, void *acc, void *pot, cudaStream_t s)
     }
 
 template <class T> int launch_l2l_t(Plan &P, int depth, cudaStream_t s) { BFM_DISPATCH_P(launch_l2l_tp, T, depth, s) }
-template <class T> int launch_leaf_t(Plan &P, void *acc, void *pot, cudaStream_t s)
-{
-    BFM_DISPATCH_P(launch_leaf_tp, T, acc, pot, s)
-}
+template <class T> int launch_l2p_t(Plan &P, cudaStream_t s) { BFM_DISPATCH_P(launch_l2p_tp, T, s) }
 
 }  // namespace
 
@@ -484,9 +484,20 @@ int launch_l2l(Plan &P, int depth, cudaStream_t s)
     return P.dtype == 0 ? launch_l2l_t<float>(P, depth, s) : launch_l2l_t<double>(P, depth, s);
 }
 
-int launch_leaf(Plan &P, void *acc, void *pot, cudaStream_t s)
+int launch_l2p(Plan &P, cudaStream_t s)
 {
-    return P.dtype == 0 ? launch_leaf_t<float>(P, acc, pot, s) : launch_leaf_t<double>(P, acc, pot, s);
+    return P.dtype == 0 ? launch_l2p_t<float>(P, s) : launch_l2p_t<double>(P, s);
+}
+
+// fp32 plans: k_p2p; fp64 plans: the double-float near field (k_p2p_df.cu)
+int launch_p2p(Plan &P, void *acc, void *pot, cudaStream_t s)
+{
+    if (P.dtype == 1) return launch_p2p_df(P, acc, pot, s);
+    k_p2p<float><<<P.num_sms * 16, LF_WARPS * 32, 0, s>>>(P.ctr, P.order, P.ctr, P.node_first, P.node_count,
+                                                          P.node_nchild, (const vec4<float> *)P.xyzm, P.idx[0],
+                                                          (const vec4<float> *)P.far, P.p2p_off, P.p2p_src,
+                                                          (float *)acc, (float *)pot);
+    return 1;
 }
 
 }  // namespace bfm

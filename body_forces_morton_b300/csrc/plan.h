@@ -100,7 +100,8 @@ int launch_m2l(Plan &P, cudaStream_t s);
 int launch_m2l_df(Plan &P, cudaStream_t s);  // fp64 plans, p <= kMaxPDf
 constexpr int kMaxPDf = 4;
 int launch_l2l(Plan &P, int depth, cudaStream_t s);
-int launch_leaf(Plan &P, void *acc, void *pot, cudaStream_t s);
+int launch_l2p(Plan &P, cudaStream_t s);
+int launch_p2p(Plan &P, void *acc, void *pot, cudaStream_t s);
 int launch_p2p_df(Plan &P, void *acc, void *pot, cudaStream_t s);
 int launch_kick(Plan &P, void *vel, const void *acc, double h, cudaStream_t s);
 int launch_drift(Plan &P, void *pos, const void *vel, double dt, cudaStream_t s);

@@ -21,7 +21,7 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "fmm.h")
 FMM_F32, FMM_F64 = 0, 1
 STATUS = {0: "FMM_OK", 1: "FMM_ERR_INVALID_ARG", 2: "FMM_ERR_OOM", 3: "FMM_ERR_CUDA", 4: "FMM_ERR_CAPACITY",
           5: "FMM_ERR_NONFINITE", 6: "FMM_ERR_INTERNAL"}
-STAGES = ("keys", "sort", "tree", "upward", "walk", "lists", "m2l", "l2l", "leaf")
+STAGES = ("keys", "sort", "tree", "upward", "walk", "lists", "m2l", "l2l", "l2p", "p2p")
 N_STAGES = len(STAGES)
 
 EXPORTS = {

@@ -74,8 +74,9 @@ enum {
     FMM_STAGE_LISTS = 5, /* interaction lists into per-receiver CSR, canonical order */
     FMM_STAGE_M2L = 6,
     FMM_STAGE_L2L = 7,
-    FMM_STAGE_LEAF = 8,  /* L2P + P2P + scatter to the caller's order */
-    FMM_N_STAGES = 9
+    FMM_STAGE_L2P = 8,   /* local expansions at the leaves' particles */
+    FMM_STAGE_P2P = 9,   /* near field + far field, scattered to the caller's order */
+    FMM_N_STAGES = 10
 };
 
 typedef struct fmm_plan fmm_plan;
