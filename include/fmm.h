@@ -51,7 +51,16 @@
 extern "C" {
 #endif
 
-/* Arithmetic type of a plan: positions, masses, expansions and accumulators. */
+/*
+ * Arithmetic type of a plan: positions, masses, expansions and accumulators.
+ * FMM_F32 computes every stage in fp32. FMM_F64 takes and returns fp64; its
+ * two ALU-bound stages, P2P and (for p <= 4) M2L, run in double-float
+ * arithmetic (unevaluated sums of two fp32 numbers, ~2^-48 relative) on the
+ * FP32 pipe, whose rate on this GPU is far above the FP64 pipe's, in
+ * power-of-two units of the root box and total mass; near-field pairs closer
+ * than 2^-8 of their leaf pair's extent, and M2L pairs outside those units'
+ * range, are evaluated in fp64. The other stages compute in fp64.
+ */
 typedef enum { FMM_F32 = 0, FMM_F64 = 1 } fmm_dtype;
 
 typedef enum {
