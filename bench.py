@@ -357,14 +357,20 @@ def p2p_roofline(res, w):
             "ms": ms, "traffic": None}
 
 
+def m2l_flops_per_pair(p):
+    """Flops of the reduced (trace-free) M2L per pair: 2 per contraction term,
+    sum_{lk} (2 lk + 1) (p - lk + 1)^2 terms, ~10 per derivative of the (p + 1)^2
+    with D_z-exponent <= 1, one add for each of the p(p - 1)/2 with exponent 2."""
+    terms = sum((2 * lk + 1) * (p - lk + 1) ** 2 for lk in range(p + 1))
+    return 2 * terms + 10 * (p + 1) ** 2 + p * (p - 1) // 2
+
+
 def m2l_roofline(res, w):
-    """Algorithmic M2L flops: 2 * C(p+6,6) (contraction) + ~10 * C(p+3,3) (derivative build) per pair.
+    """Algorithmic M2L flops per pair (m2l_flops_per_pair: 566 at p = 4) over the M2L stage time.
 
     fp64 with p <= 4 runs double-float on the FP32 pipe (k_moments_df + k_m2l_df);
     its fp64-equivalent rate is reported against the nominal FP64 peak."""
-    from math import comb
-
-    per_pair = 2 * comb(w.p + 6, 6) + 10 * comb(w.p + 3, 3)
+    per_pair = m2l_flops_per_pair(w.p)
     ms = res["stage_ms"]["m2l"]
     achieved = per_pair * res["stats"]["n_m2l"] / (ms / 1e3) / 1e12
     f32 = w.dtype == "f32"

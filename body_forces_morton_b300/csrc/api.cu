@@ -84,7 +84,7 @@ void free_nodes(Plan &P)
                     &P.node_level, &P.node_done,  &P.m2l_cnt,     &P.p2p_cnt,     &P.m2l_off,
                     &P.p2p_off,    &P.long_seg,    &P.order};
     for (int **q : ints) { dfree(*q); *q = nullptr; }
-    void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L, &P.Mdf};
+    void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L, &P.Mr};
     for (void **q : vs) { dfree(*q); *q = nullptr; }
     dfree(P.flags);
     P.flags = nullptr;
@@ -127,7 +127,7 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
     CUDA_TRY(cudaMalloc(&P.M, (size_t)P.ncp * c * e));
     CUDA_TRY(cudaMalloc(&P.Lm2l, (size_t)P.ncp * c * e));
     CUDA_TRY(cudaMalloc(&P.L, (size_t)P.ncp * c * e));
-    if (P.dtype == 1 && P.p <= kMaxPDf) CUDA_TRY(cudaMalloc(&P.Mdf, (size_t)P.ncp * c * 2 * sizeof(float)));
+    CUDA_TRY(cudaMalloc(&P.Mr, (size_t)P.nrp * c * 8));
     CUDA_TRY(cudaMemset(P.m2l_cnt, 0, c * sizeof(int)));
     CUDA_TRY(cudaMemset(P.p2p_cnt, 0, c * sizeof(int)));
     const int64_t tiles_sort = (P.n + RS_TILE - 1) / RS_TILE;
@@ -336,6 +336,8 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     P.esize = dtype == FMM_F32 ? 4 : 8;
     P.nc = (p + 1) * (p + 2) * (p + 3) / 6;
     P.ncp = (P.nc + 3) / 4 * 4;
+    P.nrc = (p + 1) * (p + 1);
+    P.nrp = (P.nrc + 3) / 4 * 4;
     auto fail = [&](fmm_status) -> fmm_plan * {
         destroy_plan(P);
         delete h;

@@ -15,8 +15,17 @@ Every index is a compile-time constant, so the coefficient arrays of the
 callers live in registers. Coefficient order: graded by total degree; within
 a degree the x exponent descends, then the y exponent.
 
-It also writes ``expansions_df_gen.cuh``: ``ExpDF<P>::m2l`` for P <= 4, the
-same M2L with every value a double-float (dfloat.cuh): the derivative
+Reduced (trace-free) M2L. D^m is harmonic, so D^m = -(D^{m-2e_z+2e_x} +
+D^{m-2e_z+2e_y}) whenever m_z >= 2. Applied to the contraction, M_n with
+n_z >= 2 folds into "reduced" moments indexed by n_z <= 1 (2l+1 per degree l),
+and the locals L_k with k_z >= 2 follow from those with k_z <= 1 by the same
+identity (their truncated sums obey it term by term). ``m2l_r`` contracts
+reduced moments into reduced locals ((p+1)^2 each; 155 instead of 210 terms at
+p = 4) and needs D^m only for m_z <= 2, the m_z = 2 ones from the identity;
+``reduce_m`` and ``expand_l`` convert from and to the full coefficients.
+
+It also writes ``expansions_df_gen.cuh``: ``ExpDF<P>::m2l_r`` for P <= 4, the
+reduced M2L with every value a double-float (dfloat.cuh): the derivative
 recurrence in double-word operations (constants split into fp32 pairs at
 generation time, exact ones applied with the cheaper forms), the contraction
 as lazily normalised product accumulations.
@@ -176,6 +185,117 @@ def gen_m2l(p):
     return b
 
 
+def reduced_table(p):
+    """Multi-indices with n_z <= 1 in coefficient order, and their reduced index."""
+    out = [n for n in table(p) if n[2] <= 1]
+    return out, {n: i for i, n in enumerate(out)}
+
+
+def reduction(n, rmap):
+    """n as a combination of reduced indices, by the trace identity: {ridx: coef}."""
+    if n[2] <= 1:
+        return {rmap[n]: 1}
+    res = {}
+    for m in ((n[0] + 2, n[1], n[2] - 2), (n[0], n[1] + 2, n[2] - 2)):
+        for k, c in reduction(m, rmap).items():
+            res[k] = res.get(k, 0) - c
+    return res
+
+
+def lin_comb(terms):
+    """'a + b - 2 * c' from [(coef, expr)]."""
+    out = ""
+    for c, e in terms:
+        if c == 0:
+            continue
+        mag = abs(c)
+        t = e if mag == 1 else f"{lit(mag)} * {e}"
+        if not out:
+            out = t if c > 0 else f"-({t})"
+        else:
+            out += f" + {t}" if c > 0 else f" - {t}"
+    return out or "T(0)"
+
+
+def gen_reduce_m(p):
+    red, rmap = reduced_table(p)
+    acc = {i: [] for i in range(len(red))}
+    for n in table(p):
+        for r, c in reduction(n, rmap).items():
+            acc[r].append((c, f"M[{idx(n)}]"))
+    b = ["template <class T> static __device__ __forceinline__ void reduce_m(const T* M, T* Mr) {"]
+    for r in range(len(red)):
+        b.append(f"  Mr[{r}] = {lin_comb(acc[r])};")
+    b.append("}")
+    return b
+
+
+def gen_expand_l(p):
+    red, rmap = reduced_table(p)
+    b = ["template <class T> static __device__ __forceinline__ void expand_l(const T* Lr, T* L) {"]
+    for k in table(p):
+        terms = sorted(reduction(k, rmap).items())
+        b.append(f"  L[{idx(k)}] = {lin_comb([(c, f'Lr[{r}]') for r, c in terms])};")
+    b.append("}")
+    return b
+
+
+def reduced_derivs(p):
+    """(slot map, lines) building D^m for m_z <= 2, |m| <= p, in a compact array."""
+    mi = [m for m in table(p) if m[2] <= 2]
+    slot = {m: i for i, m in enumerate(mi)}
+    return mi, slot
+
+
+def gen_m2l_r(p):
+    red, rmap = reduced_table(p)
+    mi, slot = reduced_derivs(p)
+    b = ["template <class T> static __device__ __forceinline__ void m2l_r(const T* M, T rx, T ry, T rz, T* L) {",
+         f"  T D[{len(mi)}];",
+         "  const T r2 = rx * rx + ry * ry + rz * rz;",
+         f"  D[{slot[(0, 0, 0)]}] = rsqrt_t(r2);"]
+    if p > 0:
+        b.append("  const T ir2 = D[0] * D[0];")
+        b.append("  const T ax = rx * ir2, ay = ry * ir2, az = rz * ir2;")
+        for a in AX:
+            for k in range(2, p + 1):
+                b.append(f"  const T a{a}{k} = a{a} * {lit(k)};")
+        for l in range(2, p + 1):
+            b.append(f"  const T c2_{l} = ir2 * {lit(-(l - 1) / l)};")
+    for n in mi[1:]:
+        if n[2] == 2:
+            continue
+        l = sum(n)
+        s1, s2 = [], []
+        for i in range(3):
+            if n[i] >= 1:
+                m = list(n)
+                m[i] -= 1
+                coef = f"a{AX[i]}" if n[i] == 1 else f"a{AX[i]}{n[i]}"
+                s1.append(f"{coef} * D[{slot[tuple(m)]}]")
+            if n[i] >= 2:
+                m = list(n)
+                m[i] -= 2
+                s2.append(f"{lit(n[i] * (n[i] - 1))} * D[{slot[tuple(m)]}]")
+        expr = f"{lit(-(2 * l - 1) / l)} * ({' + '.join(s1)})"
+        if s2:
+            expr += f" + c2_{l} * ({' + '.join(s2)})"
+        b.append(f"  D[{slot[n]}] = {expr};")
+    for n in mi:
+        if n[2] == 2:
+            a_, b_ = (n[0] + 2, n[1], 0), (n[0], n[1] + 2, 0)
+            b.append(f"  D[{slot[n]}] = -(D[{slot[a_]}] + D[{slot[b_]}]);")
+    for k in red:
+        for n in red:
+            if sum(n) + sum(k) > p:
+                continue
+            m = (n[0] + k[0], n[1] + k[1], n[2] + k[2])
+            op = "+=" if sum(n) % 2 == 1 else "-="
+            b.append(f"  L[{rmap[k]}] {op} M[{rmap[n]}] * D[{slot[m]}];")
+    b.append("}")
+    return b
+
+
 def gen_l2l(p):
     b = ["template <class T> static __device__ __forceinline__ void l2l(const T* Lp, T ex, T ey, T ez, T* Lc) {"]
     if p == 0:
@@ -249,55 +369,52 @@ def df_sum(terms):
     return acc
 
 
-def gen_derivs_df(p):
-    """Lines building df D[ncoef(p)] from df rx, ry, rz."""
-    mi = table(p)
-    L = [f"df D[{len(mi)}];",
-         "const df r2 = df_add(df_add(df_sqr(rx), df_sqr(ry)), df_sqr(rz));",
-         "D[0] = df_rsqrt(r2);"]
-    if p == 0:
-        return L
-    L.append("const df ir2 = df_sqr(D[0]);")
-    L.append("const df ax = df_mul(rx, ir2), ay = df_mul(ry, ir2), az = df_mul(rz, ir2);")
-    for a in AX:
-        for k in range(2, p + 1):
-            L.append(f"const df a{a}{k} = {df_cmul('a' + a, float(k))};")
-    for l in range(2, p + 1):
-        L.append(f"const df c2_{l} = {df_cmul('ir2', -(l - 1) / l)};")
+def gen_m2l_df(p):
+    """Double-float reduced M2L: m2l_r with double-word operations and product accumulation."""
+    red, rmap = reduced_table(p)
+    mi, slot = reduced_derivs(p)
+    b = ["static __device__ __forceinline__ void m2l_r(const df* M, df rx, df ry, df rz, dacc* L) {",
+         f"  df D[{len(mi)}];",
+         "  const df r2 = df_add(df_add(df_sqr(rx), df_sqr(ry)), df_sqr(rz));",
+         f"  D[{slot[(0, 0, 0)]}] = df_rsqrt(r2);"]
+    if p > 0:
+        b.append("  const df ir2 = df_sqr(D[0]);")
+        b.append("  const df ax = df_mul(rx, ir2), ay = df_mul(ry, ir2), az = df_mul(rz, ir2);")
+        for a in AX:
+            for k in range(2, p + 1):
+                b.append(f"  const df a{a}{k} = {df_cmul('a' + a, float(k))};")
+        for l in range(2, p + 1):
+            b.append(f"  const df c2_{l} = {df_cmul('ir2', -(l - 1) / l)};")
     for n in mi[1:]:
+        if n[2] == 2:
+            continue
         l = sum(n)
-        s1 = []
-        s2 = []
+        s1, s2 = [], []
         for i in range(3):
             if n[i] >= 1:
                 m = list(n)
                 m[i] -= 1
                 coef = f"a{AX[i]}" if n[i] == 1 else f"a{AX[i]}{n[i]}"
-                s1.append(f"df_mul({coef}, D[{idx(tuple(m))}])")
+                s1.append(f"df_mul({coef}, D[{slot[tuple(m)]}])")
             if n[i] >= 2:
                 m = list(n)
                 m[i] -= 2
-                s2.append(df_cmul(f"D[{idx(tuple(m))}]", float(n[i] * (n[i] - 1))))
+                s2.append(df_cmul(f"D[{slot[tuple(m)]}]", float(n[i] * (n[i] - 1))))
         expr = df_cmul(df_sum(s1), -(2 * l - 1) / l)
         if s2:
             expr = f"df_add({expr}, df_mul(c2_{l}, {df_sum(s2)}))"
-        L.append(f"D[{idx(n)}] = {expr};")
-    return L
-
-
-def gen_m2l_df(p):
-    b = ["static __device__ __forceinline__ void m2l(const df* M, df rx, df ry, df rz, dacc* L) {"]
-    b += ["  " + l for l in gen_derivs_df(p)]
-    mi = table(p)
-    for k in mi:
-        lk = sum(k)
-        for n in mi:
-            ln = sum(n)
-            if ln + lk > p:
+        b.append(f"  D[{slot[n]}] = {expr};")
+    for n in mi:
+        if n[2] == 2:
+            a_, b_ = (n[0] + 2, n[1], 0), (n[0], n[1] + 2, 0)
+            b.append(f"  D[{slot[n]}] = df_neg(df_add(D[{slot[a_]}], D[{slot[b_]}]));")
+    for k in red:
+        for n in red:
+            if sum(n) + sum(k) > p:
                 continue
-            j = idx((n[0] + k[0], n[1] + k[1], n[2] + k[2]))
-            mn = f"M[{idx(n)}]" if ln % 2 == 1 else f"df_neg(M[{idx(n)}])"
-            b.append(f"  mac(L[{idx(k)}], {mn}, D[{j}]);")
+            m = (n[0] + k[0], n[1] + k[1], n[2] + k[2])
+            mn = f"M[{rmap[n]}]" if sum(n) % 2 == 1 else f"df_neg(M[{rmap[n]}])"
+            b.append(f"  mac(L[{rmap[k]}], {mn}, D[{slot[m]}]);")
     b.append("}")
     return b
 
@@ -316,6 +433,7 @@ def main_df():
     for p in range(MAXP_DF + 1):
         out.append(f"template <> struct ExpDF<{p}> {{")
         out.append(f"  static constexpr int NC = {ncoef(p)};")
+        out.append(f"  static constexpr int NRC = {(p + 1) ** 2};")
         out += ["  " + l for l in gen_m2l_df(p)]
         out.append("};")
         out.append("")
@@ -343,7 +461,8 @@ def main():
     for p in range(MAXP + 1):
         out.append(f"template <> struct Exp<{p}> {{")
         out.append(f"  static constexpr int NC = {ncoef(p)};")
-        for gen in (gen_p2m, gen_m2m, gen_m2l, gen_l2l, gen_l2p):
+        out.append(f"  static constexpr int NRC = {(p + 1) ** 2};  // reduced (n_z <= 1) coefficients")
+        for gen in (gen_p2m, gen_m2m, gen_m2l, gen_l2l, gen_l2p, gen_reduce_m, gen_expand_l, gen_m2l_r):
             out += ["  " + l for l in gen(p)]
         out.append("};")
         out.append("")

@@ -8,12 +8,19 @@
 // the source particles; the derivative tensor is built on chip for every pair
 // (no per-pair operator data in memory).
 //
+// The contraction runs on reduced (trace-free) coefficients: D^m is harmonic,
+// so the moments with n_z >= 2 fold into those with n_z <= 1 once per node
+// (k_moments_r, Exp<P>::reduce_m) and only the locals with k_z <= 1 are
+// accumulated, the others following from the same identity when the receiver's
+// row is written (Exp<P>::expand_l): (p+1)^2 instead of C(p+3,3) coefficients
+// each side, 155 instead of 210 terms at p = 4.
+//
 // One warp per receiver, receivers taken from a shared counter in decreasing
 // order of list length; lane j takes the receiver's sources j, j+32, ... in
 // list order (ascending source index) and keeps a private partial L in
-// registers. The multipoles of each round of 32 sources are staged through
-// shared memory with coalesced 16-byte loads; a fixed reduction sums the
-// lanes, so the result is reproducible.
+// registers. The reduced multipoles of each round of 32 sources are staged
+// through shared memory with coalesced 16-byte loads; a fixed reduction sums
+// the lanes, so the result is reproducible.
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -29,19 +36,36 @@ template <> struct Vec16<double> { using type = double2; static constexpr int n 
 
 template <class T, int P> struct M2LShape {
     static constexpr int NC = Exp<P>::NC;
-    static constexpr int NCP = (NC + 3) / 4 * 4;      // row stride of M in global memory
-    static constexpr int STR = NCP + 1;               // odd row stride in shared memory
+    static constexpr int NCP = (NC + 3) / 4 * 4;      // row stride of M and L in global memory
+    static constexpr int NRC = Exp<P>::NRC;           // reduced coefficients
+    static constexpr int NRP = (NRC + 3) / 4 * 4;     // row stride of the reduced moments
+    static constexpr int STR = NRP + 1;               // odd row stride in shared memory
     static constexpr int V = Vec16<T>::n;             // elements per 16-byte load
-    static constexpr int NV = NCP / V;
-    static constexpr int NR = (NC + 7) / 8 * 8;       // accumulators, padded for the halving reduction
-    static constexpr size_t smem = sizeof(T) * M2L_WARPS * 32 * STR;
+    static constexpr int NV = NRP / V;
+    static constexpr int NR = (NRC + 7) / 8 * 8;      // accumulators, padded for the halving reduction
+    static constexpr size_t smem = sizeof(T) * M2L_WARPS * (32 * STR + NRC);
 };
+
+// Reduced moments of every node: Mr[b] = reduce_m(M[b]), padding zeroed.
+template <class T, int P>
+__global__ __launch_bounds__(256) void k_moments_r(int n_nodes, const T *__restrict__ M, T *__restrict__ Mr)
+{
+    using S = M2LShape<T, P>;
+    for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < n_nodes; b += gridDim.x * blockDim.x) {
+        T r[S::NRP];
+#pragma unroll
+        for (int i = S::NRC; i < S::NRP; ++i) r[i] = T(0);
+        Exp<P>::template reduce_m<T>(M + (size_t)b * S::NCP, r);
+#pragma unroll
+        for (int i = 0; i < S::NRP; ++i) Mr[(size_t)b * S::NRP + i] = r[i];
+    }
+}
 
 template <class T, int P>
 __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(int n_nodes, const int *__restrict__ order,
                                                         const int *__restrict__ off,
                                                         const int *__restrict__ src, const vec4<T> *__restrict__ nc,
-                                                        const T *__restrict__ M, T *__restrict__ Lout,
+                                                        const T *__restrict__ Mr, T *__restrict__ Lout,
                                                         DevCounters *ctr)
 {
     using S = M2LShape<T, P>;
@@ -49,6 +73,7 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(int n_nodes, const int *
     extern __shared__ __align__(16) unsigned char m2l_smem[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     T *rows = reinterpret_cast<T *>(m2l_smem) + (size_t)w * 32 * S::STR;
+    T *lred = reinterpret_cast<T *>(m2l_smem) + (size_t)M2L_WARPS * 32 * S::STR + (size_t)w * S::NRC;
     for (;;) {
         int t = 0;
         if (lane == 0) t = atomicAdd(&ctr->work_ctr[1], 1);
@@ -66,13 +91,13 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(int n_nodes, const int *
             const int b = valid ? src[q] : 0;
             const int nsrc = min(32, end - q0);
             __syncwarp();
-            // stage the multipole rows of this round's sources (16-byte loads, one row per source)
+            // stage the reduced multipole rows of this round's sources (16-byte loads, one row per source)
             for (int t0 = 0; t0 < nsrc * S::NV; t0 += 32) {
-                const int t = t0 + lane;
-                const int row = t / S::NV, col = t - row * S::NV;
+                const int tt = t0 + lane;
+                const int row = tt / S::NV, col = tt - row * S::NV;
                 const int bb = __shfl_sync(kFull, b, row & 31);
-                if (t < nsrc * S::NV) {
-                    const V16 x = __ldg(reinterpret_cast<const V16 *>(M + (size_t)bb * S::NCP) + col);
+                if (tt < nsrc * S::NV) {
+                    const V16 x = __ldg(reinterpret_cast<const V16 *>(Mr + (size_t)bb * S::NRP) + col);
                     const T *xs = reinterpret_cast<const T *>(&x);
 #pragma unroll
                     for (int i = 0; i < S::V; ++i) rows[row * S::STR + col * S::V + i] = xs[i];
@@ -81,10 +106,12 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(int n_nodes, const int *
             __syncwarp();
             if (valid) {
                 const vec4<T> cb = nc[b];
-                Exp<P>::template m2l<T>(rows + lane * S::STR, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
+                Exp<P>::template m2l_r<T>(rows + lane * S::STR, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
             }
         }
-        reduce_store<T, S::NR, S::NC>(L, lane, Lout + (size_t)a * S::NCP);
+        reduce_apply<T, S::NR, S::NRC>(L, lane, [&](int k, const T &x) { lred[k] = x; });
+        __syncwarp();
+        if (lane == 0) Exp<P>::template expand_l<T>(lred, Lout + (size_t)a * S::NCP);
     }
 }
 
@@ -92,12 +119,13 @@ template <class T, int P>
 int launch_m2l_tp(Plan &P_, cudaStream_t s)
 {
     using S = M2LShape<T, P>;
-    static_assert(S::NCP % S::V == 0, "row stride must be a whole number of 16-byte loads");
+    static_assert(S::NRP % S::V == 0, "row stride must be a whole number of 16-byte loads");
+    k_moments_r<T, P><<<P_.num_sms * 4, 256, 0, s>>>((int)P_.n_nodes, (const T *)P_.M, (T *)P_.Mr);
     cudaFuncSetAttribute(k_m2l<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::smem);
     k_m2l<T, P><<<P_.num_sms * 16, M2L_WARPS * 32, S::smem, s>>>(
         (int)P_.n_nodes, P_.order + P_.n_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
-        (const T *)P_.M, (T *)P_.Lm2l, P_.ctr);
-    return 1;
+        (const T *)P_.Mr, (T *)P_.Lm2l, P_.ctr);
+    return 2;
 }
 
 template <class T>

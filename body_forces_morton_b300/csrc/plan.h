@@ -17,6 +17,8 @@ struct Plan {
     int p = 4;
     int nc = 35;        // coefficients per expansion
     int ncp = 36;       // padded row stride (multiple of 4 elements)
+    int nrc = 25;       // reduced coefficients (p + 1)^2
+    int nrp = 28;       // their padded row stride (multiple of 4)
     double theta = 0.7;
     int leaf = 32;
     int dtype = 0;      // 0 f32, 1 f64
@@ -41,7 +43,8 @@ struct Plan {
     void *node_lo = nullptr, *node_hi = nullptr;  // T[3] per node
     void *node_c = nullptr, *node_l = nullptr;    // vec4<T>: (cx, cy, cz, |l|^2), (lx, ly, lz, 0)
     void *M = nullptr, *Lm2l = nullptr, *L = nullptr;  // T[ncp] per node
-    void *Mdf = nullptr;           // fp64 plans: moments as double-float pairs in level units, [ncp] per node
+    void *Mr = nullptr;            // reduced (n_z <= 1) moments for M2L, [nrp] 8-byte slots per node: T for
+                                   // fp32 and fp64 p >= 5, double-float pairs in level units for fp64 p <= 4
 
     // walk and lists
     int2 *frontier[2] = {nullptr, nullptr};

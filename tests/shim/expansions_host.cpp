@@ -22,6 +22,14 @@ static void run(int op, const T* a, const T* v, T* out)
     case 2: Exp<P>::template m2l<T>(a, v[0], v[1], v[2], out); break;
     case 3: Exp<P>::template l2l<T>(a, v[0], v[1], v[2], out); break;
     case 4: Exp<P>::template l2p<T>(a, v[0], v[1], v[2], out[0], out[1], out[2], out[3]); break;
+    case 5: {  // reduced M2L: expand_l(m2l_r(reduce_m(M), R))
+        T Mr[Exp<P>::NRC], Lr[Exp<P>::NRC];
+        for (int i = 0; i < Exp<P>::NRC; ++i) Lr[i] = T(0);
+        Exp<P>::template reduce_m<T>(a, Mr);
+        Exp<P>::template m2l_r<T>(Mr, v[0], v[1], v[2], Lr);
+        Exp<P>::template expand_l<T>(Lr, out);
+        break;
+    }
     }
 }
 

@@ -56,6 +56,10 @@ def test_generated_operators_match_oracle(shim, p, dtype, rtol):
         got = call(shim, p, op, M, arg, nc, dtype)
         want = fn(p, M, arg)
         np.testing.assert_allclose(got, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg=f"op {op}")
+    # reduced (trace-free) M2L: reduce the moments, contract, expand the locals
+    got = call(shim, p, 5, M, R, nc, dtype)
+    want = oracle.m2l(p, M, R)
+    np.testing.assert_allclose(got, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg="reduced m2l")
     # L2P
     dx = rng.normal(size=3) * 0.1
     got = call(shim, p, 4, M, dx, 4, dtype)
