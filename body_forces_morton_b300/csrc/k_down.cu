@@ -141,46 +141,11 @@ __device__ __forceinline__ void p2p_span(const vec4<T> *buf, int n_here, int q, 
 }
 
 // ---- fp32: two sources per instruction with the packed f32x2 arithmetic of
-// sm_100-family GPUs (one instruction issues the operation for both halves).
+// sm_100-family GPUs (one instruction issues the operation for both halves;
+// the compiler's float2 builtins let it keep the halves in register pairs).
 // Staged sources are stored pair-interleaved, (x_j, x_j+1, y_j, y_j+1, z_j,
 // z_j+1, m_j, m_j+1) per pair, so two 16-byte shared loads give four packed
 // operands; an odd tail is padded with a massless particle far away.
-typedef unsigned long long f2_t;
-__device__ __forceinline__ f2_t f2_pack(float a, float b)
-{
-    f2_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void f2_unpack(f2_t v, float &a, float &b)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b)
-{
-    f2_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f2_t f2_sub(f2_t a, f2_t b)
-{
-    f2_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b)
-{
-    f2_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c)
-{
-    f2_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
 __device__ __forceinline__ void put_pair_layout(float *fb, int k, float x, float y, float z, float m)
 {
     const int base = (k >> 1) * 8 + (k & 1);
@@ -201,23 +166,23 @@ __device__ __forceinline__ float rsqrt_ftz(float x)
     return y;
 }
 
-// Two sources (packed SX, SY, SZ, SM) acting on one receiver (packed broadcast
-// X, Y, Z); A = (phi, ax, ay, az), each the even-source and odd-source halves.
-__device__ __forceinline__ void p2p_two(f2_t SX, f2_t SY, f2_t SZ, f2_t SM, f2_t X, f2_t Y, f2_t Z, f2_t (&A)[4])
+// Two sources (packed SX, SY, SZ, SM) acting on one receiver given as the
+// negated broadcast position (NX, NY, NZ); A = (sum m/r, ax, ay, az), each the
+// even-source and odd-source halves (the potential is minus the first sum).
+__device__ __forceinline__ void p2p_two(float2 SX, float2 SY, float2 SZ, float2 SM, float2 NX, float2 NY, float2 NZ,
+                                        float2 (&A)[4])
 {
-    const f2_t dx = f2_sub(SX, X), dy = f2_sub(SY, Y), dz = f2_sub(SZ, Z);
-    f2_t r2 = f2_mul(dx, dx);
-    r2 = f2_fma(dy, dy, r2);
-    r2 = f2_fma(dz, dz, r2);
-    float ra, rb;
-    f2_unpack(r2, ra, rb);
-    const f2_t ri = f2_pack(rsqrt_ftz(ra), rsqrt_ftz(rb));
-    const f2_t mr = f2_mul(SM, ri);
-    const f2_t mr3 = f2_mul(mr, f2_mul(ri, ri));
-    A[1] = f2_fma(mr3, dx, A[1]);
-    A[2] = f2_fma(mr3, dy, A[2]);
-    A[3] = f2_fma(mr3, dz, A[3]);
-    A[0] = f2_sub(A[0], mr);
+    const float2 dx = __fadd2_rn(SX, NX), dy = __fadd2_rn(SY, NY), dz = __fadd2_rn(SZ, NZ);
+    float2 r2 = __fmul2_rn(dx, dx);
+    r2 = __ffma2_rn(dy, dy, r2);
+    r2 = __ffma2_rn(dz, dz, r2);
+    const float2 ri = make_float2(rsqrt_ftz(r2.x), rsqrt_ftz(r2.y));
+    const float2 mr = __fmul2_rn(SM, ri);
+    const float2 mr3 = __fmul2_rn(mr, __fmul2_rn(ri, ri));
+    A[1] = __ffma2_rn(mr3, dx, A[1]);
+    A[2] = __ffma2_rn(mr3, dy, A[2]);
+    A[3] = __ffma2_rn(mr3, dz, A[3]);
+    A[0] = __fadd2_rn(A[0], mr);
 }
 
 template <int CH>
@@ -246,23 +211,29 @@ __device__ __forceinline__ int stage_sources_pairs(float *fb, const float4 *__re
 }
 
 template <int K>
-__device__ __forceinline__ void p2p_span_pairs(const float *fb, int npairs, int q, int S, const f2_t (&X)[K],
-                                               const f2_t (&Y)[K], const f2_t (&Z)[K], f2_t (&A)[K][4])
+__device__ __forceinline__ void p2p_span_pairs(const float *fb, int npairs, int q, int S, const float2 (&X)[K],
+                                               const float2 (&Y)[K], const float2 (&Z)[K], float2 (&A)[K][4])
 {
-    const ulonglong2 *pb = reinterpret_cast<const ulonglong2 *>(fb);
+    const float4 *pb = reinterpret_cast<const float4 *>(fb);
     int j = q;
     for (; j + S < npairs; j += 2 * S) {
-        const ulonglong2 a0 = pb[2 * j], b0 = pb[2 * j + 1];
-        const ulonglong2 a1 = pb[2 * (j + S)], b1 = pb[2 * (j + S) + 1];
+        const float4 a0 = pb[2 * j], b0 = pb[2 * j + 1];
+        const float4 a1 = pb[2 * (j + S)], b1 = pb[2 * (j + S) + 1];
 #pragma unroll
-        for (int k = 0; k < K; ++k) p2p_two(a0.x, a0.y, b0.x, b0.y, X[k], Y[k], Z[k], A[k]);
+        for (int k = 0; k < K; ++k)
+            p2p_two(make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(b0.x, b0.y),
+                    make_float2(b0.z, b0.w), X[k], Y[k], Z[k], A[k]);
 #pragma unroll
-        for (int k = 0; k < K; ++k) p2p_two(a1.x, a1.y, b1.x, b1.y, X[k], Y[k], Z[k], A[k]);
+        for (int k = 0; k < K; ++k)
+            p2p_two(make_float2(a1.x, a1.y), make_float2(a1.z, a1.w), make_float2(b1.x, b1.y),
+                    make_float2(b1.z, b1.w), X[k], Y[k], Z[k], A[k]);
     }
     if (j < npairs) {
-        const ulonglong2 a0 = pb[2 * j], b0 = pb[2 * j + 1];
+        const float4 a0 = pb[2 * j], b0 = pb[2 * j + 1];
 #pragma unroll
-        for (int k = 0; k < K; ++k) p2p_two(a0.x, a0.y, b0.x, b0.y, X[k], Y[k], Z[k], A[k]);
+        for (int k = 0; k < K; ++k)
+            p2p_two(make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(b0.x, b0.y),
+                    make_float2(b0.z, b0.w), X[k], Y[k], Z[k], A[k]);
     }
 }
 
@@ -303,13 +274,13 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
     }
     // every other source leaf, 32 list entries at a time
     if constexpr (std::is_same<T, float>::value) {
-        f2_t X[K], Y[K], Z[K], A[K][4];
+        float2 X[K], Y[K], Z[K], A[K][4];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            X[k] = f2_pack(p[k].x, p[k].x);
-            Y[k] = f2_pack(p[k].y, p[k].y);
-            Z[k] = f2_pack(p[k].z, p[k].z);
-            A[k][0] = A[k][1] = A[k][2] = A[k][3] = f2_pack(0.0f, 0.0f);
+            X[k] = make_float2(-p[k].x, -p[k].x);
+            Y[k] = make_float2(-p[k].y, -p[k].y);
+            Z[k] = make_float2(-p[k].z, -p[k].z);
+            A[k][0] = A[k][1] = A[k][2] = A[k][3] = make_float2(0.0f, 0.0f);
         }
         float *fbuf = reinterpret_cast<float *>(buf);
         for (int lb = beg; lb < end; lb += 32) {
@@ -333,13 +304,11 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
             }
         }
 #pragma unroll
-        for (int k = 0; k < K; ++k)
+        for (int k = 0; k < K; ++k) {
+            acc[k][0] -= A[k][0].x + A[k][0].y;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                float lo, hi;
-                f2_unpack(A[k][v], lo, hi);
-                acc[k][v] += lo + hi;
-            }
+            for (int v = 1; v < 4; ++v) acc[k][v] += A[k][v].x + A[k][v].y;
+        }
     } else {
         for (int lb = beg; lb < end; lb += 32) {
             const int e = lb + lane;
