@@ -11,6 +11,7 @@
 // that would exceed one skips the write and sets a bit in the status word, and
 // the evaluation is repeated with larger buffers.
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -162,7 +163,7 @@ void destroy_plan(Plan &P)
     free_nodes(P);
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
-    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.rel); dfree(P.scratch); dfree(P.ctr);
+    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     if (P.ctr_host) cudaFreeHost(P.ctr_host);
     for (int i = 0; i < kNumEvents; ++i)
@@ -210,6 +211,7 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         // ---- phase 1
         record(P, 0, s);
         CUDA_TRY(cudaMemsetAsync(P.ctr, 0, sizeof(DevCounters), s));
+        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 2 * sizeof(GridBarrier), s));
         P.launches += launch_keys(P, pos, s);
         record(P, 1, s);
         P.launches += launch_sort(P, pos, mass, s);
@@ -350,20 +352,39 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     if (!ok(cudaGetDevice(&P.device), "cudaGetDevice")) return fail(FMM_ERR_CUDA);
     if (!ok(cudaDeviceGetAttribute(&P.num_sms, cudaDevAttrMultiProcessorCount, P.device), "SM count"))
         return fail(FMM_ERR_CUDA);
+    {
+        int coop = 0;
+        if (!ok(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, P.device), "cooperative launch"))
+            return fail(FMM_ERR_CUDA);
+        if (!coop) {
+            set_err("fmm_plan_create: the device does not support cooperative launches");
+            return fail(FMM_ERR_CUDA);
+        }
+        // co-resident blocks for the cooperative tree build: up to 4 per SM
+        // (grid barriers take up to 2048 blocks)
+        P.coop_blocks_tree = std::min(2048, P.num_sms * std::max(1, std::min(4, tree_max_blocks_per_sm())));
+        // walk: 8 blocks per SM from N = 2^19 on (large frontiers), 4 below (measured: the smaller grid
+        // syncs faster between the small generations of small trees)
+        const int wb = n >= (1 << 19) ? 8 : 4;
+        P.coop_blocks_walk = std::min(2048, P.num_sms * std::max(1, std::min(wb, walk_max_blocks_per_sm(P.dtype))));
+    }
     const size_t nn = (size_t)n, e = (size_t)P.esize;
     if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
         !ok(dalloc(P.idx[0], nn), "perm") || !ok(dalloc(P.idx[1], nn), "perm") ||
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
+        !ok(dalloc(P.gbar, 2), "grid barriers") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);
     for (int i = 0; i < kNumEvents; ++i)
         if (!ok(cudaEventCreate(&P.ev[i]), "events")) return fail(FMM_ERR_CUDA);
     const int64_t cap = minimal ? 1024 : node_estimate(P);
     if (alloc_nodes(P, cap) != FMM_OK) return fail(FMM_ERR_OOM);
-    const double lf = minimal ? 1.0 / 16 : 1.0;
-    if (alloc_lists(P, clamp_cap(8.0 * lf * cap), clamp_cap(48.0 * lf * cap), clamp_cap(12.0 * lf * cap)) != FMM_OK)
+    // list sizes per node grow like theta^-3 (the pairs a node meets before acceptance); sized for the
+    // clustered and Plummer workloads with room to spare, so that evaluations rarely regrow
+    const double lf = (minimal ? 1.0 / 16 : 1.0) * std::max(1.0, std::pow(0.7 / theta, 3.0));
+    if (alloc_lists(P, clamp_cap(16.0 * lf * cap), clamp_cap(64.0 * lf * cap), clamp_cap(24.0 * lf * cap)) != FMM_OK)
         return fail(FMM_ERR_OOM);
     return h;
 }

@@ -92,6 +92,44 @@ __device__ __forceinline__ dbl4 ld_cg(const dbl4 *p)
 
 __device__ __forceinline__ void set_error(DevCounters *c, unsigned bit) { atomicOr(&c->error, bit); }
 
+// ---- grid-wide barrier of a cooperative launch (all blocks co-resident) -----
+// One arrival counter per launch, on its own 128-byte line; it only grows:
+// barrier number k of a kernel completes when it reaches (k + 1) * gridDim.x.
+// Thread 0 of each block arrives with release semantics (after the block
+// barrier, so it publishes the whole block's writes) and waits with acquire
+// loads, bounded; the block barrier then passes the ordering on to the block's
+// other threads. Returns false, with ERR_SPIN set, if the wait gave up; every
+// block's wait is bounded the same way. (A two-level arrival tree measured no
+// faster at these grid sizes.)
+struct __align__(128) GridBarrier {
+    unsigned count;
+    unsigned pad[31];
+};
+
+__device__ __forceinline__ bool grid_barrier(GridBarrier *gb, unsigned k, DevCounters *ctr)
+{
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        cuda::atomic_ref<unsigned, cuda::thread_scope_device> c(gb->count);
+        c.fetch_add(1u, cuda::memory_order_release);
+        const unsigned target = (k + 1) * gridDim.x;
+        unsigned spins = 0;
+        while (c.load(cuda::memory_order_acquire) < target) {
+            if (++spins > (1u << 22)) {
+                set_error(ctr, ERR_SPIN);
+                ok = 0;
+                break;
+            }
+            __nanosleep(20);
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
 // ---- chained scan with decoupled look-back ---------------------------------
 // Flag word: [63:40] epoch, [39:38] state (1 = aggregate, 2 = inclusive prefix), [37:0] value.
 constexpr unsigned long long kFlagValueMask = (1ull << 38) - 1;
@@ -112,6 +150,14 @@ __device__ __forceinline__ unsigned long long flag_load(unsigned long long *p)
 {
     cuda::atomic_ref<unsigned long long, cuda::thread_scope_device> r(*p);
     return r.load(cuda::memory_order_acquire);
+}
+
+// Relaxed flag read: the flag word carries its value, nothing else is read on
+// its strength, so no acquire ordering is needed (and several can be in flight).
+__device__ __forceinline__ unsigned long long flag_load_relaxed(unsigned long long *p)
+{
+    cuda::atomic_ref<unsigned long long, cuda::thread_scope_device> r(*p);
+    return r.load(cuda::memory_order_relaxed);
 }
 
 // Exclusive prefix of `aggregate` over the tiles before `tile` in one chained
@@ -150,11 +196,60 @@ __device__ __forceinline__ unsigned long long chained_exclusive(unsigned long lo
     return excl;
 }
 
+// The same exclusive prefix for one thread, reading W predecessors' flags per
+// round (independent loads, so one round costs about one load latency): their
+// values are added from the nearest back until an inclusive prefix; a flag not
+// yet published ends the round and the next round starts at it. Bounded like
+// chained_exclusive.
+template <int W>
+__device__ __forceinline__ unsigned long long chained_exclusive_wide(unsigned long long *flags, int stride, int tile,
+                                                                     unsigned long long aggregate, unsigned epoch,
+                                                                     DevCounters *ctr)
+{
+    if (tile == 0) {
+        flag_store(flags, flag_pack(epoch, 2, aggregate));
+        return 0;
+    }
+    flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 1, aggregate));
+    unsigned long long excl = 0;
+    int t = tile - 1;
+    unsigned spins = 0;
+    const unsigned long long ep = (unsigned long long)(epoch & 0xffffffu);
+    while (t >= 0) {
+        unsigned long long f[W];
+#pragma unroll
+        for (int i = 0; i < W; ++i) f[i] = t - i >= 0 ? flag_load_relaxed(flags + (size_t)(t - i) * stride) : 0ull;
+        bool done = false, stalled = false;
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            if (done || stalled || t < 0) continue;
+            const unsigned state = (unsigned)((f[i] >> 38) & 3u);
+            if ((f[i] >> 40) != ep || state == 0) {
+                stalled = true;
+                continue;
+            }
+            excl += f[i] & kFlagValueMask;
+            if (state == 2) done = true;
+            --t;
+        }
+        if (done) break;
+        if (stalled && ++spins > kSpinLimit) {
+            set_error(ctr, ERR_SPIN);
+            break;
+        }
+    }
+    flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 2, excl + aggregate));
+    return excl;
+}
+
 // The same exclusive prefix computed by a whole warp (every lane calls it, lane
-// 0's `aggregate` counts): each round reads 32 predecessors' flags at once and
-// adds them up to the nearest inclusive prefix, so the look-back takes one
-// round per 32 tiles without an inclusive prefix. Returns the prefix to every
-// lane. Bounded like chained_exclusive.
+// 0's `aggregate` counts): each round reads 32 W predecessors' flags at once
+// (lane l, slot k holds tile - 1 - l - 32 k; relaxed loads, the flag carries
+// its value) and adds them up to the nearest inclusive prefix, so the look-back
+// advances 32 W tiles per round without an inclusive prefix -- and, when all
+// tiles run at once, inclusive prefixes spread 32 W tiles per round. Returns
+// the prefix to every lane. Bounded like chained_exclusive.
+template <int W = 1>
 __device__ __forceinline__ unsigned long long chained_exclusive_warp(unsigned long long *flags, int stride, int tile,
                                                                      unsigned long long aggregate, unsigned epoch,
                                                                      DevCounters *ctr)
@@ -170,30 +265,50 @@ __device__ __forceinline__ unsigned long long chained_exclusive_warp(unsigned lo
     int t = tile - 1;
     unsigned spins = 0;
     for (;;) {
-        const int idx = t - lane;
-        unsigned state = 2;  // before tile 0: an inclusive prefix of 0
-        unsigned long long v = 0;
-        if (idx >= 0) {
-            const unsigned long long f = flag_load(flags + (size_t)idx * stride);
-            state = (f >> 40) == ep ? (unsigned)((f >> 38) & 3u) : 0u;
-            v = f & kFlagValueMask;
+        unsigned state[W];
+        unsigned long long v[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            const int idx = t - lane - 32 * k;
+            state[k] = 2;  // before tile 0: an inclusive prefix of 0
+            v[k] = 0;
+            if (idx >= 0) {
+                const unsigned long long f = flag_load_relaxed(flags + (size_t)idx * stride);
+                state[k] = (f >> 40) == ep ? (unsigned)((f >> 38) & 3u) : 0u;
+                v[k] = f & kFlagValueMask;
+            }
         }
-        const unsigned incl_mask = __ballot_sync(kFull, state == 2);
-        const unsigned wait_mask = __ballot_sync(kFull, state == 0);
-        const int stop = incl_mask ? __ffs(incl_mask) - 1 : 31;   // lanes 0..stop are needed
-        const unsigned need = stop == 31 ? kFull : ((2u << stop) - 1u);
-        if (wait_mask & need) {
+        // nearest inclusive prefix in the window: slot kstop, lane stop
+        int kstop = W, stop = 31;
+#pragma unroll
+        for (int k = W - 1; k >= 0; --k) {
+            const unsigned incl = __ballot_sync(kFull, state[k] == 2);
+            if (incl) {
+                kstop = k;
+                stop = __ffs(incl) - 1;
+            }
+        }
+        bool wait = false;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            const unsigned need = k < kstop ? kFull : (k == kstop ? (stop == 31 ? kFull : ((2u << stop) - 1u)) : 0u);
+            wait |= (__ballot_sync(kFull, state[k] == 0) & need) != 0u;
+        }
+        if (wait) {
             if (++spins > kSpinLimit) {
                 if (lane == 0) set_error(ctr, ERR_SPIN);
                 break;
             }
             continue;
         }
-        unsigned long long s = lane <= stop ? v : 0ull;
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
-        excl += s;
-        if (incl_mask) break;
-        t -= 32;
+        unsigned long long sum = 0;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+            if (k < kstop || (k == kstop && lane <= stop)) sum += v[k];
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        excl += sum;
+        if (kstop < W) break;
+        t -= 32 * W;
     }
     if (lane == 0) flag_store(flags + (size_t)tile * stride, flag_pack(epoch, 2, excl + aggregate));
     return excl;

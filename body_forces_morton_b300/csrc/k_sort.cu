@@ -199,7 +199,7 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
             s_hist[w][d] = tot;
             tot += c;
         }
-        unsigned long long excl = chained_exclusive(flags + d, 256, tile, tot, epoch, ctr);
+        unsigned long long excl = chained_exclusive_wide<8>(flags + d, 256, tile, tot, epoch, ctr);
         // exclusive scan over digits of this pass's global histogram
         unsigned g = ctr->hist[pass][d];
         unsigned incl = g;

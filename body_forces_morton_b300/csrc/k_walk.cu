@@ -11,8 +11,9 @@
 //   otherwise split the node with the larger |l| (the lower index on a tie),
 //   never a leaf, and visit (child, other).
 // The set of pairs this produces does not depend on the visiting order, so
-// the walk runs breadth first: one kernel per frontier generation, appending
-// through warp-aggregated atomics on sharded output lists.
+// the walk runs breadth first, all frontier generations in one cooperative
+// launch with a grid barrier between generations, appending through
+// block-aggregated atomics on sharded output lists.
 //
 // Lists: per-receiver counts (taken during the walk) -> exclusive scan (one
 // kernel, decoupled look-back) -> atomic fill -> every receiver's segment sorted
@@ -44,7 +45,7 @@ __device__ __forceinline__ void shard_prefix(const int *cnt, int cap_s, int *s_p
     const int t = threadIdx.x, lane = t & 31;
     int v = 0, incl = 0;
     if (t < kShards) {
-        v = min(cnt[t], cap_s);
+        v = min(ld_cg(cnt + t), cap_s);
         incl = warp_incl_scan(v);
         if (t == 31) s_half = incl;
     }
@@ -68,131 +69,136 @@ __device__ __forceinline__ size_t shard_addr(const int *s_pre, int g, int cap_s)
     return (size_t)lo * cap_s + (g - s_pre[lo]);
 }
 
-// One generation of the walk: every frontier pair is decided and its outputs
-// (an M2L pair, a P2P pair or child pairs) are appended. Each output list is
-// split into kShards shards with their own counters; a block reserves the
-// space of a whole 256-pair tile in the shard of its index with one atomic per
-// list, so no single counter is hot.
+// The walk: `iters` generations. In each, every frontier pair is decided and
+// its outputs (an M2L pair, a P2P pair or child pairs) are appended. Each output
+// list is split into kShards shards with their own counters; a block reserves
+// the space of a whole 256-pair tile in the shard of its index with one atomic
+// per list, so no single counter is hot. The frontier and its counts were
+// written by other blocks of this launch, so they are read through L2.
 template <class T>
-__global__ __launch_bounds__(WK_THREADS) void k_walk_iter(int it, const int2 *__restrict__ fin, int2 *__restrict__ fout,
-                                                          int capf_s, const int *__restrict__ nchild,
-                                                          const int *__restrict__ child0,
-                                                          const int *__restrict__ count,
-                                                          const vec4<T> *__restrict__ nc,
-                                                          const vec4<T> *__restrict__ nl, T th2, int2 *m2l_pairs,
-                                                          int capm_s, int2 *p2p_pairs, int capp_s, int *m2l_cnt,
-                                                          int *p2p_cnt, DevCounters *ctr)
+__global__ __launch_bounds__(WK_THREADS) void k_walk_all(int iters, int2 *f0, int2 *f1, int capf_s,
+                                                         const int *__restrict__ nchild,
+                                                         const int *__restrict__ child0,
+                                                         const int *__restrict__ count,
+                                                         const vec4<T> *__restrict__ nc,
+                                                         const vec4<T> *__restrict__ nl, T th2, int2 *m2l_pairs,
+                                                         int capm_s, int2 *p2p_pairs, int capp_s, int *m2l_cnt,
+                                                         int *p2p_cnt, GridBarrier *gb, DevCounters *ctr)
 {
     __shared__ int s_pre[kShards + 1];
-    int *cnt_in = ctr->frontier_cnt[it % 3];
-    int *cnt_out = ctr->frontier_cnt[(it + 1) % 3];
-    if (blockIdx.x == 0 && threadIdx.x < kShards) ctr->frontier_cnt[(it + 2) % 3][threadIdx.x] = 0;
-    shard_prefix(cnt_in, capf_s, s_pre);
-    const int nread = s_pre[kShards];
-    const int lane = threadIdx.x & 31;
     __shared__ int s_wtot[3][WK_THREADS / 32];
     __shared__ int s_base[3];
-    long long inter_sum = 0;
-    int visited = 0, fill_max = 0;
+    const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int bshard = blockIdx.x % kShards;
-    for (int base = blockIdx.x * WK_THREADS; base < nread; base += gridDim.x * WK_THREADS) {
-        const int i = base + threadIdx.x;
-        int A = -1, B = -1, kids = 0, split = -1, other = 0, m2l = 0, p2p = 0;
-        if (i < nread) {
-            const int2 pr = fin[shard_addr(s_pre, i, capf_s)];
-            A = pr.x;
-            B = pr.y;
-            ++visited;
-            const int nA = nchild[A];
-            if (A == B) {
-                if (nA == 0) {
-                    p2p = 1;
-                    inter_sum += (long long)count[A] * count[A];
-                } else {
-                    kids = nA * (nA + 1) / 2;
-                    split = A;
-                }
-            } else {
-                const int nB = nchild[B];
-                const vec4<T> cA = nc[A], cB = nc[B], lA = nl[A], lB = nl[B];
-                const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
-                const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
-                if (s2 < mul_rn(th2, r2)) {
-                    m2l = 1;
-                } else if (nA == 0 && nB == 0) {
-                    p2p = 1;
-                    inter_sum += 2ll * count[A] * count[B];
-                } else {
-                    const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
-                    split = splitA ? A : B;
-                    other = splitA ? B : A;
-                    kids = splitA ? nA : nB;
-                }
-            }
-        }
-        // warp scans, then one exchange of the warp totals and one atomic per list per tile
-        const int im = warp_incl_scan(m2l), ip = warp_incl_scan(p2p), ik = warp_incl_scan(kids);
-        if (lane == 31) {
-            s_wtot[0][warp] = im;
-            s_wtot[1][warp] = ip;
-            s_wtot[2][warp] = ik;
-        }
-        __syncthreads();
-        if (threadIdx.x < 3) {
-            const int list = threadIdx.x;
-            int run = 0;
-            for (int w2 = 0; w2 < WK_THREADS / 32; ++w2) {
-                const int t = s_wtot[list][w2];
-                s_wtot[list][w2] = run;
-                run += t;
-            }
-            int *ctrp = list == 0 ? &ctr->n_m2l_pairs[bshard] : (list == 1 ? &ctr->n_p2p_pairs[bshard] : &cnt_out[bshard]);
-            const int b0 = run ? atomicAdd(ctrp, run) : 0;
-            s_base[list] = b0;
-            if (list == 2) fill_max = max(fill_max, b0 + run);
-        }
-        __syncthreads();
-        if (m2l) {
-            const int slot = s_base[0] + s_wtot[0][warp] + im - 1;
-            if (slot < capm_s) {
-                m2l_pairs[(size_t)bshard * capm_s + slot] = make_int2(A, B);
-                atomicAdd(&m2l_cnt[A], 1);
-                atomicAdd(&m2l_cnt[B], 1);
-            } else {
-                set_error(ctr, ERR_M2L_CAP);
-            }
-        }
-        if (p2p) {
-            const int slot = s_base[1] + s_wtot[1][warp] + ip - 1;
-            if (slot < capp_s) {
-                p2p_pairs[(size_t)bshard * capp_s + slot] = make_int2(A, B);
-                atomicAdd(&p2p_cnt[A], 1);
-                if (A != B) atomicAdd(&p2p_cnt[B], 1);
-            } else {
-                set_error(ctr, ERR_P2P_CAP);
-            }
-        }
-        if (kids) {
-            int o = s_base[2] + s_wtot[2][warp] + ik - kids;
-            int2 *dst = fout + (size_t)bshard * capf_s;
-            const int c0 = child0[split];
-            if (A == B) {
+    long long inter_sum = 0;
+    int visited = 0, fill_max = 0;
+    for (int it = 0; it < iters; ++it) {
+        const int2 *fin = (it & 1) ? f1 : f0;
+        int2 *fout = (it & 1) ? f0 : f1;
+        int *cnt_out = ctr->frontier_cnt[(it + 1) % 3];
+        if (blockIdx.x == 0 && threadIdx.x < kShards) ctr->frontier_cnt[(it + 2) % 3][threadIdx.x] = 0;
+        shard_prefix(ctr->frontier_cnt[it % 3], capf_s, s_pre);
+        const int nread = s_pre[kShards];
+        for (int base = blockIdx.x * WK_THREADS; base < nread; base += gridDim.x * WK_THREADS) {
+            const int i = base + threadIdx.x;
+            int A = -1, B = -1, kids = 0, split = -1, other = 0, m2l = 0, p2p = 0;
+            if (i < nread) {
+                const int2 pr = ld_cg(fin + shard_addr(s_pre, i, capf_s));
+                A = pr.x;
+                B = pr.y;
+                ++visited;
                 const int nA = nchild[A];
-                for (int x = 0; x < nA; ++x)
-                    for (int y = x; y < nA; ++y, ++o) {
-                        if (o < capf_s) dst[o] = make_int2(c0 + x, c0 + y);
+                if (A == B) {
+                    if (nA == 0) {
+                        p2p = 1;
+                        inter_sum += (long long)count[A] * count[A];
+                    } else {
+                        kids = nA * (nA + 1) / 2;
+                        split = A;
+                    }
+                } else {
+                    const int nB = nchild[B];
+                    const vec4<T> cA = nc[A], cB = nc[B], lA = nl[A], lB = nl[B];
+                    const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
+                    const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
+                    if (s2 < mul_rn(th2, r2)) {
+                        m2l = 1;
+                    } else if (nA == 0 && nB == 0) {
+                        p2p = 1;
+                        inter_sum += 2ll * count[A] * count[B];
+                    } else {
+                        const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
+                        split = splitA ? A : B;
+                        other = splitA ? B : A;
+                        kids = splitA ? nA : nB;
+                    }
+                }
+            }
+            // warp scans, then one exchange of the warp totals and one atomic per list per tile
+            const int im = warp_incl_scan(m2l), ip = warp_incl_scan(p2p), ik = warp_incl_scan(kids);
+            if (lane == 31) {
+                s_wtot[0][warp] = im;
+                s_wtot[1][warp] = ip;
+                s_wtot[2][warp] = ik;
+            }
+            __syncthreads();
+            if (threadIdx.x < 3) {
+                const int list = threadIdx.x;
+                int run = 0;
+                for (int w2 = 0; w2 < WK_THREADS / 32; ++w2) {
+                    const int t = s_wtot[list][w2];
+                    s_wtot[list][w2] = run;
+                    run += t;
+                }
+                int *ctrp = list == 0 ? &ctr->n_m2l_pairs[bshard] : (list == 1 ? &ctr->n_p2p_pairs[bshard] : &cnt_out[bshard]);
+                const int b0 = run ? atomicAdd(ctrp, run) : 0;
+                s_base[list] = b0;
+                if (list == 2) fill_max = max(fill_max, b0 + run);
+            }
+            __syncthreads();
+            if (m2l) {
+                const int slot = s_base[0] + s_wtot[0][warp] + im - 1;
+                if (slot < capm_s) {
+                    m2l_pairs[(size_t)bshard * capm_s + slot] = make_int2(A, B);
+                    atomicAdd(&m2l_cnt[A], 1);
+                    atomicAdd(&m2l_cnt[B], 1);
+                } else {
+                    set_error(ctr, ERR_M2L_CAP);
+                }
+            }
+            if (p2p) {
+                const int slot = s_base[1] + s_wtot[1][warp] + ip - 1;
+                if (slot < capp_s) {
+                    p2p_pairs[(size_t)bshard * capp_s + slot] = make_int2(A, B);
+                    atomicAdd(&p2p_cnt[A], 1);
+                    if (A != B) atomicAdd(&p2p_cnt[B], 1);
+                } else {
+                    set_error(ctr, ERR_P2P_CAP);
+                }
+            }
+            if (kids) {
+                int o = s_base[2] + s_wtot[2][warp] + ik - kids;
+                int2 *dst = fout + (size_t)bshard * capf_s;
+                const int c0 = child0[split];
+                if (A == B) {
+                    const int nA = nchild[A];
+                    for (int x = 0; x < nA; ++x)
+                        for (int y = x; y < nA; ++y, ++o) {
+                            if (o < capf_s) dst[o] = make_int2(c0 + x, c0 + y);
+                            else set_error(ctr, ERR_FRONTIER);
+                        }
+                } else {
+                    for (int x = 0; x < kids; ++x, ++o) {
+                        const int C = c0 + x;
+                        if (o < capf_s) dst[o] = C < other ? make_int2(C, other) : make_int2(other, C);
                         else set_error(ctr, ERR_FRONTIER);
                     }
-            } else {
-                for (int x = 0; x < kids; ++x, ++o) {
-                    const int C = c0 + x;
-                    if (o < capf_s) dst[o] = C < other ? make_int2(C, other) : make_int2(other, C);
-                    else set_error(ctr, ERR_FRONTIER);
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
+        if (!grid_barrier(gb, (unsigned)it, ctr)) break;
     }
     // per-warp statistics, one atomic each
     for (int o = 16; o > 0; o >>= 1) {
@@ -524,19 +530,29 @@ __global__ __launch_bounds__(256) void k_order_scatter(int n_nodes, const uint8_
 template <class T>
 int launch_walk_t(Plan &P, int depth, cudaStream_t s)
 {
-    const T th2 = (T)(P.theta * P.theta);
+    T th2 = (T)(P.theta * P.theta);
     k_walk_init<<<1, 1, 0, s>>>(P.frontier[0], P.ctr);
-    const int iters = 2 * depth + 1;
-    for (int it = 0; it < iters; ++it) {
-        k_walk_iter<T><<<P.num_sms * 8, WK_THREADS, 0, s>>>(
-            it, P.frontier[it & 1], P.frontier[(it + 1) & 1], (int)(P.cap_frontier / kShards), P.node_nchild,
-            P.node_child0, P.node_count, (const vec4<T> *)P.node_c, (const vec4<T> *)P.node_l, th2, P.m2l_pairs,
-            (int)(P.cap_m2l / kShards), P.p2p_pairs, (int)(P.cap_p2p / kShards), P.m2l_cnt, P.p2p_cnt, P.ctr);
-    }
-    return iters + 1;
+    int iters = 2 * depth + 1;
+    int capf_s = (int)(P.cap_frontier / kShards), capm_s = (int)(P.cap_m2l / kShards);
+    int capp_s = (int)(P.cap_p2p / kShards);
+    const vec4<T> *nc = (const vec4<T> *)P.node_c, *nl = (const vec4<T> *)P.node_l;
+    GridBarrier *gb = P.gbar + 1;
+    void *args[] = {&iters, &P.frontier[0], &P.frontier[1], &capf_s, &P.node_nchild, &P.node_child0, &P.node_count,
+                    (void *)&nc, (void *)&nl, &th2, &P.m2l_pairs, &capm_s, &P.p2p_pairs, &capp_s, &P.m2l_cnt,
+                    &P.p2p_cnt, &gb, &P.ctr};
+    cudaLaunchCooperativeKernel((const void *)k_walk_all<T>, dim3(P.coop_blocks_walk), dim3(WK_THREADS), args, 0, s);
+    return 2;
 }
 
 }  // namespace
+
+int walk_max_blocks_per_sm(int dtype)
+{
+    int b = 0;
+    if (dtype == 0) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_walk_all<float>, WK_THREADS, 0);
+    else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_walk_all<double>, WK_THREADS, 0);
+    return b;
+}
 
 int launch_walk(Plan &P, int depth, cudaStream_t s)
 {

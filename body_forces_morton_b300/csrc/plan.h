@@ -25,6 +25,8 @@ struct Plan {
     int esize = 4;      // bytes per real
     int device = 0;
     int num_sms = 148;
+    int coop_blocks_tree = 148;   // grids of the cooperative launches (co-resident blocks)
+    int coop_blocks_walk = 148;
 
     // capacities
     int64_t cap_nodes = 0, cap_frontier = 0, cap_m2l = 0, cap_p2p = 0, cap_flags = 0;
@@ -65,6 +67,7 @@ struct Plan {
 
     // status
     DevCounters *ctr = nullptr;      // device
+    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0] and walk [1] launches
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
@@ -96,6 +99,8 @@ struct Plan {
 int launch_keys(Plan &P, const void *pos, cudaStream_t s);
 int launch_sort(Plan &P, const void *pos, const void *mass, cudaStream_t s);
 int launch_tree(Plan &P, cudaStream_t s);
+int tree_max_blocks_per_sm();
+int walk_max_blocks_per_sm(int dtype);
 int launch_upward(Plan &P, cudaStream_t s);
 int launch_walk(Plan &P, int depth, cudaStream_t s);
 int launch_lists(Plan &P, cudaStream_t s);
