@@ -208,16 +208,36 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
             CUDA_TRY(cudaMemsetAsync(P.flags, 0, (size_t)P.cap_flags * sizeof(unsigned long long), s));
             P.epoch = 0;
         }
-        // ---- phase 1
+        // ---- phase 1: box, keys, sort, tree (the tree kernel records the node count and depth)
         record(P, 0, s);
         CUDA_TRY(cudaMemsetAsync(P.ctr, 0, sizeof(DevCounters), s));
-        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 2 * sizeof(GridBarrier), s));
+        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 3 * sizeof(GridBarrier), s));
         P.launches += launch_keys(P, pos, s);
         record(P, 1, s);
         P.launches += launch_sort(P, pos, mass, s);
         record(P, 2, s);
         P.launches += launch_tree(P, s);
         record(P, 3, s);
+        // ---- phase 2, launched without waiting: every kernel reads the node count (and the walk
+        // and L2L their extent) on the device, and skips the tree if its build failed
+        record(P, 4, s);
+        CUDA_TRY(cudaMemsetAsync(P.node_done, 0, (size_t)P.cap_nodes * sizeof(int), s));
+        CUDA_TRY(cudaMemsetAsync(P.m2l_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
+        CUDA_TRY(cudaMemsetAsync(P.p2p_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
+        P.launches += launch_upward(P, s);
+        record(P, 5, s);
+        P.launches += launch_walk(P, 0, s);
+        record(P, 6, s);
+        P.launches += launch_lists(P, s);
+        record(P, 7, s);
+        P.launches += launch_m2l(P, s);
+        record(P, 8, s);
+        P.launches += launch_l2l(P, 0, s);
+        record(P, 9, s);
+        P.launches += launch_l2p(P, s);
+        record(P, 11, s);
+        P.launches += launch_p2p(P, acc, pot, s);
+        record(P, 10, s);
         fmm_status st = sync_counters(P, s);
         if (st) return st;
         const DevCounters &h = *P.ctr_host;
@@ -231,36 +251,8 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
             P.retries++;
             continue;
         }
-        if (h.error) {
-            set_err("fmm_eval: device check failed in the tree build: %s", error_bits(h.error));
-            return FMM_ERR_INTERNAL;
-        }
-        int depth = 0;
-        for (int l = 0; l <= kMaxLevel; ++l)
-            if (h.level_off[l + 1] > h.level_off[l]) depth = l;
-        P.depth = depth;
-        P.n_nodes = h.level_off[depth + 1];
-        // ---- phase 2
-        record(P, 4, s);
-        CUDA_TRY(cudaMemsetAsync(P.node_done, 0, (size_t)P.n_nodes * sizeof(int), s));
-        CUDA_TRY(cudaMemsetAsync(P.m2l_cnt, 0, (size_t)P.n_nodes * sizeof(int), s));
-        CUDA_TRY(cudaMemsetAsync(P.p2p_cnt, 0, (size_t)P.n_nodes * sizeof(int), s));
-        P.launches += launch_upward(P, s);
-        record(P, 5, s);
-        P.launches += launch_walk(P, depth, s);
-        record(P, 6, s);
-        P.launches += launch_lists(P, s);
-        record(P, 7, s);
-        P.launches += launch_m2l(P, s);
-        record(P, 8, s);
-        P.launches += launch_l2l(P, depth, s);
-        record(P, 9, s);
-        P.launches += launch_l2p(P, s);
-        record(P, 11, s);
-        P.launches += launch_p2p(P, acc, pot, s);
-        record(P, 10, s);
-        st = sync_counters(P, s);
-        if (st) return st;
+        P.depth = h.depth;
+        P.n_nodes = h.n_nodes;
         const unsigned cap_bits = ERR_FRONTIER | ERR_M2L_CAP | ERR_P2P_CAP;
         if (h.error & cap_bits) {
             // sharded lists: grow to 1.5x the fullest shard (or double), times the shard count
@@ -282,15 +274,10 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
             set_err("fmm_eval: device check failed: %s", error_bits(h.error));
             return FMM_ERR_INTERNAL;
         }
-        int64_t left = 0, m2l_pairs = 0, p2p_pairs = 0;
+        int64_t m2l_pairs = 0, p2p_pairs = 0;
         for (int s2 = 0; s2 < kShards; ++s2) {
-            left += h.frontier_cnt[(2 * depth + 1) % 3][s2];
             m2l_pairs += h.n_m2l_pairs[s2];
             p2p_pairs += h.n_p2p_pairs[s2];
-        }
-        if (left != 0) {
-            set_err("fmm_eval: dual-tree walk did not finish in %d generations", 2 * depth + 1);
-            return FMM_ERR_INTERNAL;
         }
         P.n_m2l = 2 * m2l_pairs;
         P.n_p2p_pairs = p2p_pairs;
@@ -374,7 +361,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
-        !ok(dalloc(P.gbar, 2), "grid barriers") ||
+        !ok(dalloc(P.gbar, 3), "grid barriers") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);
     for (int i = 0; i < kNumEvents; ++i)

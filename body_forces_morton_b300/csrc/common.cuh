@@ -92,6 +92,15 @@ __device__ __forceinline__ dbl4 ld_cg(const dbl4 *p)
 
 __device__ __forceinline__ void set_error(DevCounters *c, unsigned bit) { atomicOr(&c->error, bit); }
 
+// Node count for the kernels after the tree build, read on the device (they are
+// launched without the host waiting for the tree): 0 when the tree build failed
+// (node capacity exceeded or a non-finite position), so that every later stage
+// skips the inconsistent tree and the evaluation retries or reports the error.
+__device__ __forceinline__ int phase2_nodes(const DevCounters *ctr)
+{
+    return (ctr->error & (ERR_NODES | ERR_NONFINITE)) ? 0 : ctr->n_nodes;
+}
+
 // ---- grid-wide barrier of a cooperative launch (all blocks co-resident) -----
 // One arrival counter per launch, on its own 128-byte line; it only grows:
 // barrier number k of a kernel completes when it reaches (k + 1) * gridDim.x.

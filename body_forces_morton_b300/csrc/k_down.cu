@@ -18,34 +18,47 @@
 #include "expansions_gen.cuh"
 #include "plan.h"
 
+#include <algorithm>
+
 namespace bfm {
 
 namespace {
 
+// L2L, all levels in one cooperative launch with a grid barrier between
+// levels: a node's complete local is its own M2L local plus its parent's
+// complete local translated to its centre. The parent's local was written by
+// another block before the barrier; the barrier's acquire orders it before
+// these (cached) loads, which siblings share.
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_l2l(int level, const DevCounters *__restrict__ ctr,
-                                             const int *__restrict__ parent, const vec4<T> *__restrict__ nc,
-                                             const T *__restrict__ Lm2l, T *__restrict__ L, int ncp)
+__global__ __launch_bounds__(256) void k_l2l_all(GridBarrier *gb, DevCounters *ctr, const int *__restrict__ parent,
+                                                 const vec4<T> *__restrict__ nc, const T *__restrict__ Lm2l,
+                                                 T *__restrict__ L, int ncp)
 {
     constexpr int NC = Exp<P>::NC;
-    const int lo = ctr->level_off[level], hi = ctr->level_off[level + 1];
-    for (int a = lo + blockIdx.x * blockDim.x + threadIdx.x; a < hi; a += gridDim.x * blockDim.x) {
-        T out[NC];
-        const T *own = Lm2l + (size_t)a * ncp;
+    const int n = phase2_nodes(ctr);
+    const int depth = n > 0 ? ctr->depth : -1;
+    for (int level = 0; level <= depth; ++level) {
+        const int lo = ctr->level_off[level], hi = min(ctr->level_off[level + 1], n);
+        for (int a = lo + blockIdx.x * blockDim.x + threadIdx.x; a < hi; a += gridDim.x * blockDim.x) {
+            T out[NC];
+            const T *own = Lm2l + (size_t)a * ncp;
 #pragma unroll
-        for (int k = 0; k < NC; ++k) out[k] = own[k];
-        if (level > 0) {
-            const int par = parent[a];
-            T lp[NC];
-            const T *pr = L + (size_t)par * ncp;
+            for (int k = 0; k < NC; ++k) out[k] = own[k];
+            if (level > 0) {
+                const int par = parent[a];
+                T lp[NC];
+                const T *pr = L + (size_t)par * ncp;
 #pragma unroll
-            for (int k = 0; k < NC; ++k) lp[k] = pr[k];
-            const vec4<T> c = nc[a], cp = nc[par];
-            Exp<P>::template l2l<T>(lp, c.x - cp.x, c.y - cp.y, c.z - cp.z, out);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) lp[k] = pr[k];
+                const vec4<T> c = nc[a], cp = nc[par];
+                Exp<P>::template l2l<T>(lp, c.x - cp.x, c.y - cp.y, c.z - cp.z, out);
+            }
+            T *dst = L + (size_t)a * ncp;
+#pragma unroll
+            for (int k = 0; k < NC; ++k) dst[k] = out[k];
         }
-        T *dst = L + (size_t)a * ncp;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) dst[k] = out[k];
+        if (level < depth && !grid_barrier(gb, (unsigned)level, ctr)) return;
     }
 }
 
@@ -71,11 +84,12 @@ __device__ __forceinline__ void p2p_one(const vec4<T> &s, T x, T y, T z, T &phi,
 // L2P: the complete local expansion of every leaf at its particles, into `far`
 // (sorted order, (phi, ax, ay, az)); the P2P kernel adds the near field.
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_l2p(int n_nodes, const int *__restrict__ first, const int *__restrict__ count,
+__global__ __launch_bounds__(256) void k_l2p(const DevCounters *__restrict__ nctr, const int *__restrict__ first, const int *__restrict__ count,
                                              const int *__restrict__ nchild, const vec4<T> *__restrict__ xyzm,
                                              const vec4<T> *__restrict__ nc, const T *__restrict__ L, int ncp,
                                              vec4<T> *__restrict__ far)
 {
+    const int n_nodes = phase2_nodes(nctr);
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
@@ -415,16 +429,27 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
 template <class T, int P>
 int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 {
-    for (int level = 0; level <= depth; ++level)
-        k_l2l<T, P><<<P_.num_sms * 4, 256, 0, s>>>(level, P_.ctr, P_.node_parent, (const vec4<T> *)P_.node_c,
-                                                   (const T *)P_.Lm2l, (T *)P_.L, P_.ncp);
-    return depth + 1;
+    (void)depth;
+    static const int occ = [] {
+        int b = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_l2l_all<T, P>, 256, 0);
+        return b;
+    }();
+    const int blocks = std::min(2048, P_.num_sms * std::max(1, std::min(4, occ)));
+    GridBarrier *gb = P_.gbar + 2;
+    const vec4<T> *nc = (const vec4<T> *)P_.node_c;
+    const T *lm = (const T *)P_.Lm2l;
+    T *l = (T *)P_.L;
+    int ncp = P_.ncp;
+    void *args[] = {&gb, &P_.ctr, &P_.node_parent, (void *)&nc, (void *)&lm, (void *)&l, &ncp};
+    cudaLaunchCooperativeKernel((const void *)k_l2l_all<T, P>, dim3(blocks), dim3(256), args, 0, s);
+    return 1;
 }
 
 template <class T, int P>
 int launch_l2p_tp(Plan &P_, cudaStream_t s)
 {
-    k_l2p<T, P><<<P_.num_sms * 8, 256, 0, s>>>((int)P_.n_nodes, P_.node_first, P_.node_count, P_.node_nchild,
+    k_l2p<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.node_first, P_.node_count, P_.node_nchild,
                                                (const vec4<T> *)P_.xyzm, (const vec4<T> *)P_.node_c,
                                                (const T *)P_.L, P_.ncp, (vec4<T> *)P_.far);
     return 1;

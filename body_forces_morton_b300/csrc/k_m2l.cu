@@ -48,8 +48,9 @@ template <class T, int P> struct M2LShape {
 
 // Reduced moments of every node: Mr[b] = reduce_m(M[b]), padding zeroed.
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_moments_r(int n_nodes, const T *__restrict__ M, T *__restrict__ Mr)
+__global__ __launch_bounds__(256) void k_moments_r(const DevCounters *__restrict__ nctr, const T *__restrict__ M, T *__restrict__ Mr)
 {
+    const int n_nodes = phase2_nodes(nctr);
     using S = M2LShape<T, P>;
     for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < n_nodes; b += gridDim.x * blockDim.x) {
         T r[S::NRP];
@@ -62,12 +63,13 @@ __global__ __launch_bounds__(256) void k_moments_r(int n_nodes, const T *__restr
 }
 
 template <class T, int P>
-__global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(int n_nodes, const int *__restrict__ order,
+__global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__restrict__ nctr, const int *__restrict__ order,
                                                         const int *__restrict__ off,
                                                         const int *__restrict__ src, const vec4<T> *__restrict__ nc,
                                                         const T *__restrict__ Mr, T *__restrict__ Lout,
                                                         DevCounters *ctr)
 {
+    const int n_nodes = phase2_nodes(nctr);
     using S = M2LShape<T, P>;
     using V16 = typename Vec16<T>::type;
     extern __shared__ __align__(16) unsigned char m2l_smem[];
@@ -120,10 +122,10 @@ int launch_m2l_tp(Plan &P_, cudaStream_t s)
 {
     using S = M2LShape<T, P>;
     static_assert(S::NRP % S::V == 0, "row stride must be a whole number of 16-byte loads");
-    k_moments_r<T, P><<<P_.num_sms * 4, 256, 0, s>>>((int)P_.n_nodes, (const T *)P_.M, (T *)P_.Mr);
+    k_moments_r<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)P_.M, (T *)P_.Mr);
     cudaFuncSetAttribute(k_m2l<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::smem);
     k_m2l<T, P><<<P_.num_sms * 16, M2L_WARPS * 32, S::smem, s>>>(
-        (int)P_.n_nodes, P_.order + P_.n_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
+        P_.ctr, P_.order + P_.cap_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
         (const T *)P_.Mr, (T *)P_.Lm2l, P_.ctr);
     return 2;
 }

@@ -54,10 +54,11 @@ template <int P> struct MDShape {
 
 // Reduced moments in their node's units: Mr[b][r] = reduce_m(M[b])_r 2^-(em + (ex - level_b) |r|).
 template <int P>
-__global__ __launch_bounds__(256) void k_moments_df(int n_nodes, const int *__restrict__ level,
+__global__ __launch_bounds__(256) void k_moments_df(const DevCounters *__restrict__ nctr, const int *__restrict__ level,
                                                     const dbl4 *__restrict__ node_l, const double *__restrict__ M,
                                                     df *__restrict__ Mr)
 {
+    const int n_nodes = phase2_nodes(nctr);
     using S = MDShape<P>;
     if (n_nodes <= 0) return;
     int ex, em;
@@ -95,13 +96,14 @@ __device__ __forceinline__ PairGeom pair_geom(const dbl4 &ca, int la, int ea, co
 // than its full register set allows to hide instruction fetch, and measured
 // faster at 80 registers with some spilling (0.50 ms) than at 253 (0.72 ms).
 template <int P>
-__global__ __launch_bounds__(MD_WARPS * 32, 6) void k_m2l_df(int n_nodes, const int *__restrict__ order,
+__global__ __launch_bounds__(MD_WARPS * 32, 6) void k_m2l_df(const DevCounters *__restrict__ nctr, const int *__restrict__ order,
                                                           const int *__restrict__ off, const int *__restrict__ src,
                                                           const dbl4 *__restrict__ nc, const int *__restrict__ level,
                                                           const dbl4 *__restrict__ node_l,
                                                           const double *__restrict__ M, const df *__restrict__ Mr,
                                                           double *__restrict__ Lout, DevCounters *ctr)
 {
+    const int n_nodes = phase2_nodes(nctr);
     using S = MDShape<P>;
     extern __shared__ __align__(16) unsigned char m2l_df_smem[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -180,11 +182,11 @@ int launch_m2l_df_p(Plan &P_, cudaStream_t s)
 {
     using S = MDShape<P>;
     static_assert(S::NRP % 2 == 0, "rows must be whole 16-byte loads");
-    k_moments_df<P><<<P_.num_sms * 4, 256, 0, s>>>((int)P_.n_nodes, P_.node_level, (const dbl4 *)P_.node_l,
+    k_moments_df<P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, P_.node_level, (const dbl4 *)P_.node_l,
                                                    (const double *)P_.M, (df *)P_.Mr);
     cudaFuncSetAttribute(k_m2l_df<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::smem);
     k_m2l_df<P><<<P_.num_sms * 16, MD_WARPS * 32, S::smem, s>>>(
-        (int)P_.n_nodes, P_.order + P_.n_nodes, P_.m2l_off, P_.m2l_src, (const dbl4 *)P_.node_c, P_.node_level,
+        P_.ctr, P_.order + P_.cap_nodes, P_.m2l_off, P_.m2l_src, (const dbl4 *)P_.node_c, P_.node_level,
         (const dbl4 *)P_.node_l, (const double *)P_.M, (const df *)P_.Mr, (double *)P_.Lm2l, P_.ctr);
     return 2;
 }

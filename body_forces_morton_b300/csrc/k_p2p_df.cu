@@ -78,12 +78,13 @@ constexpr int DF_CH = 128;  // staged source particles per warp
 // fp32's exponent range holds every intermediate of a pair separated by more
 // than 2^-42 of the box; acc = acc' 2^(em - 2 ex), phi = phi' 2^(em - ex)), split
 // into double words: rel[i] = (sx.h, sy.h, sz.h, m.h) and rel[N + i] = (sx.l, sy.l, sz.l, m.l).
-__global__ __launch_bounds__(256) void k_leaf_offsets(int n_nodes, int n, const int *__restrict__ first,
+__global__ __launch_bounds__(256) void k_leaf_offsets(const DevCounters *__restrict__ nctr, int n, const int *__restrict__ first,
                                                       const int *__restrict__ count, const int *__restrict__ nchild,
                                                       const dbl4 *__restrict__ xyzm, const dbl4 *__restrict__ nc,
                                                       const dbl4 *__restrict__ nl, const double *__restrict__ M,
                                                       float4 *__restrict__ rel)
 {
+    const int n_nodes = phase2_nodes(nctr);
     if (n_nodes <= 0) return;
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -328,7 +329,7 @@ __global__ __launch_bounds__(DF_WARPS * 32) void k_p2p_df(const DevCounters *__r
 
 int launch_p2p_df(Plan &P, void *acc, void *pot, cudaStream_t s)
 {
-    k_leaf_offsets<<<P.num_sms * 8, 256, 0, s>>>((int)P.n_nodes, (int)P.n, P.node_first, P.node_count,
+    k_leaf_offsets<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, (int)P.n, P.node_first, P.node_count,
                                                 P.node_nchild, (const dbl4 *)P.xyzm, (const dbl4 *)P.node_c,
                                                 (const dbl4 *)P.node_l, (const double *)P.M, (float4 *)P.rel);
     k_p2p_df<<<P.num_sms * 16, DF_WARPS * 32, 0, s>>>(P.ctr, P.order, P.ctr, (int)P.n, P.node_first, P.node_count,

@@ -19,6 +19,17 @@ namespace {
 
 constexpr int TR_THREADS = 128;
 
+// Node count and depth for the later stages: the deepest level holding nodes,
+// and the nodes up to it (at most the node capacity).
+__device__ void record_tree_size(DevCounters *ctr, int cap_nodes)
+{
+    int depth = 0;
+    for (int l = 0; l <= kMaxLevel; ++l)
+        if (ld_cg(&ctr->level_off[l + 1]) > ld_cg(&ctr->level_off[l])) depth = l;
+    ctr->depth = depth;
+    ctr->n_nodes = min(ld_cg(&ctr->level_off[depth + 1]), cap_nodes);
+}
+
 // All levels in one cooperative launch: a tile is 32 consecutive nodes of the
 // level, one per lane of a warp; tiles are taken from the level's ticket
 // counter. A lane finds its node's child boundaries by seven branchless
@@ -46,8 +57,10 @@ __global__ __launch_bounds__(TR_THREADS) void k_tree_all(int leaf, int cap_nodes
         const int cnt = hi - lo;
         if (cnt <= 0) {
             // no deeper nodes: the remaining level offsets all equal the node count
-            if (blockIdx.x == 0 && threadIdx.x == 0)
+            if (blockIdx.x == 0 && threadIdx.x == 0) {
                 for (int l = level + 2; l < kMaxLevel + 3; ++l) ctr->level_off[l] = ctr->level_off[level + 1];
+                record_tree_size(ctr, cap_nodes);
+            }
             return;
         }
         const int ntiles = (cnt + 31) / 32;
@@ -115,6 +128,7 @@ __global__ __launch_bounds__(TR_THREADS) void k_tree_all(int leaf, int cap_nodes
         }
         if (!grid_barrier(gb, (unsigned)level, ctr)) return;
     }
+    if (blockIdx.x == 0 && threadIdx.x == 0) record_tree_size(ctr, cap_nodes);
 }
 
 }  // namespace

@@ -44,12 +44,13 @@ __device__ __forceinline__ void store_geometry(int a, const T lo[3], const T hi[
 template <int NC> struct Padded { static constexpr int value = (NC + 7) / 8 * 8; };
 
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__restrict__ xyzm,
+__global__ __launch_bounds__(256) void k_upward(const DevCounters *__restrict__ nctr, const vec4<T> *__restrict__ xyzm,
                                                 const int *__restrict__ first, const int *__restrict__ count,
                                                 const int *__restrict__ child0, const int *__restrict__ nchild,
                                                 const int *__restrict__ parent, int *done, T *node_lo, T *node_hi,
                                                 vec4<T> *nc, vec4<T> *nl, T *M, int ncp)
 {
+    const int n_nodes = phase2_nodes(nctr);
     constexpr int NC = Exp<P>::NC;
     constexpr int NR = Padded<NC>::value;
     const int lane = threadIdx.x & 31;
@@ -131,7 +132,7 @@ __global__ __launch_bounds__(256) void k_upward(int n_nodes, const vec4<T> *__re
 template <class T, int P>
 int launch_upward_tp(Plan &P_, cudaStream_t s)
 {
-    k_upward<T, P><<<P_.num_sms * 8, 256, 0, s>>>((int)P_.n_nodes, (const vec4<T> *)P_.xyzm, P_.node_first,
+    k_upward<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, (const vec4<T> *)P_.xyzm, P_.node_first,
                                                   P_.node_count, P_.node_child0, P_.node_nchild, P_.node_parent,
                                                   P_.node_done, (T *)P_.node_lo, (T *)P_.node_hi,
                                                   (vec4<T> *)P_.node_c, (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp);

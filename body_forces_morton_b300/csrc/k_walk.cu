@@ -69,14 +69,16 @@ __device__ __forceinline__ size_t shard_addr(const int *s_pre, int g, int cap_s)
     return (size_t)lo * cap_s + (g - s_pre[lo]);
 }
 
-// The walk: `iters` generations. In each, every frontier pair is decided and
+// The walk: generations until the frontier is empty (at most `max_iters`; a
+// walk of depth D ends after 2 D + 1, so running out sets ERR_WALK). In each
+// generation every frontier pair is decided and
 // its outputs (an M2L pair, a P2P pair or child pairs) are appended. Each output
 // list is split into kShards shards with their own counters; a block reserves
 // the space of a whole 256-pair tile in the shard of its index with one atomic
 // per list, so no single counter is hot. The frontier and its counts were
 // written by other blocks of this launch, so they are read through L2.
 template <class T>
-__global__ __launch_bounds__(WK_THREADS) void k_walk_all(int iters, int2 *f0, int2 *f1, int capf_s,
+__global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0, int2 *f1, int capf_s,
                                                          const int *__restrict__ nchild,
                                                          const int *__restrict__ child0,
                                                          const int *__restrict__ count,
@@ -93,6 +95,7 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int iters, int2 *f0, in
     const int bshard = blockIdx.x % kShards;
     long long inter_sum = 0;
     int visited = 0, fill_max = 0;
+    const int iters = phase2_nodes(ctr) > 0 ? max_iters : 0;
     for (int it = 0; it < iters; ++it) {
         const int2 *fin = (it & 1) ? f1 : f0;
         int2 *fout = (it & 1) ? f0 : f1;
@@ -100,6 +103,11 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int iters, int2 *f0, in
         if (blockIdx.x == 0 && threadIdx.x < kShards) ctr->frontier_cnt[(it + 2) % 3][threadIdx.x] = 0;
         shard_prefix(ctr->frontier_cnt[it % 3], capf_s, s_pre);
         const int nread = s_pre[kShards];
+        if (nread == 0) break;  // the walk is complete (every block reads the same counts)
+        if (it == iters - 1) {
+            if (blockIdx.x == 0 && threadIdx.x == 0) set_error(ctr, ERR_WALK);
+            break;
+        }
         for (int base = blockIdx.x * WK_THREADS; base < nread; base += gridDim.x * WK_THREADS) {
             const int i = base + threadIdx.x;
             int A = -1, B = -1, kids = 0, split = -1, other = 0, m2l = 0, p2p = 0;
@@ -213,11 +221,12 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int iters, int2 *f0, in
 }
 
 // Exclusive scan of the per-receiver counts into CSR offsets (both lists at once).
-__global__ __launch_bounds__(CS_THREADS) void k_csr_scan(int n_nodes, const int *__restrict__ m2l_cnt,
+__global__ __launch_bounds__(CS_THREADS) void k_csr_scan(const DevCounters *__restrict__ nctr, const int *__restrict__ m2l_cnt,
                                                          const int *__restrict__ p2p_cnt, int *__restrict__ m2l_off,
                                                          int *__restrict__ p2p_off, unsigned long long *flags,
                                                          unsigned epoch, int slot, DevCounters *ctr)
 {
+    const int n_nodes = phase2_nodes(nctr);
     __shared__ int s_tile;
     __shared__ int s_w[2][CS_THREADS / 32];
     __shared__ long long s_ex[2];
@@ -378,11 +387,13 @@ __device__ __forceinline__ void sort_list_regs(int *src, int len)
 
 // One warp per receiver list; lists up to 256 sort in registers, up to
 // SEG_WARP_MAX in shared memory, longer ones go to a second pass.
-__global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restrict__ m2l_off, int *m2l_src,
+__global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__ nctr, int cap,
+                                                 const int *__restrict__ m2l_off, int *m2l_src,
                                                  const int *__restrict__ p2p_off, int *p2p_src, int *long_seg,
                                                  const int *__restrict__ count, uint8_t *__restrict__ key,
                                                  DevCounters *ctr)
 {
+    const int n_nodes = phase2_nodes(nctr);
     __shared__ int buf[8][SEG_WARP_MAX];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int *sv = buf[w];
@@ -407,7 +418,7 @@ __global__ __launch_bounds__(256) void k_segsort(int n_nodes, const int *__restr
                 k = len > 0 ? 32 - __clz(len) : 0;
             }
             if (lane == 0) {
-                key[(isp ? 0 : n_nodes) + a] = (uint8_t)k;
+                key[(isp ? 0 : cap) + a] = (uint8_t)k;
                 if (k || !isp) atomicAdd(&ctr->order_cnt[isp ? 0 : 1][k], 1);
             }
         }
@@ -488,9 +499,11 @@ __global__ __launch_bounds__(1024) void k_segsort_long(const int *__restrict__ m
 // positions inside a bucket may come in any order: a block counts its nodes
 // per bucket in shared memory and reserves their places with one atomic per
 // bucket.
-__global__ __launch_bounds__(256) void k_order_scatter(int n_nodes, const uint8_t *__restrict__ key, int *order,
+__global__ __launch_bounds__(256) void k_order_scatter(const DevCounters *__restrict__ nctr, int cap,
+                                                       const uint8_t *__restrict__ key, int *order,
                                                        DevCounters *ctr)
 {
+    const int n_nodes = phase2_nodes(nctr);
     __shared__ int base[2][64], s_cnt[2][64], s_pos[2][64];
     const int tid = (int)threadIdx.x;
     if (tid < 2) {
@@ -508,7 +521,7 @@ __global__ __launch_bounds__(256) void k_order_scatter(int n_nodes, const uint8_
         int kp = 0, km = 0, rp = -1, rm = -1;
         if (a < n_nodes) {
             kp = key[a];
-            km = key[n_nodes + a];
+            km = key[cap + a];
             if (kp) rp = atomicAdd(&s_cnt[0][kp], 1);
             rm = atomicAdd(&s_cnt[1][km], 1);
         }
@@ -521,7 +534,7 @@ __global__ __launch_bounds__(256) void k_order_scatter(int n_nodes, const uint8_
         __syncthreads();
         if (a < n_nodes) {
             if (kp) order[s_pos[0][kp] + rp] = a;
-            order[n_nodes + s_pos[1][km] + rm] = a;
+            order[cap + s_pos[1][km] + rm] = a;
         }
         __syncthreads();
     }
@@ -532,7 +545,8 @@ int launch_walk_t(Plan &P, int depth, cudaStream_t s)
 {
     T th2 = (T)(P.theta * P.theta);
     k_walk_init<<<1, 1, 0, s>>>(P.frontier[0], P.ctr);
-    int iters = 2 * depth + 1;
+    int iters = 2 * kMaxLevel + 2;
+    (void)depth;
     int capf_s = (int)(P.cap_frontier / kShards), capm_s = (int)(P.cap_m2l / kShards);
     int capp_s = (int)(P.cap_p2p / kShards);
     const vec4<T> *nc = (const vec4<T> *)P.node_c, *nl = (const vec4<T> *)P.node_l;
@@ -561,18 +575,18 @@ int launch_walk(Plan &P, int depth, cudaStream_t s)
 
 int launch_lists(Plan &P, cudaStream_t s)
 {
-    const int nn = (int)P.n_nodes;
+    const int cap = (int)P.cap_nodes;
     const int slot = P.next_slot();
     const unsigned ep = P.next_epoch();
-    k_csr_scan<<<P.num_sms * 4, CS_THREADS, 0, s>>>(nn, P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off, P.flags, ep, slot,
+    k_csr_scan<<<P.num_sms * 4, CS_THREADS, 0, s>>>(P.ctr, P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off, P.flags, ep, slot,
                                                     P.ctr);
     k_csr_fill<<<P.num_sms * 8, 256, 0, s>>>(P.m2l_pairs, (int)(P.cap_m2l / kShards), P.p2p_pairs,
                                              (int)(P.cap_p2p / kShards), P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off,
                                              P.m2l_src, P.p2p_src, P.ctr);
-    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(nn, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
+    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, cap, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
                                             P.node_count, P.order_key, P.ctr);
     k_segsort_long<<<P.num_sms, 1024, 0, s>>>(P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
-    k_order_scatter<<<P.num_sms * 4, 256, 0, s>>>(nn, P.order_key, P.order, P.ctr);
+    k_order_scatter<<<P.num_sms * 4, 256, 0, s>>>(P.ctr, cap, P.order_key, P.order, P.ctr);
     return 5;
 }
 

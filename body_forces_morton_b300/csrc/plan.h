@@ -67,7 +67,7 @@ struct Plan {
 
     // status
     DevCounters *ctr = nullptr;      // device
-    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0] and walk [1] launches
+    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0], walk [1], L2L [2] launches
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
