@@ -83,7 +83,7 @@ void free_nodes(Plan &P)
 {
     int **ints[] = {&P.node_first, &P.node_count, &P.node_child0, &P.node_nchild, &P.node_parent,
                     &P.node_level, &P.node_done,  &P.m2l_cnt,     &P.p2p_cnt,     &P.m2l_off,
-                    &P.p2p_off,    &P.long_seg,    &P.order};
+                    &P.p2p_off,    &P.long_seg,    &P.order,       &P.p2p_done};
     for (int **q : ints) { dfree(*q); *q = nullptr; }
     void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L, &P.Mr};
     for (void **q : vs) { dfree(*q); *q = nullptr; }
@@ -91,6 +91,10 @@ void free_nodes(Plan &P)
     P.flags = nullptr;
     dfree(P.order_key);
     P.order_key = nullptr;
+    dfree(P.p2p_items);
+    P.p2p_items = nullptr;
+    dfree(P.p2p_nch);
+    P.p2p_nch = nullptr;
 }
 
 void free_lists(Plan &P)
@@ -120,6 +124,9 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
     CUDA_TRY(dalloc(P.p2p_off, c + 1));
     CUDA_TRY(dalloc(P.long_seg, 2 * c));
     CUDA_TRY(dalloc(P.order, 2 * c));
+    CUDA_TRY(dalloc(P.p2p_items, 2 * c));
+    CUDA_TRY(dalloc(P.p2p_done, c));
+    CUDA_TRY(dalloc(P.p2p_nch, c));
     CUDA_TRY(dalloc(P.order_key, 2 * c));
     CUDA_TRY(cudaMalloc(&P.node_lo, 3 * c * e));
     CUDA_TRY(cudaMalloc(&P.node_hi, 3 * c * e));
@@ -224,6 +231,7 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         CUDA_TRY(cudaMemsetAsync(P.node_done, 0, (size_t)P.cap_nodes * sizeof(int), s));
         CUDA_TRY(cudaMemsetAsync(P.m2l_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
         CUDA_TRY(cudaMemsetAsync(P.p2p_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
+        CUDA_TRY(cudaMemsetAsync(P.p2p_done, 0, (size_t)P.cap_nodes * sizeof(int), s));
         P.launches += launch_upward(P, s);
         record(P, 5, s);
         P.launches += launch_walk(P, 0, s);

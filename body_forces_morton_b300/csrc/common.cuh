@@ -13,6 +13,12 @@ constexpr int kMaxLevel = 21;        // Morton keys carry 21 bits per axis
 constexpr int kMaxP = 8;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kShards = 64;          // the walk's outputs are split into this many independently counted shards
+// P2P work of one receiver leaf above kChunkWork interactions (or above the
+// total over the node capacity, if larger) is split into up to kMaxChunks
+// chunks of its source list, taken by different warps.
+constexpr long long kChunkWork = 1ll << 20;
+constexpr int kMaxChunks = 64;
+constexpr unsigned kSpinLimit = 1u << 22;  // iterations of any bounded wait
 
 // ---- device status word bits (ORed by kernels, read by the host) ----------
 enum : unsigned {
@@ -101,6 +107,36 @@ __device__ __forceinline__ int phase2_nodes(const DevCounters *ctr)
     return (ctr->error & (ERR_NODES | ERR_NONFINITE)) ? 0 : ctr->n_nodes;
 }
 
+// ---- chunked receivers: chunk c of a receiver applies its partial sums after
+// chunk c - 1 (which an earlier warp took). Lane 0 waits, bounded, for the
+// receiver's counter to reach c; the warp barrier passes the ordering on.
+__device__ __forceinline__ void wait_turn(int *flag, int want, DevCounters *ctr)
+{
+    if ((threadIdx.x & 31) == 0) {
+        cuda::atomic_ref<int, cuda::thread_scope_device> r(*flag);
+        unsigned spins = 0;
+        while (r.load(cuda::memory_order_acquire) != want) {
+            if (++spins > kSpinLimit) {
+                set_error(ctr, ERR_SPIN);
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    __syncwarp();
+}
+
+// After every lane's writes of chunk c: publish them and pass the turn on.
+__device__ __forceinline__ void pass_turn(int *flag, int next)
+{
+    __threadfence();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        cuda::atomic_ref<int, cuda::thread_scope_device> r(*flag);
+        r.store(next, cuda::memory_order_release);
+    }
+}
+
 // ---- grid-wide barrier of a cooperative launch (all blocks co-resident) -----
 // One arrival counter per launch, on its own 128-byte line; it only grows:
 // barrier number k of a kernel completes when it reaches (k + 1) * gridDim.x.
@@ -142,7 +178,6 @@ __device__ __forceinline__ bool grid_barrier(GridBarrier *gb, unsigned k, DevCou
 // ---- chained scan with decoupled look-back ---------------------------------
 // Flag word: [63:40] epoch, [39:38] state (1 = aggregate, 2 = inclusive prefix), [37:0] value.
 constexpr unsigned long long kFlagValueMask = (1ull << 38) - 1;
-constexpr unsigned kSpinLimit = 1u << 22;
 
 __device__ __forceinline__ unsigned long long flag_pack(unsigned epoch, unsigned state, unsigned long long v)
 {

@@ -256,11 +256,13 @@ __device__ __forceinline__ void p2p_span_pairs(const float *fb, int npairs, int 
 // walks the staged sources from offset q with stride S. Lanes at or beyond
 // R S only stage. The S partial sums of a receiver are added in order of q
 // through shared memory, so the result is reproducible.
-template <class T, int K>
-__device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, int beg, int end,
+template <class T, int K, bool CHUNKED>
+__device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, int beg, int end, int chunk, int nch,
+                                          int *done, DevCounters *ctr,
                                           const int *__restrict__ first, const int *__restrict__ count,
                                           const vec4<T> *__restrict__ xyzm, const uint32_t *__restrict__ perm,
-                                          const vec4<T> *__restrict__ far, const int *__restrict__ src,
+                                          const vec4<T> *__restrict__ far, vec4<T> *far_w,
+                                          const int *__restrict__ src,
                                           T *__restrict__ acc_out, T *__restrict__ pot_out, vec4<T> *buf,
                                           T (*red)[4], int lane)
 {
@@ -278,8 +280,8 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
 #pragma unroll
     for (int k = 0; k < K; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = T(0);
     const int qq = worker ? q : (1 << 30);  // idle lanes start past every chunk
-    // the leaf's own particles (zero separations possible)
-    for (int g0 = 0; g0 < c; g0 += CH) {
+    // the leaf's own particles (zero separations possible; the first chunk of a split receiver)
+    for (int g0 = 0; (!CHUNKED || chunk == 0) && g0 < c; g0 += CH) {
         const int n_here = min(CH, c - g0);
         __syncwarp();
         for (int k = lane; k < n_here; k += 32) buf[k] = xyzm[f + g0 + k];
@@ -345,6 +347,8 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
             }
         }
     }
+    // a split receiver's chunks add up in chunk order: wait for the previous chunk
+    if (CHUNKED && r0 == 0) wait_turn(done + a, chunk, ctr);
     // sum the S strides of each receiver in order of q
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -361,14 +365,63 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
 #pragma unroll
                 for (int v = 0; v < 4; ++v) t[v] += red[qs * R + rp][v];
             const int i = f + r0 + rr;
-            const vec4<T> fa = far[i];
-            const uint32_t o = perm[i];
-            acc_out[3 * (size_t)o] = fa.y + t[1];
-            acc_out[3 * (size_t)o + 1] = fa.z + t[2];
-            acc_out[3 * (size_t)o + 2] = fa.w + t[3];
-            if (pot_out) pot_out[o] = fa.x + t[0];
+            // the far field, plus the partial sums of the earlier chunks (written by other warps)
+            const vec4<T> fa = CHUNKED ? ld_cg(far + i) : far[i];
+            if (CHUNKED && chunk < nch - 1) {
+                far_w[i] = make4<T>(fa.x + t[0], fa.y + t[1], fa.z + t[2], fa.w + t[3]);
+            } else {
+                const uint32_t o = perm[i];
+                acc_out[3 * (size_t)o] = fa.y + t[1];
+                acc_out[3 * (size_t)o + 1] = fa.z + t[2];
+                acc_out[3 * (size_t)o + 2] = fa.w + t[3];
+                if (pot_out) pot_out[o] = fa.x + t[0];
+            }
         }
     }
+}
+
+// One work item: a receiving leaf, or one chunk of a split one (the chunk's
+// share of the source list; the own leaf goes with chunk 0; chunks apply their
+// sums in chunk order).
+template <class T, bool CHUNKED>
+__device__ __forceinline__ void p2p_item(int a, int chunk, int nch, int *done, DevCounters *ctr,
+                                         const int *__restrict__ first, const int *__restrict__ count,
+                                         const vec4<T> *__restrict__ xyzm, const uint32_t *__restrict__ perm,
+                                         const vec4<T> *__restrict__ far, vec4<T> *far_w,
+                                         const int *__restrict__ off, const int *__restrict__ src,
+                                         T *__restrict__ acc_out, T *__restrict__ pot_out, vec4<T> *buf,
+                                         T (*red)[4], int lane)
+{
+    const int f = first[a], c = count[a];
+    int beg = off[a], end = off[a + 1];
+    if (CHUNKED) {
+        const int len = end - beg;
+        end = beg + len * (chunk + 1) / nch;
+        beg = beg + len * chunk / nch;
+    }
+    for (int r0 = 0; r0 < c; r0 += 128) {
+        const int cr = min(128, c - r0);
+        // useful fraction of the lane-interactions with K receivers per lane is cr S / (32 K),
+        // S = 32 / ceil(cr / K); ties go to the larger K (fewer shared loads per interaction)
+        int best = 4, best_num = -1;
+#pragma unroll
+        for (int K = 1; K <= 4; K <<= 1) {
+            const int R = (cr + K - 1) / K;
+            if (R > 32) continue;
+            const int num = cr * (32 / R) * (4 / K);
+            if (num >= best_num) { best_num = num; best = K; }
+        }
+        if (best == 1)
+            p2p_round<T, 1, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm,
+                                     far, far_w, src, acc_out, pot_out, buf, red, lane);
+        else if (best == 2)
+            p2p_round<T, 2, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm,
+                                     far, far_w, src, acc_out, pot_out, buf, red, lane);
+        else
+            p2p_round<T, 4, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm,
+                                     far, far_w, src, acc_out, pot_out, buf, red, lane);
+    }
+    if (CHUNKED && chunk < nch - 1) pass_turn(done + a, chunk + 1);
 }
 
 // P2P for one receiving leaf per warp (leaves taken from a shared counter in
@@ -377,13 +430,15 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
 // chosen per leaf to keep the most lanes doing useful interactions; the
 // leaf's own particles are a separate masked pass, the rest runs unmasked.
 template <class T>
-__global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__restrict__ cst, const int *__restrict__ order,
+__global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__restrict__ cst,
+                                                       const int2 *__restrict__ items, int *done,
                                                        DevCounters *ctr, const int *__restrict__ first,
                                                        const int *__restrict__ count,
                                                        const int *__restrict__ nchild,
                                                        const vec4<T> *__restrict__ xyzm,
                                                        const uint32_t *__restrict__ perm,
-                                                       const vec4<T> *__restrict__ far, const int *__restrict__ off,
+                                                       const vec4<T> *__restrict__ far, vec4<T> *far_w,
+                                                       const int *__restrict__ off,
                                                        const int *__restrict__ src, T *__restrict__ acc_out,
                                                        T *__restrict__ pot_out)
 {
@@ -398,31 +453,14 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
         if (lane == 0) t = atomicAdd(&ctr->work_ctr[0], 1);
         t = __shfl_sync(kFull, t, 0);
         if (t >= n_work) break;
-        const int a = order[t];
-        const int f = first[a], c = count[a];
-        const int beg = off[a], end = off[a + 1];
-        for (int r0 = 0; r0 < c; r0 += 128) {
-            const int cr = min(128, c - r0);
-            // useful fraction of the lane-interactions with K receivers per lane is cr S / (32 K),
-            // S = 32 / ceil(cr / K); ties go to the larger K (fewer shared loads per interaction)
-            int best = 4, best_num = -1;
-#pragma unroll
-            for (int K = 1; K <= 4; K <<= 1) {
-                const int R = (cr + K - 1) / K;
-                if (R > 32) continue;
-                const int num = cr * (32 / R) * (4 / K);
-                if (num >= best_num) { best_num = num; best = K; }
-            }
-            if (best == 1)
-                p2p_round<T, 1>(a, f, c, r0, cr, beg, end, first, count, xyzm, perm, far, src, acc_out, pot_out,
-                                s_src[w], s_red[w], lane);
-            else if (best == 2)
-                p2p_round<T, 2>(a, f, c, r0, cr, beg, end, first, count, xyzm, perm, far, src, acc_out, pot_out,
-                                s_src[w], s_red[w], lane);
-            else
-                p2p_round<T, 4>(a, f, c, r0, cr, beg, end, first, count, xyzm, perm, far, src, acc_out, pot_out,
-                                s_src[w], s_red[w], lane);
-        }
+        const int2 item = items[t];
+        const int a = item.x, nch = item.y >> 8;
+        if (nch == 1)
+            p2p_item<T, false>(a, 0, 1, done, ctr, first, count, xyzm, perm, far, far_w, off, src, acc_out, pot_out,
+                               s_src[w], s_red[w], lane);
+        else
+            p2p_item<T, true>(a, item.y & 255, nch, done, ctr, first, count, xyzm, perm, far, far_w, off, src,
+                              acc_out, pot_out, s_src[w], s_red[w], lane);
     }
 }
 
@@ -487,9 +525,10 @@ int launch_l2p(Plan &P, cudaStream_t s)
 int launch_p2p(Plan &P, void *acc, void *pot, cudaStream_t s)
 {
     if (P.dtype == 1) return launch_p2p_df(P, acc, pot, s);
-    k_p2p<float><<<P.num_sms * 16, LF_WARPS * 32, 0, s>>>(P.ctr, P.order, P.ctr, P.node_first, P.node_count,
-                                                          P.node_nchild, (const vec4<float> *)P.xyzm, P.idx[0],
-                                                          (const vec4<float> *)P.far, P.p2p_off, P.p2p_src,
+    k_p2p<float><<<P.num_sms * 16, LF_WARPS * 32, 0, s>>>(P.ctr, P.p2p_items, P.p2p_done, P.ctr, P.node_first,
+                                                          P.node_count, P.node_nchild, (const vec4<float> *)P.xyzm,
+                                                          P.idx[0], (const vec4<float> *)P.far, (vec4<float> *)P.far,
+                                                          P.p2p_off, P.p2p_src,
                                                           (float *)acc, (float *)pot);
     return 1;
 }

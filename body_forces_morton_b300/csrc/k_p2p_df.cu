@@ -182,12 +182,13 @@ __device__ __forceinline__ float exact_thr2(float e)
     return fmaxf(t * t, kTinyR2);
 }
 
-template <int K>
-__device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, int beg, int end, int n,
-                                         const ExactCtx &cx, const int *__restrict__ first,
+template <int K, bool CHUNKED>
+__device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, int beg, int end, int chunk, int nch,
+                                         int *done, DevCounters *ctr, int n, const ExactCtx &cx,
+                                         const int *__restrict__ first,
                                          const int *__restrict__ count, const dbl4 *__restrict__ nc,
                                          const float4 *__restrict__ rel, const uint32_t *__restrict__ perm,
-                                         const dbl4 *__restrict__ far, const int *__restrict__ src,
+                                         dbl4 *far, const int *__restrict__ src,
                                          double *__restrict__ acc_out, double *__restrict__ pot_out, float4 *buf,
                                          int *sidx, double (*red)[4], int lane)
 {
@@ -211,7 +212,7 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
     const float ext_a = ext_scaled(ca, cx.ex);
     // the leaf's own particles (delta = 0; zero separations go to the exact branch and are skipped there)
     const float thr_own = exact_thr2(2.0f * ext_a);
-    for (int g0 = 0; g0 < c; g0 += DF_CH) {
+    for (int g0 = 0; (!CHUNKED || chunk == 0) && g0 < c; g0 += DF_CH) {
         const int n_here = min(DF_CH, c - g0);
         __syncwarp();
         for (int k = lane; k < n_here; k += 32) {
@@ -259,6 +260,8 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
         }
     }
     const int eacc = cx.em - 2 * cx.ex, epot = cx.em - cx.ex;
+    // a split receiver's chunks add up in chunk order: wait for the previous chunk
+    if (CHUNKED && r0 == 0) wait_turn(done + a, chunk, ctr);
 #pragma unroll
     for (int k = 0; k < K; ++k) {
         __syncwarp();
@@ -272,23 +275,66 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
 #pragma unroll
                 for (int v = 0; v < 4; ++v) t[v] += red[qs * R + rp][v];
             const int i = f + r0 + rr;
-            const dbl4 fa = far[i];
-            const uint32_t o = perm[i];
-            acc_out[3 * (size_t)o] = fa.y + ldexp(t[1], eacc);
-            acc_out[3 * (size_t)o + 1] = fa.z + ldexp(t[2], eacc);
-            acc_out[3 * (size_t)o + 2] = fa.w + ldexp(t[3], eacc);
-            if (pot_out) pot_out[o] = fa.x + ldexp(t[0], epot);
+            // the far field, plus the partial sums of the earlier chunks (written by other warps)
+            const dbl4 fa = CHUNKED ? ld_cg(far + i) : far[i];
+            const double sx = fa.x + ldexp(t[0], epot), sy = fa.y + ldexp(t[1], eacc);
+            const double sz = fa.z + ldexp(t[2], eacc), sw = fa.w + ldexp(t[3], eacc);
+            if (CHUNKED && chunk < nch - 1) {
+                far[i] = make4<double>(sx, sy, sz, sw);
+            } else {
+                const uint32_t o = perm[i];
+                acc_out[3 * (size_t)o] = sy;
+                acc_out[3 * (size_t)o + 1] = sz;
+                acc_out[3 * (size_t)o + 2] = sw;
+                if (pot_out) pot_out[o] = sx;
+            }
         }
     }
 }
 
-__global__ __launch_bounds__(DF_WARPS * 32) void k_p2p_df(const DevCounters *__restrict__ cst,
-                                                          const int *__restrict__ order, DevCounters *ctr, int n,
+// One work item: a receiving leaf, or one chunk of a split one (the chunk's
+// share of the source list; the own leaf goes with chunk 0; chunks apply their
+// sums in chunk order).
+template <bool CHUNKED>
+__device__ __forceinline__ void item_df(int a, int chunk, int nch, int *done, DevCounters *ctr, int n,
+                                        const ExactCtx &cx, const int *__restrict__ first,
+                                        const int *__restrict__ count, const dbl4 *__restrict__ nc,
+                                        const float4 *__restrict__ rel, const uint32_t *__restrict__ perm, dbl4 *far,
+                                        const int *__restrict__ off, const int *__restrict__ src,
+                                        double *__restrict__ acc_out, double *__restrict__ pot_out, float4 *buf,
+                                        int *sidx, double (*red)[4], int lane)
+{
+    const int f = first[a], c = count[a];
+    int beg = off[a], end = off[a + 1];
+    if (CHUNKED) {
+        const int len = end - beg;
+        end = beg + len * (chunk + 1) / nch;
+        beg = beg + len * chunk / nch;
+    }
+    for (int r0 = 0; r0 < c; r0 += 64) {
+        const int cr = min(64, c - r0);
+        // K = 2 receivers per lane unless K = 1 keeps more lanes busy
+        const int R1 = cr, R2 = (cr + 1) / 2;
+        const int num1 = R1 <= 32 ? cr * (32 / R1) * 2 : -1;
+        const int num2 = cr * (32 / R2);
+        if (num1 > num2)
+            round_df<1, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, n, cx, first, count, nc, rel,
+                                 perm, far, src, acc_out, pot_out, buf, sidx, red, lane);
+        else
+            round_df<2, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, n, cx, first, count, nc, rel,
+                                 perm, far, src, acc_out, pot_out, buf, sidx, red, lane);
+    }
+    if (CHUNKED && chunk < nch - 1) pass_turn(done + a, chunk + 1);
+}
+
+__global__ __launch_bounds__(DF_WARPS * 32, 4) void k_p2p_df(const DevCounters *__restrict__ cst,
+                                                          const int2 *__restrict__ items, int *done,
+                                                          DevCounters *ctr, int n,
                                                           const int *__restrict__ first, const int *__restrict__ count,
                                                           const dbl4 *__restrict__ xyzm, const dbl4 *__restrict__ nc,
                                                           const float4 *__restrict__ rel,
-                                                          const uint32_t *__restrict__ perm,
-                                                          const dbl4 *__restrict__ far, const int *__restrict__ off,
+                                                          const uint32_t *__restrict__ perm, dbl4 *far,
+                                                          const int *__restrict__ off,
                                                           const int *__restrict__ src, const dbl4 *__restrict__ nl,
                                                           const double *__restrict__ M, double *__restrict__ acc_out,
                                                           double *__restrict__ pot_out)
@@ -306,22 +352,14 @@ __global__ __launch_bounds__(DF_WARPS * 32) void k_p2p_df(const DevCounters *__r
         if (lane == 0) t = atomicAdd(&ctr->work_ctr[0], 1);
         t = __shfl_sync(kFull, t, 0);
         if (t >= n_work) break;
-        const int a = order[t];
-        const int f = first[a], c = count[a];
-        const int beg = off[a], end = off[a + 1];
-        for (int r0 = 0; r0 < c; r0 += 64) {
-            const int cr = min(64, c - r0);
-            // K = 2 receivers per lane unless K = 1 keeps more lanes busy
-            const int R1 = cr, R2 = (cr + 1) / 2;
-            const int num1 = R1 <= 32 ? cr * (32 / R1) * 2 : -1;
-            const int num2 = cr * (32 / R2);
-            if (num1 > num2)
-                round_df<1>(a, f, c, r0, cr, beg, end, n, cx, first, count, nc, rel, perm, far, src, acc_out, pot_out,
-                            s_src[w], s_idx[w], s_red[w], lane);
-            else
-                round_df<2>(a, f, c, r0, cr, beg, end, n, cx, first, count, nc, rel, perm, far, src, acc_out, pot_out,
-                            s_src[w], s_idx[w], s_red[w], lane);
-        }
+        const int2 item = items[t];
+        const int a = item.x, nch = item.y >> 8;
+        if (nch == 1)
+            item_df<false>(a, 0, 1, done, ctr, n, cx, first, count, nc, rel, perm, far, off, src, acc_out, pot_out,
+                           s_src[w], s_idx[w], s_red[w], lane);
+        else
+            item_df<true>(a, item.y & 255, nch, done, ctr, n, cx, first, count, nc, rel, perm, far, off, src, acc_out,
+                          pot_out, s_src[w], s_idx[w], s_red[w], lane);
     }
 }
 
@@ -332,10 +370,11 @@ int launch_p2p_df(Plan &P, void *acc, void *pot, cudaStream_t s)
     k_leaf_offsets<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, (int)P.n, P.node_first, P.node_count,
                                                 P.node_nchild, (const dbl4 *)P.xyzm, (const dbl4 *)P.node_c,
                                                 (const dbl4 *)P.node_l, (const double *)P.M, (float4 *)P.rel);
-    k_p2p_df<<<P.num_sms * 16, DF_WARPS * 32, 0, s>>>(P.ctr, P.order, P.ctr, (int)P.n, P.node_first, P.node_count,
+    k_p2p_df<<<P.num_sms * 16, DF_WARPS * 32, 0, s>>>(P.ctr, P.p2p_items, P.p2p_done, P.ctr, (int)P.n, P.node_first,
+                                                      P.node_count,
                                                       (const dbl4 *)P.xyzm, (const dbl4 *)P.node_c,
-                                                      (const float4 *)P.rel, P.idx[0],
-                                                      (const dbl4 *)P.far, P.p2p_off, P.p2p_src,
+                                                      (const float4 *)P.rel, P.idx[0], (dbl4 *)P.far, P.p2p_off,
+                                                      P.p2p_src,
                                                       (const dbl4 *)P.node_l, (const double *)P.M, (double *)acc,
                                                       (double *)pot);
     return 2;

@@ -387,7 +387,7 @@ __device__ __forceinline__ void sort_list_regs(int *src, int len)
 
 // One warp per receiver list; lists up to 256 sort in registers, up to
 // SEG_WARP_MAX in shared memory, longer ones go to a second pass.
-__global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__ nctr, int cap,
+__global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__ nctr, int cap, uint8_t *nchunks,
                                                  const int *__restrict__ m2l_off, int *m2l_src,
                                                  const int *__restrict__ p2p_off, int *p2p_src, int *long_seg,
                                                  const int *__restrict__ count, uint8_t *__restrict__ key,
@@ -405,21 +405,28 @@ __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__
         const int len = (isp ? p2p_off[a + 1] : m2l_off[a + 1]) - beg;
         int *src = (isp ? p2p_src : m2l_src) + beg;
         // work bucket of this receiver (see k_order_scatter): P2P work = count * sum of the
-        // source leaves' counts, M2L work = list length; bucket floor(log2(work)) + 1, 0 for none
+        // source leaves' counts, split into chunks of at most max(kChunkWork, total / cap) (at most
+        // kMaxChunks; so the chunks of all receivers number at most 2 cap), bucketed by the work of
+        // one chunk; M2L work = list length; bucket floor(log2(work)) + 1, 0 for none
         {
-            int k;
+            int k, nch = 1;
             if (isp) {
                 long long s = 0;
                 for (int e = lane; e < len; e += 32) s += count[src[e]];
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
                 const long long work = s * count[a];
-                k = work > 0 ? 64 - __clzll(work) : 0;
+                const long long wmax = max(kChunkWork, ctr->p2p_interactions / cap + 1);
+                nch = (int)min((long long)kMaxChunks, (work + wmax - 1) / wmax);
+                nch = max(nch, 1);
+                const long long wc = work / nch;
+                k = work > 0 ? 64 - __clzll(max(wc, 1ll)) : 0;
             } else {
                 k = len > 0 ? 32 - __clz(len) : 0;
             }
             if (lane == 0) {
                 key[(isp ? 0 : cap) + a] = (uint8_t)k;
-                if (k || !isp) atomicAdd(&ctr->order_cnt[isp ? 0 : 1][k], 1);
+                if (isp) nchunks[a] = (uint8_t)nch;
+                if (k || !isp) atomicAdd(&ctr->order_cnt[isp ? 0 : 1][k], isp ? nch : 1);
             }
         }
         if (len <= 1) continue;
@@ -498,10 +505,13 @@ __global__ __launch_bounds__(1024) void k_segsort_long(const int *__restrict__ m
 // The order decides only which warp takes which receiver, never a result, so
 // positions inside a bucket may come in any order: a block counts its nodes
 // per bucket in shared memory and reserves their places with one atomic per
-// bucket.
+// bucket. The P2P items of a receiver split into chunks take consecutive
+// places, in chunk order (a chunk's warp waits for the chunk before it, which
+// was taken earlier).
 __global__ __launch_bounds__(256) void k_order_scatter(const DevCounters *__restrict__ nctr, int cap,
-                                                       const uint8_t *__restrict__ key, int *order,
-                                                       DevCounters *ctr)
+                                                       const uint8_t *__restrict__ key,
+                                                       const uint8_t *__restrict__ nchunks, int2 *p2p_items,
+                                                       int *order, DevCounters *ctr)
 {
     const int n_nodes = phase2_nodes(nctr);
     __shared__ int base[2][64], s_cnt[2][64], s_pos[2][64];
@@ -518,11 +528,12 @@ __global__ __launch_bounds__(256) void k_order_scatter(const DevCounters *__rest
         if (tid < 128) (&s_cnt[0][0])[tid] = 0;
         __syncthreads();
         const int a = a0 + tid;
-        int kp = 0, km = 0, rp = -1, rm = -1;
+        int kp = 0, km = 0, rp = -1, rm = -1, nch = 1;
         if (a < n_nodes) {
             kp = key[a];
             km = key[cap + a];
-            if (kp) rp = atomicAdd(&s_cnt[0][kp], 1);
+            nch = nchunks[a];
+            if (kp) rp = atomicAdd(&s_cnt[0][kp], nch);
             rm = atomicAdd(&s_cnt[1][km], 1);
         }
         __syncthreads();
@@ -533,7 +544,12 @@ __global__ __launch_bounds__(256) void k_order_scatter(const DevCounters *__rest
         }
         __syncthreads();
         if (a < n_nodes) {
-            if (kp) order[s_pos[0][kp] + rp] = a;
+            if (kp)
+                for (int c = 0; c < nch; ++c) {
+                    const int slot = s_pos[0][kp] + rp + c;
+                    if (slot < 2 * cap) p2p_items[slot] = make_int2(a, c | (nch << 8));
+                    else set_error(ctr, ERR_BOUNDS);
+                }
             order[cap + s_pos[1][km] + rm] = a;
         }
         __syncthreads();
@@ -583,10 +599,10 @@ int launch_lists(Plan &P, cudaStream_t s)
     k_csr_fill<<<P.num_sms * 8, 256, 0, s>>>(P.m2l_pairs, (int)(P.cap_m2l / kShards), P.p2p_pairs,
                                              (int)(P.cap_p2p / kShards), P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off,
                                              P.m2l_src, P.p2p_src, P.ctr);
-    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, cap, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
+    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, cap, P.p2p_nch, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
                                             P.node_count, P.order_key, P.ctr);
     k_segsort_long<<<P.num_sms, 1024, 0, s>>>(P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
-    k_order_scatter<<<P.num_sms * 4, 256, 0, s>>>(P.ctr, cap, P.order_key, P.order, P.ctr);
+    k_order_scatter<<<P.num_sms * 4, 256, 0, s>>>(P.ctr, cap, P.order_key, P.p2p_nch, P.p2p_items, P.order, P.ctr);
     return 5;
 }
 

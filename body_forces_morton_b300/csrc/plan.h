@@ -55,7 +55,10 @@ struct Plan {
     int *m2l_off = nullptr, *p2p_off = nullptr;    // CSR offsets [cap_nodes + 1]
     int *m2l_src = nullptr, *p2p_src = nullptr;    // CSR sources [2 * cap]
     int *long_seg = nullptr;                       // receivers whose lists are too long for the warp sort
-    int *order = nullptr;                          // [2][cap_nodes] receivers by decreasing work (P2P, M2L)
+    int *order = nullptr;                          // [2][cap_nodes] receivers by decreasing work (M2L in [1])
+    int2 *p2p_items = nullptr;                     // [2 cap_nodes] P2P work items (receiver, chunk | chunks << 8)
+    int *p2p_done = nullptr;                       // [cap_nodes] chunks of a receiver applied so far
+    uint8_t *p2p_nch = nullptr;                    // [cap_nodes] P2P chunks of every receiver
     uint8_t *order_key = nullptr;                  // [2][cap_nodes] work bucket of every node
 
     void *scratch = nullptr;       // 64 KiB for small per-block partials

@@ -238,3 +238,32 @@ def test_fp64_m2l_wide_pairs():
     mass = rng.uniform(0.5, 1.5, len(pos)) / len(pos)
     e, r, _ = full_parity(pos, mass, 4, 0.7, 8, check_coeffs=True)
     assert _df_wide_pairs(r) > 0
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_split_p2p_receivers(dt):
+    """A dense cluster with a few particles spread over the box: the sparse
+    leaves' tight boxes are large, so their P2P lists take in thousands of
+    cluster leaves and their work is split into chunks that different warps
+    sum in chunk order. Accelerations of the sparse particles (and a sample of
+    the others) against the oracle, bitwise repeatability, and that at least
+    one receiver was split (work above 2^20 interactions)."""
+    rng = np.random.default_rng(21)
+    pos = np.vstack([0.5 + 0.02 * rng.standard_normal((60000, 3)), rng.random((40, 3))]).astype(dt)
+    mass = np.full(len(pos), 1.0 / len(pos), dtype=dt)
+    acc, pot, ex, st = gpu_eval(pos, mass, 4, 0.7, 64, exports=("node_count", "p2p_off", "p2p_src"))
+    cnt = ex["node_count"].astype(np.int64)
+    off, src = ex["p2p_off"], ex["p2p_src"]
+    work = np.array([cnt[a] * cnt[src[off[a]:off[a + 1]]].sum() for a in range(len(cnt))])
+    assert work.max() > (1 << 20)
+    mask = np.zeros(len(pos), bool)
+    mask[-40:] = True
+    mask[rng.choice(60000, 500, replace=False)] = True
+    r = oracle.fmm(pos, mass, 4, 0.7, 64, eval_mask=mask)
+    tol = TOL_ACC["f32" if dt == np.float32 else "f64"]
+    e = accel_error(acc[mask].astype(np.float64), r.acc[mask])
+    ep = pot_error(pot[mask].astype(np.float64), r.pot[mask])
+    print(f"split receivers ({np.dtype(dt).name}): max work {work.max()}, acc error {e.max():.2e}, pot {ep.max():.2e}")
+    assert e.max() <= tol and ep.max() <= tol
+    a2, p2, _, _ = gpu_eval(pos, mass, 4, 0.7, 64, repeat=3)
+    assert np.array_equal(acc, a2) and np.array_equal(pot, p2)
