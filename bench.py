@@ -17,6 +17,7 @@ sample of the same workload on this machine's host cores.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -78,6 +79,11 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # nvidia-smi's first query stalls the driver for milliseconds: let it happen before timing
+            t0 = time.perf_counter()
+            while not self.lines and time.perf_counter() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.lines = []
         except (FileNotFoundError, OSError):
             self.proc = None
 
@@ -218,6 +224,8 @@ def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_overrid
         torch.cuda.synchronize()
         step_ms, stages, launches = [], [], 0
         stats = None
+        gc.collect()
+        gc.disable()  # no collector pause inside a timed step (the host launches every kernel)
         for _ in range(steps):
             flush_l2(flush_buf)
             e0 = torch.cuda.Event(enable_timing=True)
@@ -230,6 +238,7 @@ def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_overrid
             stats = plan.stats()
             stages.append(stats["stage_ms"])
             launches += stats["launches"]
+        gc.enable()
         torch.cuda.synchronize()
     stage_avg = {k: float(np.mean([s[k] for s in stages])) for k in stages[0]}
     return {"plan": plan, "pos": pos, "mass": mass, "g": g, "step_ms": step_ms, "stage_ms": stage_avg,
@@ -313,6 +322,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "n": res["n"], "p": w.p, "theta": w.theta, "leaf": w.leaf,
                    "l2": "flushed between timed steps (256 MiB write, outside the step events)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "step_ms_spread": {"min": min(res["step_ms"]), "median": statistics.median(res["step_ms"]),
+                           "max": max(res["step_ms"]), "argmax": int(np.argmax(res["step_ms"]))},
         "stage_ms": res["stage_ms"],
         "counts": {k: st[k] for k in ("n_nodes", "n_leaves", "depth", "n_m2l", "n_p2p", "n_p2p_interactions",
                                       "walk_pairs")},

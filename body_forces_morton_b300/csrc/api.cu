@@ -175,6 +175,7 @@ void destroy_plan(Plan &P)
     if (P.ctr_host) cudaFreeHost(P.ctr_host);
     for (int i = 0; i < kNumEvents; ++i)
         if (P.ev[i]) cudaEventDestroy(P.ev[i]);
+    if (P.ev_done) cudaEventDestroy(P.ev_done);
 }
 
 int64_t clamp_cap(double v) { return (int64_t)std::min(v, 2.0e9); }
@@ -193,12 +194,25 @@ const char *error_bits(unsigned e)
     return buf;
 }
 
+// Wait for the stream by polling an event: the calls block anyway, and a busy
+// wait returns as soon as the work is done instead of after the scheduler
+// wakes a sleeping thread.
+fmm_status wait_stream(Plan &P, cudaStream_t s)
+{
+    CUDA_TRY(cudaEventRecord(P.ev_done, s));
+    cudaError_t e;
+    while ((e = cudaEventQuery(P.ev_done)) == cudaErrorNotReady) {
+    }
+    CUDA_TRY(e);
+    return FMM_OK;
+}
+
+// Copy the status block back and wait for it.
 fmm_status sync_counters(Plan &P, cudaStream_t s)
 {
     CUDA_TRY(cudaGetLastError());
     CUDA_TRY(cudaMemcpyAsync(P.ctr_host, P.ctr, sizeof(DevCounters), cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaStreamSynchronize(s));
-    return FMM_OK;
+    return wait_stream(P, s);
 }
 
 fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, void *pot, cudaStream_t s)
@@ -218,7 +232,7 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         // ---- phase 1: box, keys, sort, tree (the tree kernel records the node count and depth)
         record(P, 0, s);
         CUDA_TRY(cudaMemsetAsync(P.ctr, 0, sizeof(DevCounters), s));
-        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 3 * sizeof(GridBarrier), s));
+        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 4 * sizeof(GridBarrier), s));
         P.launches += launch_keys(P, pos, s);
         record(P, 1, s);
         P.launches += launch_sort(P, pos, mass, s);
@@ -228,7 +242,6 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         // ---- phase 2, launched without waiting: every kernel reads the node count (and the walk
         // and L2L their extent) on the device, and skips the tree if its build failed
         record(P, 4, s);
-        CUDA_TRY(cudaMemsetAsync(P.node_done, 0, (size_t)P.cap_nodes * sizeof(int), s));
         CUDA_TRY(cudaMemsetAsync(P.m2l_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
         CUDA_TRY(cudaMemsetAsync(P.p2p_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
         CUDA_TRY(cudaMemsetAsync(P.p2p_done, 0, (size_t)P.cap_nodes * sizeof(int), s));
@@ -369,11 +382,12 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
-        !ok(dalloc(P.gbar, 3), "grid barriers") ||
+        !ok(dalloc(P.gbar, 4), "grid barriers") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);
     for (int i = 0; i < kNumEvents; ++i)
         if (!ok(cudaEventCreate(&P.ev[i]), "events")) return fail(FMM_ERR_CUDA);
+    if (!ok(cudaEventCreateWithFlags(&P.ev_done, cudaEventDisableTiming), "events")) return fail(FMM_ERR_CUDA);
     const int64_t cap = minimal ? 1024 : node_estimate(P);
     if (alloc_nodes(P, cap) != FMM_OK) return fail(FMM_ERR_OOM);
     // list sizes per node grow like theta^-3 (the pairs a node meets before acceptance); sized for the
@@ -418,7 +432,7 @@ fmm_status fmm_eval_host(fmm_plan *plan, const void *pos, const void *mass, void
     if (st) return st;
     CUDA_TRY(cudaMemcpyAsync(acc_out, P.h_acc, 3 * n * e, cudaMemcpyDeviceToHost, s));
     if (pot_out) CUDA_TRY(cudaMemcpyAsync(pot_out, P.h_pot, n * e, cudaMemcpyDeviceToHost, s));
-    CUDA_TRY(cudaStreamSynchronize(s));
+    if (fmm_status w = wait_stream(P, s)) return w;
     return FMM_OK;
 }
 
@@ -448,7 +462,7 @@ fmm_status fmm_kdk_step(fmm_plan *plan, void *pos, void *vel, const void *mass, 
     kdk_launches += P.launches;
     kdk_launches += launch_kick(P, vel, P.acc_cache, 0.5 * dt, s);
     CUDA_TRY(cudaGetLastError());
-    CUDA_TRY(cudaStreamSynchronize(s));
+    if (fmm_status w = wait_stream(P, s)) return w;
     P.launches = kdk_launches;
     P.cache_valid = true;
     P.cache_pos = pos;
@@ -491,7 +505,7 @@ fmm_status fmm_kdk_step_lattice(fmm_plan *plan, void *pos, void *vel, const void
     launches += P.launches;
     launches += launch_lattice_axpy(P, vel, P.acc_cache, 0.5 * dt, vel_exp, vel_exp, s);
     CUDA_TRY(cudaGetLastError());
-    CUDA_TRY(cudaStreamSynchronize(s));
+    if (fmm_status w = wait_stream(P, s)) return w;
     P.launches = launches;
     P.cache_valid = true;
     P.cache_pos = pos;

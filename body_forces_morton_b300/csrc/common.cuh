@@ -424,6 +424,35 @@ __device__ __forceinline__ void reduce_apply(T (&v)[NR], int lane, F &&store)
     }
 }
 
+// The same over the 8 lanes of an aligned lane group (j = lane & 7): three
+// halving steps (offsets 4, 2, 1) leave lane j the NR/8 sums of its block.
+template <class T, int NR, int NC, class F>
+__device__ __forceinline__ void reduce_apply8(T (&v)[NR], int j, F &&store)
+{
+    constexpr int H1 = NR / 2, H2 = NR / 4, H3 = NR / 8;
+    T a[H1], b[H2], c[H3];
+    const bool u4 = j & 4, u2 = j & 2, u1 = j & 1;
+#pragma unroll
+    for (int i = 0; i < H1; ++i) {
+        const T send = u4 ? v[i] : v[i + H1], keep = u4 ? v[i + H1] : v[i];
+        a[i] = keep + __shfl_xor_sync(kFull, send, 4);
+    }
+#pragma unroll
+    for (int i = 0; i < H2; ++i) {
+        const T send = u2 ? a[i] : a[i + H2], keep = u2 ? a[i + H2] : a[i];
+        b[i] = keep + __shfl_xor_sync(kFull, send, 2);
+    }
+#pragma unroll
+    for (int i = 0; i < H3; ++i) {
+        const T send = u1 ? b[i] : b[i + H3], keep = u1 ? b[i + H3] : b[i];
+        c[i] = keep + __shfl_xor_sync(kFull, send, 1);
+    }
+    const int base = (u4 ? H1 : 0) + (u2 ? H2 : 0) + (u1 ? H3 : 0);
+#pragma unroll
+    for (int i = 0; i < H3; ++i)
+        if (base + i < NC) store(base + i, c[i]);
+}
+
 template <class T, int NR, int NC>
 __device__ __forceinline__ void reduce_store(T (&v)[NR], int lane, T *__restrict__ dst)
 {

@@ -70,7 +70,7 @@ struct Plan {
 
     // status
     DevCounters *ctr = nullptr;      // device
-    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0], walk [1], L2L [2] launches
+    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0], walk [1], L2L [2], upward [3]
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
@@ -83,6 +83,7 @@ struct Plan {
 
     // timing and stats of the last evaluation
     cudaEvent_t ev[kNumEvents] = {};
+    cudaEvent_t ev_done = nullptr;   // completion of the status read-back (polled)
     int ev_stage[kNumEvents] = {};
     int n_ev = 0;
     int launches = 0;
