@@ -150,9 +150,13 @@ fmm_status alloc_lists(Plan &P, int64_t cap_frontier, int64_t cap_m2l, int64_t c
 {
     free_lists(P);
     auto round_up = [](int64_t v) { return (v + kShards - 1) / kShards * kShards; };
-    cap_frontier = round_up(cap_frontier);
-    cap_m2l = round_up(cap_m2l);
-    cap_p2p = round_up(cap_p2p);
+    // every shard holds at least one walk tile's worst output: 256 pairs of up to 36 child pairs
+    // (a self pair of 8 children) for the frontier, one M2L or P2P pair each for the lists
+    // (not under BFM_FMM_FAULT=capacity, which starts every buffer small to exercise regrowth)
+    const int64_t ff = P.minimal_caps ? 1 : 36, fl = P.minimal_caps ? 1 : 256;
+    cap_frontier = round_up(std::max<int64_t>(cap_frontier, (int64_t)kShards * fl * ff));
+    cap_m2l = round_up(std::max<int64_t>(cap_m2l, (int64_t)kShards * fl));
+    cap_p2p = round_up(std::max<int64_t>(cap_p2p, (int64_t)kShards * fl));
     P.cap_frontier = cap_frontier;
     P.cap_m2l = cap_m2l;
     P.cap_p2p = cap_p2p;
@@ -343,6 +347,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     if (!h) { set_err("fmm_plan_create: out of host memory"); return nullptr; }
     Plan &P = h->P;
     P.n = n; P.p = p; P.theta = theta; P.leaf = leaf; P.dtype = (int)dtype;
+    P.minimal_caps = minimal;
     P.esize = dtype == FMM_F32 ? 4 : 8;
     P.nc = (p + 1) * (p + 2) * (p + 3) / 6;
     P.ncp = (P.nc + 3) / 4 * 4;
@@ -393,7 +398,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     // list sizes per node grow like theta^-3 (the pairs a node meets before acceptance); sized for the
     // clustered and Plummer workloads with room to spare, so that evaluations rarely regrow
     const double lf = (minimal ? 1.0 / 16 : 1.0) * std::max(1.0, std::pow(0.7 / theta, 3.0));
-    if (alloc_lists(P, clamp_cap(16.0 * lf * cap), clamp_cap(64.0 * lf * cap), clamp_cap(24.0 * lf * cap)) != FMM_OK)
+    if (alloc_lists(P, clamp_cap(32.0 * lf * cap), clamp_cap(64.0 * lf * cap), clamp_cap(24.0 * lf * cap)) != FMM_OK)
         return fail(FMM_ERR_OOM);
     return h;
 }
