@@ -17,6 +17,10 @@ namespace bfm {
 
 struct __align__(8) df {
     float h, l;
+    df() = default;
+    __host__ __device__ constexpr df(float h_, float l_) : h(h_), l(l_) {}
+    // from a constant of the generated expansion code (split at compile time for literals)
+    __host__ __device__ constexpr df(double v) : h((float)v), l((float)(v - (double)(float)v)) {}
 };
 
 __device__ __forceinline__ df df_make(float h, float l)
@@ -131,8 +135,13 @@ __device__ __forceinline__ void mac(dacc &a, const df &x, const df &y)  // a += 
 
 __device__ __forceinline__ df dacc_value(const dacc &a) { return two_sum(a.h, a.l); }
 
+// Operators, so that the generated expansion templates (P2M, L2P, ...) run in double words.
 __device__ __forceinline__ df operator+(const df &x, const df &y) { return df_add(x, y); }
+__device__ __forceinline__ df operator-(const df &x, const df &y) { return df_sub(x, y); }
+__device__ __forceinline__ df operator-(const df &x) { return df_neg(x); }
+__device__ __forceinline__ df operator*(const df &x, const df &y) { return df_mul(x, y); }
 __device__ __forceinline__ df &operator+=(df &x, const df &y) { return x = df_add(x, y); }
+__device__ __forceinline__ df &operator-=(df &x, const df &y) { return x = df_sub(x, y); }
 
 using ::__shfl_xor_sync;  // keep the CUDA overloads visible next to the one below
 __device__ __forceinline__ df __shfl_xor_sync(unsigned mask, df v, int o)
@@ -150,6 +159,21 @@ __device__ __forceinline__ void df_units(const dbl4 *__restrict__ node_l, const 
     const dbl4 l = node_l[0];
     frexp(fmax(fmax(l.x, l.y), l.z), &ex);
     frexp(M[0], &em);
+}
+
+// Total degree of coefficient n in the graded coefficient order (the first
+// index of degree d is d(d+1)(d+2)/6).
+__host__ __device__ __forceinline__ int coef_degree(int n)
+{
+    return (n >= 1) + (n >= 4) + (n >= 10) + (n >= 20) + (n >= 35) + (n >= 56) + (n >= 84) + (n >= 120);
+}
+
+// x 2^e for the unit conversions: one multiplication by an exactly built power
+// of two while 2^e is a normal double, the library ldexp otherwise.
+__device__ __forceinline__ double scale2(double x, int e)
+{
+    if (e >= -1022 && e <= 1023) return x * __longlong_as_double((long long)(1023 + e) << 52);
+    return ldexp(x, e);
 }
 
 // 2^k as an fp32 number, |k| <= 126

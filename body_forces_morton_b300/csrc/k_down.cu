@@ -555,7 +555,8 @@ int launch_l2l(Plan &P, int depth, cudaStream_t s)
 
 int launch_l2p(Plan &P, cudaStream_t s)
 {
-    return P.dtype == 0 ? launch_l2p_t<float>(P, s) : launch_l2p_t<double>(P, s);
+    if (P.dtype == 0) return launch_l2p_t<float>(P, s);
+    return P.p <= kMaxPL2pDf ? launch_l2p_df(P, s) : launch_l2p_t<double>(P, s);
 }
 
 // fp32 plans: k_p2p; fp64 plans: the double-float near field (k_p2p_df.cu)

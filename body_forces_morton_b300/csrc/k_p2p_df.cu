@@ -13,6 +13,7 @@
 // of the size of a leaf, so the separation keeps ~48 bits relative to the leaf
 // size rather than to |x|. Sums run in a fixed order (reproducible).
 #include "dfloat.cuh"
+#include "expansions_gen.cuh"
 #include "plan.h"
 
 namespace bfm {
@@ -95,8 +96,8 @@ __global__ __launch_bounds__(256) void k_leaf_offsets(const DevCounters *__restr
         const dbl4 c = nc[a];
         for (int i = first[a] + lane; i < first[a] + count[a]; i += 32) {
             const dbl4 q = xyzm[i];
-            const df x = df_from(ldexp(q.x - c.x, -ex)), y = df_from(ldexp(q.y - c.y, -ex));
-            const df z = df_from(ldexp(q.z - c.z, -ex)), m = df_from(ldexp(q.w, -em));
+            const df x = df_from(scale2(q.x - c.x, -ex)), y = df_from(scale2(q.y - c.y, -ex));
+            const df z = df_from(scale2(q.z - c.z, -ex)), m = df_from(scale2(q.w, -em));
             rel[i] = make_float4(x.h, y.h, z.h, m.h);
             rel[n + i] = make_float4(x.l, y.l, z.l, m.l);
         }
@@ -174,7 +175,7 @@ __device__ __forceinline__ void span_df(const float4 *buf, const int *sidx, int 
 }
 
 // |l| of a node (from the |l|^2 stored with its centre) in the scaled units
-__device__ __forceinline__ float ext_scaled(const dbl4 &c, int ex) { return sqrtf((float)ldexp(c.w, -2 * ex)); }
+__device__ __forceinline__ float ext_scaled(const dbl4 &c, int ex) { return sqrtf((float)scale2(c.w, -2 * ex)); }
 
 __device__ __forceinline__ float exact_thr2(float e)
 {
@@ -239,9 +240,9 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
                 lf = first[b];
                 cb = count[b];
                 const dbl4 cbc = nc[b];
-                dxl = df_from(ldexp(cbc.x - ca.x, -cx.ex));
-                dyl = df_from(ldexp(cbc.y - ca.y, -cx.ex));
-                dzl = df_from(ldexp(cbc.z - ca.z, -cx.ex));
+                dxl = df_from(scale2(cbc.x - ca.x, -cx.ex));
+                dyl = df_from(scale2(cbc.y - ca.y, -cx.ex));
+                dzl = df_from(scale2(cbc.z - ca.z, -cx.ex));
                 eb = sqrtf(dxl.h * dxl.h + dyl.h * dyl.h + dzl.h * dzl.h) + ext_scaled(cbc, cx.ex);
             }
         }
@@ -277,8 +278,8 @@ __device__ __forceinline__ void round_df(int a, int f, int c, int r0, int cr, in
             const int i = f + r0 + rr;
             // the far field, plus the partial sums of the earlier chunks (written by other warps)
             const dbl4 fa = CHUNKED ? ld_cg(far + i) : far[i];
-            const double sx = fa.x + ldexp(t[0], epot), sy = fa.y + ldexp(t[1], eacc);
-            const double sz = fa.z + ldexp(t[2], eacc), sw = fa.w + ldexp(t[3], eacc);
+            const double sx = fa.x + scale2(t[0], epot), sy = fa.y + scale2(t[1], eacc);
+            const double sz = fa.z + scale2(t[2], eacc), sw = fa.w + scale2(t[3], eacc);
             if (CHUNKED && chunk < nch - 1) {
                 far[i] = make4<double>(sx, sy, sz, sw);
             } else {
@@ -363,21 +364,93 @@ __global__ __launch_bounds__(DF_WARPS * 32, 4) void k_p2p_df(const DevCounters *
     }
 }
 
+// L2P of fp64 plans in double-float: every leaf's complete local expansion
+// evaluated at its particles (Taylor eq.), into `far` (phi, a). In exact
+// power-of-two units: lengths in the leaf level's cell bound h = 2^(ex - l),
+// masses in 2^em (df_units), so u = (x - c) / h stays below 2 and the
+// coefficients L~_k = L_k 2^(-em) h^|k| 2^(ex) are of one scale; then
+// phi = 2^(em - ex) sum L~_k u^k / k!, a = -2^(em - ex) / h sum L~_(k+e) u^k / k!.
+// The offsets come from the leaf-relative double words of k_leaf_offsets (box
+// units, scaled exactly to u), so the FP64 pipe only converts the
+// coefficients (once per leaf) and the four results.
+template <int P>
+__global__ __launch_bounds__(256) void k_l2p_df(const DevCounters *__restrict__ nctr, const int *__restrict__ first,
+                                                const int *__restrict__ count, const int *__restrict__ nchild,
+                                                const int *__restrict__ level, const float4 *__restrict__ rel, int n,
+                                                const dbl4 *__restrict__ nl, const double *__restrict__ M,
+                                                const double *__restrict__ L, int ncp, dbl4 *__restrict__ far)
+{
+    constexpr int NC = Exp<P>::NC;
+    __shared__ df s_L[8][NC];
+    const int n_nodes = phase2_nodes(nctr);
+    if (n_nodes == 0) return;
+    int ex, em;
+    df_units(nl, M, ex, em);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
+        if (nchild[a] != 0) continue;
+        const int f = first[a], c = count[a], lv = level[a];
+        __syncwarp();
+        for (int k = lane; k < NC; k += 32)
+            s_L[w][k] = df_from(scale2(L[(size_t)a * ncp + k], ex - em + (ex - lv) * coef_degree(k)));
+        __syncwarp();
+        const float su = pow2f(lv);  // box units -> leaf units
+        const int ephi = em - ex, eacc = em - ex - (ex - lv);
+        for (int i = f + lane; i < f + c; i += 32) {
+            const float4 h = rel[i], l = rel[n + i];
+            const df ux = df_scale(df(h.x, l.x), su), uy = df_scale(df(h.y, l.y), su), uz = df_scale(df(h.z, l.z), su);
+            df phi(0.0f, 0.0f), ax(0.0f, 0.0f), ay(0.0f, 0.0f), az(0.0f, 0.0f);
+            Exp<P>::template l2p<df>(s_L[w], ux, uy, uz, phi, ax, ay, az);
+            far[i] = make4<double>(scale2(df_to(phi), ephi), scale2(df_to(ax), eacc), scale2(df_to(ay), eacc),
+                                   scale2(df_to(az), eacc));
+        }
+    }
+}
+
+template <int P>
+int launch_l2p_df_p(Plan &P_, cudaStream_t s)
+{
+    // leaf-relative offsets first (they serve this kernel and the near field)
+    k_leaf_offsets<<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, (int)P_.n, P_.node_first, P_.node_count, P_.node_nchild,
+                                                  (const dbl4 *)P_.xyzm, (const dbl4 *)P_.node_c,
+                                                  (const dbl4 *)P_.node_l, (const double *)P_.M, (float4 *)P_.rel);
+    k_l2p_df<P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.node_first, P_.node_count, P_.node_nchild, P_.node_level,
+                                               (const float4 *)P_.rel, (int)P_.n, (const dbl4 *)P_.node_l,
+                                               (const double *)P_.M, (const double *)P_.L, P_.ncp, (dbl4 *)P_.far);
+    return 2;
+}
+
 }  // namespace
+
+int launch_l2p_df(Plan &P, cudaStream_t s)
+{
+    switch (P.p) {
+    case 0: return launch_l2p_df_p<0>(P, s);
+    case 1: return launch_l2p_df_p<1>(P, s);
+    case 2: return launch_l2p_df_p<2>(P, s);
+    case 3: return launch_l2p_df_p<3>(P, s);
+    case 4: return launch_l2p_df_p<4>(P, s);
+    case 5: return launch_l2p_df_p<5>(P, s);
+    default: return launch_l2p_df_p<6>(P, s);
+    }
+}
 
 int launch_p2p_df(Plan &P, void *acc, void *pot, cudaStream_t s)
 {
-    k_leaf_offsets<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, (int)P.n, P.node_first, P.node_count,
-                                                P.node_nchild, (const dbl4 *)P.xyzm, (const dbl4 *)P.node_c,
-                                                (const dbl4 *)P.node_l, (const double *)P.M, (float4 *)P.rel);
+    int launches = 1;
+    if (P.p > kMaxPL2pDf) {  // the double-float L2P, which computes the offsets, did not run
+        ++launches;
+        k_leaf_offsets<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, (int)P.n, P.node_first, P.node_count, P.node_nchild,
+                                                    (const dbl4 *)P.xyzm, (const dbl4 *)P.node_c,
+                                                    (const dbl4 *)P.node_l, (const double *)P.M, (float4 *)P.rel);
+    }
     k_p2p_df<<<P.num_sms * 16, DF_WARPS * 32, 0, s>>>(P.ctr, P.p2p_items, P.p2p_done, P.ctr, (int)P.n, P.node_first,
-                                                      P.node_count,
-                                                      (const dbl4 *)P.xyzm, (const dbl4 *)P.node_c,
+                                                      P.node_count, (const dbl4 *)P.xyzm, (const dbl4 *)P.node_c,
                                                       (const float4 *)P.rel, P.idx[0], (dbl4 *)P.far, P.p2p_off,
-                                                      P.p2p_src,
-                                                      (const dbl4 *)P.node_l, (const double *)P.M, (double *)acc,
-                                                      (double *)pot);
-    return 2;
+                                                      P.p2p_src, (const dbl4 *)P.node_l, (const double *)P.M,
+                                                      (double *)acc, (double *)pot);
+    return launches;
 }
 
 }  // namespace bfm

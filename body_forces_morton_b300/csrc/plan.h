@@ -116,6 +116,8 @@ int launch_l2l(Plan &P, int depth, cudaStream_t s);
 int launch_l2p(Plan &P, cudaStream_t s);
 int launch_p2p(Plan &P, void *acc, void *pot, cudaStream_t s);
 int launch_p2p_df(Plan &P, void *acc, void *pot, cudaStream_t s);
+int launch_l2p_df(Plan &P, cudaStream_t s);  // fp64 plans, p <= kMaxPL2pDf
+constexpr int kMaxPL2pDf = 6;
 int launch_kick(Plan &P, void *vel, const void *acc, double h, cudaStream_t s);
 int launch_drift(Plan &P, void *pos, const void *vel, double dt, cudaStream_t s);
 int launch_lattice_axpy(Plan &P, void *y, const void *x, double h, int e_y, int e_inc, cudaStream_t s);
