@@ -77,7 +77,7 @@ struct DeviceGuard {
     }
 };
 
-constexpr int RS_TILE = 4096;
+constexpr int RS_TILE = 2048;  // the radix sort's smallest tile (flags per pass: tiles x 256 digits)
 
 void free_nodes(Plan &P)
 {

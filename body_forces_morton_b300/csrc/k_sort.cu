@@ -21,8 +21,9 @@ namespace {
 constexpr int kBoxThreads = 256;
 constexpr int RS_THREADS = 256;
 constexpr int RS_WARPS = RS_THREADS / 32;
-constexpr int RS_ITEMS = 16;
-constexpr int RS_TILE = RS_THREADS * RS_ITEMS;
+// keys per thread: 16 (4096-key tiles) from N = 2^19 on, 8 (2048-key tiles, twice the
+// blocks) below, where the sort has too few tiles to fill the GPU (both measured)
+constexpr int RS_ITEMS_LARGE = 16, RS_ITEMS_SMALL = 8;
 
 __device__ __forceinline__ uint64_t spread3(uint32_t v)
 {
@@ -146,7 +147,7 @@ __global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, 
     }
 }
 
-template <class T, bool FIRST, bool LAST>
+template <class T, bool FIRST, bool LAST, int RS_ITEMS>
 __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__restrict__ kin,
                                                            const uint32_t *__restrict__ vin,
                                                            uint64_t *__restrict__ kout, uint32_t *__restrict__ vout,
@@ -164,7 +165,7 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
     __syncthreads();
     const int tile = s_tile;
     const int shift = 8 * pass;
-    const int64_t start = (int64_t)tile * RS_TILE + warp * (32 * RS_ITEMS);
+    const int64_t start = (int64_t)tile * (RS_THREADS * RS_ITEMS) + warp * (32 * RS_ITEMS);
     uint64_t k[RS_ITEMS];
     uint32_t v[RS_ITEMS];
     unsigned rank[RS_ITEMS];
@@ -263,32 +264,38 @@ int launch_keys_t(Plan &P, const void *pos, cudaStream_t s)
     return 2;
 }
 
-template <class T>
-int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
+template <class T, int ITEMS>
+int radix_passes(Plan &P, const void *pos, const void *mass, cudaStream_t s)
 {
     const int n = (int)P.n;
-    const int tiles = (n + RS_TILE - 1) / RS_TILE;
-    int launches = 0;
+    const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
     for (int pass = 0; pass < 8; ++pass) {
         const int src = pass & 1, dst = src ^ 1;
         const int slot = P.next_slot();
         const unsigned ep = P.next_epoch();
         if (pass == 0)
-            k_radix_pass<T, true, false><<<tiles, RS_THREADS, 0, s>>>(P.keys[src], nullptr, P.keys[dst], P.idx[dst], n,
-                                                                     pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
-                                                                     nullptr);
+            k_radix_pass<T, true, false, ITEMS><<<tiles, RS_THREADS, 0, s>>>(
+                P.keys[src], nullptr, P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
+                nullptr);
         else if (pass == 7)
-            k_radix_pass<T, false, true><<<tiles, RS_THREADS, 0, s>>>(
+            k_radix_pass<T, false, true, ITEMS><<<tiles, RS_THREADS, 0, s>>>(
                 P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, (const T *)pos,
                 (const T *)mass, (vec4<T> *)P.xyzm);
         else
-            k_radix_pass<T, false, false><<<tiles, RS_THREADS, 0, s>>>(P.keys[src], P.idx[src], P.keys[dst],
-                                                                      P.idx[dst], n, pass, P.flags, ep, slot, P.ctr,
-                                                                      nullptr, nullptr, nullptr);
-        ++launches;
+            k_radix_pass<T, false, false, ITEMS><<<tiles, RS_THREADS, 0, s>>>(
+                P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
+                nullptr);
     }
+    return 8;
+}
+
+template <class T>
+int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
+{
+    const int launches = P.n >= (1 << 19) ? radix_passes<T, RS_ITEMS_LARGE>(P, pos, mass, s)
+                                          : radix_passes<T, RS_ITEMS_SMALL>(P, pos, mass, s);
     // after 8 passes the sorted data is back in buffer 0
-    k_diverge<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], n, P.div, P.node_first, P.node_count, P.node_child0,
+    k_diverge<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], (int)P.n, P.div, P.node_first, P.node_count, P.node_child0,
                                            P.node_nchild, P.node_parent, P.node_level, P.ctr);
     return launches + 1;
 }
