@@ -13,6 +13,7 @@
 // four parents at a time, a lane per child (at most 8): the parent's box is
 // the union of the children's boxes and its moments the sum of the children's
 // M2M translations, reduced in a fixed order over the 8-lane group.
+#include "dfloat.cuh"
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -134,7 +135,7 @@ __global__ __launch_bounds__(256) void k_upward_all(GridBarrier *gb, DevCounters
 // waits. It keeps the FP64-bound M2M work spread over the whole pass, where
 // the level-synchronous kernel would run each level's alone.
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_upward_ticket(const DevCounters *__restrict__ nctr, const vec4<T> *__restrict__ xyzm,
+__global__ __launch_bounds__(256, 2) void k_upward_ticket(const DevCounters *__restrict__ nctr, const vec4<T> *__restrict__ xyzm,
                                                 const int *__restrict__ first, const int *__restrict__ count,
                                                 const int *__restrict__ child0, const int *__restrict__ nchild,
                                                 const int *__restrict__ parent, int *done, T *node_lo, T *node_hi,
@@ -163,7 +164,28 @@ __global__ __launch_bounds__(256) void k_upward_ticket(const DevCounters *__rest
                 hi[k] = tmax(hi[k], __shfl_xor_sync(kFull, hi[k], o));
             }
         store_geometry<T>(a, lo, hi, node_lo, node_hi, nc, nl, cen, lane == 0);
-        {
+        if constexpr (sizeof(T) == 8 && P <= kMaxPL2pDf) {
+            // P2M in double-float, in the leaf's own power-of-two units: lengths in 2^eh >= its
+            // largest half-width, masses in 2^em >= its mass (the FP64 pipe only forms the offsets)
+            T msum = T(0);
+            for (int i = f + lane; i < f + c; i += 32) msum += xyzm[i].w;
+            for (int o = 16; o > 0; o >>= 1) msum += __shfl_xor_sync(kFull, msum, o);
+            int eh, em;
+            frexp(tmax(tmax(hi[0] - lo[0], hi[1] - lo[1]), hi[2] - lo[2]) * T(0.5), &eh);
+            frexp(msum, &em);
+            df m[NR];
+#pragma unroll
+            for (int k = 0; k < NR; ++k) m[k] = df(0.0f, 0.0f);
+            for (int i = f + lane; i < f + c; i += 32) {
+                const vec4<T> q = xyzm[i];
+                Exp<P>::template p2m<df>(df_from(scale2(q.x - cen[0], -eh)), df_from(scale2(q.y - cen[1], -eh)),
+                                         df_from(scale2(q.z - cen[2], -eh)), df_from(scale2(q.w, -em)), m);
+            }
+            T *dst = M + (size_t)a * ncp;
+            reduce_apply<df, NR, NC>(m, lane, [&](int k, const df &x) {
+                dst[k] = scale2(df_to(x), em + eh * coef_degree(k));
+            });
+        } else {
             T m[NR];
 #pragma unroll
             for (int k = 0; k < NR; ++k) m[k] = T(0);
