@@ -160,6 +160,23 @@ __device__ __forceinline__ void p2p_span(const vec4<T> *buf, int n_here, int q, 
 // Staged sources are stored pair-interleaved, (x_j, x_j+1, y_j, y_j+1, z_j,
 // z_j+1, m_j, m_j+1) per pair, so two 16-byte shared loads give four packed
 // operands; an odd tail is padded with a massless particle far away.
+// Asynchronous global-to-shared copies (cp.async, L1-allocating): a warp's
+// staging issues every copy of a chunk before waiting once, instead of one
+// load latency per 32 particles.
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src)
+{
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src)
+{
+    const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 __device__ __forceinline__ void put_pair_layout(float *fb, int k, float x, float y, float z, float m)
 {
     const int base = (k >> 1) * 8 + (k & 1);
@@ -216,11 +233,16 @@ __device__ __forceinline__ int stage_sources_pairs(float *fb, const float4 *__re
         const int f = __shfl_sync(kFull, lf, lo);
         const int e = __shfl_sync(kFull, ex, lo);
         if (k < n_here) {
-            const float4 v = xyzm[f + (g - e)];
-            put_pair_layout(fb, k, v.x, v.y, v.z, v.w);
+            const float *v = reinterpret_cast<const float *>(xyzm + f + (g - e));
+            float *d = fb + (k >> 1) * 8 + (k & 1);  // the pair-interleaved slots of put_pair_layout
+            cp_async4(d, v);
+            cp_async4(d + 2, v + 1);
+            cp_async4(d + 4, v + 2);
+            cp_async4(d + 6, v + 3);
         }
     }
     if ((n_here & 1) && lane == 0) put_pair_layout(fb, n_here, 1e18f, 1e18f, 1e18f, 0.0f);
+    cp_async_wait_all();
     return (n_here + 1) >> 1;
 }
 
@@ -280,35 +302,51 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
 #pragma unroll
     for (int k = 0; k < K; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = T(0);
     const int qq = worker ? q : (1 << 30);  // idle lanes start past every chunk
+    // source leaves of the list, 32 entries at a time: lane i holds entry lb + i (first particle, count;
+    // the receiving leaf itself counts as empty). The next group's entries load while this one computes.
+    auto fetch = [&](int lb, int &fb, int &cb) {
+        const int e = lb + lane;
+        fb = 0;
+        cb = 0;
+        if (e < end) {
+            const int b = src[e];
+            if (b != a) {
+                fb = first[b];
+                cb = count[b];
+            }
+        }
+    };
+    int fb_next = 0, cb_next = 0;
+    if (beg < end) fetch(beg, fb_next, cb_next);
     // the leaf's own particles (zero separations possible; the first chunk of a split receiver)
     for (int g0 = 0; (!CHUNKED || chunk == 0) && g0 < c; g0 += CH) {
         const int n_here = min(CH, c - g0);
         __syncwarp();
-        for (int k = lane; k < n_here; k += 32) buf[k] = xyzm[f + g0 + k];
+        for (int k = lane; k < n_here; k += 32)
+#pragma unroll
+            for (int h = 0; h < (int)sizeof(vec4<T>); h += 16)
+                cp_async16(reinterpret_cast<char *>(buf + k) + h, reinterpret_cast<const char *>(xyzm + f + g0 + k) + h);
+        cp_async_wait_all();
         __syncwarp();
         p2p_span<T, true, K>(buf, n_here, qq, S, p, acc);
     }
-    // every other source leaf, 32 list entries at a time
+    // every other source leaf
     if constexpr (std::is_same<T, float>::value) {
+        // packed accumulators start from the own-leaf sums (A[0] collects +m/r, the potential is its negative)
         float2 X[K], Y[K], Z[K], A[K][4];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
             X[k] = make_float2(-p[k].x, -p[k].x);
             Y[k] = make_float2(-p[k].y, -p[k].y);
             Z[k] = make_float2(-p[k].z, -p[k].z);
-            A[k][0] = A[k][1] = A[k][2] = A[k][3] = make_float2(0.0f, 0.0f);
+            A[k][0] = make_float2(-acc[k][0], 0.0f);
+#pragma unroll
+            for (int v = 1; v < 4; ++v) A[k][v] = make_float2(acc[k][v], 0.0f);
         }
         float *fbuf = reinterpret_cast<float *>(buf);
         for (int lb = beg; lb < end; lb += 32) {
-            const int e = lb + lane;
-            int fb = 0, cb = 0;
-            if (e < end) {
-                const int b = src[e];
-                if (b != a) {
-                    fb = first[b];
-                    cb = count[b];
-                }
-            }
+            const int fb = fb_next, cb = cb_next;
+            if (lb + 32 < end) fetch(lb + 32, fb_next, cb_next);
             const int incl = warp_incl_scan(cb);
             const int tot = __shfl_sync(kFull, incl, 31);
             const int ex = incl - cb;
@@ -321,21 +359,14 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
         }
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            acc[k][0] -= A[k][0].x + A[k][0].y;
+            acc[k][0] = -(A[k][0].x + A[k][0].y);
 #pragma unroll
-            for (int v = 1; v < 4; ++v) acc[k][v] += A[k][v].x + A[k][v].y;
+            for (int v = 1; v < 4; ++v) acc[k][v] = A[k][v].x + A[k][v].y;
         }
     } else {
         for (int lb = beg; lb < end; lb += 32) {
-            const int e = lb + lane;
-            int fb = 0, cb = 0;
-            if (e < end) {
-                const int b = src[e];
-                if (b != a) {
-                    fb = first[b];
-                    cb = count[b];
-                }
-            }
+            const int fb = fb_next, cb = cb_next;
+            if (lb + 32 < end) fetch(lb + 32, fb_next, cb_next);
             const int incl = warp_incl_scan(cb);
             const int tot = __shfl_sync(kFull, incl, 31);
             const int ex = incl - cb;
