@@ -160,23 +160,6 @@ __device__ __forceinline__ void p2p_span(const vec4<T> *buf, int n_here, int q, 
 // Staged sources are stored pair-interleaved, (x_j, x_j+1, y_j, y_j+1, z_j,
 // z_j+1, m_j, m_j+1) per pair, so two 16-byte shared loads give four packed
 // operands; an odd tail is padded with a massless particle far away.
-// Asynchronous global-to-shared copies (cp.async, L1-allocating): a warp's
-// staging issues every copy of a chunk before waiting once, instead of one
-// load latency per 32 particles.
-__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src)
-{
-    const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src)
-{
-    const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(src) : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-
 __device__ __forceinline__ void put_pair_layout(float *fb, int k, float x, float y, float z, float m)
 {
     const int base = (k >> 1) * 8 + (k & 1);
