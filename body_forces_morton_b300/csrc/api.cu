@@ -1,12 +1,14 @@
 // C ABI of the FMM library: plan life cycle, the evaluation pipeline, the
 // kick-drift-kick step, statistics and inspection exports.
 //
-// An evaluation runs in two phases on the caller's stream:
-//   phase 1  root box, keys, radix sort (+ gather), octree levels;
-//            then one read-back of the small status block (node count, depth)
-//   phase 2  upward pass, dual-tree walk (2 * depth + 1 generations), lists,
-//            M2L, L2L (depth + 1 levels), L2P + P2P + scatter;
-//            then one read-back of the status block.
+// An evaluation runs in two phases on the caller's stream, with no host wait
+// between them:
+//   phase 1  root box, keys, radix sort (+ gather), octree levels (the tree
+//            kernel records the node count and depth on the device);
+//   phase 2  upward pass, dual-tree walk (until its frontier is empty), lists,
+//            M2L, L2L (ordered by level), L2P + P2P + scatter, every kernel
+//            reading the node count and depth on the device;
+//   then one read-back of the small status block.
 // Capacities of the node, frontier and pair buffers are estimates; a kernel
 // that would exceed one skips the write and sets a bit in the status word, and
 // the evaluation is repeated with larger buffers.
@@ -95,6 +97,8 @@ void free_nodes(Plan &P)
     P.p2p_items = nullptr;
     dfree(P.p2p_nch);
     P.p2p_nch = nullptr;
+    dfree(P.l2l_flag);
+    P.l2l_flag = nullptr;
 }
 
 void free_lists(Plan &P)
@@ -127,6 +131,9 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
     CUDA_TRY(dalloc(P.p2p_items, 2 * c));
     CUDA_TRY(dalloc(P.p2p_done, c));
     CUDA_TRY(dalloc(P.p2p_nch, c));
+    CUDA_TRY(dalloc(P.l2l_flag, c));
+    CUDA_TRY(cudaMemset(P.l2l_flag, 0, c * sizeof(unsigned)));
+    P.l2l_seq = 0;
     CUDA_TRY(dalloc(P.order_key, 2 * c));
     CUDA_TRY(cudaMalloc(&P.node_lo, 3 * c * e));
     CUDA_TRY(cudaMalloc(&P.node_hi, 3 * c * e));

@@ -1,4 +1,5 @@
-// Downward pass: L2L level by level, then L2P + P2P at the leaves.
+// Downward pass: L2L from the root down (one launch, ordered by level), then
+// L2P + P2P at the leaves.
 //
 // JZ-FMM page, "Combining near and far interactions", stage 3: translate each
 // parent's local Taylor expansion to its children, evaluate the expansions at
@@ -23,44 +24,6 @@
 namespace bfm {
 
 namespace {
-
-// L2L, all levels in one cooperative launch with a grid barrier between
-// levels: a node's complete local is its own M2L local plus its parent's
-// complete local translated to its centre. The parent's local was written by
-// another block before the barrier; the barrier's acquire orders it before
-// these (cached) loads, which siblings share.
-template <class T, int P>
-__global__ __launch_bounds__(256) void k_l2l_all(GridBarrier *gb, DevCounters *ctr, const int *__restrict__ parent,
-                                                 const vec4<T> *__restrict__ nc, const T *__restrict__ Lm2l,
-                                                 T *__restrict__ L, int ncp)
-{
-    constexpr int NC = Exp<P>::NC;
-    const int n = phase2_nodes(ctr);
-    const int depth = n > 0 ? ctr->depth : -1;
-    for (int level = 0; level <= depth; ++level) {
-        const int lo = ctr->level_off[level], hi = min(ctr->level_off[level + 1], n);
-        for (int a = lo + blockIdx.x * blockDim.x + threadIdx.x; a < hi; a += gridDim.x * blockDim.x) {
-            T out[NC];
-            const T *own = Lm2l + (size_t)a * ncp;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) out[k] = own[k];
-            if (level > 0) {
-                const int par = parent[a];
-                T lp[NC];
-                const T *pr = L + (size_t)par * ncp;
-#pragma unroll
-#pragma unroll
-                for (int k = 0; k < NC; ++k) lp[k] = pr[k];
-                const vec4<T> c = nc[a], cp = nc[par];
-                Exp<P>::template l2l<T>(lp, c.x - cp.x, c.y - cp.y, c.z - cp.z, out);
-            }
-            T *dst = L + (size_t)a * ncp;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) dst[k] = out[k];
-        }
-        if (level < depth && !grid_barrier(gb, (unsigned)level, ctr)) return;
-    }
-}
 
 // One source particle s acting on a receiver at (x, y, z). The self leaf may
 // hold the receiver itself (zero separation), which MASKED skips; between two
@@ -478,60 +441,87 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
     }
 }
 
-// fp32 plans' L2L: one launch per level (levels below the tree's depth exit at
-// once); measured faster than the cooperative kernel for fp32, slower for fp64.
+// L2L in one launch, without grid barriers: warps take chunks of up to 32
+// nodes of one level from a shared counter, in level order (root first). A
+// node's thread waits, bounded, until its parent's flag holds this
+// evaluation's number, which the parent's thread stores with release
+// semantics after writing the parent's complete local; then it reads that
+// local from L2 and adds its translation to its own M2L local. A chunk never
+// spans two levels, so no lane waits for a lane of its own warp; every parent
+// lies in an earlier chunk, taken by a warp already running, so the earliest
+// unfinished chunk can always finish. Levels beyond the tree's depth cost
+// nothing and there is no barrier per level.
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_l2l_level(int level, const DevCounters *__restrict__ ctr,
-                                                   const int *__restrict__ parent, const vec4<T> *__restrict__ nc,
-                                                   const T *__restrict__ Lm2l, T *__restrict__ L, int ncp)
+__global__ __launch_bounds__(256) void k_l2l_flags(DevCounters *ctr, const int *__restrict__ parent,
+                                                   const vec4<T> *__restrict__ nc, const T *__restrict__ Lm2l,
+                                                   T *L, int ncp, unsigned *flag, unsigned seq)
 {
     constexpr int NC = Exp<P>::NC;
+    __shared__ int s_off[kMaxLevel + 2];
     const int n = phase2_nodes(ctr);
-    if (n == 0 || level > ctr->depth) return;
-    const int lo = ctr->level_off[level], hi = min(ctr->level_off[level + 1], n);
-    for (int a = lo + blockIdx.x * blockDim.x + threadIdx.x; a < hi; a += gridDim.x * blockDim.x) {
+    if (n == 0) return;
+    const int depth = ctr->depth;
+    for (int l = threadIdx.x; l <= depth + 1; l += blockDim.x) s_off[l] = min(ctr->level_off[l], n);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[2], 1);
+        t = __shfl_sync(kFull, t, 0);
+        int level = -1, lo = 0, hi = 0;
+        for (int l = 0; l <= depth; ++l) {  // chunk t -> (level, node range)
+            const int nch = (s_off[l + 1] - s_off[l] + 31) >> 5;
+            if (t < nch) {
+                level = l;
+                lo = s_off[l] + 32 * t;
+                hi = min(s_off[l + 1], lo + 32);
+                break;
+            }
+            t -= nch;
+        }
+        if (level < 0) break;
+        const int a = lo + lane;
+        if (a >= hi) continue;
         T out[NC];
         const T *own = Lm2l + (size_t)a * ncp;
 #pragma unroll
         for (int k = 0; k < NC; ++k) out[k] = own[k];
         if (level > 0) {
             const int par = parent[a];
+            cuda::atomic_ref<unsigned, cuda::thread_scope_device> f(flag[par]);
+            unsigned spins = 0;
+            while (f.load(cuda::memory_order_acquire) != seq) {
+                if (++spins > kSpinLimit) {
+                    set_error(ctr, ERR_SPIN);
+                    break;
+                }
+                __nanosleep(32);
+            }
             T lp[NC];
             const T *pr = L + (size_t)par * ncp;
 #pragma unroll
-            for (int k = 0; k < NC; ++k) lp[k] = pr[k];
+            for (int k = 0; k < NC; ++k) lp[k] = ld_cg(pr + k);
             const vec4<T> c = nc[a], cp = nc[par];
             Exp<P>::template l2l<T>(lp, c.x - cp.x, c.y - cp.y, c.z - cp.z, out);
         }
         T *dst = L + (size_t)a * ncp;
 #pragma unroll
         for (int k = 0; k < NC; ++k) dst[k] = out[k];
+        cuda::atomic_ref<unsigned, cuda::thread_scope_device>(flag[a]).store(seq, cuda::memory_order_release);
     }
 }
 
 template <class T, int P>
 int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 {
-    (void)depth;
-    if constexpr (sizeof(T) == 4) {
-        for (int level = 0; level <= kMaxLevel; ++level)
-            k_l2l_level<T, P><<<P_.num_sms * 4, 256, 0, s>>>(level, P_.ctr, P_.node_parent, (const vec4<T> *)P_.node_c,
-                                                             (const T *)P_.Lm2l, (T *)P_.L, P_.ncp);
-        return kMaxLevel + 1;
+    (void)depth;  // read on the device
+    if (++P_.l2l_seq > 0x7fffffffu) {  // evaluation numbers wrapped: clear the flags and restart at 1
+        cudaMemsetAsync(P_.l2l_flag, 0, (size_t)P_.cap_nodes * sizeof(unsigned), s);
+        P_.l2l_seq = 1;
     }
-    static const int occ = [] {
-        int b = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_l2l_all<T, P>, 256, 0);
-        return b;
-    }();
-    const int blocks = std::min(2048, P_.num_sms * std::max(1, std::min(4, occ)));
-    GridBarrier *gb = P_.gbar + 2;
-    const vec4<T> *nc = (const vec4<T> *)P_.node_c;
-    const T *lm = (const T *)P_.Lm2l;
-    T *l = (T *)P_.L;
-    int ncp = P_.ncp;
-    void *args[] = {&gb, &P_.ctr, &P_.node_parent, (void *)&nc, (void *)&lm, (void *)&l, &ncp};
-    cudaLaunchCooperativeKernel((const void *)k_l2l_all<T, P>, dim3(blocks), dim3(256), args, 0, s);
+    k_l2l_flags<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, P_.node_parent, (const vec4<T> *)P_.node_c,
+                                                     (const T *)P_.Lm2l, (T *)P_.L, P_.ncp, P_.l2l_flag,
+                                                     P_.l2l_seq);
     return 1;
 }
 
