@@ -97,8 +97,8 @@ void free_nodes(Plan &P)
     P.p2p_items = nullptr;
     dfree(P.p2p_nch);
     P.p2p_nch = nullptr;
-    dfree(P.l2l_flag);
-    P.l2l_flag = nullptr;
+    dfree(P.node_flag);
+    P.node_flag = nullptr;
 }
 
 void free_lists(Plan &P)
@@ -131,9 +131,9 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
     CUDA_TRY(dalloc(P.p2p_items, 2 * c));
     CUDA_TRY(dalloc(P.p2p_done, c));
     CUDA_TRY(dalloc(P.p2p_nch, c));
-    CUDA_TRY(dalloc(P.l2l_flag, c));
-    CUDA_TRY(cudaMemset(P.l2l_flag, 0, c * sizeof(unsigned)));
-    P.l2l_seq = 0;
+    CUDA_TRY(dalloc(P.node_flag, c));
+    CUDA_TRY(cudaMemset(P.node_flag, 0, c * sizeof(unsigned)));
+    P.flag_seq = 0;
     CUDA_TRY(dalloc(P.order_key, 2 * c));
     CUDA_TRY(cudaMalloc(&P.node_lo, 3 * c * e));
     CUDA_TRY(cudaMalloc(&P.node_hi, 3 * c * e));
@@ -323,6 +323,18 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
 }
 
 }  // namespace
+
+// Node flags (upward pass, L2L) hold the number of the pass that completed the
+// node; each pass waits for its own number, so flags left by earlier passes
+// need no clearing until the numbers wrap.
+unsigned bfm::Plan::next_flag_seq(cudaStream_t s)
+{
+    if (++flag_seq > 0x7fffffffu) {
+        cudaMemsetAsync(node_flag, 0, (size_t)cap_nodes * sizeof(unsigned), s);
+        flag_seq = 1;
+    }
+    return flag_seq;
+}
 
 unsigned bfm::Plan::next_epoch()
 {

@@ -443,8 +443,8 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
 
 // L2L in one launch, without grid barriers: warps take chunks of up to 32
 // nodes of one level from a shared counter, in level order (root first). A
-// node's thread waits, bounded, until its parent's flag holds this
-// evaluation's number, which the parent's thread stores with release
+// node's thread waits, bounded, until its parent's flag holds this pass's
+// number, which the parent's thread stores with release
 // semantics after writing the parent's complete local; then it reads that
 // local from L2 and adds its translation to its own M2L local. A chunk never
 // spans two levels, so no lane waits for a lane of its own warp; every parent
@@ -515,13 +515,9 @@ template <class T, int P>
 int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 {
     (void)depth;  // read on the device
-    if (++P_.l2l_seq > 0x7fffffffu) {  // evaluation numbers wrapped: clear the flags and restart at 1
-        cudaMemsetAsync(P_.l2l_flag, 0, (size_t)P_.cap_nodes * sizeof(unsigned), s);
-        P_.l2l_seq = 1;
-    }
+    const unsigned seq = P_.next_flag_seq(s);
     k_l2l_flags<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, P_.node_parent, (const vec4<T> *)P_.node_c,
-                                                     (const T *)P_.Lm2l, (T *)P_.L, P_.ncp, P_.l2l_flag,
-                                                     P_.l2l_seq);
+                                                     (const T *)P_.Lm2l, (T *)P_.L, P_.ncp, P_.node_flag, seq);
     return 1;
 }
 

@@ -7,12 +7,11 @@
 // c = (lo + hi) / 2 of the node's tight box; l = (hi - lo) / 2 is the per-axis
 // half-width of the opening criterion.
 //
-// fp32 plans: one cooperative launch: first every leaf (a warp each: box, then P2M with a
-// fixed butterfly reduction over the lanes), then the internal nodes level by
-// level from the deepest up, a grid barrier before each level. A warp takes
-// four parents at a time, a lane per child (at most 8): the parent's box is
-// the union of the children's boxes and its moments the sum of the children's
-// M2M translations, reduced in a fixed order over the 8-lane group.
+// fp32 plans: one launch, deepest level first, a node's eight lanes waiting on
+// its children's flags (k_upward_flags): a leaf's box and P2M from its
+// particles, an internal node's box the union of its children's boxes and its
+// moments the sum of their M2M translations, both reduced in a fixed order
+// over the 8-lane group. fp64 plans: k_upward_ticket, below.
 #include "dfloat.cuh"
 #include "expansions_gen.cuh"
 #include "plan.h"
@@ -48,84 +47,109 @@ __device__ __forceinline__ void store_geometry(int a, const T lo[3], const T hi[
 
 template <int NC> struct Padded { static constexpr int value = (NC + 7) / 8 * 8; };
 
+// fp32 plans' upward pass in one launch, without grid barriers: warps take
+// chunks of four nodes of one level from a shared counter, deepest level
+// first, eight lanes per node. A leaf's group bounds and expands its own
+// particles (P2M); an internal node's group waits, bounded, until each child's
+// flag holds this pass's number (stored with release semantics once the
+// child's box and moments are written), then unites the children's boxes and
+// sums their M2M translations. Both kinds meet in the same fixed-order 8-lane
+// reductions, so no lane waits inside a shuffle. A chunk never spans two
+// levels, so no lane waits for its own warp; every child lies in an earlier
+// chunk, taken by a running warp, so the earliest unfinished chunk can always
+// finish.
 template <class T, int P>
-__global__ __launch_bounds__(256) void k_upward_all(GridBarrier *gb, DevCounters *ctr, const vec4<T> *__restrict__ xyzm,
-                                                    const int *__restrict__ first, const int *__restrict__ count,
-                                                    const int *__restrict__ child0, const int *__restrict__ nchild,
-                                                    T *node_lo, T *node_hi, vec4<T> *nc, vec4<T> *nl, T *M, int ncp)
+__global__ __launch_bounds__(256) void k_upward_flags(DevCounters *ctr, const vec4<T> *__restrict__ xyzm,
+                                                      const int *__restrict__ first, const int *__restrict__ count,
+                                                      const int *__restrict__ child0, const int *__restrict__ nchild,
+                                                      T *node_lo, T *node_hi, vec4<T> *nc, vec4<T> *nl, T *M, int ncp,
+                                                      unsigned *flag, unsigned seq)
 {
     constexpr int NC = Exp<P>::NC;
     constexpr int NR = Padded<NC>::value;
+    __shared__ int s_off[kMaxLevel + 2];
     const int n_nodes = phase2_nodes(ctr);
     if (n_nodes == 0) return;
     const int depth = ctr->depth;
-    const int lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    for (int a = wid; a < n_nodes; a += nwarps) {
-        if (nchild[a] != 0) continue;
-        // ---- leaf: box, centre, P2M
-        const int f = first[a], c = count[a];
+    for (int l = threadIdx.x; l <= depth + 1; l += blockDim.x) s_off[l] = min(ctr->level_off[l], n_nodes);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, g = lane >> 3, j = lane & 7;
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[3], 1);
+        t = __shfl_sync(kFull, t, 0);
+        int lo_n = 0, hi_n = -1;
+        for (int l = depth; l >= 0; --l) {  // chunk t -> four nodes of one level, deepest level first
+            const int nch = (s_off[l + 1] - s_off[l] + 3) >> 2;
+            if (t < nch) {
+                lo_n = s_off[l] + 4 * t;
+                hi_n = min(s_off[l + 1], lo_n + 4);
+                break;
+            }
+            t -= nch;
+        }
+        if (hi_n < 0) break;
+        const int a = lo_n + g;
+        const bool valid = a < hi_n;
+        const int nch = valid ? nchild[a] : 0;
+        const bool leaf = valid && nch == 0;
+        const int f = leaf ? first[a] : 0, c = leaf ? count[a] : 0;
+        const bool has = j < nch;
+        const int ch = has ? child0[a] + j : 0;
         T lo[3], hi[3], cen[3];
         for (int k = 0; k < 3; ++k) { lo[k] = pos_inf<T>(); hi[k] = -pos_inf<T>(); }
-        for (int i = f + lane; i < f + c; i += 32) {
-            vec4<T> q = xyzm[i];
-            lo[0] = tmin(lo[0], q.x); hi[0] = tmax(hi[0], q.x);
-            lo[1] = tmin(lo[1], q.y); hi[1] = tmax(hi[1], q.y);
-            lo[2] = tmin(lo[2], q.z); hi[2] = tmax(hi[2], q.z);
+        if (leaf) {
+            for (int i = f + j; i < f + c; i += 8) {
+                const vec4<T> q = xyzm[i];
+                lo[0] = tmin(lo[0], q.x); hi[0] = tmax(hi[0], q.x);
+                lo[1] = tmin(lo[1], q.y); hi[1] = tmax(hi[1], q.y);
+                lo[2] = tmin(lo[2], q.z); hi[2] = tmax(hi[2], q.z);
+            }
+        } else if (has) {
+            cuda::atomic_ref<unsigned, cuda::thread_scope_device> fl(flag[ch]);
+            unsigned spins = 0;
+            while (fl.load(cuda::memory_order_acquire) != seq) {
+                if (++spins > kSpinLimit) {
+                    set_error(ctr, ERR_SPIN);
+                    break;
+                }
+                __nanosleep(32);
+            }
+            for (int k = 0; k < 3; ++k) {
+                lo[k] = ld_cg(node_lo + 3 * ch + k);
+                hi[k] = ld_cg(node_hi + 3 * ch + k);
+            }
         }
-        for (int o = 16; o > 0; o >>= 1)
+        for (int o = 4; o > 0; o >>= 1)
             for (int k = 0; k < 3; ++k) {
                 lo[k] = tmin(lo[k], __shfl_xor_sync(kFull, lo[k], o));
                 hi[k] = tmax(hi[k], __shfl_xor_sync(kFull, hi[k], o));
             }
-        store_geometry<T>(a, lo, hi, node_lo, node_hi, nc, nl, cen, lane == 0);
+        store_geometry<T>(a, lo, hi, node_lo, node_hi, nc, nl, cen, valid && j == 0);
         T m[NR];
 #pragma unroll
         for (int k = 0; k < NR; ++k) m[k] = T(0);
-        for (int i = f + lane; i < f + c; i += 32) {
-            vec4<T> q = xyzm[i];
-            Exp<P>::template p2m<T>(q.x - cen[0], q.y - cen[1], q.z - cen[2], q.w, m);
-        }
-        reduce_store<T, NR, NC>(m, lane, M + (size_t)a * ncp);
-    }
-    // ---- internal nodes, deepest level first; the children's data was written by other
-    // blocks before the barrier and is read through L2
-    const int g = lane >> 3, j = lane & 7;
-    for (int level = depth - 1; level >= 0; --level) {
-        if (!grid_barrier(gb, (unsigned)(depth - 1 - level), ctr)) return;
-        const int lo_l = ctr->level_off[level], hi_l = min(ctr->level_off[level + 1], n_nodes);
-        for (int p0 = lo_l + 4 * wid; p0 < hi_l; p0 += 4 * nwarps) {
-            const int par = p0 + g;
-            const int nch = par < hi_l ? nchild[par] : 0;
-            const bool has = j < nch;
-            const int ch = has ? child0[par] + j : 0;
-            T lo[3], hi[3], cen[3];
-            for (int k = 0; k < 3; ++k) {
-                lo[k] = has ? ld_cg(node_lo + 3 * ch + k) : pos_inf<T>();
-                hi[k] = has ? ld_cg(node_hi + 3 * ch + k) : -pos_inf<T>();
+        if (leaf) {
+            for (int i = f + j; i < f + c; i += 8) {
+                const vec4<T> q = xyzm[i];
+                Exp<P>::template p2m<T>(q.x - cen[0], q.y - cen[1], q.z - cen[2], q.w, m);
             }
-            for (int o = 4; o > 0; o >>= 1)
-                for (int k = 0; k < 3; ++k) {
-                    lo[k] = tmin(lo[k], __shfl_xor_sync(kFull, lo[k], o));
-                    hi[k] = tmax(hi[k], __shfl_xor_sync(kFull, hi[k], o));
-                }
-            store_geometry<T>(par, lo, hi, node_lo, node_hi, nc, nl, cen, j == 0 && nch > 0);
-            T m[NR];
+        } else if (has) {
+            T mc[NC];
 #pragma unroll
-            for (int k = 0; k < NR; ++k) m[k] = T(0);
-            if (has) {
-                T mc[NC];
-#pragma unroll
-                for (int k = 0; k < NC; ++k) mc[k] = ld_cg(M + (size_t)ch * ncp + k);
-                const vec4<T> cc = ld_cg(nc + ch);
-                Exp<P>::template m2m<T>(mc, cc.x - cen[0], cc.y - cen[1], cc.z - cen[2], m);
-            }
-            T *dst = M + (size_t)par * ncp;
-            reduce_apply8<T, NR, NC>(m, j, [&](int k, const T &x) {
-                if (nch > 0) dst[k] = x;
-            });
+            for (int k = 0; k < NC; ++k) mc[k] = ld_cg(M + (size_t)ch * ncp + k);
+            const vec4<T> cc = ld_cg(nc + ch);
+            Exp<P>::template m2m<T>(mc, cc.x - cen[0], cc.y - cen[1], cc.z - cen[2], m);
         }
+        T *dst = M + (size_t)a * ncp;
+        reduce_apply8<T, NR, NC>(m, j, [&](int k, const T &x) {
+            if (valid) dst[k] = x;
+        });
+        // publish the group's box and moments, then the node's flag
+        __threadfence();
+        __syncwarp();
+        if (valid && j == 0)
+            cuda::atomic_ref<unsigned, cuda::thread_scope_device>(flag[a]).store(seq, cuda::memory_order_release);
     }
 }
 
@@ -252,20 +276,11 @@ int launch_upward_tp(Plan &P_, cudaStream_t s)
             (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp);
         return 1;
     } else {
-        static const int occ = [] {
-            int b = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_upward_all<T, P>, 256, 0);
-            return b;
-        }();
-        const int blocks = std::min(2048, P_.num_sms * std::max(1, std::min(8, occ)));
-        GridBarrier *gb = P_.gbar + 3;
-        const vec4<T> *xyzm = (const vec4<T> *)P_.xyzm;
-        T *lo = (T *)P_.node_lo, *hi = (T *)P_.node_hi, *M = (T *)P_.M;
-        vec4<T> *nc = (vec4<T> *)P_.node_c, *nl = (vec4<T> *)P_.node_l;
-        int ncp = P_.ncp;
-        void *args[] = {&gb, &P_.ctr, (void *)&xyzm, &P_.node_first, &P_.node_count, &P_.node_child0, &P_.node_nchild,
-                        (void *)&lo, (void *)&hi, (void *)&nc, (void *)&nl, (void *)&M, &ncp};
-        cudaLaunchCooperativeKernel((const void *)k_upward_all<T, P>, dim3(blocks), dim3(256), args, 0, s);
+        const unsigned seq = P_.next_flag_seq(s);
+        k_upward_flags<T, P><<<P_.num_sms * 4, 256, 0, s>>>(
+            P_.ctr, (const vec4<T> *)P_.xyzm, P_.node_first, P_.node_count, P_.node_child0, P_.node_nchild,
+            (T *)P_.node_lo, (T *)P_.node_hi, (vec4<T> *)P_.node_c, (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp,
+            P_.node_flag, seq);
         return 1;
     }
 }

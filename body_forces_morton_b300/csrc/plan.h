@@ -60,8 +60,8 @@ struct Plan {
     int2 *p2p_items = nullptr;                     // [2 cap_nodes] P2P work items (receiver, chunk | chunks << 8)
     int *p2p_done = nullptr;                       // [cap_nodes] chunks of a receiver applied so far
     uint8_t *p2p_nch = nullptr;                    // [cap_nodes] P2P chunks of every receiver
-    unsigned *l2l_flag = nullptr;                  // [cap_nodes] evaluation number whose complete local is written
-    unsigned l2l_seq = 0;                          // this evaluation's number (never 0 once launched)
+    unsigned *node_flag = nullptr;                 // [cap_nodes] number of the last pass that completed the node
+    unsigned flag_seq = 0;                         // the last pass number handed out (0: none)
     uint8_t *order_key = nullptr;                  // [2][cap_nodes] work bucket of every node
 
     void *scratch = nullptr;       // 64 KiB for small per-block partials
@@ -73,7 +73,7 @@ struct Plan {
 
     // status
     DevCounters *ctr = nullptr;      // device
-    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0], walk [1], upward [3] ([2] unused)
+    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0] and walk [1] ([2], [3] unused)
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
@@ -98,6 +98,7 @@ struct Plan {
     double total_ms = 0;
 
     unsigned next_epoch();
+    unsigned next_flag_seq(cudaStream_t s);  // a fresh, nonzero node_flag value for one pass
     int next_slot() { return slot++; }
 };
 
