@@ -48,6 +48,8 @@ P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r
 TRAFFIC = {
     # k_p2p<float>, clustered N = 2^20: 52.52 MB read + 4.05 MB written (one warm launch, --set full)
     ("clustered_2p20_f32", "f4562b91ce3ab6f9"): 56572672,
+    # same k_p2p code; the file changed in its L2L kernels only
+    ("clustered_2p20_f32", "d5826261d587dbe7"): 56572672,
 }
 
 
