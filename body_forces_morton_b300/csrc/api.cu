@@ -355,7 +355,9 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     if (dtype != FMM_F32 && dtype != FMM_F64) { set_err("fmm_plan_create: unknown dtype"); return nullptr; }
     // Host-side fault injection for tests (no GPU fault is ever provoked):
     //   BFM_FMM_FAULT=alloc     creation fails as if a device allocation had failed;
-    //   BFM_FMM_FAULT=capacity  buffers start minimal, so evaluations exercise the regrowth path.
+    //   BFM_FMM_FAULT=capacity  buffers start minimal, so evaluations exercise the regrowth path;
+    //   BFM_FMM_FAULT=spin      every L2L wait on a parent runs out its bound (a flag value that no
+    //                           pass stores), so evaluations report the expired wait (FMM_ERR_INTERNAL).
     const char *fault = getenv("BFM_FMM_FAULT");
     if (fault && strcmp(fault, "alloc") == 0) {
         set_err("fmm_plan_create: device allocation failed (injected by BFM_FMM_FAULT=alloc)");
@@ -367,6 +369,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     Plan &P = h->P;
     P.n = n; P.p = p; P.theta = theta; P.leaf = leaf; P.dtype = (int)dtype;
     P.minimal_caps = minimal;
+    P.fault_spin = fault && strcmp(fault, "spin") == 0;
     P.esize = dtype == FMM_F32 ? 4 : 8;
     P.nc = (p + 1) * (p + 2) * (p + 3) / 6;
     P.ncp = (P.nc + 3) / 4 * 4;

@@ -444,7 +444,8 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
 // L2L in one launch, without grid barriers: warps take chunks of up to 32
 // nodes of one level from a shared counter, in level order (root first). A
 // node's thread waits, bounded, until its parent's flag holds this pass's
-// number, which the parent's thread stores with release
+// number (`want`, equal to `seq` unless a test injects an expired wait), which
+// the parent's thread stores with release
 // semantics after writing the parent's complete local; then it reads that
 // local from L2 and adds its translation to its own M2L local. A chunk never
 // spans two levels, so no lane waits for a lane of its own warp; every parent
@@ -454,7 +455,7 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
 template <class T, int P>
 __global__ __launch_bounds__(256) void k_l2l_flags(DevCounters *ctr, const int *__restrict__ parent,
                                                    const vec4<T> *__restrict__ nc, const T *__restrict__ Lm2l,
-                                                   T *L, int ncp, unsigned *flag, unsigned seq)
+                                                   T *L, int ncp, unsigned *flag, unsigned seq, unsigned want)
 {
     constexpr int NC = Exp<P>::NC;
     __shared__ int s_off[kMaxLevel + 2];
@@ -490,7 +491,7 @@ __global__ __launch_bounds__(256) void k_l2l_flags(DevCounters *ctr, const int *
             const int par = parent[a];
             cuda::atomic_ref<unsigned, cuda::thread_scope_device> f(flag[par]);
             unsigned spins = 0;
-            while (f.load(cuda::memory_order_acquire) != seq) {
+            while (f.load(cuda::memory_order_acquire) != want) {
                 if (++spins > kSpinLimit) {
                     set_error(ctr, ERR_SPIN);
                     break;
@@ -516,8 +517,12 @@ int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 {
     (void)depth;  // read on the device
     const unsigned seq = P_.next_flag_seq(s);
+    // a parent is complete when its flag holds seq; the injected fault waits for a value no pass stores
+    // (pass numbers stay below 2^31)
+    const unsigned want = P_.fault_spin ? (seq | 0x80000000u) : seq;
     k_l2l_flags<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, P_.node_parent, (const vec4<T> *)P_.node_c,
-                                                     (const T *)P_.Lm2l, (T *)P_.L, P_.ncp, P_.node_flag, seq);
+                                                     (const T *)P_.Lm2l, (T *)P_.L, P_.ncp, P_.node_flag, seq,
+                                                     want);
     return 1;
 }
 
