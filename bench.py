@@ -50,6 +50,7 @@ TRAFFIC = {
     ("clustered_2p20_f32", "f4562b91ce3ab6f9"): 56572672,
     # same k_p2p code; the file changed in its L2L kernels only
     ("clustered_2p20_f32", "d5826261d587dbe7"): 56572672,
+    ("clustered_2p20_f32", "e6ea43d35f31e177"): 56572672,
 }
 
 
