@@ -243,7 +243,7 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         // ---- phase 1: box, keys, sort, tree (the tree kernel records the node count and depth)
         record(P, 0, s);
         CUDA_TRY(cudaMemsetAsync(P.ctr, 0, sizeof(DevCounters), s));
-        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 4 * sizeof(GridBarrier), s));
+        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 2 * sizeof(GridBarrier), s));
         P.launches += launch_keys(P, pos, s);
         record(P, 1, s);
         P.launches += launch_sort(P, pos, mass, s);
@@ -409,7 +409,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
-        !ok(dalloc(P.gbar, 4), "grid barriers") ||
+        !ok(dalloc(P.gbar, 2), "grid barriers") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);
     for (int i = 0; i < kNumEvents; ++i)

@@ -74,7 +74,7 @@ struct Plan {
 
     // status
     DevCounters *ctr = nullptr;      // device
-    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0] and walk [1] ([2], [3] unused)
+    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0] and walk [1]
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
