@@ -307,7 +307,8 @@ def run_ours(args, rank, world, local_rank):
         also[w3.name] = {"value": r3["n"] / (ms3 / 1e3), "unit": "particles/s", "ms_per_step": ms3,
                          "stage_ms": r3["stage_ms"], "dtype": "f64", "arith": F64_ARITH, "p": w3.p,
                          "theta": w3.theta, "leaf": w3.leaf, "roofline": p2p_roofline(r3, w3),
-                         "m2l_roofline": m2l_roofline(r3, w3)}
+                         "m2l_roofline": m2l_roofline(r3, w3),
+                         "eval_roofline": eval_roofline(r3, w3, ms3, *hbm_peak_gbs())}
         r3["plan"].close()
         w5 = W.WORKLOADS[5]
         also[w5.name] = bench_kdk(w5, max(3, args.steps // 2), args.warmup, torch, native, stream)
@@ -335,6 +336,7 @@ def run_ours(args, rank, world, local_rank):
                                       "walk_pairs")},
         "roofline": roof,
         "m2l_roofline": m2l_roofline(res, w),
+        "eval_roofline": eval_roofline(res, w, ms_per_step, *hbm_peak_gbs()),
         "e2e": e2e,
         "gpu_launches": res["launches"],
         "clocks": clocks,
@@ -372,6 +374,48 @@ def p2p_roofline(res, w):
             else "nominal FP64 1.25 TFLOP/s; the kernel runs double-float on the FP32 pipe",
             "flops_note": f"{P2P_FLOPS_PER_PAIR} flop per particle pair, {pairs} pairs per launch",
             "ms": ms, "traffic": None}
+
+
+def hbm_peak_gbs():
+    """HBM copy bandwidth from MEASURED_PEAKS.json (driver-written), else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError, TypeError):
+        return 6400.0, "fallback"
+
+
+def hbm_bytes_per_particle(wbytes):
+    """Algorithmic bytes per particle of the memory-bound stages (w = element width in bytes)."""
+    return {
+        "keys": 3 * wbytes + 12,    # positions read; 8-byte key and 4-byte index written
+        "sort": 24 * 8,             # 8 passes, each reading and writing key and index (12 + 12 bytes)
+        "gather": 8 * wbytes,       # position and mass read, sorted (x, y, z, m) written
+        "tree": 16,                 # sorted keys read for the node boundaries, node records amortised
+        "p2m": 4 * wbytes,          # sorted particles read once (moments amortised by the leaf size)
+        "l2p": 7 * wbytes,          # particle position read, (phi, a) written
+        "scatter": 8 * wbytes,      # (phi, a) read, caller-order outputs written
+    }
+
+
+def eval_roofline(res, w, ms_eval, hbm_gbs, hbm_source):
+    """Whole-evaluation roofline fraction: the sum over stages of algorithmic work / peak, over
+    the measured evaluation time. P2P and M2L count their flops against the ALU peak of the
+    plan's dtype (for fp64 the nominal FP64 peak, although both run double-float on the FP32
+    pipe); the memory-bound stages count hbm_bytes_per_particle against the HBM copy bandwidth.
+    Stages with no algorithmic work of their own (walk, lists, M2M, L2L) count zero."""
+    n, st = res["n"], res["stats"]
+    f32 = w.dtype == "f32"
+    alu = (FP32_PEAK_TFLOPS if f32 else FP64_PEAK_TFLOPS) * 1e12
+    p2p_ms = P2P_FLOPS_PER_PAIR * (st["n_p2p_interactions"] - n) / alu * 1e3
+    m2l_ms = m2l_flops_per_pair(w.p) * st["n_m2l"] / alu * 1e3
+    per_particle = hbm_bytes_per_particle(4 if f32 else 8)
+    hbm_ms = sum(per_particle.values()) * n / (hbm_gbs * 1e9) * 1e3
+    ideal = p2p_ms + m2l_ms + hbm_ms
+    return {"frac": ideal / ms_eval, "ideal_ms": ideal, "ms": ms_eval,
+            "terms_ms": {"p2p_alu": p2p_ms, "m2l_alu": m2l_ms, "hbm": hbm_ms},
+            "hbm_bytes_per_particle": per_particle,
+            "peaks": {"alu_tflops": alu / 1e12, "hbm_gbs": hbm_gbs, "hbm_source": hbm_source}}
 
 
 def m2l_flops_per_pair(p):
