@@ -143,6 +143,24 @@ def test_near_field_conserves_momentum():
     assert np.linalg.norm(ptot) <= 1e-12 * np.sum(m * np.linalg.norm(r.acc, axis=1))
 
 
+@pytest.mark.parametrize("wi,n", [(1, 4096), (2, 6000), (4, 6000)])
+def test_full_fmm_conserves_momentum(wi, n):
+    """With the total-degree truncation |n| + |k| <= p, the far-field forces of
+    an accepted pair are equal and opposite: summed over A's particles, L2P of
+    A's local gives -sum_k M_k(A) L_{k+e}(A), and D^m(-R) = (-1)^|m| D^m(R)
+    turns B's sum into its negative (the index set is symmetric in n and k).
+    L2L, M2M and P2M are exact polynomial identities, P2P pairs are symmetric,
+    so the whole evaluation conserves momentum to rounding. A dropped parity
+    factor, a transposed M2L operand, a wrong gradient index in L2P or a
+    truncation that is not symmetric breaks it."""
+    g = W.generate(W.WORKLOADS[wi], n=n, dtype="f64")
+    m = g["mass"]
+    for p, theta in ((2, 0.7), (4, 0.5), (5, 0.7)):
+        r = oracle.fmm(g["pos"], m, p, theta, 16)
+        ptot = np.sum(m[:, None] * r.acc, axis=0)
+        assert np.linalg.norm(ptot) <= 1e-14 * np.sum(m * np.linalg.norm(r.acc, axis=1)), (p, theta)
+
+
 def test_eval_mask_matches_full():
     g = W.generate(W.WORKLOADS[2], n=5000)
     full = oracle.fmm(g["pos"], g["mass"], 4, 0.7, 32)
