@@ -2,9 +2,10 @@
 // particles without any device allocation.
 //
 // Some callers cannot allocate device memory at the time they need keys: code
-// running inside a stream capture (an allocation would be captured or fail),
-// code that owns a fixed memory budget handed out by its own allocator, or a
-// real-time loop that must not take the driver's allocation locks. This entry
+// that owns a fixed memory budget handed out by its own allocator, a library
+// embedded in a host application that forbids device allocation after
+// start-up, or a real-time loop that must not take the driver's allocation
+// locks. This entry
 // point gives them the first stage of the FMM pipeline with nothing but the
 // caller's input and output buffers: the reduction's scratch (one partial box
 // per block, a ticket counter, the finished box and a status word) lives in a

@@ -223,9 +223,10 @@ fmm_status fmm_plan_export(const fmm_plan *plan, int what, void *dst, int64_t by
  * counterpart; this is a library convenience).
  *
  * For callers that cannot allocate device memory when they need the keys: code
- * inside a stream capture, code working within a fixed memory budget handed out
- * by its own allocator, or a real-time loop that must not take the driver's
- * allocation locks. It needs no plan: the caller passes pos [n x 3] (device,
+ * working within a fixed memory budget handed out by its own allocator, a
+ * library embedded in a host application that forbids device allocation after
+ * start-up, or a real-time loop that must not take the driver's allocation
+ * locks. It needs no plan: the caller passes pos [n x 3] (device,
  * `dtype` reals) and keys_out [n] (device, uint64, written in the caller's
  * particle order) and optionally box_out [4] (device doubles: the root cube's
  * lower corner x, y, z and its side). The keys are the same as the plan path's

@@ -1,6 +1,8 @@
 """fmm_morton_keys_noalloc, the entry point for callers that cannot allocate
-device memory (inside a stream capture, under their own memory budget, or in
-a loop that must not take the driver's allocation locks).
+device memory: code that owns a fixed device budget handed out by its own
+allocator, a library embedded in a host application that forbids device
+allocation after start-up, or a real-time loop that must not take the
+driver's allocation locks.
 
 Its keys must equal those of the plan path (fmm_eval's sorted keys mapped back
 through the sort permutation), bit for bit, on two calls in a row; the second
