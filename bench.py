@@ -388,7 +388,7 @@ def hbm_peak_gbs():
 def hbm_bytes_per_particle(wbytes):
     """Algorithmic bytes per particle of the memory-bound stages (w = element width in bytes)."""
     return {
-        "keys": 3 * wbytes + 12,    # positions read; 8-byte key and 4-byte index written
+        "keys": 3 * wbytes + 8,     # positions read, 8-byte key written (the first pass makes the index)
         "sort": 24 * 8,             # 8 passes, each reading and writing key and index (12 + 12 bytes)
         "gather": 8 * wbytes,       # position and mass read, sorted (x, y, z, m) written
         "tree": 16,                 # sorted keys read for the node boundaries, node records amortised

@@ -25,8 +25,8 @@ def test_reduced_m2l_flop_count():
 def test_hbm_bytes_per_particle():
     f32 = bench.hbm_bytes_per_particle(4)
     f64 = bench.hbm_bytes_per_particle(8)
-    assert sum(f32.values()) == 340
-    assert sum(f64.values()) == 460
+    assert sum(f32.values()) == 336
+    assert sum(f64.values()) == 456
     assert f32["sort"] == f64["sort"] == 192  # the keys do not depend on the dtype
 
 
@@ -39,7 +39,7 @@ def test_eval_roofline_sums_the_stage_terms():
     assert math.isclose(r["frac"], r["ideal_ms"] / 2.45, rel_tol=1e-12)
     # P2P: 20 flop per pair at 148 x 128 x 2 x 2.032e9 flop/s
     assert math.isclose(t["p2p_alu"], 1_274_776_446 * 20 / (148 * 128 * 2 * 2.032e9) * 1e3, rel_tol=1e-12)
-    assert math.isclose(t["hbm"], 340 * (1 << 20) / 6.5e12 * 1e3, rel_tol=1e-12)
+    assert math.isclose(t["hbm"], 336 * (1 << 20) / 6.5e12 * 1e3, rel_tol=1e-12)
     assert 0.1 < r["frac"] < 0.3
 
 
