@@ -110,8 +110,16 @@ void free_lists(Plan &P)
     P.m2l_src = P.p2p_src = nullptr;
 }
 
+// Node indices are int32 on the device and some node arrays hold two entries
+// per node, so the node capacity stays at or below 2^30.
+constexpr int64_t kMaxNodeCap = int64_t(1) << 30;
+
 fmm_status alloc_nodes(Plan &P, int64_t cap)
 {
+    if (cap > kMaxNodeCap) {
+        set_err("fmm_eval: the tree needs more than 2^30 nodes");
+        return FMM_ERR_CAPACITY;
+    }
     free_nodes(P);
     P.cap_nodes = cap;
     const size_t c = (size_t)cap, e = (size_t)P.esize;
@@ -189,10 +197,13 @@ void destroy_plan(Plan &P)
     if (P.ev_done) cudaEventDestroy(P.ev_done);
 }
 
-int64_t clamp_cap(double v) { return (int64_t)std::min(v, 2.0e9); }
+// Pair capacities stay at or below 1e9 unordered pairs, so the directed list
+// entries (two per pair) index int32 CSR offsets without wrapping; a walk that
+// needs more ends in FMM_ERR_CAPACITY after the retries.
+int64_t clamp_cap(double v) { return (int64_t)std::min(v, 1.0e9); }
 
 // Node-count and list estimates; the evaluation grows them when exceeded.
-int64_t node_estimate(const Plan &P) { return std::max<int64_t>(4096, 6 * P.n / P.leaf + 1024); }
+int64_t node_estimate(const Plan &P) { return std::min(kMaxNodeCap, std::max<int64_t>(4096, 6 * P.n / P.leaf + 1024)); }
 
 void record(Plan &P, int k, cudaStream_t s) { cudaEventRecord(P.ev[k], s); }
 
@@ -278,7 +289,8 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
             return FMM_ERR_NONFINITE;
         }
         if (h.error & ERR_NODES) {
-            st = alloc_nodes(P, 2 * P.cap_nodes);
+            // double, up to the cap; a full-size tree that still overflows reports FMM_ERR_CAPACITY
+            st = alloc_nodes(P, P.cap_nodes >= kMaxNodeCap ? 2 * P.cap_nodes : std::min(2 * P.cap_nodes, kMaxNodeCap));
             if (st) return st;
             P.retries++;
             continue;

@@ -68,7 +68,7 @@ typedef enum {
     FMM_ERR_INVALID_ARG = 1, /* bad size, order, angle, leaf size, pointer or dtype */
     FMM_ERR_OOM = 2,         /* device or host allocation failed */
     FMM_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the CUDA error) */
-    FMM_ERR_CAPACITY = 4,    /* interaction lists still overflow after the retries */
+    FMM_ERR_CAPACITY = 4,    /* lists still overflow after the retries, or over 2^30 nodes / 1e9 pairs */
     FMM_ERR_NONFINITE = 5,   /* a position is NaN or infinite */
     FMM_ERR_INTERNAL = 6     /* a device-side consistency check failed */
 } fmm_status;
