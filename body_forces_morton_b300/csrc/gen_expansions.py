@@ -23,6 +23,8 @@ identity (their truncated sums obey it term by term). ``m2l_r`` contracts
 reduced moments into reduced locals ((p+1)^2 each; 155 instead of 210 terms at
 p = 4) and needs D^m only for m_z <= 2, the m_z = 2 ones from the identity;
 ``reduce_m`` and ``expand_l`` convert from and to the full coefficients.
+``m2l_r_pair`` is both directions of one pair from one derivative tensor (for
+a mutual FMM): D^m(-R) = (-1)^{|m|} D^m(R) gives the reverse contraction.
 
 It also writes ``expansions_df_gen.cuh``: ``ExpDF<P>::m2l_r`` for P <= 4, the
 reduced M2L with every value a double-float (dfloat.cuh): the derivative
@@ -249,9 +251,46 @@ def reduced_derivs(p):
 
 def gen_m2l_r(p):
     red, rmap = reduced_table(p)
+    b = ["template <class T> static __device__ __forceinline__ void m2l_r(const T* M, T rx, T ry, T rz, T* L) {"]
+    b += reduced_derivs_body(p)
+    b += reduced_contraction(p, "M", "L", 0)
+    b.append("}")
+    return b
+
+
+def gen_m2l_r_pair(p):
+    """Both directions of one M2L pair from one derivative tensor (mutual FMM):
+    LA from MB with R = c_A - c_B as in m2l_r, and LB from MA with -R, using
+    D^m(-R) = (-1)^{|m|} D^m(R): LB_k += -(-1)^{|k|} sum_n MA_n D^{n+k}(R)."""
+    b = ["template <class T> static __device__ __forceinline__ void m2l_r_pair(const T* MA, const T* MB, T rx, T ry, "
+         "T rz, T* LA, T* LB) {"]
+    b += reduced_derivs_body(p)
+    b += reduced_contraction(p, "MB", "LA", 0)
+    b += reduced_contraction(p, "MA", "LB", 1)
+    b.append("}")
+    return b
+
+
+def reduced_contraction(p, m_name, l_name, mirrored):
+    """Contraction lines L_k += -sum (-1)^{|n|} M_n D^{n+k}; mirrored: the sign (-1)^{|k|} instead."""
+    red, rmap = reduced_table(p)
     mi, slot = reduced_derivs(p)
-    b = ["template <class T> static __device__ __forceinline__ void m2l_r(const T* M, T rx, T ry, T rz, T* L) {",
-         f"  T D[{len(mi)}];",
+    b = []
+    for k in red:
+        for n in red:
+            if sum(n) + sum(k) > p:
+                continue
+            m = (n[0] + k[0], n[1] + k[1], n[2] + k[2])
+            odd = (sum(k) if mirrored else sum(n)) % 2 == 1
+            op = "+=" if odd else "-="
+            b.append(f"  {l_name}[{rmap[k]}] {op} {m_name}[{rmap[n]}] * D[{slot[m]}];")
+    return b
+
+
+def reduced_derivs_body(p):
+    """Lines building D[] (the reduced derivative tensor of 1/r at (rx, ry, rz))."""
+    mi, slot = reduced_derivs(p)
+    b = [f"  T D[{len(mi)}];",
          "  const T r2 = rx * rx + ry * ry + rz * rz;",
          f"  D[{slot[(0, 0, 0)]}] = rsqrt_t(r2);"]
     if p > 0:
@@ -285,14 +324,6 @@ def gen_m2l_r(p):
         if n[2] == 2:
             a_, b_ = (n[0] + 2, n[1], 0), (n[0], n[1] + 2, 0)
             b.append(f"  D[{slot[n]}] = -(D[{slot[a_]}] + D[{slot[b_]}]);")
-    for k in red:
-        for n in red:
-            if sum(n) + sum(k) > p:
-                continue
-            m = (n[0] + k[0], n[1] + k[1], n[2] + k[2])
-            op = "+=" if sum(n) % 2 == 1 else "-="
-            b.append(f"  L[{rmap[k]}] {op} M[{rmap[n]}] * D[{slot[m]}];")
-    b.append("}")
     return b
 
 
@@ -462,7 +493,8 @@ def main():
         out.append(f"template <> struct Exp<{p}> {{")
         out.append(f"  static constexpr int NC = {ncoef(p)};")
         out.append(f"  static constexpr int NRC = {(p + 1) ** 2};  // reduced (n_z <= 1) coefficients")
-        for gen in (gen_p2m, gen_m2m, gen_m2l, gen_l2l, gen_l2p, gen_reduce_m, gen_expand_l, gen_m2l_r):
+        for gen in (gen_p2m, gen_m2m, gen_m2l, gen_l2l, gen_l2p, gen_reduce_m, gen_expand_l, gen_m2l_r,
+                    gen_m2l_r_pair):
             out += ["  " + l for l in gen(p)]
         out.append("};")
         out.append("")

@@ -30,6 +30,17 @@ static void run(int op, const T* a, const T* v, T* out)
         Exp<P>::template expand_l<T>(Lr, out);
         break;
     }
+    case 6: {  // both directions of one pair: a = [M_A, M_B], out = [L_A, L_B]
+        constexpr int NC = Exp<P>::NC, NRC = Exp<P>::NRC;
+        T MA[NRC], MB[NRC], LA[NRC], LB[NRC];
+        for (int i = 0; i < NRC; ++i) LA[i] = LB[i] = T(0);
+        Exp<P>::template reduce_m<T>(a, MA);
+        Exp<P>::template reduce_m<T>(a + NC, MB);
+        Exp<P>::template m2l_r_pair<T>(MA, MB, v[0], v[1], v[2], LA, LB);
+        Exp<P>::template expand_l<T>(LA, out);
+        Exp<P>::template expand_l<T>(LB, out + NC);
+        break;
+    }
     }
 }
 

@@ -60,6 +60,12 @@ def test_generated_operators_match_oracle(shim, p, dtype, rtol):
     got = call(shim, p, 5, M, R, nc, dtype)
     want = oracle.m2l(p, M, R)
     np.testing.assert_allclose(got, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg="reduced m2l")
+    # both directions of one pair from one derivative tensor (mutual M2L): L_A from M_B at R and
+    # L_B from M_A at -R, each against the oracle's one-directional M2L
+    MA = rng.normal(size=nc)
+    got = call(shim, p, 6, np.concatenate([MA, M]), R, 2 * nc, dtype)
+    for half, want in ((got[:nc], oracle.m2l(p, M, R)), (got[nc:], oracle.m2l(p, MA, -R))):
+        np.testing.assert_allclose(half, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg="pair m2l")
     # L2P
     dx = rng.normal(size=3) * 0.1
     got = call(shim, p, 4, M, dx, 4, dtype)
