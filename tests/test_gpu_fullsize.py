@@ -7,7 +7,9 @@ benchmark times.
   as theta shrinks);
 * config 4 (clustered, N = 2^20, fp32) and config 5 (clustered, N = 2^22,
   fp32, p 3, theta 0.6): tree and lists bit-exact, accelerations of a seeded
-  sample of particles against the oracle evaluated on that sample only.
+  sample of particles against the oracle evaluated on that sample only;
+* every configuration: total momentum conserved over all N particles (a
+  property of the method that holds at any size), within the parity gate.
 """
 import numpy as np
 import pytest
@@ -17,6 +19,20 @@ from body_forces_morton_b300 import workloads as W
 from gpu_helpers import ALL_STRUCT, TOL_ACC, accel_error, assert_structure_equal, gpu_eval, pot_error
 
 pytestmark = pytest.mark.gpu
+
+
+def momentum_imbalance(mass, acc):
+    """|sum_i m_i a_i| / sum_i m_i |a_i| over every particle, in fp64.
+
+    The FMM on these trees conserves momentum to rounding (total-degree
+    truncation: each accepted pair's far-field forces are equal and opposite;
+    the oracle is pinned at 1e-14). The GPU result differs from it by at most
+    its per-particle relative error, so the imbalance is bounded by that error
+    weighted by m |a|; the gates below are the parity gates, now over all N
+    particles instead of a sample."""
+    m = np.asarray(mass, np.float64)
+    a = np.asarray(acc, np.float64)
+    return np.linalg.norm((m[:, None] * a).sum(axis=0)) / np.sum(m * np.linalg.norm(a, axis=1))
 
 
 def sampled_parity(w, n_sample=3000):
@@ -29,9 +45,12 @@ def sampled_parity(w, n_sample=3000):
     r = oracle.fmm(g["pos"], g["mass"], w.p, w.theta, w.leaf, eval_mask=mask)
     e = accel_error(acc[mask].astype(np.float64), r.acc[mask])
     ep = pot_error(pot[mask].astype(np.float64), r.pot[mask])
+    dp = momentum_imbalance(g["mass"], acc)
     print(f"{w.name}: sampled acc error max {e.max():.2e} p99 {np.percentile(e, 99):.2e}, pot {ep.max():.2e}; "
+          f"momentum imbalance {dp:.2e}; "
           f"nodes {st['n_nodes']} depth {st['depth']} m2l {st['n_m2l']} p2p pairs {st['n_p2p_interactions']}")
     assert e.max() <= TOL_ACC[w.dtype] and ep.max() <= TOL_ACC[w.dtype]
+    assert dp <= TOL_ACC[w.dtype]
 
 
 def test_config3_full_parity_fp64():
@@ -42,8 +61,10 @@ def test_config3_full_parity_fp64():
     assert_structure_equal(ex, r)
     e = accel_error(acc, r.acc)
     ep = pot_error(pot, r.pot)
-    print(f"config 3 full: acc error max {e.max():.2e}, pot {ep.max():.2e}")
+    dp = momentum_imbalance(g["mass"], acc)
+    print(f"config 3 full: acc error max {e.max():.2e}, pot {ep.max():.2e}, momentum imbalance {dp:.2e}")
     assert e.max() <= 1e-10 and ep.max() <= 1e-10
+    assert dp <= 1e-10
 
 
 def test_config3_sweep_against_direct_sum():
