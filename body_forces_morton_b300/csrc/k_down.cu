@@ -229,7 +229,7 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
                                           int *done, DevCounters *ctr,
                                           const int *__restrict__ first, const int *__restrict__ count,
                                           const vec4<T> *__restrict__ xyzm, const uint32_t *__restrict__ perm,
-                                          const vec4<T> *__restrict__ far, vec4<T> *far_w,
+                                          const vec4<T> *far, vec4<T> *far_w,
                                           const int *__restrict__ src,
                                           T *__restrict__ acc_out, T *__restrict__ pot_out, vec4<T> *buf,
                                           T (*red)[4], int lane)
@@ -342,7 +342,9 @@ __device__ __forceinline__ void p2p_round(int a, int f, int c, int r0, int cr, i
 #pragma unroll
                 for (int v = 0; v < 4; ++v) t[v] += red[qs * R + rp][v];
             const int i = f + r0 + rr;
-            // the far field, plus the partial sums of the earlier chunks (written by other warps)
+            // the far field, plus the partial sums of the earlier chunks (written by other warps through
+            // far_w, which aliases far: hence no __restrict__ on either, and a coherent L2 load here, never
+            // the non-coherent read-only path)
             const vec4<T> fa = CHUNKED ? ld_cg(far + i) : far[i];
             if (CHUNKED && chunk < nch - 1) {
                 far_w[i] = make4<T>(fa.x + t[0], fa.y + t[1], fa.z + t[2], fa.w + t[3]);
@@ -364,7 +366,7 @@ template <class T, bool CHUNKED>
 __device__ __forceinline__ void p2p_item(int a, int chunk, int nch, int *done, DevCounters *ctr,
                                          const int *__restrict__ first, const int *__restrict__ count,
                                          const vec4<T> *__restrict__ xyzm, const uint32_t *__restrict__ perm,
-                                         const vec4<T> *__restrict__ far, vec4<T> *far_w,
+                                         const vec4<T> *far, vec4<T> *far_w,
                                          const int *__restrict__ off, const int *__restrict__ src,
                                          T *__restrict__ acc_out, T *__restrict__ pot_out, vec4<T> *buf,
                                          T (*red)[4], int lane)
@@ -414,7 +416,7 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
                                                        const int *__restrict__ nchild,
                                                        const vec4<T> *__restrict__ xyzm,
                                                        const uint32_t *__restrict__ perm,
-                                                       const vec4<T> *__restrict__ far, vec4<T> *far_w,
+                                                       const vec4<T> *far, vec4<T> *far_w,
                                                        const int *__restrict__ off,
                                                        const int *__restrict__ src, T *__restrict__ acc_out,
                                                        T *__restrict__ pot_out)

@@ -4,9 +4,11 @@ This module only draws inputs (positions, masses, velocities). It holds none of
 the FMM arithmetic, so both the CUDA path and the CPU oracle can take their
 inputs from here without sharing any method code.
 
-The five workloads follow the configurations the JZ-FMM page evaluates the
-method on (uniform cube, Plummer spheres, clustered box, KDK run). All draws
-use ``numpy.random.default_rng(seed)`` and are fully reproducible.
+The five workloads are this library's benchmark configurations (uniform
+cube, Plummer spheres, clustered box, KDK run). The pages evaluate none of
+them; the jaccpot issue's far-field timings (N = 1e4 and 1e5, theta = 0.7,
+order 4, leaf 32) are the context the Plummer sizes echo. All draws use
+``numpy.random.default_rng(seed)`` and are fully reproducible.
 
 Recipes (all lengths in the same units, G = 1, total mass 1):
 

@@ -33,9 +33,10 @@
  *    N entries. Outputs come back in the caller's particle order.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). All GPU work is enqueued on it. The calls are blocking: they
- *    return once the results are complete and checked (they synchronise the
- *    stream twice: once after the tree build to size the launches, once at the
- *    end to read the device-side status word).
+ *    return once the results are complete and checked. Every kernel reads the
+ *    tree's size from device memory, so the stream is synchronised once per
+ *    evaluation, at the end, to read back the device-side status word (an
+ *    evaluation that overflowed a buffer is then repeated with grown buffers).
  *  - A plan is not thread-safe: one call in flight per plan.
  *  - Errors are returned as status codes, never as a process abort; the reason
  *    is available from fmm_last_error() on the calling thread.

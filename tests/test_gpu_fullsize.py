@@ -9,7 +9,8 @@ benchmark times.
   fp32, p 3, theta 0.6): tree and lists bit-exact, accelerations of a seeded
   sample of particles against the oracle evaluated on that sample only;
 * every configuration: total momentum conserved over all N particles (a
-  property of the method that holds at any size), within the parity gate.
+  property of the method that holds at any size) at the rounding level of
+  the dtype, not merely within the parity gate.
 """
 import numpy as np
 import pytest
@@ -20,6 +21,14 @@ from gpu_helpers import ALL_STRUCT, TOL_ACC, accel_error, assert_structure_equal
 
 pytestmark = pytest.mark.gpu
 
+# The whole evaluation conserves momentum to rounding (the far-field forces of
+# an accepted node pair are equal and opposite under the total-degree
+# truncation; the near-field lists are symmetric). Measured on a B300: fp64
+# 3.5e-16 (Plummer 1e5); fp32 1.1e-9 (clustered 2^20) and 3.9e-10 (clustered
+# 2^22). The gates sit about 10x above those, far below the parity gates (1e-10,
+# 1e-4), so an asymmetric truncation or a dropped term fails them.
+MOMENTUM_GATE = {"f64": 5e-15, "f32": 1e-8}
+
 
 def momentum_imbalance(mass, acc):
     """|sum_i m_i a_i| / sum_i m_i |a_i| over every particle, in fp64.
@@ -28,8 +37,8 @@ def momentum_imbalance(mass, acc):
     truncation: each accepted pair's far-field forces are equal and opposite;
     the oracle is pinned at 1e-14). The GPU result differs from it by at most
     its per-particle relative error, so the imbalance is bounded by that error
-    weighted by m |a|; the gates below are the parity gates, now over all N
-    particles instead of a sample."""
+    weighted by m |a|; in practice it stays at the rounding level of the
+    dtype, which MOMENTUM_GATE bounds."""
     m = np.asarray(mass, np.float64)
     a = np.asarray(acc, np.float64)
     return np.linalg.norm((m[:, None] * a).sum(axis=0)) / np.sum(m * np.linalg.norm(a, axis=1))
@@ -50,7 +59,7 @@ def sampled_parity(w, n_sample=3000):
           f"momentum imbalance {dp:.2e}; "
           f"nodes {st['n_nodes']} depth {st['depth']} m2l {st['n_m2l']} p2p pairs {st['n_p2p_interactions']}")
     assert e.max() <= TOL_ACC[w.dtype] and ep.max() <= TOL_ACC[w.dtype]
-    assert dp <= TOL_ACC[w.dtype]
+    assert dp <= MOMENTUM_GATE[w.dtype]
 
 
 def test_config3_full_parity_fp64():
@@ -64,7 +73,7 @@ def test_config3_full_parity_fp64():
     dp = momentum_imbalance(g["mass"], acc)
     print(f"config 3 full: acc error max {e.max():.2e}, pot {ep.max():.2e}, momentum imbalance {dp:.2e}")
     assert e.max() <= 1e-10 and ep.max() <= 1e-10
-    assert dp <= 1e-10
+    assert dp <= MOMENTUM_GATE["f64"]
 
 
 def test_config3_sweep_against_direct_sum():

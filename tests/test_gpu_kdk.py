@@ -75,20 +75,33 @@ def run_forward_back(n, steps, dt=1e-3):
     x1, v1 = tp.cpu().numpy(), tv.cpu().numpy()
     side = (x0.max(axis=0) - x0.min(axis=0)).max()
     dx = np.linalg.norm(x1 - x0, axis=1) / side
-    return dx, x_mid, x0, np.linalg.norm(p_mid - p_start)
+    scale = np.sum(m * np.linalg.norm(v0, axis=1))
+    return dx, x_mid, x0, np.linalg.norm(p_mid - p_start) / scale
+
+
+# Momentum change over the 20 forward steps relative to sum_i m_i |v_i|: the
+# force conserves momentum to rounding, so the kicks do too. Measured on a B300:
+# plain step 3.4e-15, lattice step 4.5e-14 (each kick rounds every increment to
+# the 2^-40 lattice). Gates about 10x above.
+MOMENTUM_GATE_PLAIN = 5e-14
+MOMENTUM_GATE_LATTICE = 5e-13
 
 
 def test_plain_float_reversibility_report_fp64():
     """Config-5 companion with the plain float step: N = 2^18 fp64, 20 steps
-    forward then 20 back. Unsoftened close encounters (omega dt > 1) amplify
-    rounding when run backwards, so only the bulk returns to ~1e-11; the
-    number is reported, the exact gate is the lattice step below."""
+    forward then 20 back. This step does NOT meet the 1e-9 bar for every
+    particle: unsoftened close encounters (omega dt > 1) amplify rounding when
+    run backwards, so a few particles return with errors near 1e-2 while the
+    bulk returns to ~1e-11. The max and p99.9 are printed (and reported by the
+    benchmark); the gate here is the median and momentum. The
+    1e-9 bar for every particle is met, exactly, by the lattice step below."""
     dx, x_mid, x0, dp = run_forward_back(1 << 18, 20)
     moved = np.max(np.abs(x_mid - x0))
-    print(f"plain reversibility: max {dx.max():.3e} p99.9 {np.percentile(dx, 99.9):.3e} median {np.median(dx):.3e}; "
-          f"moved {moved:.3e}; |dP| {dp:.3e}")
+    print(f"plain reversibility: max {dx.max():.3e} p99.9 {np.percentile(dx, 99.9):.3e} "
+          f"p99 {np.percentile(dx, 99):.3e} median {np.median(dx):.3e}; moved {moved:.3e}; |dP|/sum m|v| {dp:.3e}")
     assert moved > 1e-6
     assert np.median(dx) < 1e-9
+    assert dp <= MOMENTUM_GATE_PLAIN
 
 
 def snap(a, e):
@@ -115,15 +128,16 @@ def test_lattice_reversibility_fp64_2p18():
         for _ in range(20):
             pl.kdk_step_lattice(tp, tv, tm, 1e-3)
         x_mid = tp.cpu().numpy()
-        dp = np.linalg.norm((m[:, None] * (tv.cpu().numpy() - v0)).sum(axis=0))
+        dp = np.linalg.norm((m[:, None] * (tv.cpu().numpy() - v0)).sum(axis=0)) / np.sum(m * np.linalg.norm(v0, axis=1))
         for _ in range(20):
             pl.kdk_step_lattice(tp, tv, tm, -1e-3)
     x1, v1 = tp.cpu().numpy(), tv.cpu().numpy()
     side = (x0.max(axis=0) - x0.min(axis=0)).max()
     err = np.max(np.linalg.norm(x1 - x0, axis=1)) / side
-    print(f"lattice reversibility: max {err:.3e}; moved {np.max(np.abs(x_mid - x0)):.3e}; |dP| {dp:.3e}")
+    print(f"lattice reversibility: max {err:.3e}; moved {np.max(np.abs(x_mid - x0)):.3e}; |dP|/sum m|v| {dp:.3e}")
     assert np.max(np.abs(x_mid - x0)) > 1e-6
     assert err <= 1e-9
+    assert dp <= MOMENTUM_GATE_LATTICE
     assert np.array_equal(x1, x0) and np.array_equal(v1, v0)
 
 

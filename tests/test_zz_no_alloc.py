@@ -52,9 +52,34 @@ def test_noalloc_keys_equal_plan_keys_twice(dtype):
         native.fmm_morton_keys_noalloc(tp, n, dt_code, keys, box, stream=torch.cuda.current_stream())
         got = keys.cpu().numpy().view(np.uint64)
         assert np.array_equal(got, want)
-        lo = g["pos"].min(axis=0)
-        side = (g["pos"].max(axis=0) - lo).max()
-        assert np.array_equal(box.cpu().numpy(), np.array([*lo, side], dtype=np.float64))
+        assert np.array_equal(box.cpu().numpy(), expected_box(g["pos"]))
+
+
+def expected_box(pos):
+    """Lower corner and side of the root cube; the side is 1 when every point coincides."""
+    lo = pos.min(axis=0)
+    side = (pos.max(axis=0) - lo).max()
+    return np.array([*lo, side if side > 0 else 1.0], dtype=np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64"])
+@pytest.mark.parametrize("n", [1, 1 << 21])
+def test_noalloc_edges(dtype, n):
+    """The capacity edge (n = 2^21: every one of the 1024 partial-box slots is
+    used) and a single particle (a degenerate box whose side falls back to 1)."""
+    import torch
+
+    from body_forces_morton_b300 import native
+
+    dt_code = native.FMM_F32 if dtype == "f32" else native.FMM_F64
+    g = W.generate(W.WORKLOADS[4], n=n, dtype=dtype)
+    want = plan_keys(g["pos"], g["mass"], dtype)
+    tp = torch.from_numpy(g["pos"]).cuda()
+    keys = torch.empty(n, dtype=torch.int64, device="cuda")
+    box = torch.empty(4, dtype=torch.float64, device="cuda")
+    native.fmm_morton_keys_noalloc(tp, n, dt_code, keys, box, stream=torch.cuda.current_stream())
+    assert np.array_equal(keys.cpu().numpy().view(np.uint64), want)
+    assert np.array_equal(box.cpu().numpy(), expected_box(g["pos"]))
 
 
 def test_noalloc_rejects_too_many_particles():
