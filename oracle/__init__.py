@@ -48,8 +48,12 @@ def lib():
         L.orc_result_free.argtypes = [C.POINTER(_Result)]
         L.orc_kdk_step.argtypes = [i64, vp, vp, vp, vp, dbl, i32, dbl, i32, i32]
         L.orc_kdk_lattice_step.argtypes = [i64, vp, vp, vp, vp, dbl, i32, i32, i32, dbl, i32, i32]
+        L.orc_p2m_dipole.argtypes = [i32, i64, vp, vp, vp, vp, vp]
+        L.orc_l2p_hess.argtypes = [i32, vp, vp, vp]
+        L.orc_fmm_vjp.argtypes = [i32, i64, vp, vp, vp, vp, i32, dbl, i32, i32, vp, vp]
         for f in ("orc_direct_sum", "orc_derivs", "orc_p2m", "orc_m2m", "orc_m2l", "orc_l2l",
-                  "orc_l2p", "orc_keys", "orc_fmm", "orc_kdk_step", "orc_kdk_lattice_step"):
+                  "orc_l2p", "orc_keys", "orc_fmm", "orc_kdk_step", "orc_kdk_lattice_step",
+                  "orc_p2m_dipole", "orc_l2p_hess", "orc_fmm_vjp"):
             getattr(L, f).restype = i32
         L.orc_result_free.restype = None
         _lib = L
@@ -166,6 +170,26 @@ def l2l(p: int, Lp, e) -> np.ndarray:
     Lc = np.zeros(ncoef(p))
     _check(lib().orc_l2l(p, _ptr(Lp), _ptr(e), _ptr(Lc)), "l2l")
     return Lc
+
+
+def p2m_dipole(p: int, pos, q, d, c) -> np.ndarray:
+    """Moments of sources with monopoles q (None = 0) and dipoles d [n x 3] about c."""
+    pos = np.ascontiguousarray(pos, dtype=np.float64).reshape(-1, 3)
+    d = np.ascontiguousarray(d, dtype=np.float64).reshape(-1, 3)
+    qq = None if q is None else np.ascontiguousarray(q, dtype=np.float64)
+    c = np.ascontiguousarray(c, dtype=np.float64)
+    M = np.zeros(ncoef(p))
+    _check(lib().orc_p2m_dipole(p, len(pos), _ptr(pos), _ptr(qq), _ptr(d), _ptr(c), _ptr(M)), "p2m_dipole")
+    return M
+
+
+def l2p_hess(p: int, L, dx) -> np.ndarray:
+    """Hessian (xx, xy, xz, yy, yz, zz) of the local series L at offset dx."""
+    L = np.ascontiguousarray(L, dtype=np.float64)
+    dx = np.ascontiguousarray(dx, dtype=np.float64)
+    H = np.zeros(6)
+    _check(lib().orc_l2p_hess(p, _ptr(L), _ptr(dx), _ptr(H)), "l2p_hess")
+    return H
 
 
 def l2p(p: int, L, dx):
@@ -290,6 +314,24 @@ def fmm(pos, mass, p: int = 4, theta: float = 0.7, leaf: int = 32, eval_mask=Non
     finally:
         lib().orc_result_free(C.byref(r))
     return out
+
+
+def fmm_vjp(pos, mass, acc_bar, pot_bar=None, p: int = 4, theta: float = 0.7, leaf: int = 32, nthreads: int = 0):
+    """Vector-Jacobian product of one FMM evaluation (see orc_fmm_vjp): returns (pos_bar [n x 3],
+    mass_bar [n]) for the cotangents acc_bar [n x 3] and pot_bar [n] (or None), in fp64."""
+    pos = np.ascontiguousarray(pos)
+    mass = np.ascontiguousarray(mass)
+    if pos.dtype != mass.dtype or pos.dtype not in (np.float32, np.float64):
+        raise TypeError("pos and mass must share a float32/float64 dtype")
+    dt = DTYPE_F32 if pos.dtype == np.float32 else DTYPE_F64
+    ab = np.ascontiguousarray(acc_bar, dtype=np.float64).reshape(-1, 3)
+    pb = None if pot_bar is None else np.ascontiguousarray(pot_bar, dtype=np.float64)
+    n = len(mass)
+    xb = np.zeros((n, 3))
+    mb = np.zeros(n)
+    _check(lib().orc_fmm_vjp(dt, n, _ptr(pos), _ptr(mass), _ptr(ab), _ptr(pb), p, float(theta), leaf, nthreads,
+                             _ptr(xb), _ptr(mb)), "fmm_vjp")
+    return xb, mb
 
 
 def kdk_step(pos, vel, mass, acc, dt: float, p: int, theta: float, leaf: int, nthreads: int = 0):

@@ -302,6 +302,60 @@ int orc_l2p(int p, const double *L, const double *dx, double *pot, double *acc)
     return ORC_OK;
 }
 
+/*
+ * Dipole P2M (used by the VJP below): a source at x_j = c + s with monopole q and dipole d has the
+ * potential -G (q + d . grad_{x_j}) 1/|y - x_j|, so its moments are
+ *   M_n += q s^n / n! + sum_alpha d_alpha s^{n - e_alpha} / (n - e_alpha)!,
+ * the position derivative of the point-mass moments in the direction d.
+ */
+int orc_p2m_dipole(int p, int64_t n, const double *pos, const double *q, const double *d, const double *c,
+                   double *M)
+{
+    if (p < 0 || p > ORC_MAXP) return ORC_EINVAL;
+    int nc = orc_ncoef(p);
+    int mi[ORC_NCMAX][3];
+    mi_table(p, mi);
+    for (int64_t j = 0; j < n; ++j) {
+        double s[3] = {pos[3 * j] - c[0], pos[3 * j + 1] - c[1], pos[3 * j + 2] - c[2]};
+        for (int a = 0; a < nc; ++a) {
+            const int *m = mi[a];
+            double v = (q ? q[j] : 0.0) * mono_over_fact(s, m);
+            for (int al = 0; al < 3; ++al) {
+                if (m[al] < 1) continue;
+                int r[3] = {m[0], m[1], m[2]};
+                r[al] -= 1;
+                v += d[3 * j + al] * mono_over_fact(s, r);
+            }
+            M[a] += v;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Hessian of the local series (the next derivative after L2P's gradient):
+ *   d_alpha d_beta Phi(c + dx) = sum_{|k| <= p-2} L_{k + e_alpha + e_beta} dx^k / k!
+ * added to H = (xx, xy, xz, yy, yz, zz). */
+int orc_l2p_hess(int p, const double *L, const double *dx, double *H)
+{
+    if (p < 0 || p > ORC_MAXP) return ORC_EINVAL;
+    int nc = orc_ncoef(p);
+    int mi[ORC_NCMAX][3];
+    mi_table(p, mi);
+    static const int pa[6] = {0, 0, 0, 1, 1, 2}, pb[6] = {0, 1, 2, 1, 2, 2};
+    for (int a = 0; a < nc; ++a) {
+        const int *k = mi[a];
+        if (k[0] + k[1] + k[2] > p - 2) continue;
+        double t = mono_over_fact(dx, k);
+        for (int h = 0; h < 6; ++h) {
+            int q[3] = {k[0], k[1], k[2]};
+            q[pa[h]] += 1;
+            q[pb[h]] += 1;
+            H[h] += L[orc_mindex(q[0], q[1], q[2])] * t;
+        }
+    }
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Morton keys (21 bits per axis, x most significant within each 3-bit digit) */
 /* ------------------------------------------------------------------------ */
@@ -888,4 +942,144 @@ int orc_kdk_lattice_step(int64_t n, double *pos, double *vel, const double *mass
     orc_result_free(&r);
     for (int64_t i = 0; i < 3 * n; ++i) vel[i] += to_lattice(acc[i] * h, idv, dv);
     return ORC_OK;
+}
+
+/*
+ * Vector-Jacobian product of one FMM evaluation (JZ-FMM page, "Differentiating the force
+ * calculation": one contribution comes from the next higher derivative in the original evaluation,
+ * the other from an FMM in which the force sensitivities act as dipole moments).
+ *
+ * Given cotangents abar_i of the accelerations and (optionally, NULL = 0) pbar_i of the potentials,
+ * with the loss sensitivity sum_i abar_i . a_i + pbar_i phi_i, it returns
+ *   xbar_k = m_k grad Phi_s(x_k) - Hess Phi(x_k) abar_k - pbar_k a_k,     mbar_k = Phi_s(x_k),
+ * where Phi is the forward potential (its Hessian: L2P one order higher, plus the direct term of
+ * every near pair) and Phi_s the potential of sources at every particle with monopole pbar_j and
+ * dipole -abar_j,
+ *   Phi_s(y) = -G sum_{j} [pbar_j / |y - x_j| - abar_j . (y - x_j) / |y - x_j|^3]   (r = 0 skipped),
+ * evaluated by the same tree, centres, p, theta and lists as the forward evaluation (dipole P2M,
+ * then the forward M2M, M2L, L2L and L2P, plus the direct near field). Why: with the centres and
+ * lists fixed, the evaluation is a_i = -grad_{x_i} sum_k m_k K(x_i, x_k) with a pair kernel K that
+ * is symmetric in its two particles (the total-degree truncation; D^m(-R) = (-1)^{|m|} D^m(R)),
+ * so the derivative through a source's moments is the dipole FMM, and the derivative through the
+ * evaluation point is the Hessian of the forward potential. These are therefore the exact
+ * derivatives of the evaluation with the tree and the expansion centres held fixed.
+ *
+ * pos, mass in dtype (fp32 inputs are widened exactly); abar [n*3], pbar [n] or NULL, and the
+ * outputs pos_bar [n*3], mass_bar [n] are fp64 in the caller's order.
+ */
+int orc_fmm_vjp(int dtype, int64_t n, const void *pos_in, const void *mass_in, const double *abar,
+                const double *pbar, int p, double theta, int leaf, int nthreads, double *pos_bar, double *mass_bar)
+{
+    if (!abar || !pos_bar || !mass_bar) return ORC_EINVAL;
+    orc_result r;
+    int st = orc_fmm(dtype, n, pos_in, mass_in, p, theta, leaf, NULL, 0, nthreads, &r);
+    if (st) return st;
+    const int64_t nn = r.n_nodes;
+    const int nc = r.nc;
+    double *xs = malloc(sizeof(double) * 3 * (size_t)n), *ms = malloc(sizeof(double) * (size_t)n);
+    double *as = malloc(sizeof(double) * 3 * (size_t)n), *qs = malloc(sizeof(double) * (size_t)n);
+    double *ds = malloc(sizeof(double) * 3 * (size_t)n);
+    double *Ms = calloc((size_t)nn * nc, sizeof(double)), *Lsm = calloc((size_t)nn * nc, sizeof(double));
+    double *Ls = calloc((size_t)nn * nc, sizeof(double));
+    if (!xs || !ms || !as || !qs || !ds || !Ms || !Lsm || !Ls) { st = ORC_ENOMEM; goto out; }
+    /* sorted copies: positions, masses, cotangents; the dipole of particle j is -abar_j */
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t o = r.perm[i];
+        for (int d = 0; d < 3; ++d) {
+            xs[3 * i + d] = dtype == ORC_DTYPE_F32 ? (double)((const float *)pos_in)[3 * o + d]
+                                                   : ((const double *)pos_in)[3 * o + d];
+            as[3 * i + d] = abar[3 * o + d];
+            ds[3 * i + d] = -abar[3 * o + d];
+        }
+        ms[i] = dtype == ORC_DTYPE_F32 ? (double)((const float *)mass_in)[o] : ((const double *)mass_in)[o];
+        qs[i] = pbar ? pbar[o] : 0.0;
+    }
+    /* source FMM, upward: dipole P2M at the leaves, M2M to the parents (same centres) */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 64)
+#endif
+    for (int64_t a = 0; a < nn; ++a)
+        if (r.nchild[a] == 0)
+            orc_p2m_dipole(p, r.count[a], xs + 3 * (int64_t)r.first[a], qs + r.first[a], ds + 3 * (int64_t)r.first[a],
+                           r.centre + 3 * a, Ms + a * nc);
+    for (int l = r.depth - 1; l >= 0; --l) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 64)
+#endif
+        for (int64_t a = r.level_off[l]; a < r.level_off[l + 1]; ++a)
+            for (int c = 0; c < r.nchild[a]; ++c) {
+                int64_t ch = r.child0[a] + c;
+                double dd[3] = {r.centre[3 * ch] - r.centre[3 * a], r.centre[3 * ch + 1] - r.centre[3 * a + 1],
+                                r.centre[3 * ch + 2] - r.centre[3 * a + 2]};
+                orc_m2m(p, Ms + ch * nc, dd, Ms + a * nc);
+            }
+    }
+    /* M2L over the forward lists */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 16)
+#endif
+    for (int64_t a = 0; a < nn; ++a)
+        for (int64_t q = r.m2l_off[a]; q < r.m2l_off[a + 1]; ++q) {
+            int64_t b = r.m2l_src[q];
+            double R[3] = {r.centre[3 * a] - r.centre[3 * b], r.centre[3 * a + 1] - r.centre[3 * b + 1],
+                           r.centre[3 * a + 2] - r.centre[3 * b + 2]};
+            orc_m2l(p, Ms + b * nc, R, Lsm + a * nc);
+        }
+    /* L2L, parents before children */
+    for (int64_t a = 0; a < nn; ++a) {
+        int64_t par = r.parent[a];
+        if (par >= 0) {
+            double e[3] = {r.centre[3 * a] - r.centre[3 * par], r.centre[3 * a + 1] - r.centre[3 * par + 1],
+                           r.centre[3 * a + 2] - r.centre[3 * par + 2]};
+            orc_l2l(p, Ls + par * nc, e, Ls + a * nc);
+        }
+        for (int c = 0; c < nc; ++c) Ls[a * nc + c] += Lsm[a * nc + c];
+    }
+    /* leaves: far parts from the local series, near parts over the P2P lists */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic, 16)
+#endif
+    for (int64_t a = 0; a < nn; ++a) {
+        if (r.nchild[a] != 0) continue;
+        for (int64_t i = r.first[a]; i < (int64_t)r.first[a] + r.count[a]; ++i) {
+            int64_t o = r.perm[i];
+            double dx[3] = {xs[3 * i] - r.centre[3 * a], xs[3 * i + 1] - r.centre[3 * a + 1],
+                            xs[3 * i + 2] - r.centre[3 * a + 2]};
+            double phis = 0.0, ngs[3] = {0.0, 0.0, 0.0}, H[6] = {0, 0, 0, 0, 0, 0};
+            orc_l2p(p, Ls + a * nc, dx, &phis, ngs);      /* Phi_s and -grad Phi_s */
+            orc_l2p_hess(p, r.L + a * nc, dx, H);         /* Hessian of the forward potential */
+            double gs[3] = {-ngs[0], -ngs[1], -ngs[2]};
+            for (int64_t q = r.p2p_off[a]; q < r.p2p_off[a + 1]; ++q) {
+                int64_t b = r.p2p_src[q];
+                for (int64_t j = r.first[b]; j < (int64_t)r.first[b] + r.count[b]; ++j) {
+                    double u[3] = {xs[3 * i] - xs[3 * j], xs[3 * i + 1] - xs[3 * j + 1], xs[3 * i + 2] - xs[3 * j + 2]};
+                    double r2 = u[0] * u[0] + u[1] * u[1] + u[2] * u[2];
+                    if (r2 == 0.0) continue;
+                    double rr = sqrt(r2), ir3 = 1.0 / (r2 * rr), ir5 = ir3 / r2;
+                    /* forward: Phi += -m_j / r, Hessian m_j (r^2 delta - 3 u u) / r^5 */
+                    H[0] += ms[j] * (r2 - 3.0 * u[0] * u[0]) * ir5;
+                    H[1] += ms[j] * (-3.0 * u[0] * u[1]) * ir5;
+                    H[2] += ms[j] * (-3.0 * u[0] * u[2]) * ir5;
+                    H[3] += ms[j] * (r2 - 3.0 * u[1] * u[1]) * ir5;
+                    H[4] += ms[j] * (-3.0 * u[1] * u[2]) * ir5;
+                    H[5] += ms[j] * (r2 - 3.0 * u[2] * u[2]) * ir5;
+                    /* sources: Phi_s += -q_j / r - d_j . u / r^3 and its gradient
+                       q_j u / r^3 - d_j / r^3 + 3 (d_j . u) u / r^5 */
+                    const double *dj = ds + 3 * j;
+                    double du = dj[0] * u[0] + dj[1] * u[1] + dj[2] * u[2];
+                    phis += -qs[j] / rr - du * ir3;
+                    for (int d = 0; d < 3; ++d) gs[d] += qs[j] * u[d] * ir3 - dj[d] * ir3 + 3.0 * du * u[d] * ir5;
+                }
+            }
+            const double *ab = as + 3 * i;
+            double Ha[3] = {H[0] * ab[0] + H[1] * ab[1] + H[2] * ab[2], H[1] * ab[0] + H[3] * ab[1] + H[4] * ab[2],
+                            H[2] * ab[0] + H[4] * ab[1] + H[5] * ab[2]};
+            for (int d = 0; d < 3; ++d) pos_bar[3 * o + d] = ms[i] * gs[d] - Ha[d] - qs[i] * r.acc[3 * o + d];
+            mass_bar[o] = phis;
+        }
+    }
+out:
+    free(xs); free(ms); free(as); free(qs); free(ds); free(Ms); free(Lsm); free(Ls);
+    orc_result_free(&r);
+    return st;
 }
