@@ -480,4 +480,14 @@ __device__ __forceinline__ void cp_async16(void *dst_smem, const void *src)
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+// Groups of asynchronous copies: commit closes the thread's copies issued so
+// far into a group; wait_group<N> returns once at most N of the thread's
+// groups are still in flight (so with one group per pipeline stage, N = 1
+// waits for all but the newest).
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait_group()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 }  // namespace bfm

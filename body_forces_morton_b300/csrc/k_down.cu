@@ -380,33 +380,19 @@ __device__ __forceinline__ void p2p_item(int a, int chunk, int nch, int *done, D
     }
     for (int r0 = 0; r0 < c; r0 += 128) {
         const int cr = min(128, c - r0);
-        // useful fraction of the lane-interactions with K receivers per lane is cr S / (32 K),
-        // S = 32 / ceil(cr / K); ties go to the larger K (fewer shared loads per interaction)
-        int best = 4, best_num = -1;
-#pragma unroll
-        for (int K = 1; K <= 4; K <<= 1) {
-            const int R = (cr + K - 1) / K;
-            if (R > 32) continue;
-            const int num = cr * (32 / R) * (4 / K);
-            if (num >= best_num) { best_num = num; best = K; }
-        }
-        if (best == 1)
-            p2p_round<T, 1, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm,
-                                     far, far_w, src, acc_out, pot_out, buf, red, lane);
-        else if (best == 2)
-            p2p_round<T, 2, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm,
-                                     far, far_w, src, acc_out, pot_out, buf, red, lane);
-        else
-            p2p_round<T, 4, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm,
-                                     far, far_w, src, acc_out, pot_out, buf, red, lane);
+        // four receivers per lane (R = ceil(cr / 4) lanes, the sources split S = 32 / R ways): measured
+        // faster than choosing 1, 2 or 4 per leaf to keep the most lanes busy, because four receivers
+        // per lane give each staged source four times the arithmetic and the lane more independent
+        // chains than the idle lanes of small leaves cost
+        p2p_round<T, 4, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm, far,
+                                 far_w, src, acc_out, pot_out, buf, red, lane);
     }
     if (CHUNKED && chunk < nch - 1) pass_turn(done + a, chunk + 1);
 }
 
 // P2P for one receiving leaf per warp (leaves taken from a shared counter in
 // decreasing order of work), plus the far field from `far`, scattered to the
-// caller's order. The receivers per lane K (1, 2 or 4) are
-// chosen per leaf to keep the most lanes doing useful interactions; the
+// caller's order. Each lane takes up to four receivers of the leaf; the
 // leaf's own particles are a separate masked pass, the rest runs unmasked.
 template <class T>
 __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__restrict__ cst,
