@@ -35,33 +35,44 @@ sys.path.insert(0, ROOT)
 from body_forces_morton_b300 import workloads as W  # noqa: E402
 
 # Peaks: HBM copy bandwidth from the driver-written measurement; FP32 / FP64
-# pipe peaks derived from unit counts and the maximum SM clock (148 SMs x 128
-# FP32 lanes x 2 flop per FMA x 2.032 GHz; FP64: the nominal 1.25 TFLOP/s).
-FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
-FP64_PEAK_TFLOPS = 1.25
-F64_ARITH = ("fp64 inputs and outputs; M2L (p <= 4) and P2P in double-float arithmetic (fp32 pairs, "
-             "~2^-48 relative) on the FP32 pipe, the other stages in fp64")
+# pipe peaks derived from unit counts and the maximum SM clock: 148 SMs x 128
+# FP32 lanes x 2 flop per FMA x 2.032 GHz = 77.0 TFLOP/s (38.5e12 FP32 lane
+# operations/s); FP64: 148 SMs x 2 FMA per clock x 2 flop x 2.032 GHz = 1.20
+# TFLOP/s (the FP64 FMA rate ncu reports per SM).
+SM_CLOCK_HZ = 2.032e9
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * SM_CLOCK_HZ / 1e12
+FP32_LANE_OPS_PEAK = 148 * 128 * SM_CLOCK_HZ  # FP32 pipe lane-operations per second (an FFMA counts once)
+FP64_PEAK_TFLOPS = 148 * 2 * 2 * SM_CLOCK_HZ / 1e12
+F64_ARITH = ("fp64 inputs and outputs; M2L (p <= 4), L2P and leaf P2M (p <= 6) and P2P in double-float "
+             "arithmetic (fp32 pairs, ~2^-48 relative) on the FP32 pipe, the other stages in fp64")
+F64_IEEE_ARITH = "IEEE fp64 in every stage (fmm_plan_set_f64_ieee)"
 P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r^2), 3 FMA (a), 1 add (phi) ~ 19 + 1
 
-# DRAM traffic of the leaf kernel per launch, from the ncu capture committed
-# under profiles/ (bytes); keyed by the hash of the kernel source it was taken on.
-TRAFFIC = {
-    # k_p2p<float>, clustered N = 2^20: 52.52 MB read + 4.05 MB written (one warm launch, --set full)
-    ("clustered_2p20_f32", "f4562b91ce3ab6f9"): 56572672,
-    # same k_p2p code; the file changed in its L2L kernels only
-    ("clustered_2p20_f32", "d5826261d587dbe7"): 56572672,
-    ("clustered_2p20_f32", "e6ea43d35f31e177"): 56572672,
-    # same k_p2p code; the expansion header gained an operator that k_p2p does not use
-    ("clustered_2p20_f32", "0abb2f5ba077255d"): 56572672,
-}
+# The double-float kernels run on the FP32 pipe, so their roofline is that
+# pipe: FP32 FMA-pipe lane operations they issue per pair (an FFMA counted
+# once, like the pipe does), times pairs, over time, against
+# FP32_LANE_OPS_PEAK. The per-pair counts are ncu's
+# sm__thread_inst_executed_pipe_fma_pred_on over the pairs of one launch (Plummer
+# 1e5 fp64, p 4), keyed by the hash of the kernel sources they were counted on;
+# a changed kernel reports null until it is counted again.
+DF_FMA_OPS_PER_PAIR = {}
+
+# DRAM traffic of the P2P kernel per launch (dram__bytes_read.sum +
+# dram__bytes_write.sum, one warm launch of clustered N = 2^20 fp32), keyed by
+# the hash of the kernel sources it was taken on; null once they change.
+TRAFFIC = {}
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=("k_down.cu", "expansions_gen.cuh", "common.cuh")):
     h = hashlib.sha256()
-    for f in ("k_down.cu", "expansions_gen.cuh", "common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "body_forces_morton_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+DF_SOURCES = {"k_p2p_df": ("k_p2p_df.cu", "dfloat.cuh", "common.cuh"),
+              "k_m2l_df": ("k_m2l_df.cu", "expansions_df_gen.cuh", "dfloat.cuh", "common.cuh")}
 
 
 def env_rank():
@@ -192,40 +203,80 @@ def aggregate_over_ranks(local_ms: float, n_local: int, world: int, dist=None, d
     return world * n_local / (total / 1e3), total
 
 
-def bench_kdk(w, steps, warmup, torch, native, stream):
+KDK_WARMUP, KDK_STEPS = 3, 5  # the KDK leg's fixed window (the clustered state evolves from step to step)
+
+
+def bench_kdk(w, torch, native, stream):
     """Particles/s per kick-drift-kick step (one force evaluation per step, the
-    step's first kick reuses the cached acceleration)."""
+    step's first kick reuses the cached acceleration). The state evolves (the
+    halos' velocities are not in equilibrium, so their cores collapse and the
+    near field grows), so the leg always times the same steps, KDK_WARMUP + 1
+    to KDK_WARMUP + KDK_STEPS from the seeded initial state, whatever --steps
+    and --warmup say."""
     g = W.generate(w)
     tdt = torch.float32 if w.dtype == "f32" else torch.float64
     pos = torch.from_numpy(g["pos"]).to("cuda", tdt)
     vel = torch.from_numpy(g["vel"]).to("cuda", tdt)
     mass = torch.from_numpy(g["mass"]).to("cuda", tdt)
     with native.Plan(w.n, w.p, w.theta, w.leaf, w.dtype) as plan, torch.cuda.stream(stream):
-        for _ in range(warmup):
+        for _ in range(KDK_WARMUP):
             plan.kdk_step(pos, vel, mass, 1e-3, stream=stream)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(steps):
+        for _ in range(KDK_STEPS):
             plan.kdk_step(pos, vel, mass, 1e-3, stream=stream)
         e1.record(stream)
         e1.synchronize()
-        ms = e0.elapsed_time(e1) / steps
+        ms = e0.elapsed_time(e1) / KDK_STEPS
     return {"value": w.n / (ms / 1e3), "unit": "particles/s per KDK step", "ms_per_step": ms, "dtype": w.dtype,
-            "p": w.p, "theta": w.theta, "leaf": w.leaf, "n": w.n}
+            "p": w.p, "theta": w.theta, "leaf": w.leaf, "n": w.n,
+            "window": f"steps {KDK_WARMUP + 1}..{KDK_WARMUP + KDK_STEPS} from the seeded initial state"}
 
 
-def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_override=None):
+def bench_reversibility(torch, native, steps=20, dt=1e-3):
+    """Config 5's companion: N = 2^18 fp64, `steps` steps forward then back, with the
+    plain floating-point step and with the integer-lattice step; the return error
+    max_i |x_i^end - x_i^0| / box side (and the plain step's percentiles)."""
+    w = W.KDK_REVERSIBILITY
+    g = W.generate(w)
+    side = float((g["pos"].max(axis=0) - g["pos"].min(axis=0)).max())
+    out = {"n": w.n, "dtype": "f64", "steps": steps, "dt": dt, "p": w.p, "theta": w.theta, "leaf": w.leaf}
+    with native.Plan(w.n, w.p, w.theta, w.leaf, "f64") as plan:
+        for mode in ("plain", "lattice"):
+            x0 = g["pos"].copy()
+            v0 = g["vel"].copy()
+            if mode == "lattice":
+                q = 2.0 ** -40
+                x0, v0 = np.rint(x0 / q) * q, np.rint(v0 / q) * q
+            tp = torch.from_numpy(x0.copy()).cuda()
+            tv = torch.from_numpy(v0.copy()).cuda()
+            tm = torch.from_numpy(g["mass"]).cuda()
+            plan.kdk_reset()
+            step = plan.kdk_step if mode == "plain" else plan.kdk_step_lattice
+            for sgn in (1.0, -1.0):
+                for _ in range(steps):
+                    step(tp, tv, tm, sgn * dt)
+            err = np.linalg.norm(tp.cpu().numpy() - x0, axis=1) / side
+            out[mode] = {"max": float(err.max()), "p99_9": float(np.percentile(err, 99.9)),
+                         "median": float(np.median(err)), "bit_exact": bool(np.array_equal(tp.cpu().numpy(), x0))}
+    out["note"] = ("the plain fp64 step misses 1e-9 for a few chaotic close pairs (unsoftened); "
+                   "the lattice step returns bit for bit")
+    return out
+
+
+def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_override=None, dtype=None, f64_ieee=False):
     """Times `steps` evaluations; returns dict with per-step ms, stage ms, stats."""
     n = n_override or w.n
-    g = W.generate(w, n=n)
-    tdt = torch.float32 if w.dtype == "f32" else torch.float64
+    dtype = dtype or w.dtype
+    g = W.generate(w, n=n, dtype=dtype)
+    tdt = torch.float32 if dtype == "f32" else torch.float64
     pos = torch.from_numpy(g["pos"]).to("cuda", tdt)
     mass = torch.from_numpy(g["mass"]).to("cuda", tdt)
     acc = torch.empty_like(pos)
     pot = torch.empty_like(mass)
-    plan = native.Plan(n, w.p, w.theta, w.leaf, w.dtype)
+    plan = native.Plan(n, w.p, w.theta, w.leaf, dtype, f64_ieee=f64_ieee)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             plan.eval(pos, mass, acc, pot, stream=stream)
@@ -300,20 +351,39 @@ def run_ours(args, rank, world, local_rank):
                                            device="cuda")
     ms_per_step = total_ms
 
-    # secondary point: N = 1e5 fp64 Plummer
+    # secondary points: the other configurations and the benchmark spec's exact sizes
     also = {}
     if not args.no_also:
+        n_also = max(3, args.steps // 2)
+
+        def leg(w, name, n=None, dtype=None, f64_ieee=False, roofs=False):
+            r = bench_workload(w, n_also, args.warmup, torch, native, stream, flush_buf, n_override=n, dtype=dtype,
+                               f64_ieee=f64_ieee)
+            ms = float(np.median(r["step_ms"]))  # median: a rare driver stall of ~3 ms would skew a short mean
+            dt = dtype or w.dtype
+            d = {"value": r["n"] / (ms / 1e3), "unit": "particles/s", "ms_per_step": ms, "n": r["n"], "dtype": dt,
+                 "step_ms_spread": {"min": min(r["step_ms"]), "max": max(r["step_ms"]), "steps": len(r["step_ms"])},
+                 "p": w.p, "theta": w.theta, "leaf": w.leaf, "stage_ms": r["stage_ms"],
+                 "counts": {k: r["stats"][k] for k in ("n_nodes", "n_m2l", "n_p2p_interactions")}}
+            if dt == "f64":
+                d["arith"] = F64_IEEE_ARITH if f64_ieee else F64_ARITH
+            if roofs:
+                d["roofline"] = p2p_roofline(r, w, dt, f64_ieee)
+                d["m2l_roofline"] = m2l_roofline(r, w, dt, f64_ieee)
+                d["eval_roofline"] = eval_roofline(r, w, ms, *hbm_peak_gbs(), dtype=dt, f64_ieee=f64_ieee)
+            r["plan"].close()
+            also[name] = d
+
         w3 = W.WORKLOADS[3]
-        r3 = bench_workload(w3, max(3, args.steps // 2), args.warmup, torch, native, stream, flush_buf)
-        ms3 = float(np.mean(r3["step_ms"]))
-        also[w3.name] = {"value": r3["n"] / (ms3 / 1e3), "unit": "particles/s", "ms_per_step": ms3,
-                         "stage_ms": r3["stage_ms"], "dtype": "f64", "arith": F64_ARITH, "p": w3.p,
-                         "theta": w3.theta, "leaf": w3.leaf, "roofline": p2p_roofline(r3, w3),
-                         "m2l_roofline": m2l_roofline(r3, w3),
-                         "eval_roofline": eval_roofline(r3, w3, ms3, *hbm_peak_gbs())}
-        r3["plan"].close()
+        leg(w3, w3.name, roofs=True)
+        leg(w3, w3.name + "_ieee", f64_ieee=True, roofs=True)
+        leg(W.WORKLOADS[1], W.WORKLOADS[1].name)
+        leg(W.WORKLOADS[2], W.WORKLOADS[2].name)
+        leg(w, "clustered_1e6_f32", n=1000000, dtype="f32")
+        leg(w, "clustered_1e6_f64", n=1000000, dtype="f64")
         w5 = W.WORKLOADS[5]
-        also[w5.name] = bench_kdk(w5, max(3, args.steps // 2), args.warmup, torch, native, stream)
+        also[w5.name] = bench_kdk(w5, torch, native, stream)
+        also["kdk_reversibility_2p18_f64"] = bench_reversibility(torch, native)
 
     e2e = None
     if not args.no_e2e:
@@ -358,24 +428,42 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
-def p2p_roofline(res, w):
+def df_pipe_roofline(kernel, pairs, ms):
+    """Double-float kernel against the FP32 pipe that executes it (see DF_FMA_OPS_PER_PAIR)."""
+    src = kernel_source_hash(DF_SOURCES[kernel])
+    ops = DF_FMA_OPS_PER_PAIR.get((kernel, src))
+    out = {"kernel": kernel, "bound": "alu", "unit": "FP32 lane-ops/s", "peak": FP32_LANE_OPS_PEAK,
+           "peak_note": "derived: 148 SM x 128 FP32 lanes x 2.032 GHz", "source_hash": src}
+    if ops is None:
+        out.update({"achieved": None, "frac": None, "note": "FMA-pipe operations per pair not counted on this source"})
+    else:
+        achieved = ops * pairs / (ms / 1e3)
+        out.update({"achieved": achieved, "frac": achieved / FP32_LANE_OPS_PEAK, "fma_ops_per_pair": ops})
+    return out
+
+
+def p2p_roofline(res, w, dtype=None, f64_ieee=False):
     """P2P kernel (near field, plus adding the far field and the scatter) against the ALU peak.
 
-    fp32: 20 flop per particle pair against the FP32 peak. fp64: the same 20
-    fp64-equivalent flop against the nominal FP64 peak, although the kernel
-    computes in double-float on the FP32 pipe (so frac can exceed 1)."""
+    fp32: 20 flop per particle pair against the FP32 peak. fp64 IEEE: the same
+    against the FP64 peak. fp64 double-float: against the FP32 pipe it runs on
+    (df_pipe_roofline), with the fp64-equivalent rate reported beside it."""
+    dtype = dtype or w.dtype
     st = res["stats"]
     ms = res["stage_ms"]["p2p"]
     pairs = st["n_p2p_interactions"] - res["n"]  # zero-separation self pairs are skipped
     achieved = P2P_FLOPS_PER_PAIR * pairs / (ms / 1e3) / 1e12
-    f32 = w.dtype == "f32"
-    peak = FP32_PEAK_TFLOPS if f32 else FP64_PEAK_TFLOPS
-    return {"kernel": "k_p2p" if f32 else "k_p2p_df (+ k_leaf_offsets)", "bound": "alu", "achieved": achieved,
-            "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-            "peak_note": "derived: 148 SM x 128 FP32 lanes x 2 x 2.032 GHz" if f32
-            else "nominal FP64 1.25 TFLOP/s; the kernel runs double-float on the FP32 pipe",
-            "flops_note": f"{P2P_FLOPS_PER_PAIR} flop per particle pair, {pairs} pairs per launch",
-            "ms": ms, "traffic": None}
+    flops_note = f"{P2P_FLOPS_PER_PAIR} flop per particle pair, {pairs} pairs per launch"
+    if dtype == "f32" or f64_ieee:
+        peak = FP32_PEAK_TFLOPS if dtype == "f32" else FP64_PEAK_TFLOPS
+        return {"kernel": "k_p2p" if dtype == "f32" else "k_p2p<double>", "bound": "alu", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_note": "derived: 148 SM x 128 FP32 lanes x 2 x 2.032 GHz" if dtype == "f32"
+                else "derived: 148 SM x 2 FP64 FMA x 2 x 2.032 GHz",
+                "flops_note": flops_note, "ms": ms, "traffic": None}
+    out = df_pipe_roofline("k_p2p_df", pairs, ms)
+    out.update({"ms": ms, "fp64_equivalent_tflops": achieved, "flops_note": flops_note, "traffic": None})
+    return out
 
 
 def hbm_peak_gbs():
@@ -400,18 +488,19 @@ def hbm_bytes_per_particle(wbytes):
     }
 
 
-def eval_roofline(res, w, ms_eval, hbm_gbs, hbm_source):
+def eval_roofline(res, w, ms_eval, hbm_gbs, hbm_source, dtype=None, f64_ieee=False):
     """Whole-evaluation roofline fraction: the sum over stages of algorithmic work / peak, over
     the measured evaluation time. P2P and M2L count their flops against the ALU peak of the
-    plan's dtype (for fp64 the nominal FP64 peak, although both run double-float on the FP32
-    pipe); the memory-bound stages count hbm_bytes_per_particle against the HBM copy bandwidth.
-    Stages with no algorithmic work of their own (walk, lists, M2M, L2L) count zero."""
+    pipe they run on (FP32 for fp32 plans and for the double-float stages of fp64 plans, whose
+    fp64-equivalent flops are counted against the FP32 peak; FP64 for IEEE fp64 plans); the
+    memory-bound stages count hbm_bytes_per_particle against the HBM copy bandwidth. Stages
+    with no algorithmic work of their own (walk, lists, M2M, L2L) count zero."""
+    dtype = dtype or w.dtype
     n, st = res["n"], res["stats"]
-    f32 = w.dtype == "f32"
-    alu = (FP32_PEAK_TFLOPS if f32 else FP64_PEAK_TFLOPS) * 1e12
+    alu = (FP64_PEAK_TFLOPS if f64_ieee else FP32_PEAK_TFLOPS) * 1e12
     p2p_ms = P2P_FLOPS_PER_PAIR * (st["n_p2p_interactions"] - n) / alu * 1e3
     m2l_ms = m2l_flops_per_pair(w.p) * st["n_m2l"] / alu * 1e3
-    per_particle = hbm_bytes_per_particle(4 if f32 else 8)
+    per_particle = hbm_bytes_per_particle(4 if dtype == "f32" else 8)
     hbm_ms = sum(per_particle.values()) * n / (hbm_gbs * 1e9) * 1e3
     ideal = p2p_ms + m2l_ms + hbm_ms
     return {"frac": ideal / ms_eval, "ideal_ms": ideal, "ms": ms_eval,
@@ -428,19 +517,23 @@ def m2l_flops_per_pair(p):
     return 2 * terms + 10 * (p + 1) ** 2 + p * (p - 1) // 2
 
 
-def m2l_roofline(res, w):
-    """Algorithmic M2L flops per pair (m2l_flops_per_pair: 566 at p = 4) over the M2L stage time.
-
-    fp64 with p <= 4 runs double-float on the FP32 pipe (k_moments_df + k_m2l_df);
-    its fp64-equivalent rate is reported against the nominal FP64 peak."""
+def m2l_roofline(res, w, dtype=None, f64_ieee=False):
+    """Algorithmic M2L flops per pair (m2l_flops_per_pair: 566 at p = 4) over the M2L stage time,
+    against the FP32 peak (fp32), the FP64 peak (IEEE fp64), or, for the double-float kernels of
+    fp64 plans with p <= 4, the FP32 pipe they run on (df_pipe_roofline)."""
+    dtype = dtype or w.dtype
     per_pair = m2l_flops_per_pair(w.p)
     ms = res["stage_ms"]["m2l"]
-    achieved = per_pair * res["stats"]["n_m2l"] / (ms / 1e3) / 1e12
-    f32 = w.dtype == "f32"
-    peak = FP32_PEAK_TFLOPS if f32 else FP64_PEAK_TFLOPS
-    kernel = "k_m2l" if f32 or w.p > 4 else "k_m2l_df (+ k_moments_df)"
-    return {"kernel": kernel, "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "flops_per_pair": per_pair, "pairs": res["stats"]["n_m2l"], "ms": ms}
+    pairs = res["stats"]["n_m2l"]
+    achieved = per_pair * pairs / (ms / 1e3) / 1e12
+    if dtype == "f32" or f64_ieee or w.p > 4:
+        peak = FP64_PEAK_TFLOPS if dtype == "f64" else FP32_PEAK_TFLOPS
+        return {"kernel": "k_m2l" if dtype == "f32" else "k_m2l<double>", "bound": "alu", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "flops_per_pair": per_pair,
+                "pairs": pairs, "ms": ms}
+    out = df_pipe_roofline("k_m2l_df", pairs, ms)
+    out.update({"ms": ms, "pairs": pairs, "fp64_equivalent_tflops": achieved, "flops_per_pair": per_pair})
+    return out
 
 
 def main():
@@ -452,7 +545,7 @@ def main():
     ap.add_argument("--workload", default="clustered_2p20_f32")
     ap.add_argument("--cpu-sample", type=int, default=1 << 20)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
-    ap.add_argument("--no-also", action="store_true", help="skip the secondary N=1e5 fp64 point")
+    ap.add_argument("--no-also", action="store_true", help="skip the secondary points (other configs, KDK)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     args = ap.parse_args()
     rank, world, local_rank = env_rank()

@@ -191,6 +191,7 @@ void destroy_plan(Plan &P)
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
     dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
+    dfree(P.vjp_acc); dfree(P.vjp_src); dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
     if (P.ctr_host) cudaFreeHost(P.ctr_host);
     for (int i = 0; i < kNumEvents; ++i)
         if (P.ev[i]) cudaEventDestroy(P.ev[i]);
@@ -556,6 +557,61 @@ fmm_status fmm_kdk_step_lattice(fmm_plan *plan, void *pos, void *vel, const void
 void fmm_kdk_reset(fmm_plan *plan)
 {
     if (plan) plan->P.cache_valid = false;
+}
+
+fmm_status fmm_plan_set_f64_ieee(fmm_plan *plan, int on)
+{
+    g_err.clear();
+    if (!plan) { set_err("fmm_plan_set_f64_ieee: NULL plan"); return FMM_ERR_INVALID_ARG; }
+    if (plan->P.dtype != FMM_F64 && on) {
+        set_err("fmm_plan_set_f64_ieee: only fp64 plans have a double-float mode to switch off");
+        return FMM_ERR_INVALID_ARG;
+    }
+    plan->P.f64_ieee = on != 0;
+    plan->P.cache_valid = false;
+    return FMM_OK;
+}
+
+fmm_status fmm_vjp(fmm_plan *plan, const void *pos, const void *mass, const void *acc_bar, const void *pot_bar,
+                   void *pos_bar, void *mass_bar, void *stream)
+{
+    g_err.clear();
+    if (!plan || !pos || !mass || !acc_bar || !pos_bar || !mass_bar) {
+        set_err("fmm_vjp: plan, pos, mass, acc_bar, pos_bar and mass_bar must be non-NULL");
+        return FMM_ERR_INVALID_ARG;
+    }
+    Plan &P = plan->P;
+    DeviceGuard g(P.device);
+    cudaStream_t s = (cudaStream_t)stream;
+    P.cache_valid = false;
+    const size_t e = (size_t)P.esize, n = (size_t)P.n;
+    if (!P.vjp_acc) {
+        CUDA_TRY(cudaMalloc(&P.vjp_acc, 3 * n * e));
+        CUDA_TRY(cudaMalloc(&P.vjp_src, 4 * n * e));
+    }
+    // the forward evaluation: tree, lists, complete locals and accelerations
+    fmm_status st = eval_device(P, pos, mass, P.vjp_acc, nullptr, s);
+    if (st) return st;
+    const int fwd_launches = P.launches;
+    if (P.vjp_cap_nodes < P.cap_nodes) {
+        dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
+        P.Ms = P.Lsm = P.Ls = nullptr;
+        P.vjp_cap_nodes = 0;
+        const size_t bytes = (size_t)P.cap_nodes * P.ncp * e;
+        CUDA_TRY(cudaMalloc(&P.Ms, bytes));
+        CUDA_TRY(cudaMalloc(&P.Lsm, bytes));
+        CUDA_TRY(cudaMalloc(&P.Ls, bytes));
+        P.vjp_cap_nodes = P.cap_nodes;
+    }
+    const int vjp_launches = launch_vjp(P, acc_bar, pot_bar, pos_bar, mass_bar, s);
+    st = sync_counters(P, s);
+    if (st) return st;
+    if (P.ctr_host->error) {
+        set_err("fmm_vjp: device check failed: %s", error_bits(P.ctr_host->error));
+        return FMM_ERR_INTERNAL;
+    }
+    P.launches = fwd_launches + vjp_launches;
+    return FMM_OK;
 }
 
 void fmm_destroy(fmm_plan *plan)

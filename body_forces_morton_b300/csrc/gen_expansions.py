@@ -10,6 +10,11 @@ functions templated on the real type (float / double):
        l r^2 D^n = -(2l-1) sum_i n_i R_i D^{n-e_i} - (l-1) sum_i n_i(n_i-1) D^{n-2e_i}
   l2l  Lc_k += sum_{j>=k} Lp_j e^{j-k} / (j-k)!               (downward translation)
   l2p  phi = sum_k L_k x^k/k!,  a = -sum_k L_{k+e_a} x^k/k!   (Taylor eq.)
+  p2m_dip   M_n += q s^n/n! + sum_a d_a s^{n-e_a}/(n-e_a)!     (sources of the
+            FMM VJP: monopole q and dipole d; JZ-FMM page, "Differentiating
+            the force calculation")
+  l2p_hess  H_ab += sum_{|k|<=P-2} L_{k+e_a+e_b} x^k/k!        (the next higher
+            derivative of the local series, for the same VJP)
 
 Every index is a compile-time constant, so the coefficient arrays of the
 callers live in registers. Coefficient order: graded by total degree; within
@@ -369,6 +374,55 @@ def gen_l2p(p):
     return b
 
 
+def gen_p2m_dip(p):
+    """Moments of one source with monopole q and dipole (dx, dy, dz) at offset s:
+    M_n += q s^n / n! + sum_a d_a s^{n - e_a} / (n - e_a)! (the FMM VJP's sources)."""
+    b = ["template <class T> static __device__ __forceinline__ void p2m_dip(T sx, T sy, T sz, T q, T dx, T dy, T dz,"
+         " T* M) {"]
+    if p == 0:
+        b.append("  (void)sx; (void)sy; (void)sz; (void)dx; (void)dy; (void)dz;")
+    b += ["  " + l for l in scaled_coords(p, "s", "sx", "sy", "sz")]
+    b += ["  " + l for l in mono_recurrence(p, None, "s", "t")]
+    for n in table(p):
+        terms = [f"q * t[{idx(n)}]"]
+        for a, d in zip(range(3), ("dx", "dy", "dz")):
+            if n[a] >= 1:
+                m = list(n)
+                m[a] -= 1
+                terms.append(f"{d} * t[{idx(tuple(m))}]")
+        b.append(f"  M[{idx(n)}] += " + " + ".join(terms) + ";")
+    b.append("}")
+    return b
+
+
+def gen_l2p_hess(p):
+    """Hessian (xx, xy, xz, yy, yz, zz) of the local series at offset (dx, dy, dz), added to H:
+    d_a d_b Phi = sum_{|k| <= p - 2} L_{k + e_a + e_b} dx^k / k!."""
+    b = ["template <class T> static __device__ __forceinline__ void l2p_hess(const T* L, T dx, T dy, T dz, T* H) {"]
+    if p < 2:
+        b.append("  (void)L; (void)dx; (void)dy; (void)dz; (void)H;")
+        b.append("}")
+        return b
+    q = p - 2
+    if q > 0:
+        b += ["  " + l for l in scaled_coords(q, "x", "dx", "dy", "dz")]
+        b += ["  " + l for l in mono_recurrence(q, None, "x", "u")]
+    else:
+        b.append("  (void)dx; (void)dy; (void)dz;")
+        b.append("  T u[1]; u[0] = T(1);")
+    pairs = [(0, 0), (0, 1), (0, 2), (1, 1), (1, 2), (2, 2)]
+    for h, (a1, a2) in enumerate(pairs):
+        terms = []
+        for k in table(q):
+            m = list(k)
+            m[a1] += 1
+            m[a2] += 1
+            terms.append(f"L[{idx(tuple(m))}] * u[{idx(k)}]")
+        b.append(f"  H[{h}] += " + " + ".join(terms) + ";")
+    b.append("}")
+    return b
+
+
 MAXP_DF = 4
 
 
@@ -494,7 +548,7 @@ def main():
         out.append(f"  static constexpr int NC = {ncoef(p)};")
         out.append(f"  static constexpr int NRC = {(p + 1) ** 2};  // reduced (n_z <= 1) coefficients")
         for gen in (gen_p2m, gen_m2m, gen_m2l, gen_l2l, gen_l2p, gen_reduce_m, gen_expand_l, gen_m2l_r,
-                    gen_m2l_r_pair):
+                    gen_m2l_r_pair, gen_p2m_dip, gen_l2p_hess):
             out += ["  " + l for l in gen(p)]
         out.append("};")
         out.append("")

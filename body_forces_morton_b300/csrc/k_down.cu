@@ -549,19 +549,25 @@ int launch_l2l(Plan &P, int depth, cudaStream_t s)
 int launch_l2p(Plan &P, cudaStream_t s)
 {
     if (P.dtype == 0) return launch_l2p_t<float>(P, s);
-    return P.p <= kMaxPL2pDf ? launch_l2p_df(P, s) : launch_l2p_t<double>(P, s);
+    return P.p <= kMaxPL2pDf && !P.f64_ieee ? launch_l2p_df(P, s) : launch_l2p_t<double>(P, s);
 }
 
-// fp32 plans: k_p2p; fp64 plans: the double-float near field (k_p2p_df.cu)
+// fp32 plans: k_p2p<float>; fp64 plans: the double-float near field (k_p2p_df.cu), or k_p2p<double> in
+// IEEE fp64 when the plan asks for it
+template <class T>
+int launch_p2p_t(Plan &P, void *acc, void *pot, cudaStream_t s)
+{
+    k_p2p<T><<<P.num_sms * 16, LF_WARPS * 32, 0, s>>>(P.ctr, P.p2p_items, P.p2p_done, P.ctr, P.node_first,
+                                                      P.node_count, P.node_nchild, (const vec4<T> *)P.xyzm, P.idx[0],
+                                                      (const vec4<T> *)P.far, (vec4<T> *)P.far, P.p2p_off, P.p2p_src,
+                                                      (T *)acc, (T *)pot);
+    return 1;
+}
+
 int launch_p2p(Plan &P, void *acc, void *pot, cudaStream_t s)
 {
-    if (P.dtype == 1) return launch_p2p_df(P, acc, pot, s);
-    k_p2p<float><<<P.num_sms * 16, LF_WARPS * 32, 0, s>>>(P.ctr, P.p2p_items, P.p2p_done, P.ctr, P.node_first,
-                                                          P.node_count, P.node_nchild, (const vec4<float> *)P.xyzm,
-                                                          P.idx[0], (const vec4<float> *)P.far, (vec4<float> *)P.far,
-                                                          P.p2p_off, P.p2p_src,
-                                                          (float *)acc, (float *)pot);
-    return 1;
+    if (P.dtype == 0) return launch_p2p_t<float>(P, acc, pot, s);
+    return P.f64_ieee ? launch_p2p_t<double>(P, acc, pot, s) : launch_p2p_df(P, acc, pot, s);
 }
 
 }  // namespace bfm

@@ -181,7 +181,7 @@ int launch_m2l_t(Plan &P, const void *M, void *Lout, cudaStream_t s)
 int launch_m2l(Plan &P, cudaStream_t s)
 {
     if (P.dtype == 0) return launch_m2l_t<float>(P, P.M, P.Lm2l, s);
-    return P.p <= kMaxPDf ? launch_m2l_df(P, s) : launch_m2l_t<double>(P, P.M, P.Lm2l, s);
+    return P.p <= kMaxPDf && !P.f64_ieee ? launch_m2l_df(P, s) : launch_m2l_t<double>(P, P.M, P.Lm2l, s);
 }
 
 int launch_m2l_plain(Plan &P, const void *M, void *Lout, cudaStream_t s)

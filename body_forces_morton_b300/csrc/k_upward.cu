@@ -163,7 +163,7 @@ __global__ __launch_bounds__(256, 2) void k_upward_ticket(const DevCounters *__r
                                                 const int *__restrict__ first, const int *__restrict__ count,
                                                 const int *__restrict__ child0, const int *__restrict__ nchild,
                                                 const int *__restrict__ parent, int *done, T *node_lo, T *node_hi,
-                                                vec4<T> *nc, vec4<T> *nl, T *M, int ncp)
+                                                vec4<T> *nc, vec4<T> *nl, T *M, int ncp, bool use_df)
 {
     const int n_nodes = phase2_nodes(nctr);
     constexpr int NC = Exp<P>::NC;
@@ -188,7 +188,7 @@ __global__ __launch_bounds__(256, 2) void k_upward_ticket(const DevCounters *__r
                 hi[k] = tmax(hi[k], __shfl_xor_sync(kFull, hi[k], o));
             }
         store_geometry<T>(a, lo, hi, node_lo, node_hi, nc, nl, cen, lane == 0);
-        if constexpr (sizeof(T) == 8 && P <= kMaxPL2pDf) {
+        if (sizeof(T) == 8 && P <= kMaxPL2pDf && use_df) {
             // P2M in double-float, in the leaf's own power-of-two units: lengths in 2^eh >= its
             // largest half-width, masses in 2^em >= its mass (the FP64 pipe only forms the offsets)
             T msum = T(0);
@@ -273,7 +273,7 @@ int launch_upward_tp(Plan &P_, cudaStream_t s)
         k_upward_ticket<T, P><<<P_.num_sms * 8, 256, 0, s>>>(
             P_.ctr, (const vec4<T> *)P_.xyzm, P_.node_first, P_.node_count, P_.node_child0, P_.node_nchild,
             P_.node_parent, P_.node_done, (T *)P_.node_lo, (T *)P_.node_hi, (vec4<T> *)P_.node_c,
-            (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp);
+            (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp, !P_.f64_ieee);
         return 1;
     } else {
         const unsigned seq = P_.next_flag_seq(s);

@@ -22,6 +22,7 @@ struct Plan {
     double theta = 0.7;
     int leaf = 32;
     int dtype = 0;      // 0 f32, 1 f64
+    bool f64_ieee = false;  // fp64 plans: every stage in IEEE fp64 (default: the ALU-bound stages in double-float)
     int esize = 4;      // bytes per real
     int device = 0;
     int num_sms = 148;
@@ -80,6 +81,12 @@ struct Plan {
     // host-buffer staging (fmm_eval_host), allocated on first use
     void *h_pos = nullptr, *h_mass = nullptr, *h_acc = nullptr, *h_pot = nullptr;
 
+    // VJP (fmm_vjp), allocated on first use: the forward accelerations (caller's order), the sources
+    // (pbar, -abar) in the tree's order, and the source moments, M2L locals and complete locals
+    void *vjp_acc = nullptr, *vjp_src = nullptr;
+    void *Ms = nullptr, *Lsm = nullptr, *Ls = nullptr;
+    int64_t vjp_cap_nodes = 0;
+
     // KDK acceleration cache, caller's order
     void *acc_cache = nullptr;
     bool cache_valid = false;
@@ -115,6 +122,8 @@ int launch_walk(Plan &P, int depth, cudaStream_t s);
 int launch_lists(Plan &P, cudaStream_t s);
 int launch_m2l(Plan &P, cudaStream_t s);
 int launch_m2l_df(Plan &P, cudaStream_t s);  // fp64 plans, p <= kMaxPDf
+int launch_m2l_plain(Plan &P, const void *M, void *Lout, cudaStream_t s);  // plain arithmetic, given buffers
+int launch_vjp(Plan &P, const void *abar, const void *pbar, void *pos_bar, void *mass_bar, cudaStream_t s);
 constexpr int kMaxPDf = 4;
 int launch_l2l(Plan &P, int depth, cudaStream_t s);
 int launch_l2p(Plan &P, cudaStream_t s);

@@ -159,6 +159,40 @@ fmm_status fmm_kdk_step(fmm_plan *plan, void *pos, void *vel, const void *mass, 
 fmm_status fmm_kdk_step_lattice(fmm_plan *plan, void *pos, void *vel, const void *mass, double dt, int pos_exp,
                                 int vel_exp, void *stream);
 
+/*
+ * Arithmetic of an fp64 plan. By default (on = 0) the ALU-bound stages of an
+ * fp64 plan -- M2L for p <= 4, L2P and the leaf P2M for p <= 6, and P2P --
+ * compute in double-float (pairs of fp32 values, about 48 significant bits) on
+ * the FP32 pipe, because the B300's FP64 rate is about 1/64 of its FP32 rate;
+ * the results stay within 1e-12 of the fp64 oracle. on = 1 runs every stage in
+ * IEEE fp64 instead (slower; the pages' own precision). Applies to the next
+ * evaluation. FMM_ERR_INVALID_ARG for a NULL plan or on = 1 on an fp32 plan.
+ */
+fmm_status fmm_plan_set_f64_ieee(fmm_plan *plan, int on);
+
+/*
+ * Vector-Jacobian product of one evaluation (JZ-FMM page, "Differentiating the
+ * force calculation": one contribution from the next higher derivative of the
+ * original evaluation, one from an FMM with the force sensitivities acting as
+ * dipole moments). For the loss l = sum_i acc_bar_i . a_i + pot_bar_i phi_i it
+ * writes pos_bar = dl/dx [n x 3] and mass_bar = dl/dm [n]:
+ *     pos_bar_k  = m_k grad Phi_s(x_k) - Hess Phi(x_k) acc_bar_k - pot_bar_k a_k
+ *     mass_bar_k = Phi_s(x_k),
+ * Phi the forward potential, Phi_s the potential of sources at every particle
+ * with monopole pot_bar_j and dipole -acc_bar_j (self terms omitted), both on the
+ * forward evaluation's tree, centres and lists: the exact derivatives of the
+ * evaluation with the tree and the expansion centres held fixed (moving a
+ * particle that bounds a node's box also moves that node's centre, which this
+ * does not differentiate; the effect is of the order of the FMM's error).
+ * Arguments are DEVICE arrays in the plan's dtype and the caller's particle
+ * order; pot_bar may be NULL (zero). The call runs the forward evaluation
+ * first (it does not reuse an earlier one), allocates the plan's VJP buffers on
+ * first use, blocks until done and returns FMM_ERR_INTERNAL if a device check
+ * failed. It invalidates the kick-drift-kick acceleration cache.
+ */
+fmm_status fmm_vjp(fmm_plan *plan, const void *pos, const void *mass, const void *acc_bar, const void *pot_bar,
+                   void *pos_bar, void *mass_bar, void *stream);
+
 /* Drop the cached acceleration of fmm_kdk_step (the next step evaluates it afresh). */
 void fmm_kdk_reset(fmm_plan *plan);
 

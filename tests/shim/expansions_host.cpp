@@ -30,6 +30,8 @@ static void run(int op, const T* a, const T* v, T* out)
         Exp<P>::template expand_l<T>(Lr, out);
         break;
     }
+    case 7: Exp<P>::template p2m_dip<T>(v[0], v[1], v[2], v[3], v[4], v[5], v[6], out); break;  // s, q, d
+    case 8: Exp<P>::template l2p_hess<T>(a, v[0], v[1], v[2], out); break;
     case 6: {  // both directions of one pair: a = [M_A, M_B], out = [L_A, L_B]
         constexpr int NC = Exp<P>::NC, NRC = Exp<P>::NRC;
         T MA[NRC], MB[NRC], LA[NRC], LB[NRC];

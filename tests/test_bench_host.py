@@ -43,11 +43,36 @@ def test_eval_roofline_sums_the_stage_terms():
     assert 0.1 < r["frac"] < 0.3
 
 
-def test_eval_roofline_fp64_uses_the_fp64_peak():
+def test_eval_roofline_fp64_peaks_follow_the_pipe():
     w = W.WORKLOADS[3]
-    r = bench.eval_roofline(fake_result(100_000, 48_723_340, 1_000_000), w, 2.14, 6500.0, "measured")
-    assert r["peaks"]["alu_tflops"] == bench.FP64_PEAK_TFLOPS
-    assert math.isclose(r["terms_ms"]["p2p_alu"], 48_723_340 * 20 / 1.25e12 * 1e3, rel_tol=1e-12)
+    res = fake_result(100_000, 48_723_340, 1_000_000)
+    # double-float stages run on the FP32 pipe
+    r = bench.eval_roofline(res, w, 2.14, 6500.0, "measured")
+    assert r["peaks"]["alu_tflops"] == bench.FP32_PEAK_TFLOPS
+    # IEEE fp64: the FP64 pipe, 148 SMs x 2 FMA per clock x 2 flop x 2.032 GHz
+    r = bench.eval_roofline(res, w, 2.14, 6500.0, "measured", dtype="f64", f64_ieee=True)
+    assert math.isclose(r["peaks"]["alu_tflops"], 148 * 2 * 2 * 2.032e9 / 1e12, rel_tol=1e-12)
+    assert math.isclose(r["terms_ms"]["p2p_alu"], 48_723_340 * 20 / (148 * 4 * 2.032e9) * 1e3, rel_tol=1e-12)
+
+
+def test_df_roofline_uses_the_fp32_pipe_and_counted_operations():
+    res = {"n": 100_000, "stats": {"n_p2p_interactions": 48_823_340, "n_m2l": 1_833_964},
+           "stage_ms": {"p2p": 0.5, "m2l": 0.4}}
+    w = W.WORKLOADS[3]
+    key = ("k_p2p_df", bench.kernel_source_hash(bench.DF_SOURCES["k_p2p_df"]))
+    saved = dict(bench.DF_FMA_OPS_PER_PAIR)
+    try:
+        bench.DF_FMA_OPS_PER_PAIR.clear()
+        r = bench.p2p_roofline(res, w)
+        assert r["frac"] is None and r["unit"] == "FP32 lane-ops/s"
+        bench.DF_FMA_OPS_PER_PAIR[key] = 100.0
+        r = bench.p2p_roofline(res, w)
+        assert math.isclose(r["achieved"], 100.0 * 48_723_340 / 0.5e-3, rel_tol=1e-12)
+        assert math.isclose(r["frac"], r["achieved"] / (148 * 128 * 2.032e9), rel_tol=1e-12)
+        assert math.isclose(r["fp64_equivalent_tflops"], 20 * 48_723_340 / 0.5e-3 / 1e12, rel_tol=1e-12)
+    finally:
+        bench.DF_FMA_OPS_PER_PAIR.clear()
+        bench.DF_FMA_OPS_PER_PAIR.update(saved)
 
 
 def test_hbm_peak_reads_the_measured_file():

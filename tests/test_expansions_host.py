@@ -66,6 +66,16 @@ def test_generated_operators_match_oracle(shim, p, dtype, rtol):
     got = call(shim, p, 6, np.concatenate([MA, M]), R, 2 * nc, dtype)
     for half, want in ((got[:nc], oracle.m2l(p, M, R)), (got[nc:], oracle.m2l(p, MA, -R))):
         np.testing.assert_allclose(half, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg="pair m2l")
+    # the VJP's operators: a source with monopole q and dipole d, and the local series' Hessian
+    q, dd = 0.4, rng.normal(size=3)
+    got = call(shim, p, 7, np.zeros(1), [*s, q, *dd], nc, dtype)
+    want = oracle.p2m_dipole(p, s[None, :], [q], dd[None, :], np.zeros(3))
+    np.testing.assert_allclose(got, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg="p2m_dip")
+    dxh = rng.normal(size=3) * 0.1
+    got = call(shim, p, 8, M, dxh, 6, dtype)
+    want = oracle.l2p_hess(p, M, dxh)
+    np.testing.assert_allclose(got, want, rtol=rtol, atol=rtol * max(np.abs(want).max(), 1e-300),
+                               err_msg="l2p_hess")
     # L2P
     dx = rng.normal(size=3) * 0.1
     got = call(shim, p, 4, M, dx, 4, dtype)
