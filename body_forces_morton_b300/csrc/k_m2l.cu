@@ -18,14 +18,15 @@
 // One warp per receiver, receivers taken from a shared counter in decreasing
 // order of list length; lane j takes the receiver's sources j, j+32, ... in
 // list order (ascending source index) and keeps a private partial L in
-// registers. Each lane copies its own source's reduced multipole row into
-// shared memory with 16-byte asynchronous copies, one round of 32 sources
-// ahead of the round it computes (double buffer, one copy group per round),
-// and reads it back with 16-byte loads; rows sit an odd number of 16-byte
-// units apart, so the lanes' reads of their own rows are free of bank
-// conflicts. No lane touches another lane's row, so the pipeline needs no
-// warp synchronisation. A fixed reduction sums the lanes, so the result is
-// reproducible.
+// registers. The reduced multipole rows of a round's 32 sources are copied
+// into shared memory with 16-byte asynchronous copies one round ahead of the
+// round that uses them (double buffer, one copy group per round), coalesced:
+// a group of NV lanes streams one row (NV 16-byte pieces), so one copy
+// instruction reads whole rows instead of 32 scattered 16-byte pieces (those
+// kept the L1 at ~90 % of its request throughput). Each lane then reads its
+// own source's row back with 16-byte loads; rows sit an odd number of 16-byte
+// units apart, so these reads are free of bank conflicts. A fixed reduction
+// sums the lanes, so the result is reproducible.
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -98,19 +99,33 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__res
     using S = M2LShape<T, P>;
     extern __shared__ __align__(16) unsigned char m2l_smem[];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    T *const slot = reinterpret_cast<T *>(m2l_smem) + (size_t)w * 2 * 32 * S::STR + lane * S::STR;  // buffer 0
-    T *const slot1 = slot + 32 * S::STR;                                                                 // buffer 1
+    T *const rows0 = reinterpret_cast<T *>(m2l_smem) + (size_t)w * 2 * 32 * S::STR;  // buffer 0
+    T *const rows1 = rows0 + 32 * S::STR;                                               // buffer 1
+    T *const slot = rows0 + lane * S::STR, *const slot1 = rows1 + lane * S::STR;        // this lane's row
     T *lred = reinterpret_cast<T *>(m2l_smem) + (size_t)M2L_WARPS * 2 * 32 * S::STR + (size_t)w * S::NRC;
-    // copy source q's row (if q is in the list) into dst; returns its centre
-    auto stage = [&](int q, int end, T *dst, bool &valid) {
+    // the copy layout: G rows per copy instruction, row r = r0 + g streamed by lanes g NV .. g NV + NV - 1
+    // (rows longer than 32 pieces take CPR passes of all 32 lanes)
+    constexpr int G = S::NV <= 32 ? 32 / S::NV : 1;
+    constexpr int CPR = S::NV <= 32 ? 1 : (S::NV + 31) / 32;
+    const int g = S::NV <= 32 ? lane / S::NV : 0;
+    const int c0 = S::NV <= 32 ? lane - g * S::NV : lane;
+    // copy the rows of sources q0 .. q0 + 31 (those in the list) into the buffer at rows0;
+    // returns this lane's source centre
+    auto stage = [&](int q0, int end, T *rows0, bool &valid) {
+        const int q = q0 + lane;
         valid = q < end;
-        vec4<T> cb = make4<T>(T(0), T(0), T(0), T(0));
-        if (valid) {
-            const int b = src[q];
-            cb = nc[b];
-            const T *g = Mr + (size_t)b * S::NRP;
+        const int b = valid ? src[q] : -1;
+        const vec4<T> cb = valid ? nc[b] : make4<T>(T(0), T(0), T(0), T(0));
 #pragma unroll
-            for (int c = 0; c < S::NV; ++c) cp_async16(dst + c * S::V, g + c * S::V);
+        for (int r0 = 0; r0 < 32; r0 += G) {
+            const int r = r0 + g;
+            const int br = __shfl_sync(kFull, b, r & 31);
+            if (g < G && r < 32 && br >= 0)
+#pragma unroll
+                for (int cc = 0; cc < CPR; ++cc) {
+                    const int c = c0 + cc * 32;
+                    if (c < S::NV) cp_async16(rows0 + r * S::STR + c * S::V, Mr + (size_t)br * S::NRP + c * S::V);
+                }
         }
         cp_async_commit();
         return cb;
@@ -127,12 +142,14 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__res
 #pragma unroll
         for (int k = 0; k < S::NR; ++k) L[k] = T(0);
         bool valid;
-        vec4<T> cb = stage(beg + lane, end, slot, valid);
+        vec4<T> cb = stage(beg, end, rows0, valid);
         int cur = 0;
         for (int q0 = beg; q0 < end; q0 += 32) {
             bool valid_n;
-            const vec4<T> cb_n = stage(q0 + 32 + lane, end, cur ? slot : slot1, valid_n);
-            cp_async_wait_group<1>();  // this lane's copies of the current round have landed
+            __syncwarp();  // every lane is done with the buffer the next round's rows go to
+            const vec4<T> cb_n = stage(q0 + 32, end, cur ? rows0 : rows1, valid_n);
+            cp_async_wait_group<1>();  // this lane's copies of the current round have landed,
+            __syncwarp();              // and so have every other lane's
             if (valid) m2l_apply_row<T, P>(cur ? slot1 : slot, ca, cb, L);
             valid = valid_n;
             cb = cb_n;
