@@ -17,6 +17,7 @@ sample of the same workload on this machine's host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import gc
 import hashlib
 import json
@@ -274,7 +275,8 @@ def bench_reversibility(torch, native, steps=20, dt=1e-3):
     return out
 
 
-def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_override=None, dtype=None, f64_ieee=False):
+def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_override=None, dtype=None, f64_ieee=False,
+                   m2l_rotation=False):
     """Times `steps` evaluations; returns dict with per-step ms, stage ms, stats."""
     n = n_override or w.n
     dtype = dtype or w.dtype
@@ -284,7 +286,7 @@ def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_overrid
     mass = torch.from_numpy(g["mass"]).to("cuda", tdt)
     acc = torch.empty_like(pos)
     pot = torch.empty_like(mass)
-    plan = native.Plan(n, w.p, w.theta, w.leaf, dtype, f64_ieee=f64_ieee)
+    plan = native.Plan(n, w.p, w.theta, w.leaf, dtype, f64_ieee=f64_ieee, m2l_rotation=m2l_rotation)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             plan.eval(pos, mass, acc, pot, stream=stream)
@@ -364,9 +366,9 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_also:
         n_also = max(3, args.steps // 2)
 
-        def leg(w, name, n=None, dtype=None, f64_ieee=False, roofs=False):
+        def leg(w, name, n=None, dtype=None, f64_ieee=False, roofs=False, m2l_rotation=False):
             r = bench_workload(w, n_also, args.warmup, torch, native, stream, flush_buf, n_override=n, dtype=dtype,
-                               f64_ieee=f64_ieee)
+                               f64_ieee=f64_ieee, m2l_rotation=m2l_rotation)
             ms = float(np.median(r["step_ms"]))  # median: a rare driver stall of ~3 ms would skew a short mean
             dt = dtype or w.dtype
             d = {"value": r["n"] / (ms / 1e3), "unit": "particles/s", "ms_per_step": ms, "n": r["n"], "dtype": dt,
@@ -374,7 +376,8 @@ def run_ours(args, rank, world, local_rank):
                  "p": w.p, "theta": w.theta, "leaf": w.leaf, "stage_ms": r["stage_ms"],
                  "counts": {k: r["stats"][k] for k in ("n_nodes", "n_m2l", "n_p2p_interactions")}}
             if dt == "f64":
-                d["arith"] = F64_IEEE_ARITH if f64_ieee else F64_ARITH
+                d["arith"] = F64_IEEE_ARITH if f64_ieee or m2l_rotation else F64_ARITH
+            d["m2l_operator"] = "rotation (solid harmonics)" if m2l_rotation else "reduced Cartesian"
             if roofs:
                 d["roofline"] = p2p_roofline(r, w, dt, f64_ieee)
                 d["m2l_roofline"] = m2l_roofline(r, w, dt, f64_ieee)
@@ -389,6 +392,11 @@ def run_ours(args, rank, world, local_rank):
         leg(W.WORKLOADS[2], W.WORKLOADS[2].name)
         leg(w, "clustered_1e6_f32", n=1000000, dtype="f32")
         leg(w, "clustered_1e6_f64", n=1000000, dtype="f64")
+        # the two M2L operators (same result): p = 4 at the default workload, p = 8 on the Plummer recipe
+        leg(w, w.name + "_m2l_rotation", m2l_rotation=True)
+        w3p8 = dataclasses.replace(w3, name="plummer_1e5_f32_p8", p=8, dtype="f32")
+        leg(w3p8, w3p8.name)
+        leg(w3p8, w3p8.name + "_m2l_rotation", m2l_rotation=True)
         w5 = W.WORKLOADS[5]
         also[w5.name] = bench_kdk(w5, torch, native, stream)
         also["kdk_reversibility_2p18_f64"] = bench_reversibility(torch, native)

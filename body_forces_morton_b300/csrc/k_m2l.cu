@@ -29,6 +29,7 @@
 // sums the lanes, so the result is reproducible.
 #include "expansions_gen.cuh"
 #include "plan.h"
+#include "rotation_gen.cuh"
 
 namespace bfm {
 
@@ -54,8 +55,35 @@ template <class T, int P> struct M2LShape {
     static constexpr size_t smem = sizeof(T) * M2L_WARPS * (2 * 32 * STR + NRC);
 };
 
-// Reduced moments of every node: Mr[b] = reduce_m(M[b]), padding zeroed.
-template <class T, int P>
+// The two M2L operators on rows of (p+1)^2 coefficients: `prep` turns a node's
+// moments into its row, `pair` adds one source row's translation to a
+// receiver's accumulators, `finish` turns the accumulators into the complete
+// Cartesian local. The results are the same (the total-degree truncation);
+// the per-pair work differs.
+//   OpReduced:  the reduced (trace-free) Cartesian contraction, D^n(R) built
+//               by recurrence (the default);
+//   OpRotation: real solid harmonics, each pair rotated so that R lies on z,
+//               translated along z and rotated back (jaccpot issue 152, item
+//               1: the rotations built on chip from the separation).
+template <int P> struct OpReduced {
+    template <class T> static __device__ __forceinline__ void prep(const T *M, T *r) { Exp<P>::template reduce_m<T>(M, r); }
+    template <class T> static __device__ __forceinline__ void pair(const T *r, T rx, T ry, T rz, T *L)
+    {
+        Exp<P>::template m2l_r<T>(r, rx, ry, rz, L);
+    }
+    template <class T> static __device__ __forceinline__ void finish(const T *l, T *L) { Exp<P>::template expand_l<T>(l, L); }
+};
+template <int P> struct OpRotation {
+    template <class T> static __device__ __forceinline__ void prep(const T *M, T *r) { Rot<P>::template to_sph<T>(M, r); }
+    template <class T> static __device__ __forceinline__ void pair(const T *r, T rx, T ry, T rz, T *L)
+    {
+        Rot<P>::template m2l<T>(r, rx, ry, rz, L);
+    }
+    template <class T> static __device__ __forceinline__ void finish(const T *l, T *L) { Rot<P>::template from_sph<T>(l, L); }
+};
+
+// Rows of every node: Mr[b] = prep(M[b]), padding zeroed.
+template <class T, int P, class Op>
 __global__ __launch_bounds__(256) void k_moments_r(const DevCounters *__restrict__ nctr, const T *__restrict__ M, T *__restrict__ Mr)
 {
     const int n_nodes = phase2_nodes(nctr);
@@ -64,7 +92,7 @@ __global__ __launch_bounds__(256) void k_moments_r(const DevCounters *__restrict
         T r[S::NRP];
 #pragma unroll
         for (int i = S::NRC; i < S::NRP; ++i) r[i] = T(0);
-        Exp<P>::template reduce_m<T>(M + (size_t)b * S::NCP, r);
+        Op::template prep<T>(M + (size_t)b * S::NCP, r);
 #pragma unroll
         for (int i = 0; i < S::NRP; ++i) Mr[(size_t)b * S::NRP + i] = r[i];
     }
@@ -72,7 +100,7 @@ __global__ __launch_bounds__(256) void k_moments_r(const DevCounters *__restrict
 
 // One source of the current round: its reduced row (in this lane's shared
 // slot) translated to the receiver's centre ca and added to L.
-template <class T, int P>
+template <class T, int P, class Op>
 __device__ __forceinline__ void m2l_apply_row(const T *row, const vec4<T> &ca, const vec4<T> &cb,
                                               T (&L)[M2LShape<T, P>::NR])
 {
@@ -82,13 +110,13 @@ __device__ __forceinline__ void m2l_apply_row(const T *row, const vec4<T> &ca, c
         T m[S::NRP];
 #pragma unroll
         for (int c = 0; c < S::NV; ++c) *reinterpret_cast<V16 *>(m + c * S::V) = reinterpret_cast<const V16 *>(row)[c];
-        Exp<P>::template m2l_r<T>(m, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
+        Op::template pair<T>(m, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
     } else {
-        Exp<P>::template m2l_r<T>(row, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
+        Op::template pair<T>(row, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L);
     }
 }
 
-template <class T, int P>
+template <class T, int P, class Op>
 __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__restrict__ nctr, const int *__restrict__ order,
                                                         const int *__restrict__ off,
                                                         const int *__restrict__ src, const vec4<T> *__restrict__ nc,
@@ -150,7 +178,7 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__res
             const vec4<T> cb_n = stage(q0 + 32, end, cur ? rows0 : rows1, valid_n);
             cp_async_wait_group<1>();  // this lane's copies of the current round have landed,
             __syncwarp();              // and so have every other lane's
-            if (valid) m2l_apply_row<T, P>(cur ? slot1 : slot, ca, cb, L);
+            if (valid) m2l_apply_row<T, P, Op>(cur ? slot1 : slot, ca, cb, L);
             valid = valid_n;
             cb = cb_n;
             cur ^= 1;
@@ -158,23 +186,30 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__res
         cp_async_wait_all();
         reduce_apply<T, S::NR, S::NRC>(L, lane, [&](int k, const T &x) { lred[k] = x; });
         __syncwarp();
-        if (lane == 0) Exp<P>::template expand_l<T>(lred, Lout + (size_t)a * S::NCP);
+        if (lane == 0) Op::template finish<T>(lred, Lout + (size_t)a * S::NCP);
         __syncwarp();
     }
+}
+
+template <class T, int P, class Op>
+int launch_m2l_op(Plan &P_, const void *M, void *Lout, cudaStream_t s)
+{
+    using S = M2LShape<T, P>;
+    static_assert(S::NRP % S::V == 0, "row stride must be a whole number of 16-byte loads");
+    static_assert(S::smem <= 227 * 1024, "M2L staging exceeds shared memory");
+    k_moments_r<T, P, Op><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)M, (T *)P_.Mr);
+    cudaFuncSetAttribute(k_m2l<T, P, Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::smem);
+    k_m2l<T, P, Op><<<P_.num_sms * 16, M2L_WARPS * 32, S::smem, s>>>(
+        P_.ctr, P_.order + P_.cap_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
+        (const T *)P_.Mr, (T *)Lout, P_.ctr);
+    return 2;
 }
 
 template <class T, int P>
 int launch_m2l_tp(Plan &P_, const void *M, void *Lout, cudaStream_t s)
 {
-    using S = M2LShape<T, P>;
-    static_assert(S::NRP % S::V == 0, "row stride must be a whole number of 16-byte loads");
-    static_assert(S::smem <= 227 * 1024, "M2L staging exceeds shared memory");
-    k_moments_r<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)M, (T *)P_.Mr);
-    cudaFuncSetAttribute(k_m2l<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::smem);
-    k_m2l<T, P><<<P_.num_sms * 16, M2L_WARPS * 32, S::smem, s>>>(
-        P_.ctr, P_.order + P_.cap_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
-        (const T *)P_.Mr, (T *)Lout, P_.ctr);
-    return 2;
+    return P_.m2l_rotation ? launch_m2l_op<T, P, OpRotation<P>>(P_, M, Lout, s)
+                           : launch_m2l_op<T, P, OpReduced<P>>(P_, M, Lout, s);
 }
 
 template <class T>
@@ -198,7 +233,8 @@ int launch_m2l_t(Plan &P, const void *M, void *Lout, cudaStream_t s)
 int launch_m2l(Plan &P, cudaStream_t s)
 {
     if (P.dtype == 0) return launch_m2l_t<float>(P, P.M, P.Lm2l, s);
-    return P.p <= kMaxPDf && !P.f64_ieee ? launch_m2l_df(P, s) : launch_m2l_t<double>(P, P.M, P.Lm2l, s);
+    return P.p <= kMaxPDf && !P.f64_ieee && !P.m2l_rotation ? launch_m2l_df(P, s)
+                                                            : launch_m2l_t<double>(P, P.M, P.Lm2l, s);
 }
 
 int launch_m2l_plain(Plan &P, const void *M, void *Lout, cudaStream_t s)

@@ -23,6 +23,7 @@ struct Plan {
     int leaf = 32;
     int dtype = 0;      // 0 f32, 1 f64
     bool f64_ieee = false;  // fp64 plans: every stage in IEEE fp64 (default: the ALU-bound stages in double-float)
+    bool m2l_rotation = false;  // M2L by rotation to the z axis in solid harmonics (default: reduced Cartesian)
     int esize = 4;      // bytes per real
     int device = 0;
     int num_sms = 148;
@@ -67,6 +68,7 @@ struct Plan {
     uint8_t *order_key = nullptr;                  // [2][cap_nodes] work bucket of every node
 
     void *scratch = nullptr;       // 64 KiB for small per-block partials
+    unsigned *rs_counts = nullptr; // radix sort: [256 digits][tiles] digit counts, then output offsets
 
     // chained-scan flags
     unsigned long long *flags = nullptr;

@@ -90,8 +90,9 @@ def lib():
         L.fmm_morton_keys_noalloc.argtypes = [vp, i64, i32, vp, vp, vp]
         L.fmm_vjp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.fmm_plan_set_f64_ieee.argtypes = [vp, i32]
+        L.fmm_plan_set_m2l_rotation.argtypes = [vp, i32]
         for f in ("fmm_eval", "fmm_eval_host", "fmm_kdk_step", "fmm_kdk_step_lattice", "fmm_plan_stats", "fmm_plan_export",
-                  "fmm_morton_keys_noalloc", "fmm_vjp", "fmm_plan_set_f64_ieee"):
+                  "fmm_morton_keys_noalloc", "fmm_vjp", "fmm_plan_set_f64_ieee", "fmm_plan_set_m2l_rotation"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -158,6 +159,10 @@ def fmm_plan_set_f64_ieee(plan, on: bool):
     _check(lib().fmm_plan_set_f64_ieee(plan, 1 if on else 0))
 
 
+def fmm_plan_set_m2l_rotation(plan, on: bool):
+    _check(lib().fmm_plan_set_m2l_rotation(plan, 1 if on else 0))
+
+
 def fmm_vjp(plan, pos, mass, acc_bar, pot_bar, pos_bar, mass_bar, stream=None):
     _check(lib().fmm_vjp(plan, _ptr(pos), _ptr(mass), _ptr(acc_bar), _ptr(pot_bar), _ptr(pos_bar), _ptr(mass_bar),
                          _stream(stream)))
@@ -208,17 +213,19 @@ def fmm_plan_export(plan, what: str, dtype=None) -> np.ndarray:
 class Plan:
     """RAII wrapper: ``with Plan(n, p, theta, leaf, "f32") as pl: pl.eval(pos, mass, acc, pot)``."""
 
-    def __init__(self, n, p=4, theta=0.7, leaf=32, dtype="f32", f64_ieee=False):
+    def __init__(self, n, p=4, theta=0.7, leaf=32, dtype="f32", f64_ieee=False, m2l_rotation=False):
         self.n, self.p, self.theta, self.leaf = int(n), int(p), float(theta), int(leaf)
         self.dtype = dtype
         self.np_dtype = np.float32 if dtype == "f32" else np.float64
         self.handle = fmm_plan_create(n, p, theta, leaf, FMM_F32 if dtype == "f32" else FMM_F64)
-        if f64_ieee:
-            try:
+        try:
+            if f64_ieee:
                 fmm_plan_set_f64_ieee(self.handle, True)
-            except FmmError:
-                self.close()
-                raise
+            if m2l_rotation:
+                fmm_plan_set_m2l_rotation(self.handle, True)
+        except FmmError:
+            self.close()
+            raise
 
     def eval(self, pos, mass, acc_out, pot_out=None, stream=None):
         fmm_eval(self.handle, pos, mass, acc_out, pot_out, stream)

@@ -171,6 +171,22 @@ fmm_status fmm_kdk_step_lattice(fmm_plan *plan, void *pos, void *vel, const void
 fmm_status fmm_plan_set_f64_ieee(fmm_plan *plan, int on);
 
 /*
+ * M2L operator of the plan. on = 0 (default): the reduced (trace-free)
+ * Cartesian contraction, the derivative tensor of 1/r built by recurrence per
+ * pair. on = 1: the rotation-based M2L of jaccpot issue 152 (item 1, "An
+ * on-chip-rotation ... M2L kernel"): in real solid harmonics, each source
+ * multipole is rotated so that the separation lies on the z axis, translated
+ * along z (a translation that only couples equal orders m), and the local is
+ * rotated back, the rotations built on chip from the separation. Both keep
+ * every term of total degree <= p, so they give the same result up to
+ * rounding; the per-pair work differs (O(p^3) here against the reduced
+ * contraction's O(p^4), with larger constants, so the Cartesian form is the
+ * faster one for p <= 8). fp64 plans with rotation run their M2L in IEEE fp64.
+ * Applies to the next evaluation; FMM_ERR_INVALID_ARG for a NULL plan.
+ */
+fmm_status fmm_plan_set_m2l_rotation(fmm_plan *plan, int on);
+
+/*
  * Vector-Jacobian product of one evaluation (JZ-FMM page, "Differentiating the
  * force calculation": one contribution from the next higher derivative of the
  * original evaluation, one from an FMM with the force sensitivities acting as

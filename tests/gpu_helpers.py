@@ -8,7 +8,8 @@ STRUCT_INT = ("node_first", "node_count", "node_child0", "node_nchild", "node_pa
 TOL_ACC = {"f64": 1e-10, "f32": 1e-4}
 
 
-def gpu_eval(pos, mass, p, theta, leaf, want_pot=True, exports=(), plan=None, repeat=1, f64_ieee=False):
+def gpu_eval(pos, mass, p, theta, leaf, want_pot=True, exports=(), plan=None, repeat=1, f64_ieee=False,
+             m2l_rotation=False):
     """One evaluation through fmm_eval on cuda:0; returns (acc, pot, exports, stats)."""
     import torch
 
@@ -17,7 +18,7 @@ def gpu_eval(pos, mass, p, theta, leaf, want_pot=True, exports=(), plan=None, re
     dt = "f32" if pos.dtype == np.float32 else "f64"
     n = len(mass)
     own = plan is None
-    pl = plan or native.Plan(n, p, theta, leaf, dt, f64_ieee=f64_ieee)
+    pl = plan or native.Plan(n, p, theta, leaf, dt, f64_ieee=f64_ieee, m2l_rotation=m2l_rotation)
     try:
         tp = torch.from_numpy(np.ascontiguousarray(pos)).cuda()
         tm = torch.from_numpy(np.ascontiguousarray(mass)).cuda()

@@ -10,6 +10,7 @@ inline float rsqrt_t(float x) { return 1.0f / std::sqrt(x); }
 inline double rsqrt_t(double x) { return 1.0 / std::sqrt(x); }
 }  // namespace bfm
 #include "../../body_forces_morton_b300/csrc/expansions_gen.cuh"
+#include "../../body_forces_morton_b300/csrc/rotation_gen.cuh"
 
 using namespace bfm;
 
@@ -32,6 +33,14 @@ static void run(int op, const T* a, const T* v, T* out)
     }
     case 7: Exp<P>::template p2m_dip<T>(v[0], v[1], v[2], v[3], v[4], v[5], v[6], out); break;  // s, q, d
     case 8: Exp<P>::template l2p_hess<T>(a, v[0], v[1], v[2], out); break;
+    case 9: {  // rotation-based M2L: from_sph(m2l(to_sph(M), R))
+        T Q[Rot<P>::NS], Ls[Rot<P>::NS];
+        for (int i = 0; i < Rot<P>::NS; ++i) Ls[i] = T(0);
+        Rot<P>::template to_sph<T>(a, Q);
+        Rot<P>::template m2l<T>(Q, v[0], v[1], v[2], Ls);
+        Rot<P>::template from_sph<T>(Ls, out);
+        break;
+    }
     case 6: {  // both directions of one pair: a = [M_A, M_B], out = [L_A, L_B]
         constexpr int NC = Exp<P>::NC, NRC = Exp<P>::NRC;
         T MA[NRC], MB[NRC], LA[NRC], LB[NRC];

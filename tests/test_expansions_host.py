@@ -66,6 +66,12 @@ def test_generated_operators_match_oracle(shim, p, dtype, rtol):
     got = call(shim, p, 6, np.concatenate([MA, M]), R, 2 * nc, dtype)
     for half, want in ((got[:nc], oracle.m2l(p, M, R)), (got[nc:], oracle.m2l(p, MA, -R))):
         np.testing.assert_allclose(half, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg="pair m2l")
+    # rotation-based M2L (rotate R onto z, translate along z, rotate back) against the Cartesian M2L,
+    # for a general separation and for separations on the +z and -z axes (azimuth undefined)
+    for Rr in (R, np.array([0.0, 0.0, 1.7]), np.array([0.0, 0.0, -0.9]), np.array([-0.3, 0.0, 0.0])):
+        got = call(shim, p, 9, M, Rr, nc, dtype)
+        want = oracle.m2l(p, M, Rr)
+        np.testing.assert_allclose(got, want, rtol=rtol, atol=rtol * np.abs(want).max(), err_msg=f"rotation m2l {Rr}")
     # the VJP's operators: a source with monopole q and dipole d, and the local series' Hessian
     q, dd = 0.4, rng.normal(size=3)
     got = call(shim, p, 7, np.zeros(1), [*s, q, *dd], nc, dtype)
