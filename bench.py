@@ -244,6 +244,37 @@ def bench_kdk(w, torch, native, stream):
             "window": f"steps {KDK_WARMUP + 1}..{KDK_WARMUP + KDK_STEPS} from the seeded initial state"}
 
 
+def bench_vjp(w, steps, warmup, torch, native, stream):
+    """One fmm_vjp (the forward evaluation it runs first, then the dipole FMM and
+    the leaf terms) per step, particles/s; seeded random cotangents."""
+    g = W.generate(w)
+    tdt = torch.float32 if w.dtype == "f32" else torch.float64
+    pos = torch.from_numpy(g["pos"]).to("cuda", tdt)
+    mass = torch.from_numpy(g["mass"]).to("cuda", tdt)
+    rng = np.random.default_rng(7)
+    abar = torch.from_numpy(rng.normal(size=(w.n, 3))).to("cuda", tdt)
+    pbar = torch.from_numpy(rng.normal(size=w.n)).to("cuda", tdt)
+    xbar = torch.empty_like(pos)
+    mbar = torch.empty_like(mass)
+    ms = []
+    with native.Plan(w.n, w.p, w.theta, w.leaf, w.dtype) as plan, torch.cuda.stream(stream):
+        for _ in range(warmup):
+            plan.vjp(pos, mass, abar, pbar, xbar, mbar, stream=stream)
+        torch.cuda.synchronize()
+        for _ in range(steps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            plan.vjp(pos, mass, abar, pbar, xbar, mbar, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        launches = plan.stats()["launches"]
+    m = float(np.median(ms))
+    return {"value": w.n / (m / 1e3), "unit": "particles/s per VJP (forward evaluation included)", "ms_per_step": m,
+            "dtype": w.dtype, "p": w.p, "theta": w.theta, "leaf": w.leaf, "n": w.n, "launches": launches}
+
+
 def bench_reversibility(torch, native, steps=20, dt=1e-3):
     """Config 5's companion: N = 2^18 fp64, `steps` steps forward then back, with the
     plain floating-point step and with the integer-lattice step; the return error
@@ -353,7 +384,19 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     sampler.start()
     t_wall = time.perf_counter()
-    res = bench_workload(w, args.steps, args.warmup, torch, native, stream, flush_buf)
+    if args.vjp:
+        r = bench_vjp(w, args.steps, args.warmup, torch, native, stream)
+        clocks = sampler.stop()
+        if rank == 0:
+            print(json.dumps({"metric": "FMM VJP particles/s", "value": r["value"], "unit": r["unit"],
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+                              "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator)",
+                              "config": {"workload": w.name, "n": w.n, "p": w.p, "theta": w.theta, "leaf": w.leaf},
+                              "gpu_launches": r["launches"] * args.steps, "clocks": clocks}), flush=True)
+        return
+    res = bench_workload(w, args.steps, args.warmup, torch, native, stream, flush_buf,
+                         m2l_rotation=args.m2l_rotation)
     barrier()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
@@ -400,6 +443,7 @@ def run_ours(args, rank, world, local_rank):
         w5 = W.WORKLOADS[5]
         also[w5.name] = bench_kdk(w5, torch, native, stream)
         also["kdk_reversibility_2p18_f64"] = bench_reversibility(torch, native)
+        also[w.name + "_vjp"] = bench_vjp(w, n_also, args.warmup, torch, native, stream)
 
     e2e = None
     if not args.no_e2e:
@@ -563,6 +607,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--no-also", action="store_true", help="skip the secondary points (other configs, KDK)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--m2l-rotation", action="store_true", help="main leg: the rotation-based M2L")
+    ap.add_argument("--vjp", action="store_true", help="main leg: fmm_vjp (forward evaluation + adjoint) per step")
     args = ap.parse_args()
     rank, world, local_rank = env_rank()
     if args.impl == "reference":

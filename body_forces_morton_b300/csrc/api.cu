@@ -190,7 +190,6 @@ void destroy_plan(Plan &P)
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
     dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar);
-    dfree(P.rs_counts);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     dfree(P.vjp_acc); dfree(P.vjp_src); dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
     if (P.ctr_host) cudaFreeHost(P.ctr_host);
@@ -423,7 +422,6 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
-        !ok(dalloc(P.rs_counts, (size_t)256 * ((nn + 2047) / 2048)), "radix counts") ||
         !ok(dalloc(P.gbar, 2), "grid barriers") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);

@@ -68,7 +68,6 @@ struct Plan {
     uint8_t *order_key = nullptr;                  // [2][cap_nodes] work bucket of every node
 
     void *scratch = nullptr;       // 64 KiB for small per-block partials
-    unsigned *rs_counts = nullptr; // radix sort: [256 digits][tiles] digit counts, then output offsets
 
     // chained-scan flags
     unsigned long long *flags = nullptr;
