@@ -22,11 +22,14 @@
 //                   children (m2m), in a fixed order;
 //   M2L and L2L     the forward kernels on the source moments (plain
 //                   arithmetic in the plan's dtype);
-//   k_vjp_leaf      per leaf, a lane per particle: Phi_s and its gradient from
-//                   the source locals, the forward Hessian from L
-//                   (Exp<P>::l2p_hess), plus the direct terms of every pair in
-//                   the leaf's P2P list, sources staged in shared memory; the
-//                   result combined as above and written in the caller's order.
+//   k_vjp_far       a thread per particle: Phi_s and its gradient from the
+//                   source locals, the forward Hessian from L
+//                   (Exp<P>::l2p_hess), combined with the particle's own
+//                   cotangents into (Phi_s, xbar) of the far field;
+//   k_vjp_near      the P2P lists, with the work items, lane layout, staging and
+//                   chunk order of the forward near field: per pair the direct
+//                   terms of Phi_s, of m_i grad Phi_s and of -Hess Phi abar_i,
+//                   added to the far field and written in the caller's order.
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -34,8 +37,10 @@ namespace bfm {
 
 namespace {
 
-constexpr int VJP_WARPS = 4;
-constexpr int VJP_CH = 64;  // staged source particles per warp
+constexpr int VJP_WARPS = 4;                                                // warps per block of k_vjp_near
+template <class T> struct VjpChunk { static constexpr int value = 128; };  // staged sources per warp
+template <> struct VjpChunk<double> { static constexpr int value = 64; };
+constexpr int kVjpK = 4;                                                    // receivers per lane of k_vjp_near
 
 template <class T>
 __global__ __launch_bounds__(256) void k_vjp_sources(int n, const uint32_t *__restrict__ perm,
@@ -85,88 +90,256 @@ __global__ __launch_bounds__(128) void k_vjp_up(const DevCounters *__restrict__ 
     }
 }
 
-// The leaves: a warp per leaf, a lane per receiving particle (rounds of 32).
+// Far field of the VJP at the leaves' particles, in the sorted order (a warp
+// per leaf, a lane per particle): far = (Phi_s, m_i grad Phi_s - H abar_i -
+// pbar_i a_i) with Phi_s and its gradient from the source locals Ls and the
+// forward Hessian H from the forward locals L.
 template <class T, int P>
-__global__ __launch_bounds__(VJP_WARPS * 32) void k_vjp_leaf(
-    const DevCounters *__restrict__ ctr, const int *__restrict__ first, const int *__restrict__ count,
-    const int *__restrict__ nchild, const vec4<T> *__restrict__ nc, const vec4<T> *__restrict__ xyzm,
-    const vec4<T> *__restrict__ src, const uint32_t *__restrict__ perm, const T *__restrict__ L,
-    const T *__restrict__ Ls, int ncp, const int *__restrict__ off, const int *__restrict__ lsrc,
-    const T *__restrict__ acc_fwd, T *__restrict__ pos_bar, T *__restrict__ mass_bar)
+__global__ __launch_bounds__(256) void k_vjp_far(const DevCounters *__restrict__ ctr, const int *__restrict__ first,
+                                                 const int *__restrict__ count, const int *__restrict__ nchild,
+                                                 const vec4<T> *__restrict__ nc, const vec4<T> *__restrict__ xyzm,
+                                                 const vec4<T> *__restrict__ src, const uint32_t *__restrict__ perm,
+                                                 const T *__restrict__ L, const T *__restrict__ Ls, int ncp,
+                                                 const T *__restrict__ acc_fwd, vec4<T> *__restrict__ far)
 {
-    __shared__ vec4<T> s_x[VJP_WARPS][VJP_CH];
-    __shared__ vec4<T> s_s[VJP_WARPS][VJP_CH];
     const int n_nodes = phase2_nodes(ctr);
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
         if (nchild[a] != 0) continue;
         const int f = first[a], c = count[a];
         const vec4<T> ca = nc[a];
-        const int beg = off[a], end = off[a + 1];
-        for (int r0 = 0; r0 < c; r0 += 32) {
-            const int i = f + r0 + lane;
-            const bool mine = r0 + lane < c;
-            const vec4<T> xi = xyzm[mine ? i : f];
+        for (int i = f + lane; i < f + c; i += 32) {
+            const vec4<T> xi = xyzm[i], si = src[i];
             const T dx = xi.x - ca.x, dy = xi.y - ca.y, dz = xi.z - ca.z;
-            // far field: Phi_s and -grad Phi_s from the source locals, the forward Hessian from L
             T phis = T(0), ngx = T(0), ngy = T(0), ngz = T(0);
             Exp<P>::template l2p<T>(Ls + (size_t)a * ncp, dx, dy, dz, phis, ngx, ngy, ngz);
             T H[6] = {T(0), T(0), T(0), T(0), T(0), T(0)};
             Exp<P>::template l2p_hess<T>(L + (size_t)a * ncp, dx, dy, dz, H);
-            T gx = -ngx, gy = -ngy, gz = -ngz;
-            // near field over the leaf's P2P list (the leaf itself included; zero separations skipped)
-            for (int q = beg; q < end; ++q) {
-                const int b = lsrc[q];
-                const int fb = first[b], cb = count[b];
-                for (int g0 = 0; g0 < cb; g0 += VJP_CH) {
-                    const int nh = min(VJP_CH, cb - g0);
-                    __syncwarp();
-                    for (int k = lane; k < nh; k += 32) {
-                        s_x[w][k] = xyzm[fb + g0 + k];
-                        s_s[w][k] = src[fb + g0 + k];
-                    }
-                    __syncwarp();
-                    for (int k = 0; k < nh; ++k) {
-                        const vec4<T> xj = s_x[w][k], sj = s_s[w][k];
-                        const T ux = xi.x - xj.x, uy = xi.y - xj.y, uz = xi.z - xj.z;
-                        const T r2 = ux * ux + uy * uy + uz * uz;
-                        if (r2 == T(0)) continue;
-                        const T ri = rsqrt_t(r2);
-                        const T ir2 = ri * ri, ir3 = ri * ir2, ir5 = ir3 * ir2;
-                        // forward: Hessian of -m_j / r is m_j (r^2 delta - 3 u u) / r^5
-                        const T m3 = xj.w * ir3, m5 = T(3) * xj.w * ir5;
-                        H[0] += m3 - m5 * ux * ux;
-                        H[1] -= m5 * ux * uy;
-                        H[2] -= m5 * ux * uz;
-                        H[3] += m3 - m5 * uy * uy;
-                        H[4] -= m5 * uy * uz;
-                        H[5] += m3 - m5 * uz * uz;
-                        // sources (monopole q = sj.x, dipole d = sj.yzw): Phi_s += -q / r - d.u / r^3,
-                        // grad Phi_s += q u / r^3 - d / r^3 + 3 (d.u) u / r^5
-                        const T du = sj.y * ux + sj.z * uy + sj.w * uz;
-                        phis -= sj.x * ri + du * ir3;
-                        const T cu = sj.x * ir3 + T(3) * du * ir5;
-                        gx += cu * ux - sj.y * ir3;
-                        gy += cu * uy - sj.z * ir3;
-                        gz += cu * uz - sj.w * ir3;
-                    }
-                }
-            }
-            if (mine) {
-                const uint32_t o = perm[i];
-                const vec4<T> si = src[i];
-                const T abx = -si.y, aby = -si.z, abz = -si.w;  // the particle's own cotangent abar
-                const T hx = H[0] * abx + H[1] * aby + H[2] * abz;
-                const T hy = H[1] * abx + H[3] * aby + H[4] * abz;
-                const T hz = H[2] * abx + H[4] * aby + H[5] * abz;
-                const T *ai = acc_fwd + 3 * (size_t)o;
-                pos_bar[3 * (size_t)o] = xi.w * gx - hx - si.x * ai[0];
-                pos_bar[3 * (size_t)o + 1] = xi.w * gy - hy - si.x * ai[1];
-                pos_bar[3 * (size_t)o + 2] = xi.w * gz - hz - si.x * ai[2];
-                mass_bar[o] = phis;
+            const T bx = -si.y, by = -si.z, bz = -si.w;  // the particle's own cotangent abar
+            const T hx = H[0] * bx + H[1] * by + H[2] * bz;
+            const T hy = H[1] * bx + H[3] * by + H[4] * bz;
+            const T hz = H[2] * bx + H[4] * by + H[5] * bz;
+            const T *ai = acc_fwd + 3 * (size_t)perm[i];
+            far[i] = make4<T>(phis, -xi.w * ngx - hx - si.x * ai[0], -xi.w * ngy - hy - si.x * ai[1],
+                              -xi.w * ngz - hz - si.x * ai[2]);
+        }
+    }
+}
+
+// One source j (position and mass xj; monopole q and dipole d in sj = (q, d))
+// acting on one receiver i (position and mass p, cotangent b = abar_i), with
+// u = x_i - x_j:
+//   A[0] += -q / r - d.u / r^3                                  (Phi_s)
+//   A[1..3] += u (m_i q / r^3 + 3 (m_i d.u + m_j b.u) / r^5) - m_i d / r^3
+//   A[4] += m_j / r^3
+// so that m_i grad Phi_s - Hess Phi b of the pair is A[1..3] - A[4] b (the
+// Hessian of -m_j / r is m_j (r^2 I - 3 u u^T) / r^5). The own leaf holds the
+// receiver itself (zero separation), which MASKED skips.
+template <class T, bool MASKED>
+__device__ __forceinline__ void vjp_pair(const vec4<T> &xj, const vec4<T> &sj, const vec4<T> &p, const vec4<T> &b,
+                                         T (&A)[5])
+{
+    const T ux = p.x - xj.x, uy = p.y - xj.y, uz = p.z - xj.z;
+    const T r2 = ux * ux + uy * uy + uz * uz;
+    T ri = rsqrt_t(r2);
+    if (MASKED) ri = r2 > T(0) ? ri : T(0);
+    const T ir2 = ri * ri, ir3 = ir2 * ri, ir5 = T(3) * ir3 * ir2;
+    const T wd = sj.y * ux + sj.z * uy + sj.w * uz;
+    const T wb = b.x * ux + b.y * uy + b.z * uz;
+    A[0] -= sj.x * ri + wd * ir3;
+    const T cu = p.w * sj.x * ir3 + (p.w * wd + xj.w * wb) * ir5;
+    const T mi3 = p.w * ir3;
+    A[1] += cu * ux - mi3 * sj.y;
+    A[2] += cu * uy - mi3 * sj.z;
+    A[3] += cu * uz - mi3 * sj.w;
+    A[4] += xj.w * ir3;
+}
+
+// Interactions of the staged sources q, q + S, ... with K receivers.
+template <class T, bool MASKED, int K>
+__device__ __forceinline__ void vjp_span(const vec4<T> *bx, const vec4<T> *bs, int n_here, int q, int S,
+                                         const vec4<T> (&p)[K], const vec4<T> (&b)[K], T (&A)[K][5])
+{
+    for (int j = q; j < n_here; j += S) {
+        const vec4<T> xj = bx[j], sj = bs[j];
+#pragma unroll
+        for (int k = 0; k < K; ++k) vjp_pair<T, MASKED>(xj, sj, p[k], b[k], A[k]);
+    }
+}
+
+// Copy one particle's position-mass and source records into shared memory.
+template <class T>
+__device__ __forceinline__ void vjp_copy(vec4<T> *dx, vec4<T> *ds, const vec4<T> *sx, const vec4<T> *ss)
+{
+#pragma unroll
+    for (int h = 0; h < (int)sizeof(vec4<T>); h += 16) {
+        cp_async16(reinterpret_cast<char *>(dx) + h, reinterpret_cast<const char *>(sx) + h);
+        cp_async16(reinterpret_cast<char *>(ds) + h, reinterpret_cast<const char *>(ss) + h);
+    }
+}
+
+// Stage sources [g0, g0 + CH) of the concatenation of the current group's
+// source leaves. Lane i holds the group's i-th leaf: first particle fb and
+// exclusive prefix ex of the counts (ascending over the lanes).
+template <class T, int CH>
+__device__ __forceinline__ int vjp_stage(vec4<T> *bx, vec4<T> *bs, const vec4<T> *__restrict__ xyzm,
+                                         const vec4<T> *__restrict__ src, int fb, int ex, int tot, int g0, int lane)
+{
+    const int n_here = min(CH, tot - g0);
+    for (int k0 = 0; k0 < n_here; k0 += 32) {  // warp-uniform: every lane takes part in the shuffles
+        const int k = k0 + lane;
+        const int g = g0 + k;
+        int lo = 0;  // last lane whose leaf starts at or before g
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {
+            const int exm = __shfl_sync(kFull, ex, lo + step);
+            lo = exm <= g ? lo + step : lo;
+        }
+        const int f = __shfl_sync(kFull, fb, lo);
+        const int e = __shfl_sync(kFull, ex, lo);
+        if (k < n_here) vjp_copy<T>(bx + k, bs + k, xyzm + f + (g - e), src + f + (g - e));
+    }
+    cp_async_wait_all();
+    return n_here;
+}
+
+// One round of up to 32 K receivers [r0, r0 + cr) of leaf a, laid out as in
+// the forward near field: lane = q R + rp (rp < R = ceil(cr / K), q < S =
+// 32 / R) holds receivers rp + k R, k < K, and walks the staged sources from
+// offset q with stride S; lanes at or beyond R S only stage. The S partial
+// sums of a receiver are added in order of q, and a split receiver's chunks in
+// chunk order, so the result is reproducible.
+template <class T, int K, bool CHUNKED>
+__device__ __forceinline__ void vjp_round(int a, int f, int c, int r0, int cr, int beg, int end, int chunk, int nch,
+                                          int *done, DevCounters *ctr, const int *__restrict__ first,
+                                          const int *__restrict__ count, const vec4<T> *__restrict__ xyzm,
+                                          const vec4<T> *__restrict__ src, const uint32_t *__restrict__ perm,
+                                          const vec4<T> *far, vec4<T> *far_w, const int *__restrict__ lsrc,
+                                          T *__restrict__ pos_bar, T *__restrict__ mass_bar, vec4<T> *bx,
+                                          vec4<T> *bs, T (*red)[4], int lane)
+{
+    constexpr int CH = VjpChunk<T>::value;
+    const int R = (cr + K - 1) / K, S = 32 / R;
+    const int rp = lane % R, q = lane / R;
+    vec4<T> p[K], b[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int rr = rp + k * R;
+        const int i = f + r0 + (rr < cr ? rr : 0);
+        p[k] = xyzm[i];
+        const vec4<T> si = src[i];
+        b[k] = make4<T>(-si.y, -si.z, -si.w, T(0));
+    }
+    T A[K][5];
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+#pragma unroll
+        for (int v = 0; v < 5; ++v) A[k][v] = T(0);
+    const int qq = q < S ? q : (1 << 30);  // idle lanes start past every chunk
+    // the leaf's own particles (zero separations possible; the first chunk of a split receiver)
+    for (int g0 = 0; (!CHUNKED || chunk == 0) && g0 < c; g0 += CH) {
+        const int n_here = min(CH, c - g0);
+        __syncwarp();
+        for (int k = lane; k < n_here; k += 32) vjp_copy<T>(bx + k, bs + k, xyzm + f + g0 + k, src + f + g0 + k);
+        cp_async_wait_all();
+        __syncwarp();
+        vjp_span<T, true, K>(bx, bs, n_here, qq, S, p, b, A);
+    }
+    // every other source leaf of the list, 32 entries at a time (lane i holds entry lb + i)
+    for (int lb = beg; lb < end; lb += 32) {
+        const int e = lb + lane;
+        int fb = 0, cb = 0;
+        if (e < end) {
+            const int bb = lsrc[e];
+            if (bb != a) {
+                fb = first[bb];
+                cb = count[bb];
             }
         }
+        const int incl = warp_incl_scan(cb);
+        const int tot = __shfl_sync(kFull, incl, 31);
+        const int ex = incl - cb;
+        for (int g0 = 0; g0 < tot; g0 += CH) {
+            __syncwarp();
+            const int n_here = vjp_stage<T, CH>(bx, bs, xyzm, src, fb, ex, tot, g0, lane);
+            __syncwarp();
+            vjp_span<T, false, K>(bx, bs, n_here, qq, S, p, b, A);
+        }
+    }
+    if (CHUNKED && r0 == 0) wait_turn(done + a, chunk, ctr);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        __syncwarp();
+        red[lane][0] = A[k][0];
+        red[lane][1] = A[k][1] - A[k][4] * b[k].x;
+        red[lane][2] = A[k][2] - A[k][4] * b[k].y;
+        red[lane][3] = A[k][3] - A[k][4] * b[k].z;
+        __syncwarp();
+        const int rr = rp + k * R;
+        if (q == 0 && rr < cr) {
+            T t[4] = {red[rp][0], red[rp][1], red[rp][2], red[rp][3]};
+            for (int qs = 1; qs < S; ++qs)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) t[v] += red[qs * R + rp][v];
+            const int i = f + r0 + rr;
+            // the far field plus the earlier chunks' partial sums (written by other warps through far_w,
+            // which aliases far: a coherent L2 load then)
+            const vec4<T> fa = CHUNKED ? ld_cg(far + i) : far[i];
+            if (CHUNKED && chunk < nch - 1) {
+                far_w[i] = make4<T>(fa.x + t[0], fa.y + t[1], fa.z + t[2], fa.w + t[3]);
+            } else {
+                const uint32_t o = perm[i];
+                pos_bar[3 * (size_t)o] = fa.y + t[1];
+                pos_bar[3 * (size_t)o + 1] = fa.z + t[2];
+                pos_bar[3 * (size_t)o + 2] = fa.w + t[3];
+                mass_bar[o] = fa.x + t[0];
+            }
+        }
+    }
+}
+
+// The near field of the VJP: the forward evaluation's P2P work items (a
+// receiving leaf, or one chunk of a split one), taken from a shared counter
+// in decreasing order of work, a warp each.
+template <class T, int K>
+__global__ __launch_bounds__(VJP_WARPS * 32) void k_vjp_near(
+    const DevCounters *__restrict__ cst, const int2 *__restrict__ items, int *done, DevCounters *ctr,
+    const int *__restrict__ first, const int *__restrict__ count, const vec4<T> *__restrict__ xyzm,
+    const vec4<T> *__restrict__ src, const uint32_t *__restrict__ perm, const vec4<T> *far, vec4<T> *far_w,
+    const int *__restrict__ off, const int *__restrict__ lsrc, T *__restrict__ pos_bar, T *__restrict__ mass_bar)
+{
+    constexpr int CH = VjpChunk<T>::value;
+    __shared__ vec4<T> s_x[VJP_WARPS][CH];
+    __shared__ vec4<T> s_s[VJP_WARPS][CH];
+    __shared__ T s_red[VJP_WARPS][32][4];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int n_work = 0;
+    for (int bkt = 1; bkt < 64; ++bkt) n_work += cst->order_cnt[0][bkt];
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[0], 1);
+        t = __shfl_sync(kFull, t, 0);
+        if (t >= n_work) break;
+        const int2 item = items[t];
+        const int a = item.x, nch = item.y >> 8, chunk = item.y & 255;
+        const int f = first[a], c = count[a];
+        int beg = off[a], end = off[a + 1];
+        if (nch > 1) {
+            const int len = end - beg;
+            end = beg + len * (chunk + 1) / nch;
+            beg = beg + len * chunk / nch;
+        }
+        for (int r0 = 0; r0 < c; r0 += 32 * K) {
+            const int cr = min(32 * K, c - r0);
+            if (nch == 1)
+                vjp_round<T, K, false>(a, f, c, r0, cr, beg, end, 0, 1, done, ctr, first, count, xyzm, src, perm,
+                                       far, far_w, lsrc, pos_bar, mass_bar, s_x[w], s_s[w], s_red[w], lane);
+            else
+                vjp_round<T, K, true>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, src,
+                                      perm, far, far_w, lsrc, pos_bar, mass_bar, s_x[w], s_s[w], s_red[w], lane);
+        }
+        if (nch > 1 && chunk < nch - 1) pass_turn(done + a, chunk + 1);
     }
 }
 
@@ -195,11 +368,19 @@ int launch_vjp_tp(Plan &P_, const void *abar, const void *pbar, void *pos_bar, v
     launches += launch_l2l(P_, P_.depth, s);
     P_.Lm2l = fwd_lm2l;
     P_.L = fwd_l;
-    k_vjp_leaf<T, P><<<P_.num_sms * 8, VJP_WARPS * 32, 0, s>>>(
-        P_.ctr, P_.node_first, P_.node_count, P_.node_nchild, (const vec4<T> *)P_.node_c, (const vec4<T> *)P_.xyzm,
-        (const vec4<T> *)P_.vjp_src, P_.idx[0], (const T *)P_.L, (const T *)P_.Ls, P_.ncp, P_.p2p_off, P_.p2p_src,
-        (const T *)P_.vjp_acc, (T *)pos_bar, (T *)mass_bar);
-    return launches + 1;
+    k_vjp_far<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.node_first, P_.node_count, P_.node_nchild,
+                                                   (const vec4<T> *)P_.node_c, (const vec4<T> *)P_.xyzm,
+                                                   (const vec4<T> *)P_.vjp_src, P_.idx[0], (const T *)P_.L,
+                                                   (const T *)P_.Ls, P_.ncp, (const T *)P_.vjp_acc,
+                                                   (vec4<T> *)P_.far);
+    // the near field takes the forward evaluation's work items afresh (work counter 0 was reset above
+    // and neither M2L nor L2L uses it); its chunk flags start again from zero
+    cudaMemsetAsync(P_.p2p_done, 0, (size_t)P_.cap_nodes * sizeof(int), s);
+    k_vjp_near<T, kVjpK><<<P_.num_sms * 16, VJP_WARPS * 32, 0, s>>>(
+        P_.ctr, P_.p2p_items, P_.p2p_done, P_.ctr, P_.node_first, P_.node_count, (const vec4<T> *)P_.xyzm,
+        (const vec4<T> *)P_.vjp_src, P_.idx[0], (const vec4<T> *)P_.far, (vec4<T> *)P_.far, P_.p2p_off,
+        P_.p2p_src, (T *)pos_bar, (T *)mass_bar);
+    return launches + 2;
 }
 
 template <class T>
