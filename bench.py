@@ -47,6 +47,8 @@ FP64_PEAK_TFLOPS = 148 * 2 * 2 * SM_CLOCK_HZ / 1e12
 F64_ARITH = ("fp64 inputs and outputs; M2L (p <= 4), L2P and leaf P2M (p <= 6) and P2P in double-float "
              "arithmetic (fp32 pairs, ~2^-48 relative) on the FP32 pipe, the other stages in fp64")
 F64_IEEE_ARITH = "IEEE fp64 in every stage (fmm_plan_set_f64_ieee)"
+F64_MUTUAL_ARITH = ("fp64 inputs and outputs; mutual M2L and P2P in IEEE fp64, L2P and leaf P2M (p <= 6) in "
+                    "double-float, the other stages in fp64")
 P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r^2), 3 FMA (a), 1 add (phi) ~ 19 + 1
 
 # The double-float kernels run on the FP32 pipe, so their roofline is that
@@ -307,7 +309,7 @@ def bench_reversibility(torch, native, steps=20, dt=1e-3):
 
 
 def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_override=None, dtype=None, f64_ieee=False,
-                   m2l_rotation=False):
+                   m2l_rotation=False, mutual=False):
     """Times `steps` evaluations; returns dict with per-step ms, stage ms, stats."""
     n = n_override or w.n
     dtype = dtype or w.dtype
@@ -317,7 +319,7 @@ def bench_workload(w, steps, warmup, torch, native, stream, flush_buf, n_overrid
     mass = torch.from_numpy(g["mass"]).to("cuda", tdt)
     acc = torch.empty_like(pos)
     pot = torch.empty_like(mass)
-    plan = native.Plan(n, w.p, w.theta, w.leaf, dtype, f64_ieee=f64_ieee, m2l_rotation=m2l_rotation)
+    plan = native.Plan(n, w.p, w.theta, w.leaf, dtype, f64_ieee=f64_ieee, m2l_rotation=m2l_rotation, mutual=mutual)
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             plan.eval(pos, mass, acc, pot, stream=stream)
@@ -396,7 +398,7 @@ def run_ours(args, rank, world, local_rank):
                               "gpu_launches": r["launches"] * args.steps, "clocks": clocks}), flush=True)
         return
     res = bench_workload(w, args.steps, args.warmup, torch, native, stream, flush_buf,
-                         m2l_rotation=args.m2l_rotation)
+                         m2l_rotation=args.m2l_rotation, mutual=args.mutual)
     barrier()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
@@ -409,9 +411,9 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_also:
         n_also = max(3, args.steps // 2)
 
-        def leg(w, name, n=None, dtype=None, f64_ieee=False, roofs=False, m2l_rotation=False):
+        def leg(w, name, n=None, dtype=None, f64_ieee=False, roofs=False, m2l_rotation=False, mutual=False):
             r = bench_workload(w, n_also, args.warmup, torch, native, stream, flush_buf, n_override=n, dtype=dtype,
-                               f64_ieee=f64_ieee, m2l_rotation=m2l_rotation)
+                               f64_ieee=f64_ieee, m2l_rotation=m2l_rotation, mutual=mutual)
             ms = float(np.median(r["step_ms"]))  # median: a rare driver stall of ~3 ms would skew a short mean
             dt = dtype or w.dtype
             d = {"value": r["n"] / (ms / 1e3), "unit": "particles/s", "ms_per_step": ms, "n": r["n"], "dtype": dt,
@@ -419,8 +421,11 @@ def run_ours(args, rank, world, local_rank):
                  "p": w.p, "theta": w.theta, "leaf": w.leaf, "stage_ms": r["stage_ms"],
                  "counts": {k: r["stats"][k] for k in ("n_nodes", "n_m2l", "n_p2p_interactions")}}
             if dt == "f64":
-                d["arith"] = F64_IEEE_ARITH if f64_ieee or m2l_rotation else F64_ARITH
+                d["arith"] = (F64_IEEE_ARITH if f64_ieee or m2l_rotation else
+                              F64_MUTUAL_ARITH if mutual else F64_ARITH)
             d["m2l_operator"] = "rotation (solid harmonics)" if m2l_rotation else "reduced Cartesian"
+            if mutual:
+                d["mutual"] = True
             if roofs:
                 d["roofline"] = p2p_roofline(r, w, dt, f64_ieee)
                 d["m2l_roofline"] = m2l_roofline(r, w, dt, f64_ieee)
@@ -440,6 +445,9 @@ def run_ours(args, rank, world, local_rank):
         w3p8 = dataclasses.replace(w3, name="plummer_1e5_f32_p8", p=8, dtype="f32")
         leg(w3p8, w3p8.name)
         leg(w3p8, w3p8.name + "_m2l_rotation", m2l_rotation=True)
+        # the mutual evaluation (each unordered pair once, both directions; same result)
+        leg(w, w.name + "_mutual", mutual=True)
+        leg(w3, w3.name + "_mutual", mutual=True)
         w5 = W.WORKLOADS[5]
         also[w5.name] = bench_kdk(w5, torch, native, stream)
         also["kdk_reversibility_2p18_f64"] = bench_reversibility(torch, native)
@@ -460,7 +468,9 @@ def run_ours(args, rank, world, local_rank):
         **({"arith": F64_ARITH} if w.dtype == "f64" else {}), "data": "synthetic (seeded generator)",
         "config": {"workload": w.name, "n": res["n"], "p": w.p, "theta": w.theta, "leaf": w.leaf,
                    "l2": "flushed between timed steps (256 MiB write, outside the step events)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   **({"mutual": True} if args.mutual else {}),
+                   **({"m2l_operator": "rotation (solid harmonics)"} if args.m2l_rotation else {})},
         "step_ms_spread": {"min": min(res["step_ms"]), "median": statistics.median(res["step_ms"]),
                            "max": max(res["step_ms"]), "argmax": int(np.argmax(res["step_ms"]))},
         "stage_ms": res["stage_ms"],
@@ -608,6 +618,7 @@ def main():
     ap.add_argument("--no-also", action="store_true", help="skip the secondary points (other configs, KDK)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--m2l-rotation", action="store_true", help="main leg: the rotation-based M2L")
+    ap.add_argument("--mutual", action="store_true", help="main leg: the mutual evaluation (fmm_plan_set_mutual)")
     ap.add_argument("--vjp", action="store_true", help="main leg: fmm_vjp (forward evaluation + adjoint) per step")
     args = ap.parse_args()
     rank, world, local_rank = env_rank()

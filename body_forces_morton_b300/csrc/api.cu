@@ -184,6 +184,66 @@ fmm_status alloc_lists(Plan &P, int64_t cap_frontier, int64_t cap_m2l, int64_t c
     return FMM_OK;
 }
 
+void free_mutual(Plan &P)
+{
+    dfree(P.mut_lo); dfree(P.mut_mir_m2l); dfree(P.mut_mir_p2p); dfree(P.mut_base);
+    dfree(P.mut_rm2l); dfree(P.mut_lpart); dfree(P.mut_rp2p); dfree(P.mut_own);
+    P.mut_lo = P.mut_mir_m2l = P.mut_mir_p2p = nullptr;
+    P.mut_base = nullptr;
+    P.mut_rm2l = P.mut_lpart = P.mut_rp2p = P.mut_own = nullptr;
+    P.mut_for_nodes = 0;
+    P.mut_cap_rp = P.mut_cap_em = P.mut_cap_ep = 0;
+}
+
+// Buffers of the mutual evaluation. Their sizes follow the lists the walk
+// produces, so they are not taken from the list capacities (which grow like
+// theta^-3 and can reach 1e9 pairs): they start at estimates (32 partner sums
+// per particle, 128 M2L and 48 P2P entries per node, or 1 under
+// BFM_FMM_FAULT=capacity), a kernel compares them with the actual sizes, and
+// an evaluation that finds one short grows it and repeats. A size <= 0 asks
+// for the estimate.
+fmm_status ensure_mutual(Plan &P, long long want_rp, long long want_em, long long want_ep)
+{
+    const size_t e = (size_t)P.esize;
+    if (P.mut_for_nodes != P.cap_nodes) {
+        dfree(P.mut_lo); dfree(P.mut_base); dfree(P.mut_lpart);
+        P.mut_lo = nullptr; P.mut_base = nullptr; P.mut_lpart = nullptr;
+        const size_t c = (size_t)P.cap_nodes;
+        CUDA_TRY(dalloc(P.mut_lo, 3 * c));
+        CUDA_TRY(dalloc(P.mut_base, c + 1));
+        CUDA_TRY(cudaMalloc(&P.mut_lpart, (size_t)P.nrp * c * e));
+        P.mut_for_nodes = P.cap_nodes;
+    }
+    if (!P.mut_own) CUDA_TRY(cudaMalloc(&P.mut_own, 4 * (size_t)P.n * e));
+    const bool m = P.minimal_caps;
+    if (want_rp <= 0) want_rp = m ? 1 : std::max<long long>(32 * (long long)P.n, 65536);
+    if (want_em <= 0) want_em = m ? 1 : std::min<long long>(2 * P.cap_m2l, 128 * P.cap_nodes);
+    if (want_ep <= 0) want_ep = m ? 1 : std::min<long long>(2 * P.cap_p2p, 48 * P.cap_nodes);
+    if (!P.mut_rp2p || P.mut_cap_rp < want_rp) {
+        dfree(P.mut_rp2p);
+        P.mut_rp2p = nullptr;
+        P.mut_cap_rp = 0;
+        CUDA_TRY(cudaMalloc(&P.mut_rp2p, 4 * (size_t)want_rp * e));
+        P.mut_cap_rp = want_rp;
+    }
+    if (!P.mut_rm2l || P.mut_cap_em < want_em) {
+        dfree(P.mut_rm2l); dfree(P.mut_mir_m2l);
+        P.mut_rm2l = nullptr; P.mut_mir_m2l = nullptr;
+        P.mut_cap_em = 0;
+        CUDA_TRY(dalloc(P.mut_mir_m2l, (size_t)want_em));
+        CUDA_TRY(cudaMalloc(&P.mut_rm2l, (size_t)P.nrp * (size_t)want_em * e));
+        P.mut_cap_em = want_em;
+    }
+    if (!P.mut_mir_p2p || P.mut_cap_ep < want_ep) {
+        dfree(P.mut_mir_p2p);
+        P.mut_mir_p2p = nullptr;
+        P.mut_cap_ep = 0;
+        CUDA_TRY(dalloc(P.mut_mir_p2p, (size_t)want_ep));
+        P.mut_cap_ep = want_ep;
+    }
+    return FMM_OK;
+}
+
 void destroy_plan(Plan &P)
 {
     free_nodes(P);
@@ -192,6 +252,7 @@ void destroy_plan(Plan &P)
     dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     dfree(P.vjp_acc); dfree(P.vjp_src); dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
+    free_mutual(P);
     if (P.ctr_host) cudaFreeHost(P.ctr_host);
     for (int i = 0; i < kNumEvents; ++i)
         if (P.ev[i]) cudaEventDestroy(P.ev[i]);
@@ -211,9 +272,10 @@ void record(Plan &P, int k, cudaStream_t s) { cudaEventRecord(P.ev[k], s); }
 const char *error_bits(unsigned e)
 {
     static thread_local char buf[160];
-    snprintf(buf, sizeof(buf), "%s%s%s%s%s%s%s%s", e & ERR_NONFINITE ? "nonfinite " : "", e & ERR_NODES ? "nodes " : "",
+    snprintf(buf, sizeof(buf), "%s%s%s%s%s%s%s%s%s", e & ERR_NONFINITE ? "nonfinite " : "", e & ERR_NODES ? "nodes " : "",
              e & ERR_FRONTIER ? "frontier " : "", e & ERR_M2L_CAP ? "m2l " : "", e & ERR_P2P_CAP ? "p2p " : "",
-             e & ERR_SPIN ? "spin-limit " : "", e & ERR_BOUNDS ? "bounds " : "", e & ERR_WALK ? "walk " : "");
+             e & ERR_SPIN ? "spin-limit " : "", e & ERR_BOUNDS ? "bounds " : "", e & ERR_WALK ? "walk " : "",
+             e & ERR_MUT_CAP ? "mutual-buffer " : "");
     return buf;
 }
 
@@ -248,6 +310,10 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
     for (int attempt = 0; attempt < 8; ++attempt) {
         P.slot = 0;
         P.launches = 0;
+        if (P.mutual) {
+            fmm_status sm = ensure_mutual(P, 0, 0, 0);
+            if (sm) return sm;
+        }
         if (P.epoch > (1u << 24) - 512) {
             CUDA_TRY(cudaMemsetAsync(P.flags, 0, (size_t)P.cap_flags * sizeof(unsigned long long), s));
             P.epoch = 0;
@@ -311,6 +377,14 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
             if (h.error & ERR_M2L_CAP) cm = clamp_cap(std::max(2.0 * cm, 1.5 * kShards * (double)mmax));
             if (h.error & ERR_P2P_CAP) cp = clamp_cap(std::max(2.0 * cp, 1.5 * kShards * (double)pmax));
             st = alloc_lists(P, cf, cm, cp);
+            if (st) return st;
+            P.retries++;
+            continue;
+        }
+        if (h.error & ERR_MUT_CAP) {
+            // a mutual-evaluation buffer was short (its writes were skipped): grow it and repeat
+            auto grow = [](long long need) { return need > 0 ? need + need / 4 + 1024 : 0; };
+            st = ensure_mutual(P, grow(h.mut_need[0]), grow(h.mut_need[1]), grow(h.mut_need[2]));
             if (st) return st;
             P.retries++;
             continue;
@@ -576,7 +650,24 @@ fmm_status fmm_plan_set_m2l_rotation(fmm_plan *plan, int on)
 {
     g_err.clear();
     if (!plan) { set_err("fmm_plan_set_m2l_rotation: NULL plan"); return FMM_ERR_INVALID_ARG; }
+    if (on && plan->P.mutual) {
+        set_err("fmm_plan_set_m2l_rotation: a mutual plan uses the reduced Cartesian operator");
+        return FMM_ERR_INVALID_ARG;
+    }
     plan->P.m2l_rotation = on != 0;
+    plan->P.cache_valid = false;
+    return FMM_OK;
+}
+
+fmm_status fmm_plan_set_mutual(fmm_plan *plan, int on)
+{
+    g_err.clear();
+    if (!plan) { set_err("fmm_plan_set_mutual: NULL plan"); return FMM_ERR_INVALID_ARG; }
+    if (on && plan->P.m2l_rotation) {
+        set_err("fmm_plan_set_mutual: the mutual M2L uses the reduced Cartesian operator; switch the rotation off first");
+        return FMM_ERR_INVALID_ARG;
+    }
+    plan->P.mutual = on != 0;
     plan->P.cache_valid = false;
     return FMM_OK;
 }

@@ -30,6 +30,7 @@ enum : unsigned {
     ERR_SPIN = 1u << 5,       // a bounded wait gave up
     ERR_BOUNDS = 1u << 6,     // an index check failed (skipped access)
     ERR_WALK = 1u << 7,       // walk did not terminate in the expected iterations
+    ERR_MUT_CAP = 1u << 8,    // a mutual-evaluation buffer too small (needed sizes in mut_need)
 };
 
 // ---- per-evaluation device counters (zeroed at the start of every evaluation)
@@ -50,6 +51,8 @@ struct DevCounters {
     long long p2p_interactions;
     int n_long;                    // list segments too long for the warp sort
     int pad;
+    long long mut_need[3];         // mutual buffers needed (set with ERR_MUT_CAP): P2P share slots, M2L
+                                   // list entries, P2P list entries
     int order_cnt[2][64];          // work buckets (0: P2P receivers, 1: M2L receivers)
     int order_cur[2][64];
     int work_ctr[4];               // dynamic work counters

@@ -566,6 +566,7 @@ int launch_p2p_t(Plan &P, void *acc, void *pot, cudaStream_t s)
 
 int launch_p2p(Plan &P, void *acc, void *pot, cudaStream_t s)
 {
+    if (P.mutual) return launch_p2p_mutual(P, acc, pot, s);
     if (P.dtype == 0) return launch_p2p_t<float>(P, acc, pot, s);
     return P.f64_ieee ? launch_p2p_t<double>(P, acc, pot, s) : launch_p2p_df(P, acc, pot, s);
 }

@@ -191,6 +191,142 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__res
     }
 }
 
+// ---- mutual M2L (the scheme is described in k_mutual.cu) ----------------------
+// Pass 1: a warp per receiver a (the M2L work order), a lane per entry of a's
+// upper part (sources b > a). Exp<P>::m2l_r_pair gives both directions from
+// one derivative tensor: a's share stays in the lane's accumulators, b's share
+// (reduced coefficients) is stored in the row of the mirrored entry. The lanes'
+// sums are added by the fixed reduction into a's own reduced share.
+template <class T, int P>
+__global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l_mut1(const DevCounters *__restrict__ nctr,
+                                                             const int *__restrict__ order, const int *__restrict__ off,
+                                                             const int *__restrict__ src, const int *__restrict__ lo,
+                                                             const int *__restrict__ mir, const vec4<T> *__restrict__ nc,
+                                                             const T *__restrict__ Mr, T *__restrict__ rbuf,
+                                                             long long rows, T *__restrict__ lpart, DevCounters *ctr)
+{
+    using S = M2LShape<T, P>;
+    using V16 = typename Vec16<T>::type;
+    __shared__ __align__(16) T s_ma[M2L_WARPS][S::NRP];
+    const int n_nodes = phase2_nodes(nctr);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[1], 1);
+        t = __shfl_sync(kFull, t, 0);
+        if (t >= n_nodes) break;
+        const int a = order[t];
+        const int u0 = off[a] + lo[a], end = off[a + 1];
+        const vec4<T> ca = nc[a];
+        __syncwarp();
+        for (int k = lane; k < S::NRP; k += 32) s_ma[w][k] = Mr[(size_t)a * S::NRP + k];
+        __syncwarp();
+        T L[S::NR];
+#pragma unroll
+        for (int k = 0; k < S::NR; ++k) L[k] = T(0);
+        for (int q = u0 + lane; q < end; q += 32) {
+            const int b = src[q], m = q < rows ? mir[q] : -1;
+            const vec4<T> cb = nc[b];
+            const T *rowb = Mr + (size_t)b * S::NRP;
+            T lb[S::NRP];
+#pragma unroll
+            for (int k = 0; k < S::NRP; ++k) lb[k] = T(0);
+            if constexpr (S::REG) {
+                T mb[S::NRP];
+#pragma unroll
+                for (int c = 0; c < S::NV; ++c) *reinterpret_cast<V16 *>(mb + c * S::V) = reinterpret_cast<const V16 *>(rowb)[c];
+                Exp<P>::template m2l_r_pair<T>(s_ma[w], mb, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L, lb);
+            } else {
+                Exp<P>::template m2l_r_pair<T>(s_ma[w], rowb, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L, lb);
+            }
+            if (m >= 0 && m < rows) {
+                V16 *dst = reinterpret_cast<V16 *>(rbuf + (size_t)m * S::NRP);
+#pragma unroll
+                for (int c = 0; c < S::NV; ++c) dst[c] = *reinterpret_cast<const V16 *>(lb + c * S::V);
+            } else {
+                set_error(ctr, ERR_BOUNDS);
+            }
+        }
+        reduce_apply<T, S::NR, S::NRC>(L, lane, [&](int k, const T &x) { lpart[(size_t)a * S::NRP + k] = x; });
+    }
+}
+
+// Pass 2: a warp per node: the rows of its lower part (written by the partners'
+// pass 1) summed over the lanes in a fixed order, added to its own share and
+// expanded to the complete Cartesian local.
+template <class T, int P>
+__global__ __launch_bounds__(256) void k_m2l_mut2(const DevCounters *__restrict__ nctr, const int *__restrict__ off,
+                                                  const int *__restrict__ lo, const T *__restrict__ rbuf, long long rows,
+                                                  const T *__restrict__ lpart, T *__restrict__ Lout, DevCounters *ctr)
+{
+    using S = M2LShape<T, P>;
+    using V16 = typename Vec16<T>::type;
+    __shared__ T s_l[8][S::NRP];
+    const int n_nodes = phase2_nodes(nctr);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
+        const int beg = off[a], stop = beg + lo[a];
+        T L[S::NR];
+#pragma unroll
+        for (int k = 0; k < S::NR; ++k) L[k] = T(0);
+        for (int q = beg + lane; q < stop; q += 32) {
+            if (q >= rows) {
+                set_error(ctr, ERR_BOUNDS);
+                break;
+            }
+            const V16 *row = reinterpret_cast<const V16 *>(rbuf + (size_t)q * S::NRP);
+#pragma unroll
+            for (int c = 0; c < S::NV; ++c) {
+                T v[S::V];
+                *reinterpret_cast<V16 *>(v) = row[c];
+#pragma unroll
+                for (int e = 0; e < S::V; ++e)
+                    if (c * S::V + e < S::NRC) L[c * S::V + e] += v[e];
+            }
+        }
+        reduce_apply<T, S::NR, S::NRC>(L, lane, [&](int k, const T &x) { s_l[w][k] = x; });
+        __syncwarp();
+        if (lane == 0) {
+            T l[S::NRP];
+#pragma unroll
+            for (int k = 0; k < S::NRC; ++k) l[k] = lpart[(size_t)a * S::NRP + k] + s_l[w][k];
+            OpReduced<P>::template finish<T>(l, Lout + (size_t)a * S::NCP);
+        }
+        __syncwarp();
+    }
+}
+
+template <class T, int P>
+int launch_m2l_mutual_tp(Plan &P_, cudaStream_t s)
+{
+    const int launches = launch_mutual_index(P_, s);
+    const long long rows = P_.mut_cap_em;
+    k_moments_r<T, P, OpReduced<P>><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)P_.M, (T *)P_.Mr);
+    k_m2l_mut1<T, P><<<P_.num_sms * 16, M2L_WARPS * 32, 0, s>>>(
+        P_.ctr, P_.order + P_.cap_nodes, P_.m2l_off, P_.m2l_src, P_.mut_lo, P_.mut_mir_m2l,
+        (const vec4<T> *)P_.node_c, (const T *)P_.Mr, (T *)P_.mut_rm2l, rows, (T *)P_.mut_lpart, P_.ctr);
+    k_m2l_mut2<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.m2l_off, P_.mut_lo, (const T *)P_.mut_rm2l, rows,
+                                                    (const T *)P_.mut_lpart, (T *)P_.Lm2l, P_.ctr);
+    return launches + 3;
+}
+
+template <class T>
+int launch_m2l_mutual_t(Plan &P, cudaStream_t s)
+{
+    switch (P.p) {
+    case 0: return launch_m2l_mutual_tp<T, 0>(P, s);
+    case 1: return launch_m2l_mutual_tp<T, 1>(P, s);
+    case 2: return launch_m2l_mutual_tp<T, 2>(P, s);
+    case 3: return launch_m2l_mutual_tp<T, 3>(P, s);
+    case 4: return launch_m2l_mutual_tp<T, 4>(P, s);
+    case 5: return launch_m2l_mutual_tp<T, 5>(P, s);
+    case 6: return launch_m2l_mutual_tp<T, 6>(P, s);
+    case 7: return launch_m2l_mutual_tp<T, 7>(P, s);
+    default: return launch_m2l_mutual_tp<T, 8>(P, s);
+    }
+}
+
 template <class T, int P, class Op>
 int launch_m2l_op(Plan &P_, const void *M, void *Lout, cudaStream_t s)
 {
@@ -232,6 +368,8 @@ int launch_m2l_t(Plan &P, const void *M, void *Lout, cudaStream_t s)
 
 int launch_m2l(Plan &P, cudaStream_t s)
 {
+    // mutual plans: both directions per unordered pair, plain arithmetic in the plan's dtype
+    if (P.mutual) return P.dtype == 0 ? launch_m2l_mutual_t<float>(P, s) : launch_m2l_mutual_t<double>(P, s);
     if (P.dtype == 0) return launch_m2l_t<float>(P, P.M, P.Lm2l, s);
     return P.p <= kMaxPDf && !P.f64_ieee && !P.m2l_rotation ? launch_m2l_df(P, s)
                                                             : launch_m2l_t<double>(P, P.M, P.Lm2l, s);

@@ -9,8 +9,10 @@
 //
 // Radix sort: 8 passes of 8 bits. Each pass is one kernel: a block takes a
 // 4096-key tile from a ticket counter, ranks its keys per digit with warp
-// match_any (stable within the tile), and finds the tile's output offset per
-// digit with a decoupled look-back over the earlier tiles. The last pass also
+// match_any (stable within the tile), finds the tile's output offset per digit
+// with a decoupled look-back over the earlier tiles, reorders the tile by digit
+// in shared memory and writes it out in runs of consecutive positions (one
+// digit's keys of a tile are contiguous in the output). The last pass also
 // gathers (x, y, z, m) into sorted order.
 #include "plan.h"
 
@@ -155,9 +157,14 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
                                                            int slot, DevCounters *ctr, const T *__restrict__ pos,
                                                            const T *__restrict__ mass, vec4<T> *__restrict__ xyzm)
 {
+    constexpr int TILE = RS_THREADS * RS_ITEMS;
+    extern __shared__ __align__(16) unsigned char rs_smem[];
+    uint64_t *const s_k = reinterpret_cast<uint64_t *>(rs_smem);   // the tile in digit order
+    uint32_t *const s_v = reinterpret_cast<uint32_t *>(s_k + TILE);
     __shared__ unsigned s_hist[RS_WARPS][256];
-    __shared__ unsigned s_base[256];
-    __shared__ unsigned s_wsum[RS_WARPS];
+    __shared__ unsigned s_lstart[256];  // tile-local start of each digit
+    __shared__ unsigned s_base[256];    // global position of the tile's first key of each digit, minus s_lstart
+    __shared__ unsigned s_wsum[2][RS_WARPS];
     __shared__ int s_tile;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < RS_WARPS * 256; i += RS_THREADS) (&s_hist[0][0])[i] = 0;
@@ -165,7 +172,7 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
     __syncthreads();
     const int tile = s_tile;
     const int shift = 8 * pass;
-    const int64_t start = (int64_t)tile * (RS_THREADS * RS_ITEMS) + warp * (32 * RS_ITEMS);
+    const int64_t start = (int64_t)tile * TILE + warp * (32 * RS_ITEMS);
     uint64_t k[RS_ITEMS];
     uint32_t v[RS_ITEMS];
     unsigned rank[RS_ITEMS];
@@ -190,7 +197,9 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
         __syncwarp();
     }
     __syncthreads();
-    // per digit: warp offsets within the tile, tile total, look-back, global base
+    // per digit: warp offsets within the tile, tile total, look-back, and two exclusive scans over the
+    // digits (the pass's global histogram: where the digit starts in the output; the tile's counts:
+    // where it starts in the tile)
     {
         const int d = tid;
         unsigned tot = 0;
@@ -201,37 +210,60 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
             tot += c;
         }
         unsigned long long excl = chained_exclusive_wide<8>(flags + d, 256, tile, tot, epoch, ctr);
-        // exclusive scan over digits of this pass's global histogram
-        unsigned g = ctr->hist[pass][d];
-        unsigned incl = g;
+        const unsigned g = ctr->hist[pass][d];
+        unsigned incl = g, inct = tot;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            unsigned t = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += t;
+            const unsigned t = __shfl_up_sync(kFull, incl, o);
+            const unsigned u = __shfl_up_sync(kFull, inct, o);
+            if (lane >= o) {
+                incl += t;
+                inct += u;
+            }
         }
-        if (lane == 31) s_wsum[warp] = incl;
+        if (lane == 31) {
+            s_wsum[0][warp] = incl;
+            s_wsum[1][warp] = inct;
+        }
         __syncthreads();
-        unsigned wbase = 0;
-        for (int w = 0; w < warp; ++w) wbase += s_wsum[w];
-        s_base[d] = wbase + incl - g + (unsigned)excl;
+        unsigned wbase = 0, wbase_t = 0;
+        for (int w = 0; w < warp; ++w) {
+            wbase += s_wsum[0][w];
+            wbase_t += s_wsum[1][w];
+        }
+        const unsigned lstart = wbase_t + inct - tot;
+        s_lstart[d] = lstart;
+        s_base[d] = wbase + incl - g + (unsigned)excl - lstart;  // unsigned: the difference wraps back
     }
     __syncthreads();
+    // the tile into shared memory in digit order (stable: warps, then items, then lanes in input order)
 #pragma unroll
     for (int j = 0; j < RS_ITEMS; ++j) {
-        const int64_t i = start + j * 32 + lane;
-        if (i < n) {
+        if (start + j * 32 + lane < n) {
             const unsigned d = (unsigned)((k[j] >> shift) & 255u);
-            const unsigned out = s_base[d] + s_hist[warp][d] + rank[j];
-            if (out < (unsigned)n) {
-                kout[out] = k[j];
-                vout[out] = v[j];
-                if (LAST) {
-                    const T *q = pos + 3 * (int64_t)v[j];
-                    xyzm[out] = make4<T>(q[0], q[1], q[2], mass[v[j]]);
-                }
-            } else {
-                set_error(ctr, ERR_BOUNDS);
+            const unsigned local = s_lstart[d] + s_hist[warp][d] + rank[j];
+            s_k[local] = k[j];
+            s_v[local] = v[j];
+        }
+    }
+    __syncthreads();
+    // and out: consecutive keys of one digit go to consecutive positions
+    const int64_t left = (int64_t)n - (int64_t)tile * TILE;
+    const int tile_n = left < TILE ? (int)left : TILE;
+    for (int i = tid; i < tile_n; i += RS_THREADS) {
+        const uint64_t key = s_k[i];
+        const uint32_t val = s_v[i];
+        const unsigned d = (unsigned)((key >> shift) & 255u);
+        const unsigned out = s_base[d] + (unsigned)i;
+        if (out < (unsigned)n) {
+            kout[out] = key;
+            vout[out] = val;
+            if (LAST) {
+                const T *q = pos + 3 * (int64_t)val;
+                xyzm[out] = make4<T>(q[0], q[1], q[2], mass[val]);
             }
+        } else {
+            set_error(ctr, ERR_BOUNDS);
         }
     }
 }
@@ -269,20 +301,24 @@ int radix_passes(Plan &P, const void *pos, const void *mass, cudaStream_t s)
 {
     const int n = (int)P.n;
     const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
+    const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
+    cudaFuncSetAttribute(k_radix_pass<T, true, false, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(k_radix_pass<T, false, false, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(k_radix_pass<T, false, true, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     for (int pass = 0; pass < 8; ++pass) {
         const int src = pass & 1, dst = src ^ 1;
         const int slot = P.next_slot();
         const unsigned ep = P.next_epoch();
         if (pass == 0)
-            k_radix_pass<T, true, false, ITEMS><<<tiles, RS_THREADS, 0, s>>>(
+            k_radix_pass<T, true, false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
                 P.keys[src], nullptr, P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
                 nullptr);
         else if (pass == 7)
-            k_radix_pass<T, false, true, ITEMS><<<tiles, RS_THREADS, 0, s>>>(
+            k_radix_pass<T, false, true, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
                 P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, (const T *)pos,
                 (const T *)mass, (vec4<T> *)P.xyzm);
         else
-            k_radix_pass<T, false, false, ITEMS><<<tiles, RS_THREADS, 0, s>>>(
+            k_radix_pass<T, false, false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
                 P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
                 nullptr);
     }

@@ -24,6 +24,7 @@ struct Plan {
     int dtype = 0;      // 0 f32, 1 f64
     bool f64_ieee = false;  // fp64 plans: every stage in IEEE fp64 (default: the ALU-bound stages in double-float)
     bool m2l_rotation = false;  // M2L by rotation to the z axis in solid harmonics (default: reduced Cartesian)
+    bool mutual = false;        // M2L and P2P once per unordered pair, both directions (plain arithmetic)
     int esize = 4;      // bytes per real
     int device = 0;
     int num_sms = 148;
@@ -88,6 +89,18 @@ struct Plan {
     void *Ms = nullptr, *Lsm = nullptr, *Ls = nullptr;
     int64_t vjp_cap_nodes = 0;
 
+    // mutual evaluation (fmm_plan_set_mutual), allocated on first use and grown when an evaluation reports
+    // one short: per node the lower-part lengths of the M2L and P2P lists and the start of the P2P upper
+    // part [3][cap_nodes], the P2P share slots [cap_nodes + 1] and the own reduced M2L share [cap_nodes]
+    // rows; per M2L list entry the mirrored entry and the partner's reduced share (a row) [mut_cap_em]; per
+    // P2P list entry the mirrored entry [mut_cap_ep]; the partners' P2P sums [mut_cap_rp] and the own P2P
+    // sums [n]
+    int *mut_lo = nullptr, *mut_mir_m2l = nullptr, *mut_mir_p2p = nullptr;
+    long long *mut_base = nullptr;
+    void *mut_rm2l = nullptr, *mut_lpart = nullptr, *mut_rp2p = nullptr, *mut_own = nullptr;
+    long long mut_cap_rp = 0, mut_cap_em = 0, mut_cap_ep = 0;
+    int64_t mut_for_nodes = 0;     // node capacity the per-node buffers were sized for
+
     // KDK acceleration cache, caller's order
     void *acc_cache = nullptr;
     bool cache_valid = false;
@@ -124,6 +137,8 @@ int launch_lists(Plan &P, cudaStream_t s);
 int launch_m2l(Plan &P, cudaStream_t s);
 int launch_m2l_df(Plan &P, cudaStream_t s);  // fp64 plans, p <= kMaxPDf
 int launch_m2l_plain(Plan &P, const void *M, void *Lout, cudaStream_t s);  // plain arithmetic, given buffers
+int launch_mutual_index(Plan &P, cudaStream_t s);  // mutual plans: lower parts, mirrored entries, P2P slots
+int launch_p2p_mutual(Plan &P, void *acc, void *pot, cudaStream_t s);
 int launch_vjp(Plan &P, const void *abar, const void *pbar, void *pos_bar, void *mass_bar, cudaStream_t s);
 constexpr int kMaxPDf = 4;
 int launch_l2l(Plan &P, int depth, cudaStream_t s);

@@ -91,8 +91,10 @@ def lib():
         L.fmm_vjp.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
         L.fmm_plan_set_f64_ieee.argtypes = [vp, i32]
         L.fmm_plan_set_m2l_rotation.argtypes = [vp, i32]
+        L.fmm_plan_set_mutual.argtypes = [vp, i32]
         for f in ("fmm_eval", "fmm_eval_host", "fmm_kdk_step", "fmm_kdk_step_lattice", "fmm_plan_stats", "fmm_plan_export",
-                  "fmm_morton_keys_noalloc", "fmm_vjp", "fmm_plan_set_f64_ieee", "fmm_plan_set_m2l_rotation"):
+                  "fmm_morton_keys_noalloc", "fmm_vjp", "fmm_plan_set_f64_ieee", "fmm_plan_set_m2l_rotation",
+                  "fmm_plan_set_mutual"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -163,6 +165,10 @@ def fmm_plan_set_m2l_rotation(plan, on: bool):
     _check(lib().fmm_plan_set_m2l_rotation(plan, 1 if on else 0))
 
 
+def fmm_plan_set_mutual(plan, on: bool):
+    _check(lib().fmm_plan_set_mutual(plan, 1 if on else 0))
+
+
 def fmm_vjp(plan, pos, mass, acc_bar, pot_bar, pos_bar, mass_bar, stream=None):
     _check(lib().fmm_vjp(plan, _ptr(pos), _ptr(mass), _ptr(acc_bar), _ptr(pot_bar), _ptr(pos_bar), _ptr(mass_bar),
                          _stream(stream)))
@@ -213,7 +219,7 @@ def fmm_plan_export(plan, what: str, dtype=None) -> np.ndarray:
 class Plan:
     """RAII wrapper: ``with Plan(n, p, theta, leaf, "f32") as pl: pl.eval(pos, mass, acc, pot)``."""
 
-    def __init__(self, n, p=4, theta=0.7, leaf=32, dtype="f32", f64_ieee=False, m2l_rotation=False):
+    def __init__(self, n, p=4, theta=0.7, leaf=32, dtype="f32", f64_ieee=False, m2l_rotation=False, mutual=False):
         self.n, self.p, self.theta, self.leaf = int(n), int(p), float(theta), int(leaf)
         self.dtype = dtype
         self.np_dtype = np.float32 if dtype == "f32" else np.float64
@@ -223,6 +229,8 @@ class Plan:
                 fmm_plan_set_f64_ieee(self.handle, True)
             if m2l_rotation:
                 fmm_plan_set_m2l_rotation(self.handle, True)
+            if mutual:
+                fmm_plan_set_mutual(self.handle, True)
         except FmmError:
             self.close()
             raise

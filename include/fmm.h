@@ -182,9 +182,29 @@ fmm_status fmm_plan_set_f64_ieee(fmm_plan *plan, int on);
  * rounding; the per-pair work differs (O(p^3) here against the reduced
  * contraction's O(p^4), with larger constants, so the Cartesian form is the
  * faster one for p <= 8). fp64 plans with rotation run their M2L in IEEE fp64.
- * Applies to the next evaluation; FMM_ERR_INVALID_ARG for a NULL plan.
+ * Applies to the next evaluation; FMM_ERR_INVALID_ARG for a NULL plan or, with
+ * on != 0, a mutual plan.
  */
 fmm_status fmm_plan_set_m2l_rotation(fmm_plan *plan, int on);
+
+/*
+ * Mutual (symmetric) evaluation of the interaction lists (jaccpot issue 152,
+ * "Mutual FMM"): each unordered accepted pair of nodes is evaluated once for
+ * both receivers, one derivative tensor per M2L pair (D^m(-R) = (-1)^{|m|}
+ * D^m(R)) and one separation and reciprocal square root per particle pair with
+ * equal and opposite forces. The result is the same truncation as the default
+ * evaluation, equal to it up to rounding. Sums stay deterministic (bit for bit
+ * from run to run): the receiver with the lower node index evaluates the pair,
+ * the partner's share goes to a buffer slot and is added by a second pass in
+ * list order. M2L and P2P then run in plain arithmetic of the plan's dtype
+ * (IEEE fp64 in fp64 plans). The plan allocates the buffers on first use: about
+ * 2 x (M2L list capacity) x (p+1)^2 reals plus 32 particle sums per particle,
+ * grown and the evaluation repeated when that is short. on != 0 switches it on.
+ * FMM_ERR_INVALID_ARG for a NULL plan or together with the rotation-based M2L
+ * (the mutual M2L uses the reduced Cartesian operator). Applies to the next
+ * evaluation.
+ */
+fmm_status fmm_plan_set_mutual(fmm_plan *plan, int on);
 
 /*
  * Vector-Jacobian product of one evaluation (JZ-FMM page, "Differentiating the

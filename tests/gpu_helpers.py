@@ -9,7 +9,7 @@ TOL_ACC = {"f64": 1e-10, "f32": 1e-4}
 
 
 def gpu_eval(pos, mass, p, theta, leaf, want_pot=True, exports=(), plan=None, repeat=1, f64_ieee=False,
-             m2l_rotation=False):
+             m2l_rotation=False, mutual=False):
     """One evaluation through fmm_eval on cuda:0; returns (acc, pot, exports, stats)."""
     import torch
 
@@ -18,7 +18,7 @@ def gpu_eval(pos, mass, p, theta, leaf, want_pot=True, exports=(), plan=None, re
     dt = "f32" if pos.dtype == np.float32 else "f64"
     n = len(mass)
     own = plan is None
-    pl = plan or native.Plan(n, p, theta, leaf, dt, f64_ieee=f64_ieee, m2l_rotation=m2l_rotation)
+    pl = plan or native.Plan(n, p, theta, leaf, dt, f64_ieee=f64_ieee, m2l_rotation=m2l_rotation, mutual=mutual)
     try:
         tp = torch.from_numpy(np.ascontiguousarray(pos)).cuda()
         tm = torch.from_numpy(np.ascontiguousarray(mass)).cuda()
