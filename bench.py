@@ -59,18 +59,18 @@ P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r
 # 1e5 fp64, p 4), keyed by the hash of the kernel sources they were counted on;
 # a changed kernel reports null until it is counted again.
 DF_FMA_OPS_PER_PAIR = {
-    # k_p2p_df: 9.098e9 FMA-pipe thread instructions (all scalar) over 48,723,340 pairs
-    ("k_p2p_df", "b04c73bca64b05b5"): 186.73,
-    # k_m2l_df<4>: 6.076e9 over 1,833,964 pairs (the moments' conversion kernel is not counted)
-    ("k_m2l_df", "8abd40a956ca8c69"): 3313.1,
+    # k_p2p_df: 9.099e9 FMA-pipe thread instructions (all scalar) over 48,723,340 pairs
+    ("k_p2p_df", "37308ee123d17f5b"): 186.75,
+    # k_m2l_df<4>: 6.078e9 over 1,833,964 pairs (the moments' conversion kernel is not counted)
+    ("k_m2l_df", "41ac065d4f26709d"): 3314.2,
 }
 
 # DRAM traffic of the P2P kernel per launch (dram__bytes_read.sum +
 # dram__bytes_write.sum, one warm launch of clustered N = 2^20 fp32), keyed by
 # the hash of the kernel sources it was taken on; null once they change.
 TRAFFIC = {
-    # k_p2p<float>: 52,489,472 B read + 3,557,376 B written
-    ("clustered_2p20_f32", "9738739f59191ee1"): 56046848,
+    # k_p2p<float>: 52,501,248 B read + 3,610,368 B written
+    ("clustered_2p20_f32", "9f77dfe283537a4e"): 56111616,
 }
 
 
