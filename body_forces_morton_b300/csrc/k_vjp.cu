@@ -17,9 +17,10 @@
 // complete forward locals L and the accelerations):
 //   k_vjp_sources   the cotangents in the tree's particle order, as the
 //                   sources' (monopole, dipole) = (pbar, -abar);
-//   k_vjp_up        per level, deepest first: a leaf's moments from its
-//                   particles (Exp<P>::p2m_dip), an internal node's from its
-//                   children (m2m), in a fixed order;
+//   k_vjp_up        one launch, deepest level first, eight lanes per node: a
+//                   leaf's moments from its particles (Exp<P>::p2m_dip), an
+//                   internal node's from its children (m2m) once their flags
+//                   are set, summed in a fixed order;
 //   M2L and L2L     the forward kernels on the source moments (plain
 //                   arithmetic in the plan's dtype);
 //   k_vjp_far       a thread per particle: Phi_s and its gradient from the
@@ -54,39 +55,87 @@ __global__ __launch_bounds__(256) void k_vjp_sources(int n, const uint32_t *__re
     }
 }
 
-// Source moments of the nodes of one level (a thread per node).
+// Source moments of every node in one launch, ordered like the forward upward
+// pass of fp32 plans (without the boxes, which the forward evaluation left):
+// warps take chunks of four nodes of one level from a shared counter, deepest
+// level first, eight lanes per node. A leaf's lanes expand its particles'
+// sources (Exp<P>::p2m_dip); an internal node's lanes wait, bounded, until each
+// child's flag holds this pass's number and add its M2M translation. A fixed
+// 8-lane reduction sums the lanes; the node's flag is then stored with release
+// semantics. A chunk never spans two levels and every child lies in an earlier
+// chunk, taken by a running warp, so the earliest unfinished chunk can always
+// finish.
 template <class T, int P>
-__global__ __launch_bounds__(128) void k_vjp_up(const DevCounters *__restrict__ ctr, int level,
-                                                const int *__restrict__ first, const int *__restrict__ count,
-                                                const int *__restrict__ child0, const int *__restrict__ nchild,
-                                                const vec4<T> *__restrict__ nc, const vec4<T> *__restrict__ xyzm,
-                                                const vec4<T> *__restrict__ src, T *__restrict__ Ms, int ncp)
+__global__ __launch_bounds__(256) void k_vjp_up(DevCounters *ctr, const int *__restrict__ first,
+                                                const int *__restrict__ count, const int *__restrict__ child0,
+                                                const int *__restrict__ nchild, const vec4<T> *__restrict__ nc,
+                                                const vec4<T> *__restrict__ xyzm, const vec4<T> *__restrict__ src,
+                                                T *Ms, int ncp, unsigned *flag, unsigned seq)
 {
     constexpr int NC = Exp<P>::NC;
+    constexpr int NR = (NC + 7) / 8 * 8;
+    __shared__ int s_off[kMaxLevel + 2];
     const int n_nodes = phase2_nodes(ctr);
-    const int lo = min(ctr->level_off[level], n_nodes), hi = min(ctr->level_off[level + 1], n_nodes);
-    for (int a = lo + blockIdx.x * blockDim.x + threadIdx.x; a < hi; a += gridDim.x * blockDim.x) {
-        T M[NC];
+    if (n_nodes == 0) return;
+    const int depth = ctr->depth;
+    for (int l = threadIdx.x; l <= depth + 1; l += blockDim.x) s_off[l] = min(ctr->level_off[l], n_nodes);
+    __syncthreads();
+    const int lane = threadIdx.x & 31, g = lane >> 3, j = lane & 7;
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[3], 1);
+        t = __shfl_sync(kFull, t, 0);
+        int lo_n = 0, hi_n = -1;
+        for (int l = depth; l >= 0; --l) {  // chunk t -> four nodes of one level, deepest level first
+            const int nch = (s_off[l + 1] - s_off[l] + 3) >> 2;
+            if (t < nch) {
+                lo_n = s_off[l] + 4 * t;
+                hi_n = min(s_off[l + 1], lo_n + 4);
+                break;
+            }
+            t -= nch;
+        }
+        if (hi_n < 0) break;
+        const int a = lo_n + g;
+        const bool valid = a < hi_n;
+        const int nch = valid ? nchild[a] : 0;
+        const bool leaf = valid && nch == 0;
+        const bool has = j < nch;
+        const vec4<T> c = valid ? nc[a] : make4<T>(T(0), T(0), T(0), T(0));
+        T m[NR];
 #pragma unroll
-        for (int k = 0; k < NC; ++k) M[k] = T(0);
-        const vec4<T> c = nc[a];
-        const int nch = nchild[a];
-        if (nch == 0) {
+        for (int k = 0; k < NR; ++k) m[k] = T(0);
+        if (leaf) {
             const int f = first[a], e = f + count[a];
-            for (int i = f; i < e; ++i) {
-                const vec4<T> x = xyzm[i], s = src[i];
-                Exp<P>::template p2m_dip<T>(x.x - c.x, x.y - c.y, x.z - c.z, s.x, s.y, s.z, s.w, M);
+            for (int i = f + j; i < e; i += 8) {
+                const vec4<T> x = xyzm[i], sv = src[i];
+                Exp<P>::template p2m_dip<T>(x.x - c.x, x.y - c.y, x.z - c.z, sv.x, sv.y, sv.z, sv.w, m);
             }
-        } else {
-            const int c0 = child0[a];
-            for (int ch = c0; ch < c0 + nch; ++ch) {
-                const vec4<T> cc = nc[ch];
-                Exp<P>::template m2m<T>(Ms + (size_t)ch * ncp, cc.x - c.x, cc.y - c.y, cc.z - c.z, M);
+        } else if (has) {
+            const int ch = child0[a] + j;
+            cuda::atomic_ref<unsigned, cuda::thread_scope_device> fl(flag[ch]);
+            unsigned spins = 0;
+            while (fl.load(cuda::memory_order_acquire) != seq) {
+                if (++spins > kSpinLimit) {
+                    set_error(ctr, ERR_SPIN);
+                    break;
+                }
+                __nanosleep(32);
             }
+            T mc[NC];
+#pragma unroll
+            for (int k = 0; k < NC; ++k) mc[k] = ld_cg(Ms + (size_t)ch * ncp + k);
+            const vec4<T> cc = nc[ch];
+            Exp<P>::template m2m<T>(mc, cc.x - c.x, cc.y - c.y, cc.z - c.z, m);
         }
         T *dst = Ms + (size_t)a * ncp;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) dst[k] = M[k];
+        reduce_apply8<T, NR, NC>(m, j, [&](int k, const T &x) {
+            if (valid) dst[k] = x;
+        });
+        __threadfence();
+        __syncwarp();
+        if (valid && j == 0)
+            cuda::atomic_ref<unsigned, cuda::thread_scope_device>(flag[a]).store(seq, cuda::memory_order_release);
     }
 }
 
@@ -349,17 +398,15 @@ int launch_vjp_tp(Plan &P_, const void *abar, const void *pbar, void *pos_bar, v
     const int n = (int)P_.n;
     k_vjp_sources<T><<<P_.num_sms * 4, 256, 0, s>>>(n, P_.idx[0], (const T *)abar, (const T *)pbar,
                                                      (vec4<T> *)P_.vjp_src);
-    int launches = 1;
-    for (int l = P_.depth; l >= 0; --l) {
-        k_vjp_up<T, P><<<P_.num_sms * 2, 128, 0, s>>>(P_.ctr, l, P_.node_first, P_.node_count, P_.node_child0,
-                                                      P_.node_nchild, (const vec4<T> *)P_.node_c,
-                                                      (const vec4<T> *)P_.xyzm, (const vec4<T> *)P_.vjp_src,
-                                                      (T *)P_.Ms, P_.ncp);
-        ++launches;
-    }
-    // the M2L and L2L kernels take their receivers from work counters that the forward evaluation
-    // ran to the end: start them afresh
+    // the work counters of the forward evaluation ran to their ends: start them afresh (the source
+    // moments take counter 3, M2L 1, L2L 2, the near field 0)
     cudaMemsetAsync(P_.ctr->work_ctr, 0, sizeof(P_.ctr->work_ctr), s);
+    const unsigned seq = P_.next_flag_seq(s);
+    k_vjp_up<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, P_.node_first, P_.node_count, P_.node_child0,
+                                                  P_.node_nchild, (const vec4<T> *)P_.node_c,
+                                                  (const vec4<T> *)P_.xyzm, (const vec4<T> *)P_.vjp_src, (T *)P_.Ms,
+                                                  P_.ncp, P_.node_flag, seq);
+    int launches = 2;
     launches += launch_m2l_plain(P_, P_.Ms, P_.Lsm, s);
     // L2L of the source locals: the forward kernel on the source buffers
     void *fwd_lm2l = P_.Lm2l, *fwd_l = P_.L;
