@@ -193,12 +193,23 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__res
 
 // ---- mutual M2L (the scheme is described in k_mutual.cu) ----------------------
 // Pass 1: a warp per receiver a (the M2L work order), a lane per entry of a's
-// upper part (sources b > a). Exp<P>::m2l_r_pair gives both directions from
-// one derivative tensor: a's share stays in the lane's accumulators, b's share
-// (reduced coefficients) is stored in the row of the mirrored entry. The lanes'
-// sums are added by the fixed reduction into a's own reduced share.
+// upper part (sources b > a), with the rows staged as in k_m2l (coalesced
+// asynchronous copies one round ahead). Exp<P>::m2l_r_pair gives both
+// directions from one derivative tensor: a's share stays in the lane's
+// accumulators, b's share (reduced coefficients) goes through the lane's
+// shared slot to the row of the mirrored entry, written by groups of lanes that
+// stream whole rows. The lanes' sums are added by the fixed reduction into a's
+// own reduced share.
 template <class T, int P>
-__global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l_mut1(const DevCounters *__restrict__ nctr,
+struct MutShape {
+    using S = M2LShape<T, P>;
+    static constexpr size_t per_warp = sizeof(T) * (3 * 32 * S::STR + S::NRP);
+    static constexpr int W = 4 * per_warp <= 200 * 1024 ? 4 : (2 * per_warp <= 200 * 1024 ? 2 : 1);  // warps per block
+    static constexpr size_t smem = W * per_warp;
+};
+
+template <class T, int P>
+__global__ __launch_bounds__(MutShape<T, P>::W * 32) void k_m2l_mut1(const DevCounters *__restrict__ nctr,
                                                              const int *__restrict__ order, const int *__restrict__ off,
                                                              const int *__restrict__ src, const int *__restrict__ lo,
                                                              const int *__restrict__ mir, const vec4<T> *__restrict__ nc,
@@ -207,9 +218,37 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l_mut1(const DevCounters *
 {
     using S = M2LShape<T, P>;
     using V16 = typename Vec16<T>::type;
-    __shared__ __align__(16) T s_ma[M2L_WARPS][S::NRP];
+    extern __shared__ __align__(16) unsigned char m2l_smem[];
     const int n_nodes = phase2_nodes(nctr);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    T *const rows0 = reinterpret_cast<T *>(m2l_smem) + (size_t)w * 3 * 32 * S::STR;
+    T *const rows1 = rows0 + 32 * S::STR;
+    T *const outb = rows1 + 32 * S::STR;                        // partner shares of the round, a row per lane
+    T *const s_ma = reinterpret_cast<T *>(m2l_smem) + (size_t)MutShape<T, P>::W * 3 * 32 * S::STR + (size_t)w * S::NRP;
+    T *const slot = rows0 + lane * S::STR, *const slot1 = rows1 + lane * S::STR, *const oslot = outb + lane * S::STR;
+    constexpr int G = S::NV <= 32 ? 32 / S::NV : 1;
+    constexpr int CPR = S::NV <= 32 ? 1 : (S::NV + 31) / 32;
+    const int g = S::NV <= 32 ? lane / S::NV : 0;
+    const int c0 = S::NV <= 32 ? lane - g * S::NV : lane;
+    auto stage = [&](int q0, int end, T *rbase, bool &valid) {
+        const int q = q0 + lane;
+        valid = q < end;
+        const int b = valid ? src[q] : -1;
+        const vec4<T> cb = valid ? nc[b] : make4<T>(T(0), T(0), T(0), T(0));
+#pragma unroll
+        for (int r0 = 0; r0 < 32; r0 += G) {
+            const int r = r0 + g;
+            const int br = __shfl_sync(kFull, b, r & 31);
+            if (g < G && r < 32 && br >= 0)
+#pragma unroll
+                for (int cc = 0; cc < CPR; ++cc) {
+                    const int c = c0 + cc * 32;
+                    if (c < S::NV) cp_async16(rbase + r * S::STR + c * S::V, Mr + (size_t)br * S::NRP + c * S::V);
+                }
+        }
+        cp_async_commit();
+        return cb;
+    };
     for (;;) {
         int t = 0;
         if (lane == 0) t = atomicAdd(&ctr->work_ctr[1], 1);
@@ -219,34 +258,60 @@ __global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l_mut1(const DevCounters *
         const int u0 = off[a] + lo[a], end = off[a + 1];
         const vec4<T> ca = nc[a];
         __syncwarp();
-        for (int k = lane; k < S::NRP; k += 32) s_ma[w][k] = Mr[(size_t)a * S::NRP + k];
-        __syncwarp();
+        for (int k = lane; k < S::NRP; k += 32) s_ma[k] = Mr[(size_t)a * S::NRP + k];
         T L[S::NR];
 #pragma unroll
         for (int k = 0; k < S::NR; ++k) L[k] = T(0);
-        for (int q = u0 + lane; q < end; q += 32) {
-            const int b = src[q], m = q < rows ? mir[q] : -1;
-            const vec4<T> cb = nc[b];
-            const T *rowb = Mr + (size_t)b * S::NRP;
-            T lb[S::NRP];
+        bool valid;
+        vec4<T> cb = stage(u0, end, rows0, valid);
+        int cur = 0;
+        for (int q0 = u0; q0 < end; q0 += 32) {
+            bool valid_n;
+            __syncwarp();
+            const vec4<T> cb_n = stage(q0 + 32, end, cur ? rows0 : rows1, valid_n);
+            cp_async_wait_group<1>();
+            __syncwarp();
+            const int q = q0 + lane;
+            const int m = valid && q < rows ? mir[q] : -1;
+            if (valid) {
+                T lb[S::NRP];
 #pragma unroll
-            for (int k = 0; k < S::NRP; ++k) lb[k] = T(0);
-            if constexpr (S::REG) {
-                T mb[S::NRP];
+                for (int k = 0; k < S::NRP; ++k) lb[k] = T(0);
+                const T *row = cur ? slot1 : slot;
+                if constexpr (S::REG) {
+                    T mb[S::NRP];
 #pragma unroll
-                for (int c = 0; c < S::NV; ++c) *reinterpret_cast<V16 *>(mb + c * S::V) = reinterpret_cast<const V16 *>(rowb)[c];
-                Exp<P>::template m2l_r_pair<T>(s_ma[w], mb, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L, lb);
-            } else {
-                Exp<P>::template m2l_r_pair<T>(s_ma[w], rowb, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L, lb);
+                    for (int c = 0; c < S::NV; ++c)
+                        *reinterpret_cast<V16 *>(mb + c * S::V) = reinterpret_cast<const V16 *>(row)[c];
+                    Exp<P>::template m2l_r_pair<T>(s_ma, mb, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L, lb);
+                } else {
+                    Exp<P>::template m2l_r_pair<T>(s_ma, row, ca.x - cb.x, ca.y - cb.y, ca.z - cb.z, L, lb);
+                }
+#pragma unroll
+                for (int c = 0; c < S::NV; ++c)
+                    reinterpret_cast<V16 *>(oslot)[c] = *reinterpret_cast<const V16 *>(lb + c * S::V);
             }
-            if (m >= 0 && m < rows) {
-                V16 *dst = reinterpret_cast<V16 *>(rbuf + (size_t)m * S::NRP);
+            if (valid && !(m >= 0 && m < rows)) set_error(ctr, ERR_BOUNDS);
+            __syncwarp();
+            // the round's partner shares to their rows, whole rows per group of lanes
 #pragma unroll
-                for (int c = 0; c < S::NV; ++c) dst[c] = *reinterpret_cast<const V16 *>(lb + c * S::V);
-            } else {
-                set_error(ctr, ERR_BOUNDS);
+            for (int r0 = 0; r0 < 32; r0 += G) {
+                const int r = r0 + g;
+                const int mr = __shfl_sync(kFull, (m >= 0 && m < rows) ? m : -1, r & 31);
+                if (g < G && r < 32 && mr >= 0)
+#pragma unroll
+                    for (int cc = 0; cc < CPR; ++cc) {
+                        const int c = c0 + cc * 32;
+                        if (c < S::NV)
+                            reinterpret_cast<V16 *>(rbuf + (size_t)mr * S::NRP)[c] =
+                                reinterpret_cast<const V16 *>(outb + r * S::STR)[c];
+                    }
             }
+            valid = valid_n;
+            cb = cb_n;
+            cur ^= 1;
         }
+        cp_async_wait_all();
         reduce_apply<T, S::NR, S::NRC>(L, lane, [&](int k, const T &x) { lpart[(size_t)a * S::NRP + k] = x; });
     }
 }
@@ -303,7 +368,10 @@ int launch_m2l_mutual_tp(Plan &P_, cudaStream_t s)
     const int launches = launch_mutual_index(P_, s);
     const long long rows = P_.mut_cap_em;
     k_moments_r<T, P, OpReduced<P>><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)P_.M, (T *)P_.Mr);
-    k_m2l_mut1<T, P><<<P_.num_sms * 16, M2L_WARPS * 32, 0, s>>>(
+    using MS = MutShape<T, P>;
+    static_assert(MS::smem <= 227 * 1024, "mutual M2L staging exceeds shared memory");
+    cudaFuncSetAttribute(k_m2l_mut1<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MS::smem);
+    k_m2l_mut1<T, P><<<P_.num_sms * 16 * (4 / MS::W), MS::W * 32, MS::smem, s>>>(
         P_.ctr, P_.order + P_.cap_nodes, P_.m2l_off, P_.m2l_src, P_.mut_lo, P_.mut_mir_m2l,
         (const vec4<T> *)P_.node_c, (const T *)P_.Mr, (T *)P_.mut_rm2l, rows, (T *)P_.mut_lpart, P_.ctr);
     k_m2l_mut2<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.m2l_off, P_.mut_lo, (const T *)P_.mut_rm2l, rows,
