@@ -307,7 +307,9 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         return FMM_ERR_INVALID_ARG;
     }
     P.retries = 0;
-    for (int attempt = 0; attempt < 8; ++attempt) {
+    // each attempt that finds a buffer short grows it and repeats; from minimal buffers the node, frontier,
+    // list and mutual-evaluation buffers can each take a regrowth or two
+    for (int attempt = 0; attempt < 12; ++attempt) {
         P.slot = 0;
         P.launches = 0;
         if (P.mutual) {
