@@ -397,7 +397,7 @@ def run_ours(args, rank, world, local_rank):
                               "config": {"workload": w.name, "n": w.n, "p": w.p, "theta": w.theta, "leaf": w.leaf},
                               "gpu_launches": r["launches"] * args.steps, "clocks": clocks}), flush=True)
         return
-    res = bench_workload(w, args.steps, args.warmup, torch, native, stream, flush_buf,
+    res = bench_workload(w, args.steps, args.warmup, torch, native, stream, flush_buf, n_override=args.n,
                          m2l_rotation=args.m2l_rotation, mutual=args.mutual)
     barrier()
     t_wall = time.perf_counter() - t_wall
@@ -460,7 +460,7 @@ def run_ours(args, rank, world, local_rank):
     st = res["stats"]
     src_hash = kernel_source_hash()
     roof = p2p_roofline(res, w)
-    roof["traffic"] = TRAFFIC.get((w.name, src_hash))
+    roof["traffic"] = TRAFFIC.get((w.name, src_hash)) if args.n is None else None  # captured at the recipe's N
     line = {
         "metric": "FMM eval particles/s", "value": value, "unit": "particles/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -619,6 +619,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--m2l-rotation", action="store_true", help="main leg: the rotation-based M2L")
     ap.add_argument("--mutual", action="store_true", help="main leg: the mutual evaluation (fmm_plan_set_mutual)")
+    ap.add_argument("--n", type=int, default=None,
+                    help="main leg: this many particles of the workload's recipe (small ncu captures)")
     ap.add_argument("--vjp", action="store_true", help="main leg: fmm_vjp (forward evaluation + adjoint) per step")
     args = ap.parse_args()
     rank, world, local_rank = env_rank()
