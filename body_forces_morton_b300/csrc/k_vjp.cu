@@ -31,6 +31,8 @@
 //                   chunk order of the forward near field: per pair the direct
 //                   terms of Phi_s, of m_i grad Phi_s and of -Hess Phi abar_i,
 //                   added to the far field and written in the caller's order.
+#include <type_traits>
+
 #include "expansions_gen.cuh"
 #include "plan.h"
 
@@ -41,7 +43,9 @@ namespace {
 constexpr int VJP_WARPS = 4;                                                // warps per block of k_vjp_near
 template <class T> struct VjpChunk { static constexpr int value = 128; };  // staged sources per warp
 template <> struct VjpChunk<double> { static constexpr int value = 64; };
-constexpr int kVjpK = 4;                                                    // receivers per lane of k_vjp_near
+// receivers per lane of k_vjp_near: four in the scalar (fp64) path, two in the packed fp32 path
+template <class T> struct VjpK { static constexpr int value = 4; };
+template <> struct VjpK<float> { static constexpr int value = 2; };
 
 template <class T>
 __global__ __launch_bounds__(256) void k_vjp_sources(int n, const uint32_t *__restrict__ perm,
@@ -348,6 +352,211 @@ __device__ __forceinline__ void vjp_round(int a, int f, int c, int r0, int cr, i
     }
 }
 
+// ---- fp32: two sources per instruction in packed f32x2 arithmetic ----------
+// The staged sources are stored pair-interleaved, per pair of sources (x, y,
+// z, m, q, d_x, d_y, d_z) with the two sources' values adjacent (16 floats), so
+// four 16-byte shared loads give eight packed operands; an odd tail is padded
+// with a massless, source-free particle far away. With u = x_j - x_i the pair
+// terms become Phi_s += d.u / r^3 - q / r (accumulated as two sums, Q and P),
+// X += c u - m_i d / r^3 with c = 3 (m_i d.u + m_j b.u) / r^5 - m_i q / r^3,
+// and SM += m_j / r^3, the same quantities as vjp_pair with u of the opposite
+// sign; the receiver's mass enters negated once per receiver, so no pair
+// needs a negation.
+struct VjpRecv {
+    float2 nx, ny, nz, m, nm, bx, by, bz;  // -x_i (both halves), m_i, -m_i, abar_i
+};
+
+__device__ __forceinline__ float rsqrt_approx_ftz(float x)
+{
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <bool MASKED>
+__device__ __forceinline__ void vjp_two(const float4 &s0, const float4 &s1, const float4 &s2, const float4 &s3,
+                                        const VjpRecv &r, float2 (&A)[6])
+{
+    const float2 ux = __fadd2_rn(make_float2(s0.x, s0.y), r.nx);
+    const float2 uy = __fadd2_rn(make_float2(s0.z, s0.w), r.ny);
+    const float2 uz = __fadd2_rn(make_float2(s1.x, s1.y), r.nz);
+    const float2 mj = make_float2(s1.z, s1.w), qj = make_float2(s2.x, s2.y);
+    const float2 dx = make_float2(s2.z, s2.w), dy = make_float2(s3.x, s3.y), dz = make_float2(s3.z, s3.w);
+    float2 r2 = __fmul2_rn(ux, ux);
+    r2 = __ffma2_rn(uy, uy, r2);
+    r2 = __ffma2_rn(uz, uz, r2);
+    float2 ri = make_float2(rsqrt_approx_ftz(r2.x), rsqrt_approx_ftz(r2.y));
+    if (MASKED) ri = make_float2(r2.x > 0.0f ? ri.x : 0.0f, r2.y > 0.0f ? ri.y : 0.0f);
+    const float2 ir2 = __fmul2_rn(ri, ri);
+    const float2 ir3 = __fmul2_rn(ir2, ri);
+    const float2 ir5 = __fmul2_rn(ir3, __fmul2_rn(ir2, make_float2(3.0f, 3.0f)));
+    float2 wd = __fmul2_rn(dx, ux);
+    wd = __ffma2_rn(dy, uy, wd);
+    wd = __ffma2_rn(dz, uz, wd);
+    float2 wb = __fmul2_rn(r.bx, ux);
+    wb = __ffma2_rn(r.by, uy, wb);
+    wb = __ffma2_rn(r.bz, uz, wb);
+    A[0] = __ffma2_rn(qj, ri, A[0]);   // P = sum q / r
+    A[1] = __ffma2_rn(wd, ir3, A[1]);  // Q = sum d.u / r^3
+    float2 t = __fmul2_rn(r.m, wd);
+    t = __ffma2_rn(mj, wb, t);
+    const float2 cu = __ffma2_rn(r.nm, __fmul2_rn(qj, ir3), __fmul2_rn(t, ir5));
+    const float2 nmi3 = __fmul2_rn(r.nm, ir3);
+    A[2] = __ffma2_rn(nmi3, dx, __ffma2_rn(cu, ux, A[2]));
+    A[3] = __ffma2_rn(nmi3, dy, __ffma2_rn(cu, uy, A[3]));
+    A[4] = __ffma2_rn(nmi3, dz, __ffma2_rn(cu, uz, A[4]));
+    A[5] = __ffma2_rn(mj, ir3, A[5]);  // SM = sum m_j / r^3
+}
+
+// Source k of the staging buffer into its pair-interleaved slots (asynchronous 4-byte copies).
+__device__ __forceinline__ void vjp_copy_pair(float *fb, int k, const float4 *x, const float4 *sv)
+{
+    float *d = fb + (k >> 1) * 16 + (k & 1);
+    const float *a = reinterpret_cast<const float *>(x), *b = reinterpret_cast<const float *>(sv);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        cp_async4(d + 2 * v, a + v);
+        cp_async4(d + 8 + 2 * v, b + v);
+    }
+}
+
+__device__ __forceinline__ void vjp_pad_pair(float *fb, int k)
+{
+    float *d = fb + (k >> 1) * 16 + (k & 1);
+    d[0] = d[2] = d[4] = 1e18f;
+    d[6] = d[8] = d[10] = d[12] = d[14] = 0.0f;
+}
+
+template <int CH>
+__device__ __forceinline__ int vjp_stage_pairs(float *fb, const float4 *__restrict__ xyzm,
+                                               const float4 *__restrict__ src, int lf, int ex, int tot, int g0,
+                                               int lane)
+{
+    const int n_here = min(CH, tot - g0);
+    for (int k0 = 0; k0 < n_here; k0 += 32) {  // warp-uniform: every lane takes part in the shuffles
+        const int k = k0 + lane;
+        const int g = g0 + k;
+        int lo = 0;
+#pragma unroll
+        for (int step = 16; step > 0; step >>= 1) {
+            const int exm = __shfl_sync(kFull, ex, lo + step);
+            lo = exm <= g ? lo + step : lo;
+        }
+        const int f = __shfl_sync(kFull, lf, lo);
+        const int e = __shfl_sync(kFull, ex, lo);
+        if (k < n_here) vjp_copy_pair(fb, k, xyzm + f + (g - e), src + f + (g - e));
+    }
+    if ((n_here & 1) && lane == 0) vjp_pad_pair(fb, n_here);
+    cp_async_wait_all();
+    return (n_here + 1) >> 1;
+}
+
+template <int K, bool MASKED>
+__device__ __forceinline__ void vjp_span_pairs(const float *fb, int npairs, int q, int S, const VjpRecv (&r)[K],
+                                               float2 (&A)[K][6])
+{
+    const float4 *pb = reinterpret_cast<const float4 *>(fb);
+    for (int j = q; j < npairs; j += S) {
+        const float4 s0 = pb[4 * j], s1 = pb[4 * j + 1], s2 = pb[4 * j + 2], s3 = pb[4 * j + 3];
+#pragma unroll
+        for (int k = 0; k < K; ++k) vjp_two<MASKED>(s0, s1, s2, s3, r[k], A[k]);
+    }
+}
+
+// vjp_round for fp32 plans: the same lane layout and order of sums, the pair
+// terms by vjp_two on pair-interleaved sources.
+template <int K, bool CHUNKED>
+__device__ __forceinline__ void vjp_round_f32(int a, int f, int c, int r0, int cr, int beg, int end, int chunk,
+                                              int nch, int *done, DevCounters *ctr, const int *__restrict__ first,
+                                              const int *__restrict__ count, const float4 *__restrict__ xyzm,
+                                              const float4 *__restrict__ src, const uint32_t *__restrict__ perm,
+                                              const float4 *far, float4 *far_w, const int *__restrict__ lsrc,
+                                              float *__restrict__ pos_bar, float *__restrict__ mass_bar, float *fb,
+                                              float (*red)[4], int lane)
+{
+    constexpr int CH = VjpChunk<float>::value;
+    const int R = (cr + K - 1) / K, S = 32 / R;
+    const int rp = lane % R, q = lane / R;
+    VjpRecv rv[K];
+    float2 A[K][6];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int rr = rp + k * R;
+        const int i = f + r0 + (rr < cr ? rr : 0);
+        const float4 x = xyzm[i], sv = src[i];
+        rv[k].nx = make_float2(-x.x, -x.x);
+        rv[k].ny = make_float2(-x.y, -x.y);
+        rv[k].nz = make_float2(-x.z, -x.z);
+        rv[k].m = make_float2(x.w, x.w);
+        rv[k].nm = make_float2(-x.w, -x.w);
+        rv[k].bx = make_float2(-sv.y, -sv.y);
+        rv[k].by = make_float2(-sv.z, -sv.z);
+        rv[k].bz = make_float2(-sv.w, -sv.w);
+#pragma unroll
+        for (int v = 0; v < 6; ++v) A[k][v] = make_float2(0.0f, 0.0f);
+    }
+    const int qq = q < S ? q : (1 << 30);
+    // the leaf's own particles (zero separations masked; the first chunk of a split receiver)
+    for (int g0 = 0; (!CHUNKED || chunk == 0) && g0 < c; g0 += CH) {
+        const int n_here = min(CH, c - g0);
+        __syncwarp();
+        for (int k = lane; k < n_here; k += 32) vjp_copy_pair(fb, k, xyzm + f + g0 + k, src + f + g0 + k);
+        if ((n_here & 1) && lane == 0) vjp_pad_pair(fb, n_here);
+        cp_async_wait_all();
+        __syncwarp();
+        vjp_span_pairs<K, true>(fb, (n_here + 1) >> 1, qq, S, rv, A);
+    }
+    for (int lb = beg; lb < end; lb += 32) {
+        const int e = lb + lane;
+        int fs = 0, cs = 0;
+        if (e < end) {
+            const int bb = lsrc[e];
+            if (bb != a) {
+                fs = first[bb];
+                cs = count[bb];
+            }
+        }
+        const int incl = warp_incl_scan(cs);
+        const int tot = __shfl_sync(kFull, incl, 31);
+        const int ex = incl - cs;
+        for (int g0 = 0; g0 < tot; g0 += CH) {
+            __syncwarp();
+            const int npairs = vjp_stage_pairs<CH>(fb, xyzm, src, fs, ex, tot, g0, lane);
+            __syncwarp();
+            vjp_span_pairs<K, false>(fb, npairs, qq, S, rv, A);
+        }
+    }
+    if (CHUNKED && r0 == 0) wait_turn(done + a, chunk, ctr);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const float sm = A[k][5].x + A[k][5].y;
+        __syncwarp();
+        red[lane][0] = (A[k][1].x + A[k][1].y) - (A[k][0].x + A[k][0].y);
+        red[lane][1] = (A[k][2].x + A[k][2].y) - sm * rv[k].bx.x;
+        red[lane][2] = (A[k][3].x + A[k][3].y) - sm * rv[k].by.x;
+        red[lane][3] = (A[k][4].x + A[k][4].y) - sm * rv[k].bz.x;
+        __syncwarp();
+        const int rr = rp + k * R;
+        if (q == 0 && rr < cr) {
+            float t[4] = {red[rp][0], red[rp][1], red[rp][2], red[rp][3]};
+            for (int qs = 1; qs < S; ++qs)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) t[v] += red[qs * R + rp][v];
+            const int i = f + r0 + rr;
+            const float4 fa = CHUNKED ? ld_cg(far + i) : far[i];
+            if (CHUNKED && chunk < nch - 1) {
+                far_w[i] = make_float4(fa.x + t[0], fa.y + t[1], fa.z + t[2], fa.w + t[3]);
+            } else {
+                const uint32_t o = perm[i];
+                pos_bar[3 * (size_t)o] = fa.y + t[1];
+                pos_bar[3 * (size_t)o + 1] = fa.z + t[2];
+                pos_bar[3 * (size_t)o + 2] = fa.w + t[3];
+                mass_bar[o] = fa.x + t[0];
+            }
+        }
+    }
+}
+
 // The near field of the VJP: the forward evaluation's P2P work items (a
 // receiving leaf, or one chunk of a split one), taken from a shared counter
 // in decreasing order of work, a warp each.
@@ -359,8 +568,7 @@ __global__ __launch_bounds__(VJP_WARPS * 32) void k_vjp_near(
     const int *__restrict__ off, const int *__restrict__ lsrc, T *__restrict__ pos_bar, T *__restrict__ mass_bar)
 {
     constexpr int CH = VjpChunk<T>::value;
-    __shared__ vec4<T> s_x[VJP_WARPS][CH];
-    __shared__ vec4<T> s_s[VJP_WARPS][CH];
+    __shared__ __align__(16) unsigned char s_buf[VJP_WARPS][2 * CH * sizeof(vec4<T>)];  // staged sources
     __shared__ T s_red[VJP_WARPS][32][4];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int n_work = 0;
@@ -379,14 +587,25 @@ __global__ __launch_bounds__(VJP_WARPS * 32) void k_vjp_near(
             end = beg + len * (chunk + 1) / nch;
             beg = beg + len * chunk / nch;
         }
+        vec4<T> *const bx = reinterpret_cast<vec4<T> *>(s_buf[w]), *const bs = bx + CH;
         for (int r0 = 0; r0 < c; r0 += 32 * K) {
             const int cr = min(32 * K, c - r0);
-            if (nch == 1)
-                vjp_round<T, K, false>(a, f, c, r0, cr, beg, end, 0, 1, done, ctr, first, count, xyzm, src, perm,
-                                       far, far_w, lsrc, pos_bar, mass_bar, s_x[w], s_s[w], s_red[w], lane);
-            else
-                vjp_round<T, K, true>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, src,
-                                      perm, far, far_w, lsrc, pos_bar, mass_bar, s_x[w], s_s[w], s_red[w], lane);
+            if constexpr (std::is_same<T, float>::value) {
+                float *const fb = reinterpret_cast<float *>(s_buf[w]);  // CH sources of 8 floats
+                if (nch == 1)
+                    vjp_round_f32<K, false>(a, f, c, r0, cr, beg, end, 0, 1, done, ctr, first, count, xyzm, src,
+                                            perm, far, far_w, lsrc, pos_bar, mass_bar, fb, s_red[w], lane);
+                else
+                    vjp_round_f32<K, true>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm,
+                                           src, perm, far, far_w, lsrc, pos_bar, mass_bar, fb, s_red[w], lane);
+            } else {
+                if (nch == 1)
+                    vjp_round<T, K, false>(a, f, c, r0, cr, beg, end, 0, 1, done, ctr, first, count, xyzm, src,
+                                           perm, far, far_w, lsrc, pos_bar, mass_bar, bx, bs, s_red[w], lane);
+                else
+                    vjp_round<T, K, true>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm,
+                                          src, perm, far, far_w, lsrc, pos_bar, mass_bar, bx, bs, s_red[w], lane);
+            }
         }
         if (nch > 1 && chunk < nch - 1) pass_turn(done + a, chunk + 1);
     }
@@ -423,7 +642,7 @@ int launch_vjp_tp(Plan &P_, const void *abar, const void *pbar, void *pos_bar, v
     // the near field takes the forward evaluation's work items afresh (work counter 0 was reset above
     // and neither M2L nor L2L uses it); its chunk flags start again from zero
     cudaMemsetAsync(P_.p2p_done, 0, (size_t)P_.cap_nodes * sizeof(int), s);
-    k_vjp_near<T, kVjpK><<<P_.num_sms * 16, VJP_WARPS * 32, 0, s>>>(
+    k_vjp_near<T, VjpK<T>::value><<<P_.num_sms * 16, VJP_WARPS * 32, 0, s>>>(
         P_.ctr, P_.p2p_items, P_.p2p_done, P_.ctr, P_.node_first, P_.node_count, (const vec4<T> *)P_.xyzm,
         (const vec4<T> *)P_.vjp_src, P_.idx[0], (const vec4<T> *)P_.far, (vec4<T> *)P_.far, P_.p2p_off,
         P_.p2p_src, (T *)pos_bar, (T *)mass_bar);
