@@ -293,7 +293,13 @@ def reduced_contraction(p, m_name, l_name, mirrored):
 
 
 def reduced_derivs_body(p):
-    """Lines building D[] (the reduced derivative tensor of 1/r at (rx, ry, rz))."""
+    """Lines building D[] (the reduced derivative tensor of 1/r at (rx, ry, rz)).
+
+    The recurrence l r^2 D^n = -(2l-1) sum_i n_i R_i D^{n-e_i}
+    - (l-1) sum_i n_i (n_i-1) D^{n-2e_i} with its constants folded into
+    per-level coefficients, A_{l,i,m} = a_i (-(2l-1)/l) m (a = R / r^2) and
+    C_{l,c} = (1/r^2) (-(l-1)/l) c, so each D^n is a sum of coefficient-times-D
+    terms (one product and a chain of fused multiply-adds)."""
     mi, slot = reduced_derivs(p)
     b = [f"  T D[{len(mi)}];",
          "  const T r2 = rx * rx + ry * ry + rz * rz;",
@@ -301,30 +307,39 @@ def reduced_derivs_body(p):
     if p > 0:
         b.append("  const T ir2 = D[0] * D[0];")
         b.append("  const T ax = rx * ir2, ay = ry * ir2, az = rz * ir2;")
-        for a in AX:
-            for k in range(2, p + 1):
-                b.append(f"  const T a{a}{k} = a{a} * {lit(k)};")
-        for l in range(2, p + 1):
-            b.append(f"  const T c2_{l} = ir2 * {lit(-(l - 1) / l)};")
+    need_a, need_c, terms_of = [], [], {}
     for n in mi[1:]:
         if n[2] == 2:
             continue
         l = sum(n)
-        s1, s2 = [], []
+        terms = []
         for i in range(3):
             if n[i] >= 1:
                 m = list(n)
                 m[i] -= 1
-                coef = f"a{AX[i]}" if n[i] == 1 else f"a{AX[i]}{n[i]}"
-                s1.append(f"{coef} * D[{slot[tuple(m)]}]")
+                if l == 1:
+                    terms.append((f"(-a{AX[i]})", slot[tuple(m)]))
+                else:
+                    key = (l, i, n[i])
+                    if key not in need_a:
+                        need_a.append(key)
+                    terms.append((f"A{l}{AX[i]}{n[i]}", slot[tuple(m)]))
             if n[i] >= 2:
                 m = list(n)
                 m[i] -= 2
-                s2.append(f"{lit(n[i] * (n[i] - 1))} * D[{slot[tuple(m)]}]")
-        expr = f"{lit(-(2 * l - 1) / l)} * ({' + '.join(s1)})"
-        if s2:
-            expr += f" + c2_{l} * ({' + '.join(s2)})"
-        b.append(f"  D[{slot[n]}] = {expr};")
+                key = (l, n[i] * (n[i] - 1))
+                if key not in need_c:
+                    need_c.append(key)
+                terms.append((f"C{l}_{key[1]}", slot[tuple(m)]))
+        terms_of[n] = terms
+    for l, i, m in need_a:
+        b.append(f"  const T A{l}{AX[i]}{m} = a{AX[i]} * {lit(-(2 * l - 1) / l * m)};")
+    for l, c in need_c:
+        b.append(f"  const T C{l}_{c} = ir2 * {lit(-(l - 1) / l * c)};")
+    for n in mi[1:]:
+        if n[2] == 2:
+            continue
+        b.append(f"  D[{slot[n]}] = " + " + ".join(f"{c} * D[{sl}]" for c, sl in terms_of[n]) + ";")
     for n in mi:
         if n[2] == 2:
             a_, b_ = (n[0] + 2, n[1], 0), (n[0], n[1] + 2, 0)
