@@ -33,6 +33,7 @@
 //                part's buffered sums in list order and the far field, written
 //                in the caller's order.
 #include <climits>
+#include <type_traits>
 
 #include "expansions_gen.cuh"
 #include "plan.h"
@@ -368,9 +369,319 @@ __global__ __launch_bounds__(256) void k_p2p_mut2(const DevCounters *__restrict_
     }
 }
 
+// ---- fp32: the mutual near field on the forward near field's lane layout ----
+// k_p2p_mutf replaces k_p2p_mut1 for fp32 plans. A round holds up to 32 K
+// receivers of leaf a: lane = q R + rp (rp < R = ceil(cr / K), q < S = 32 / R)
+// holds receivers rp + k R, k < K; the lanes of group q walk the staged
+// partner particles in pairs q, q + S, ..., two sources per f32x2
+// instruction. For each source pair a lane sums the reaction of its K
+// receivers in registers; every MF_FLUSH steps the group's R partial reactions
+// of each pair go through shared memory and are added in order of rp by one lane
+// of the group (a transpose: lane rp of the group finishes the flush's rp-th
+// pair), which adds them to the pair's buffer slots. Receivers beyond the leaf
+// (the last round's padding) carry zero mass, so they react with nothing.
+constexpr int MF_WARPS = 4;
+constexpr int MF_CH = 256;    // staged partner particles per chunk
+constexpr int MF_K = 4;       // receivers per lane
+constexpr int MF_FLUSH = 6;   // source-pair steps per flush of the partial reactions (shared memory: 4 blocks per SM)
+
+struct MfWarp {
+    float pos[MF_CH * 4];              // pair-interleaved (x0, x1, y0, y1, z0, z1, m0, m1) per source pair
+    long long dst[MF_CH];              // share slot of each staged particle (-1: a padding particle)
+    float4 part[MF_FLUSH][32][2];      // a flush's partial reactions: step, lane, two float4 of packed halves
+    float red[32][4];                  // the receivers' sums over the S groups
+};
+
+__device__ __forceinline__ float rsqrt_fast(float x)
+{
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Sources (SX, SY, SZ, SM: two particles) and one receiver (negated position
+// NX, NY, NZ and mass MI, both halves equal): the receiver's sums A (sum m_j /
+// r, then the acceleration) and the sources' reaction B (their potential, then
+// their acceleration), in packed halves.
+__device__ __forceinline__ void mf_pair(float2 SX, float2 SY, float2 SZ, float2 SM, float2 NX, float2 NY, float2 NZ,
+                                        float2 NMI, float2 (&A)[4], float2 (&B)[4])
+{
+    const float2 dx = __fadd2_rn(SX, NX), dy = __fadd2_rn(SY, NY), dz = __fadd2_rn(SZ, NZ);
+    float2 r2 = __fmul2_rn(dx, dx);
+    r2 = __ffma2_rn(dy, dy, r2);
+    r2 = __ffma2_rn(dz, dz, r2);
+    const float2 ri = make_float2(rsqrt_fast(r2.x), rsqrt_fast(r2.y));
+    const float2 ri2 = __fmul2_rn(ri, ri);
+    const float2 mr = __fmul2_rn(SM, ri);
+    const float2 mr3 = __fmul2_rn(mr, ri2);
+    A[0] = __fadd2_rn(A[0], mr);
+    A[1] = __ffma2_rn(mr3, dx, A[1]);
+    A[2] = __ffma2_rn(mr3, dy, A[2]);
+    A[3] = __ffma2_rn(mr3, dz, A[3]);
+    const float2 nmr = __fmul2_rn(NMI, ri);  // -m_i / r
+    const float2 nmr3 = __fmul2_rn(nmr, ri2);
+    B[0] = __fadd2_rn(B[0], nmr);            // the sources' potential
+    B[1] = __ffma2_rn(nmr3, dx, B[1]);       // and acceleration, -m_i (x_j - x_i) / r^3
+    B[2] = __ffma2_rn(nmr3, dy, B[2]);
+    B[3] = __ffma2_rn(nmr3, dz, B[3]);
+}
+
+// One source of the own leaf (zero separations masked) on one receiver, scalar.
+__device__ __forceinline__ void mf_own(const float4 &s, float x, float y, float z, float (&a)[4])
+{
+    const float dx = s.x - x, dy = s.y - y, dz = s.z - z;
+    const float r2 = dx * dx + dy * dy + dz * dz;
+    const float ri = r2 > 0.0f ? rsqrt_fast(r2) : 0.0f;
+    const float mr = s.w * ri;
+    const float mr3 = mr * ri * ri;
+    a[0] += mr;
+    a[1] += mr3 * dx;
+    a[2] += mr3 * dy;
+    a[3] += mr3 * dz;
+}
+
+__device__ __forceinline__ void mf_put_pad(float *pb, int k)
+{
+    float *d = pb + (k >> 1) * 8 + (k & 1);
+    d[0] = d[2] = d[4] = 1e18f;
+    d[6] = 0.0f;
+}
+
+// Add a finished flush: lane rp < nf of group q adds the R partials of source
+// pair (pair0 + (t0 + rp) S) in order of rp' and adds the two sources' sums to
+// their slots (round 0 stores, later rounds of the same receiver add).
+__device__ __forceinline__ void mf_flush(MfWarp &W, int nf, int t0, int q, int rp, int R, int S, bool worker,
+                                         int npairs, bool first_round, float4 *rbuf, long long cap_rp,
+                                         DevCounters *ctr)
+{
+    __syncwarp();
+    if (worker && rp < nf) {
+        const int j = q + (t0 + rp) * S;  // the pair this lane finishes
+        if (j < npairs) {
+            float4 u = W.part[rp][q * R][0], v = W.part[rp][q * R][1];
+            for (int r = 1; r < R; ++r) {
+                const float4 u2 = W.part[rp][q * R + r][0], v2 = W.part[rp][q * R + r][1];
+                u = make_float4(u.x + u2.x, u.y + u2.y, u.z + u2.z, u.w + u2.w);
+                v = make_float4(v.x + v2.x, v.y + v2.y, v.z + v2.z, v.w + v2.w);
+            }
+            // u = (pot0, pot1, ax0, ax1), v = (ay0, ay1, az0, az1)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const long long d = W.dst[2 * j + h];
+                if (d < 0) continue;
+                if (d >= cap_rp) {
+                    set_error(ctr, ERR_BOUNDS);
+                    continue;
+                }
+                float4 val = h == 0 ? make_float4(u.x, u.z, v.x, v.z) : make_float4(u.y, u.w, v.y, v.w);
+                if (!first_round) {
+                    const float4 old = rbuf[d];
+                    val = make_float4(old.x + val.x, old.y + val.y, old.z + val.z, old.w + val.w);
+                }
+                rbuf[d] = val;
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// One round of up to 32 K receivers [r0, r0 + cr) of leaf a against the upper
+// entries [ub, ue) of its list (and, for the first chunk, its own leaf).
+template <bool CHUNKED>
+__device__ __forceinline__ void mf_round(int a, int f, int c, int r0, int cr, int ub, int ue, int chunk, int *done,
+                                         DevCounters *ctr, const int *__restrict__ first,
+                                         const int *__restrict__ count, const float4 *__restrict__ xyzm,
+                                         const int *__restrict__ off, const int *__restrict__ src,
+                                         const int *__restrict__ mir, long long cap_ep,
+                                         const long long *__restrict__ base, long long cap_rp, float4 *rbuf,
+                                         float4 *own, MfWarp &W, int lane)
+{
+    constexpr int K = MF_K;
+    const int R = (cr + K - 1) / K, S = 32 / R;
+    const int rp = lane % R, q = lane / R;
+    const bool worker = q < S;
+    const int F = R < MF_FLUSH ? R : MF_FLUSH;  // steps per flush: a group's lanes finish one pair each
+    float2 NX[K], NY[K], NZ[K], NMI[K];
+    float2 A[K][4];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const int rr = rp + k * R;
+        const bool valid = rr < cr;
+        const float4 x = xyzm[f + r0 + (valid ? rr : 0)];
+        NX[k] = make_float2(-x.x, -x.x);
+        NY[k] = make_float2(-x.y, -x.y);
+        NZ[k] = make_float2(-x.z, -x.z);
+        NMI[k] = valid ? make_float2(-x.w, -x.w) : make_float2(0.0f, 0.0f);  // padding receivers: no reaction
+#pragma unroll
+        for (int v = 0; v < 4; ++v) A[k][v] = make_float2(0.0f, 0.0f);
+    }
+    // the leaf's own particles, directed (zero separations masked), with the first chunk
+    if (!CHUNKED || chunk == 0) {
+        float o[K][4];
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) o[k][v] = 0.0f;
+        float4 *buf = reinterpret_cast<float4 *>(W.pos);
+        for (int g0 = 0; g0 < c; g0 += MF_CH) {
+            const int n_here = min(MF_CH, c - g0);
+            __syncwarp();
+            for (int k = lane; k < n_here; k += 32) buf[k] = xyzm[f + g0 + k];
+            __syncwarp();
+            if (worker)
+                for (int j = q; j < n_here; j += S) {
+                    const float4 s4 = buf[j];
+#pragma unroll
+                    for (int k = 0; k < K; ++k) mf_own(s4, -NX[k].x, -NY[k].x, -NZ[k].x, o[k]);
+                }
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k)
+#pragma unroll
+            for (int v = 0; v < 4; ++v) A[k][v].x += o[k][v];
+    }
+    const float4 *pb = reinterpret_cast<const float4 *>(W.pos);
+    // the upper partners, 32 list entries at a time (lane i holds entry lb + i and its share slot)
+    for (int lb = ub; lb < ue; lb += 32) {
+        const int e = lb + lane;
+        int fb = 0, cb = 0;
+        long long sl = -1;
+        if (e < ue) {
+            const int b = src[e];
+            const int m = e < cap_ep ? mir[e] : -1;
+            fb = first[b];
+            cb = count[b];
+            sl = m >= 0 ? base[b] + (long long)(m - off[b]) * cb : -1;
+        }
+        const int incl = warp_incl_scan(cb);
+        const int tot = __shfl_sync(kFull, incl, 31);
+        const int ex = incl - cb;
+        for (int g0 = 0; g0 < tot; g0 += MF_CH) {
+            const int n_here = min(MF_CH, tot - g0);
+            __syncwarp();
+            for (int k0 = 0; k0 < n_here; k0 += 32) {  // warp-uniform: every lane takes part in the shuffles
+                const int k = k0 + lane;
+                const int g = g0 + k;
+                int lo = 0;  // last lane whose leaf starts at or before g
+#pragma unroll
+                for (int step = 16; step > 0; step >>= 1) {
+                    const int exm = __shfl_sync(kFull, ex, lo + step);
+                    lo = exm <= g ? lo + step : lo;
+                }
+                const int fs = __shfl_sync(kFull, fb, lo);
+                const int es = __shfl_sync(kFull, ex, lo);
+                const long long ss = __shfl_sync(kFull, sl, lo);
+                if (k < n_here) {
+                    const float *v = reinterpret_cast<const float *>(xyzm + fs + (g - es));
+                    float *d = W.pos + (k >> 1) * 8 + (k & 1);
+                    cp_async4(d, v);
+                    cp_async4(d + 2, v + 1);
+                    cp_async4(d + 4, v + 2);
+                    cp_async4(d + 6, v + 3);
+                    W.dst[k] = ss >= 0 ? ss + (g - es) : -1;
+                }
+            }
+            if ((n_here & 1) && lane == 0) {
+                mf_put_pad(W.pos, n_here);
+                W.dst[n_here] = -1;
+            }
+            cp_async_wait_all();
+            __syncwarp();
+            const int npairs = (n_here + 1) >> 1;
+            const int T = (npairs + S - 1) / S;  // steps: pair q + t S of group q at step t
+            for (int t0 = 0; t0 < T; t0 += F) {
+                const int nf = min(F, T - t0);
+                for (int tt = 0; tt < nf; ++tt) {
+                    const int j = q + (t0 + tt) * S;
+                    float2 B[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                                   make_float2(0.0f, 0.0f)};
+                    if (worker && j < npairs) {
+                        const float4 p0 = pb[2 * j], p1 = pb[2 * j + 1];
+                        const float2 SX = make_float2(p0.x, p0.y), SY = make_float2(p0.z, p0.w);
+                        const float2 SZ = make_float2(p1.x, p1.y), SM = make_float2(p1.z, p1.w);
+#pragma unroll
+                        for (int k = 0; k < K; ++k) mf_pair(SX, SY, SZ, SM, NX[k], NY[k], NZ[k], NMI[k], A[k], B);
+                    }
+                    W.part[tt][lane][0] = make_float4(B[0].x, B[0].y, B[1].x, B[1].y);
+                    W.part[tt][lane][1] = make_float4(B[2].x, B[2].y, B[3].x, B[3].y);
+                }
+                mf_flush(W, nf, t0, q, rp, R, S, worker, npairs, r0 == 0, rbuf, cap_rp, ctr);
+            }
+        }
+    }
+    // the receivers' sums over the S groups, then the chunks of a split receiver in chunk order
+    if (CHUNKED && r0 == 0) wait_turn(done + a, chunk, ctr);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        __syncwarp();
+        W.red[lane][0] = A[k][0].x + A[k][0].y;
+        W.red[lane][1] = A[k][1].x + A[k][1].y;
+        W.red[lane][2] = A[k][2].x + A[k][2].y;
+        W.red[lane][3] = A[k][3].x + A[k][3].y;
+        __syncwarp();
+        const int rr = rp + k * R;
+        if (q == 0 && rr < cr) {
+            float t[4] = {W.red[rp][0], W.red[rp][1], W.red[rp][2], W.red[rp][3]};
+            for (int qs = 1; qs < S; ++qs)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) t[v] += W.red[qs * R + rp][v];
+            const int i = f + r0 + rr;
+            float4 v = make_float4(-t[0], t[1], t[2], t[3]);
+            if (CHUNKED && chunk > 0) {
+                const float4 prev = ld_cg(own + i);  // the earlier chunks' sums, written by other warps
+                v = make_float4(prev.x + v.x, prev.y + v.y, prev.z + v.z, prev.w + v.w);
+            }
+            own[i] = v;
+        }
+    }
+}
+
+__global__ __launch_bounds__(MF_WARPS * 32) void k_p2p_mutf(
+    const DevCounters *__restrict__ cst, const int2 *__restrict__ items, int *done, DevCounters *ctr,
+    const int *__restrict__ first, const int *__restrict__ count, const float4 *__restrict__ xyzm,
+    const int *__restrict__ off, const int *__restrict__ src, const int *__restrict__ up_p2p,
+    const int *__restrict__ mir, long long cap_ep, const long long *__restrict__ base, long long cap_rp,
+    float4 *rbuf, float4 *own)
+{
+    extern __shared__ __align__(16) unsigned char mf_smem[];
+    MfWarp &W = reinterpret_cast<MfWarp *>(mf_smem)[threadIdx.x >> 5];
+    const int lane = threadIdx.x & 31;
+    int n_work = 0;
+    for (int bkt = 1; bkt < 64; ++bkt) n_work += cst->order_cnt[0][bkt];
+    for (;;) {
+        int t = 0;
+        if (lane == 0) t = atomicAdd(&ctr->work_ctr[0], 1);
+        t = __shfl_sync(kFull, t, 0);
+        if (t >= n_work) break;
+        const int2 item = items[t];
+        const int a = item.x, nch = item.y >> 8, chunk = item.y & 255;
+        const int f = first[a], c = count[a];
+        const int u0 = off[a] + up_p2p[a], ulen = off[a + 1] - u0;
+        const int ub = u0 + (int)((long long)ulen * chunk / nch), ue = u0 + (int)((long long)ulen * (chunk + 1) / nch);
+        for (int r0 = 0; r0 < c; r0 += 32 * MF_K) {
+            const int cr = min(32 * MF_K, c - r0);
+            if (nch == 1)
+                mf_round<false>(a, f, c, r0, cr, ub, ue, 0, done, ctr, first, count, xyzm, off, src, mir, cap_ep,
+                                base, cap_rp, rbuf, own, W, lane);
+            else
+                mf_round<true>(a, f, c, r0, cr, ub, ue, chunk, done, ctr, first, count, xyzm, off, src, mir, cap_ep,
+                               base, cap_rp, rbuf, own, W, lane);
+        }
+        if (nch > 1 && chunk < nch - 1) pass_turn(done + a, chunk + 1);
+    }
+}
+
 template <class T>
 int launch_p2p_mutual_t(Plan &P, void *acc, void *pot, cudaStream_t s)
 {
+    if constexpr (std::is_same<T, float>::value) {
+        const int smem = MF_WARPS * (int)sizeof(MfWarp);
+        cudaFuncSetAttribute(k_p2p_mutf, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        k_p2p_mutf<<<P.num_sms * 16, MF_WARPS * 32, smem, s>>>(
+            P.ctr, P.p2p_items, P.p2p_done, P.ctr, P.node_first, P.node_count, (const float4 *)P.xyzm, P.p2p_off,
+            P.p2p_src, P.mut_lo + 2 * P.cap_nodes, P.mut_mir_p2p, P.mut_cap_ep, P.mut_base, P.mut_cap_rp,
+            (float4 *)P.mut_rp2p, (float4 *)P.mut_own);
+    } else
     k_p2p_mut1<T><<<P.num_sms * 16, MUT_WARPS * 32, 0, s>>>(
         P.ctr, P.p2p_items, P.p2p_done, P.ctr, P.node_first, P.node_count, (const vec4<T> *)P.xyzm, P.p2p_off, P.p2p_src,
         P.mut_lo + 2 * P.cap_nodes, P.mut_mir_p2p, P.mut_cap_ep, P.mut_base, P.mut_cap_rp, (vec4<T> *)P.mut_rp2p,

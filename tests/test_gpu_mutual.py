@@ -171,3 +171,44 @@ def test_mutual_buffers_regrow_to_the_same_result(tmp_path):
     print(f"regrowths: {normal['retries']} normal, {small['retries']} from minimal buffers")
     assert small["retries"] > normal["retries"]
     assert np.array_equal(np.load(tmp_path / "n.npy"), np.load(tmp_path / "s.npy"))
+
+
+def test_vjp_and_kdk_on_a_mutual_plan():
+    """A mutual plan's forward evaluation feeds fmm_vjp and fmm_kdk_step like the default one: the VJP (its
+    own stages are the same) agrees with the default plan's to rounding, and so does one KDK step."""
+    import torch
+
+    from body_forces_morton_b300 import native
+
+    w = W.WORKLOADS[4]
+    n = 40000
+    g = W.generate(w, n=n)
+    rng = np.random.default_rng(31)
+    ab = rng.normal(size=(n, 3)).astype(np.float32)
+    pb = rng.normal(size=n).astype(np.float32)
+    out = {}
+    for mutual in (False, True):
+        tp = torch.from_numpy(g["pos"]).cuda()
+        tm = torch.from_numpy(g["mass"]).cuda()
+        xb = torch.empty_like(tp)
+        mb = torch.empty_like(tm)
+        vel = torch.zeros_like(tp)
+        with native.Plan(n, w.p, w.theta, w.leaf, "f32", mutual=mutual) as pl:
+            pl.vjp(tp, tm, torch.from_numpy(ab).cuda(), torch.from_numpy(pb).cuda(), xb, mb)
+            torch.cuda.synchronize()
+            x2 = tp.clone()
+            pl.kdk_step(x2, vel, tm, 1e-3)
+            torch.cuda.synchronize()
+            out[mutual] = (xb.cpu().numpy(), mb.cpu().numpy(), x2.cpu().numpy(), vel.cpu().numpy())
+    d, m = out[False], out[True]
+    ex = accel_error(m[0].astype(np.float64), d[0].astype(np.float64))
+    ev = accel_error(m[3].astype(np.float64), d[3].astype(np.float64))
+    print(f"mutual against default: pos_bar {ex.max():.2e}, KDK velocity {ev.max():.2e}")
+    # the VJP's inputs (the forward accelerations, the lists) agree to fp32 rounding, so its outputs do
+    # too, up to the cancellation its own fp32 gate allows. The KDK velocity adds the force at the drifted
+    # positions, which already differ at the rounding level between the plans, and close pairs amplify
+    # that (1 / r^3); each plan's forces are within the parity gate of the oracle, which bounds it
+    # (measured 2.8e-5)
+    assert ex.max() <= 5e-3 and np.percentile(ex, 99) <= 1e-4
+    assert ev.max() <= TOL_ACC["f32"]
+    assert np.abs(m[2] - d[2]).max() <= 1e-6 * np.abs(d[2]).max()
