@@ -388,7 +388,9 @@ constexpr int MF_FLUSH = 6;   // source-pair steps per flush of the partial reac
 struct MfWarp {
     float pos[MF_CH * 4];              // pair-interleaved (x0, x1, y0, y1, z0, z1, m0, m1) per source pair
     long long dst[MF_CH];              // share slot of each staged particle (-1: a padding particle)
-    float4 part[MF_FLUSH][32][2];      // a flush's partial reactions: step, lane, two float4 of packed halves
+    float4 part[MF_FLUSH][65];         // a flush's partial reactions: step, then lane x two float4 of packed
+                                       // halves, rows padded to an odd number of 16-byte units (the finishing
+                                       // lanes read down a column)
     float red[32][4];                  // the receivers' sums over the S groups
 };
 
@@ -458,12 +460,18 @@ __device__ __forceinline__ void mf_flush(MfWarp &W, int nf, int t0, int q, int r
     if (worker && rp < nf) {
         const int j = q + (t0 + rp) * S;  // the pair this lane finishes
         if (j < npairs) {
-            float4 u = W.part[rp][q * R][0], v = W.part[rp][q * R][1];
-            for (int r = 1; r < R; ++r) {
-                const float4 u2 = W.part[rp][q * R + r][0], v2 = W.part[rp][q * R + r][1];
-                u = make_float4(u.x + u2.x, u.y + u2.y, u.z + u2.z, u.w + u2.w);
-                v = make_float4(v.x + v2.x, v.y + v2.y, v.z + v2.z, v.w + v2.w);
+            float4 u = W.part[rp][2 * (q * R)], v = W.part[rp][2 * (q * R) + 1];
+            float2 u0 = make_float2(u.x, u.y), u1 = make_float2(u.z, u.w);
+            float2 v0 = make_float2(v.x, v.y), v1 = make_float2(v.z, v.w);
+            for (int r = 1; r < R; ++r) {  // packed adds, in order of r
+                const float4 u2 = W.part[rp][2 * (q * R + r)], v2 = W.part[rp][2 * (q * R + r) + 1];
+                u0 = __fadd2_rn(u0, make_float2(u2.x, u2.y));
+                u1 = __fadd2_rn(u1, make_float2(u2.z, u2.w));
+                v0 = __fadd2_rn(v0, make_float2(v2.x, v2.y));
+                v1 = __fadd2_rn(v1, make_float2(v2.z, v2.w));
             }
+            u = make_float4(u0.x, u0.y, u1.x, u1.y);
+            v = make_float4(v0.x, v0.y, v1.x, v1.y);
             // u = (pot0, pot1, ax0, ax1), v = (ay0, ay1, az0, az1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -541,11 +549,13 @@ __device__ __forceinline__ void mf_round(int a, int f, int c, int r0, int cr, in
             for (int v = 0; v < 4; ++v) A[k][v].x += o[k][v];
     }
     const float4 *pb = reinterpret_cast<const float4 *>(W.pos);
-    // the upper partners, 32 list entries at a time (lane i holds entry lb + i and its share slot)
-    for (int lb = ub; lb < ue; lb += 32) {
+    // the upper partners, 32 list entries at a time (lane i holds entry lb + i and its share slot); the
+    // next group's entries load while this one computes
+    auto fetch = [&](int lb, int &fb, int &cb, long long &sl) {
         const int e = lb + lane;
-        int fb = 0, cb = 0;
-        long long sl = -1;
+        fb = 0;
+        cb = 0;
+        sl = -1;
         if (e < ue) {
             const int b = src[e];
             const int m = e < cap_ep ? mir[e] : -1;
@@ -553,6 +563,14 @@ __device__ __forceinline__ void mf_round(int a, int f, int c, int r0, int cr, in
             cb = count[b];
             sl = m >= 0 ? base[b] + (long long)(m - off[b]) * cb : -1;
         }
+    };
+    int fb_n = 0, cb_n = 0;
+    long long sl_n = -1;
+    if (ub < ue) fetch(ub, fb_n, cb_n, sl_n);
+    for (int lb = ub; lb < ue; lb += 32) {
+        const int fb = fb_n, cb = cb_n;
+        const long long sl = sl_n;
+        if (lb + 32 < ue) fetch(lb + 32, fb_n, cb_n, sl_n);
         const int incl = warp_incl_scan(cb);
         const int tot = __shfl_sync(kFull, incl, 31);
         const int ex = incl - cb;
@@ -602,8 +620,8 @@ __device__ __forceinline__ void mf_round(int a, int f, int c, int r0, int cr, in
 #pragma unroll
                         for (int k = 0; k < K; ++k) mf_pair(SX, SY, SZ, SM, NX[k], NY[k], NZ[k], NMI[k], A[k], B);
                     }
-                    W.part[tt][lane][0] = make_float4(B[0].x, B[0].y, B[1].x, B[1].y);
-                    W.part[tt][lane][1] = make_float4(B[2].x, B[2].y, B[3].x, B[3].y);
+                    W.part[tt][2 * lane] = make_float4(B[0].x, B[0].y, B[1].x, B[1].y);
+                    W.part[tt][2 * lane + 1] = make_float4(B[2].x, B[2].y, B[3].x, B[3].y);
                 }
                 mf_flush(W, nf, t0, q, rp, R, S, worker, npairs, r0 == 0, rbuf, cap_rp, ctr);
             }

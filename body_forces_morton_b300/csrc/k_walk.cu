@@ -603,10 +603,12 @@ int launch_lists(Plan &P, cudaStream_t s)
     k_csr_fill<<<P.num_sms * 8, 256, 0, s>>>(P.m2l_pairs, (int)(P.cap_m2l / kShards), P.p2p_pairs,
                                              (int)(P.cap_p2p / kShards), P.m2l_cnt, P.p2p_cnt, P.m2l_off, P.p2p_off,
                                              P.m2l_src, P.p2p_src, P.ctr);
-    // mutual plans split heavy receivers much finer: their near-field kernel walks each partner leaf in
-    // dependent steps of one pair per lane, so one warp on a receiver with a long list would be the tail
-    const long long chunk_work = P.mutual ? kChunkWorkMutual : kChunkWork;
-    const int max_chunks = P.mutual ? kMaxChunksMutual : kMaxChunks;
+    // fp64 mutual plans split heavy receivers much finer: their near-field kernel walks each partner leaf
+    // in dependent steps of one pair per lane, so one warp on a receiver with a long list would be the
+    // tail (the fp32 mutual kernel has the forward near field's lane layout and its chunks)
+    const bool fine = P.mutual && P.dtype != 0;
+    const long long chunk_work = fine ? kChunkWorkMutual : kChunkWork;
+    const int max_chunks = fine ? kMaxChunksMutual : kMaxChunks;
     k_segsort<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, cap, chunk_work, max_chunks, P.p2p_nch, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
                                             P.node_count, P.order_key, P.ctr);
     k_segsort_long<<<P.num_sms, 1024, 0, s>>>(P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
