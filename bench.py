@@ -154,8 +154,9 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def time_oracle(w, n_sample, steps=1):
-    """Oracle FMM (as it stands) on the first n_sample particles' recipe; particles/s."""
+def time_oracle(w, n_sample, steps=1, nthreads=0):
+    """Oracle FMM (as it stands) on the first n_sample particles' recipe; particles/s.
+    nthreads 0 takes every host core (OpenMP over receivers), 1 runs single-threaded."""
     import oracle
 
     g = W.generate(w, n=n_sample)
@@ -163,9 +164,25 @@ def time_oracle(w, n_sample, steps=1):
     ts = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        oracle.fmm(g["pos"], g["mass"], w.p, w.theta, w.leaf, nthreads=0)
+        oracle.fmm(g["pos"], g["mass"], w.p, w.theta, w.leaf, nthreads=nthreads)
         ts.append(time.perf_counter() - t0)
     return n_sample / statistics.median(ts), statistics.median(ts)
+
+
+def time_direct_sums():
+    """The oracle's O(N^2) direct sum (Kahan-compensated, fp64, every host core) on the configurations
+    where it runs in full: uniform 4096 and Plummer 1e4; particles/s and seconds."""
+    import oracle
+
+    out = {}
+    for idx in (1, 2):
+        wk = W.WORKLOADS[idx]
+        g = W.generate(wk)
+        t0 = time.perf_counter()
+        oracle.direct_sum(g["pos"], g["mass"], nthreads=0)
+        t = time.perf_counter() - t0
+        out[wk.name] = {"value": wk.n / t, "unit": "particles/s", "s": t}
+    return out
 
 
 def run_reference(args, rank, world):
@@ -488,9 +505,14 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and not args.no_cpu:
         v, t = time_oracle(w, args.cpu_sample, steps=3)
+        n1 = max(1, args.cpu_sample // 16)
+        v1, t1 = time_oracle(w, n1, steps=1, nthreads=1)
         line["cpu_baseline"] = {"value": v, "unit": "particles/s", "cores": cpu_cores(), "kind": "oracle",
                                 "sample": f"full oracle FMM (fp64 expansions, OpenMP) on N={args.cpu_sample} "
-                                          f"particles of the {w.name} recipe, median of 3 runs ({t:.1f} s each)"}
+                                          f"particles of the {w.name} recipe, median of 3 runs ({t:.1f} s each)",
+                                "single_thread": {"value": v1, "unit": "particles/s", "cores": 1,
+                                                  "sample": f"the same on N={n1}, one run ({t1:.1f} s)"},
+                                "direct_sum": time_direct_sums()}
     res["plan"].close()
     if rank == 0:
         print(json.dumps(line), flush=True)
