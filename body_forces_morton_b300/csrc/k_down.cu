@@ -380,12 +380,19 @@ __device__ __forceinline__ void p2p_item(int a, int chunk, int nch, int *done, D
     }
     for (int r0 = 0; r0 < c; r0 += 128) {
         const int cr = min(128, c - r0);
-        // four receivers per lane (R = ceil(cr / 4) lanes, the sources split S = 32 / R ways): measured
-        // faster than choosing 1, 2 or 4 per leaf to keep the most lanes busy, because four receivers
-        // per lane give each staged source four times the arithmetic and the lane more independent
-        // chains than the idle lanes of small leaves cost
-        p2p_round<T, 4, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm, far,
-                                 far_w, src, acc_out, pot_out, buf, red, lane);
+        // four receivers per lane (R = ceil(cr / 4) lanes, the sources split S = 32 / R ways), or three
+        // where that leaves fewer lane slots idle (17 particles: 6 lanes x 3 = 18 slots over 5 source
+        // groups, against 5 x 4 = 20): measured faster than four alone. Two receivers per lane (tried as
+        // 2 or 4) was slower: each staged source then feeds too little arithmetic.
+        const int R4 = (cr + 3) / 4, R3 = (cr + 2) / 3;
+        const float e4 = (float)cr / (4 * R4) * (float)(R4 * (32 / R4)) / 32.0f;
+        const float e3 = R3 <= 32 ? (float)cr / (3 * R3) * (float)(R3 * (32 / R3)) / 32.0f : 0.0f;
+        if (e3 > e4 * 1.02f)
+            p2p_round<T, 3, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm, far,
+                                     far_w, src, acc_out, pot_out, buf, red, lane);
+        else
+            p2p_round<T, 4, CHUNKED>(a, f, c, r0, cr, beg, end, chunk, nch, done, ctr, first, count, xyzm, perm, far,
+                                     far_w, src, acc_out, pot_out, buf, red, lane);
     }
     if (CHUNKED && chunk < nch - 1) pass_turn(done + a, chunk + 1);
 }
