@@ -116,8 +116,16 @@ __device__ __forceinline__ void m2l_apply_row(const T *row, const vec4<T> &ca, c
     }
 }
 
+// Blocks per SM the fp32 reduced-operator kernel is compiled for: more resident
+// warps hide the row loads' latency (measured: 0.229 ms at 4 blocks, 0.221 at
+// 5, 0.218 at 6 for p = 4); beyond these the registers spill.
+template <class T, int P, class Op> struct M2LMinBlocks { static constexpr int value = 1; };
+template <int P> struct M2LMinBlocks<float, P, OpReduced<P>> {
+    static constexpr int value = P <= 3 ? 8 : (P == 4 ? 6 : 1);
+};
+
 template <class T, int P, class Op>
-__global__ __launch_bounds__(M2L_WARPS * 32) void k_m2l(const DevCounters *__restrict__ nctr, const int *__restrict__ order,
+__global__ __launch_bounds__(M2L_WARPS * 32, M2LMinBlocks<T, P, Op>::value) void k_m2l(const DevCounters *__restrict__ nctr, const int *__restrict__ order,
                                                         const int *__restrict__ off,
                                                         const int *__restrict__ src, const vec4<T> *__restrict__ nc,
                                                         const T *__restrict__ Mr, T *__restrict__ Lout,
