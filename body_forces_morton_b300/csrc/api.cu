@@ -249,7 +249,7 @@ void destroy_plan(Plan &P)
     free_nodes(P);
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
-    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar);
+    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.vwin); dfree(P.tree_cc); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     dfree(P.vjp_acc); dfree(P.vjp_src); dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
     free_mutual(P);
@@ -257,6 +257,9 @@ void destroy_plan(Plan &P)
     for (int i = 0; i < kNumEvents; ++i)
         if (P.ev[i]) cudaEventDestroy(P.ev[i]);
     if (P.ev_done) cudaEventDestroy(P.ev_done);
+    if (P.ev_pos) cudaEventDestroy(P.ev_pos);
+    if (P.ev_mass) cudaEventDestroy(P.ev_mass);
+    if (P.side) cudaStreamDestroy(P.side);
 }
 
 // Pair capacities stay at or below 1e9 unordered pairs, so the directed list
@@ -496,6 +499,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
         !ok(dalloc(P.idx[0], nn), "perm") || !ok(dalloc(P.idx[1], nn), "perm") ||
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
+        !ok(dalloc(P.vwin, nn), "tree windows") || !ok(dalloc(P.tree_cc, tree_cc_ints(n)), "tree counts") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
         !ok(dalloc(P.gbar, 2), "grid barriers") ||
@@ -541,11 +545,26 @@ fmm_status fmm_eval_host(fmm_plan *plan, const void *pos, const void *mass, void
         CUDA_TRY(cudaMalloc(&P.h_acc, 3 * n * e));
         CUDA_TRY(cudaMalloc(&P.h_pot, n * e));
     }
+    if (!P.side) {
+        CUDA_TRY(cudaStreamCreateWithFlags(&P.side, cudaStreamNonBlocking));
+        CUDA_TRY(cudaEventCreateWithFlags(&P.ev_pos, cudaEventDisableTiming));
+        CUDA_TRY(cudaEventCreateWithFlags(&P.ev_mass, cudaEventDisableTiming));
+    }
     P.cache_valid = false;
+    // positions first, at the full link rate; the masses follow on the side stream, after the positions
+    // (so that the two copies do not share the link), while the box, the keys and the radix passes run
     CUDA_TRY(cudaMemcpyAsync(P.h_pos, pos, 3 * n * e, cudaMemcpyHostToDevice, s));
-    CUDA_TRY(cudaMemcpyAsync(P.h_mass, mass, n * e, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaEventRecord(P.ev_pos, s));
+    CUDA_TRY(cudaStreamWaitEvent(P.side, P.ev_pos, 0));
+    CUDA_TRY(cudaMemcpyAsync(P.h_mass, mass, n * e, cudaMemcpyHostToDevice, P.side));
+    CUDA_TRY(cudaEventRecord(P.ev_mass, P.side));
+    P.mass_wait = P.ev_mass;
     fmm_status st = eval_device(P, P.h_pos, P.h_mass, P.h_acc, pot_out ? P.h_pot : nullptr, s);
-    if (st) return st;
+    P.mass_wait = nullptr;
+    if (st) {
+        cudaStreamSynchronize(P.side);  // the copy into the plan's buffer ends before the call returns
+        return st;
+    }
     CUDA_TRY(cudaMemcpyAsync(acc_out, P.h_acc, 3 * n * e, cudaMemcpyDeviceToHost, s));
     if (pot_out) CUDA_TRY(cudaMemcpyAsync(pot_out, P.h_pot, n * e, cudaMemcpyDeviceToHost, s));
     if (fmm_status w = wait_stream(P, s)) return w;

@@ -19,6 +19,10 @@ constexpr int kShards = 64;          // the walk's outputs are split into this m
 constexpr long long kChunkWork = 1ll << 20;
 constexpr int kMaxChunks = 64;
 constexpr unsigned kSpinLimit = 1u << 22;  // iterations of any bounded wait
+// polls of a chunk-turn wait (wait_turn), the first 4096 64 ns apart and the rest 1 us apart: about
+// 17 s. The earlier chunk of a receiving leaf of thousands of particles can take most of a second in
+// double-float arithmetic, since a chunk's first round waits for the earlier chunk's every round
+constexpr unsigned kTurnSpinLimit = 1u << 24;
 
 // ---- device status word bits (ORed by kernels, read by the host) ----------
 enum : unsigned {
@@ -119,11 +123,11 @@ __device__ __forceinline__ void wait_turn(int *flag, int want, DevCounters *ctr)
         cuda::atomic_ref<int, cuda::thread_scope_device> r(*flag);
         unsigned spins = 0;
         while (r.load(cuda::memory_order_acquire) != want) {
-            if (++spins > kSpinLimit) {
+            if (++spins > kTurnSpinLimit) {
                 set_error(ctr, ERR_SPIN);
                 break;
             }
-            __nanosleep(64);
+            __nanosleep(spins < 4096 ? 64 : 1024);
         }
     }
     __syncwarp();

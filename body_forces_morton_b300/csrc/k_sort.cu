@@ -313,11 +313,12 @@ int radix_passes(Plan &P, const void *pos, const void *mass, cudaStream_t s)
             k_radix_pass<T, true, false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
                 P.keys[src], nullptr, P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
                 nullptr);
-        else if (pass == 7)
+        else if (pass == 7) {
+            if (P.mass_wait) cudaStreamWaitEvent(s, P.mass_wait, 0);  // masses still arriving on a side stream
             k_radix_pass<T, false, true, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
                 P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, (const T *)pos,
                 (const T *)mass, (vec4<T> *)P.xyzm);
-        else
+        } else
             k_radix_pass<T, false, false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
                 P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
                 nullptr);

@@ -42,6 +42,8 @@ struct Plan {
     void *xyzm = nullptr;          // sorted particles, vec4<T> (x, y, z, m)
     void *far = nullptr;           // far field at the sorted particles, vec4<T> (phi, ax, ay, az)
     uint8_t *div = nullptr;        // divergence level of consecutive sorted keys
+    uint8_t *vwin = nullptr;       // per sorted position: the deepest level whose run around it holds > leaf keys
+    int *tree_cc = nullptr;        // per level and chunk of positions: node counts, then their offsets
     void *rel = nullptr;           // fp64 plans: leaf-relative particles as double-float float4 [2][N]
 
     // node buffers
@@ -109,6 +111,10 @@ struct Plan {
     // timing and stats of the last evaluation
     cudaEvent_t ev[kNumEvents] = {};
     cudaEvent_t ev_done = nullptr;   // completion of the status read-back (polled)
+    // host-buffer evaluations: the mass upload runs on a side stream while the keys and the first
+    // radix passes run; the pass that gathers the masses waits on mass_wait when it is set
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_pos = nullptr, ev_mass = nullptr, mass_wait = nullptr;
     int ev_stage[kNumEvents] = {};
     int n_ev = 0;
     int launches = 0;
@@ -129,6 +135,7 @@ struct Plan {
 int launch_keys(Plan &P, const void *pos, cudaStream_t s);
 int launch_sort(Plan &P, const void *pos, const void *mass, cudaStream_t s);
 int launch_tree(Plan &P, cudaStream_t s);
+size_t tree_cc_ints(int64_t n);  // size of Plan::tree_cc for n particles
 int tree_max_blocks_per_sm();
 int walk_max_blocks_per_sm(int dtype);
 int launch_upward(Plan &P, cudaStream_t s);

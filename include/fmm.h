@@ -128,7 +128,9 @@ fmm_status fmm_eval(fmm_plan *plan, const void *pos, const void *mass, void *acc
 /*
  * Same evaluation with HOST buffers (pageable or pinned): the call copies pos and
  * mass to plan-owned device memory, evaluates, and copies acc (and pot, unless
- * NULL) back before returning.
+ * NULL) back before returning. The mass copy runs on a plan-owned side stream,
+ * ordered after the position copy, while the first stages run on `stream`; both
+ * have ended when the call returns, on success and on error.
  */
 fmm_status fmm_eval_host(fmm_plan *plan, const void *pos, const void *mass, void *acc_out, void *pot_out,
                          void *stream);

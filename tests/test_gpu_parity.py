@@ -109,6 +109,22 @@ def test_coincident_particles_and_depth_limit():
     assert r.depth == 21 and st["depth"] == 21
 
 
+@pytest.mark.parametrize("dt", ["f32", "f64"])
+@pytest.mark.parametrize("leaf", [1, 2048, 4096, 4097, 9000])
+def test_tree_window_and_level_builds(leaf, dt):
+    """Leaves up to 4096 build every level at once (windows over the divergence levels of the sorted keys);
+    larger leaves take the level-by-level build. Both give the oracle's tree bit for bit, across tile and
+    chunk edges of the window build (40000 clustered keys, depth up to 21)."""
+    n = 40000
+    g = W.generate(W.WORKLOADS[4], n=n, dtype=dt)
+    mask = np.zeros(n, bool)
+    mask[::997] = True
+    _, _, ex, st = gpu_eval(g["pos"], g["mass"], 2, 0.7, leaf, exports=ALL_STRUCT)
+    r = oracle.fmm(g["pos"], g["mass"], 2, 0.7, leaf, eval_mask=mask)
+    assert_structure_equal(ex, r)
+    assert st["depth"] == r.depth
+
+
 def test_tiny_theta_equals_direct_sum():
     g = W.generate(W.WORKLOADS[2], n=4000)
     acc, pot, _, _ = gpu_eval(g["pos"], g["mass"], 4, 1e-6, 16)
