@@ -59,10 +59,10 @@ P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r
 # 1e5 fp64, p 4), keyed by the hash of the kernel sources they were counted on;
 # a changed kernel reports null until it is counted again.
 DF_FMA_OPS_PER_PAIR = {
-    # k_p2p_df: 9.099e9 FMA-pipe thread instructions (all scalar) over 48,723,340 pairs
-    ("k_p2p_df", "37308ee123d17f5b"): 186.75,
-    # k_m2l_df<4>: 6.078e9 over 1,833,964 pairs (the moments' conversion kernel is not counted)
-    ("k_m2l_df", "41ac065d4f26709d"): 3314.2,
+    # k_p2p_df: 9,097,899,392 FMA-pipe thread instructions (all scalar) over 48,823,340 pairs
+    ("k_p2p_df", "ced2e98ffaa7e256"): 186.34,
+    # k_m2l_df<4>: 6,073,018,112 over 1,833,964 pairs (the moments' conversion kernel is not counted)
+    ("k_m2l_df", "61a2aad5e1163c40"): 3311.4,
 }
 
 # DRAM traffic of the P2P kernel per launch (dram__bytes_read.sum +

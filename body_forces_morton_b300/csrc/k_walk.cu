@@ -108,25 +108,32 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0
             if (blockIdx.x == 0 && threadIdx.x == 0) set_error(ctr, ERR_WALK);
             break;
         }
-        for (int base = blockIdx.x * WK_THREADS; base < nread; base += gridDim.x * WK_THREADS) {
+        // each thread's next frontier pair is loaded one tile ahead, so its latency overlaps the
+        // current tile's decisions, reservations and writes
+        const int stride = gridDim.x * WK_THREADS;
+        int2 pr_next = make_int2(-1, -1);
+        if (blockIdx.x * WK_THREADS + threadIdx.x < nread)
+            pr_next = ld_cg(fin + shard_addr(s_pre, blockIdx.x * WK_THREADS + threadIdx.x, capf_s));
+        for (int base = blockIdx.x * WK_THREADS; base < nread; base += stride) {
             const int i = base + threadIdx.x;
-            int A = -1, B = -1, kids = 0, split = -1, other = 0, m2l = 0, p2p = 0;
+            const int2 pr = pr_next;
+            if (i + stride < nread) pr_next = ld_cg(fin + shard_addr(s_pre, i + stride, capf_s));
+            int A = -1, B = -1, kids = 0, other = 0, m2l = 0, p2p = 0, c0 = 0;
             if (i < nread) {
-                const int2 pr = ld_cg(fin + shard_addr(s_pre, i, capf_s));
                 A = pr.x;
                 B = pr.y;
                 ++visited;
-                const int nA = nchild[A];
+                const int nA = nchild[A], c0A = child0[A];
                 if (A == B) {
                     if (nA == 0) {
                         p2p = 1;
                         inter_sum += (long long)count[A] * count[A];
                     } else {
                         kids = nA * (nA + 1) / 2;
-                        split = A;
+                        c0 = c0A;
                     }
                 } else {
-                    const int nB = nchild[B];
+                    const int nB = nchild[B], c0B = child0[B];
                     const vec4<T> cA = nc[A], cB = nc[B], lA = nl[A], lB = nl[B];
                     const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
                     const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
@@ -137,9 +144,9 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0
                         inter_sum += 2ll * count[A] * count[B];
                     } else {
                         const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
-                        split = splitA ? A : B;
                         other = splitA ? B : A;
                         kids = splitA ? nA : nB;
+                        c0 = splitA ? c0A : c0B;
                     }
                 }
             }
@@ -188,7 +195,6 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0
             if (kids) {
                 int o = s_base[2] + s_wtot[2][warp] + ik - kids;
                 int2 *dst = fout + (size_t)bshard * capf_s;
-                const int c0 = child0[split];
                 if (A == B) {
                     const int nA = nchild[A];
                     for (int x = 0; x < nA; ++x)
