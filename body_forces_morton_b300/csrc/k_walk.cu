@@ -316,57 +316,66 @@ __device__ __forceinline__ void cmpswap(int *v, int i, int j)
     if (b < a) { v[i] = b; v[j] = a; }
 }
 
-// Warp-wide ascending bitonic sort of 32 NR keys, key e = 32 j + lane in v[j]:
-// the flip-first network of cmpswap above. The flip partner of e is e ^ (k-1),
-// the half-cleaner partner e ^ d; partners in another lane come by shuffle,
-// partners in the same lane (distance >= 32) are registers. New values are
-// always computed from old ones.
+// Warp-wide ascending bitonic sort of 32 NR keys in the blocked layout: key
+// e = NR lane + j in v[j], so partners at distances below NR are registers of
+// the same lane and only the longer distances go through shuffles (15 of the
+// 36 stages at NR = 8). The network is the flip-first one of cmpswap above:
+// merge level k first compares e with its mirror e ^ (k - 1), then the
+// half-cleaners compare e with e ^ d, d = k/4 .. 1; the lower key of a pair
+// keeps the minimum. New values are always computed from old ones.
 template <int NR>
 __device__ __forceinline__ void warp_sort(int (&v)[NR])
 {
-    constexpr int LOGN = 5 + (NR == 1 ? 0 : NR == 2 ? 1 : NR == 4 ? 2 : 3);
+    constexpr int N = 32 * NR;
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int lk = 1; lk <= LOGN; ++lk) {
-        const int k = 1 << lk;
-        if (k <= 32) {
+    for (int k = 2; k <= N; k <<= 1) {
+        if (k <= NR) {
+            // mirror inside the lane: pairs (j, j ^ (k - 1)) with bit k/2 of j clear
 #pragma unroll
             for (int j = 0; j < NR; ++j) {
-                const int other = __shfl_xor_sync(kFull, v[j], k - 1);
-                const bool lower = (lane & (k >> 1)) == 0;
-                v[j] = lower ? min(v[j], other) : max(v[j], other);
+                const int pj = j ^ (k - 1);
+                if ((j & (k >> 1)) == 0) {
+                    const int a = v[j], b = v[pj];
+                    v[j] = min(a, b);
+                    v[pj] = max(a, b);
+                }
             }
         } else {
-            const int jm = (k >> 5) - 1;
-            int nv[NR];
+            // mirror across lanes: lane ^ (k/NR - 1), register NR - 1 - j
+            const int m = k / NR - 1;
+            const bool lower = (lane & ((k >> 1) / NR)) == 0;
 #pragma unroll
-            for (int j = 0; j < NR; ++j) {
-                const int other = __shfl_xor_sync(kFull, v[j ^ jm], 31);
-                const bool lower = (j & (k >> 6)) == 0;
-                nv[j] = lower ? min(v[j], other) : max(v[j], other);
+            for (int j = 0; j < NR / 2; ++j) {
+                const int oa = __shfl_xor_sync(kFull, v[NR - 1 - j], m);
+                const int ob = __shfl_xor_sync(kFull, v[j], m);
+                const int a = v[j], b = v[NR - 1 - j];
+                v[j] = lower ? min(a, oa) : max(a, oa);
+                v[NR - 1 - j] = lower ? min(b, ob) : max(b, ob);
             }
-#pragma unroll
-            for (int j = 0; j < NR; ++j) v[j] = nv[j];
+            if constexpr (NR == 1) {
+                const int o = __shfl_xor_sync(kFull, v[0], m);
+                v[0] = lower ? min(v[0], o) : max(v[0], o);
+            }
         }
 #pragma unroll
-        for (int lj = lk - 2; lj >= 0; --lj) {
-            const int d = 1 << lj;
-            if (d >= 32) {
-                const int dj = d >> 5;
+        for (int d = k >> 2; d >= 1; d >>= 1) {
+            if (d < NR) {
 #pragma unroll
                 for (int j = 0; j < NR; ++j) {
-                    if ((j & dj) == 0) {
-                        const int a = v[j], b = v[j + dj];
+                    if ((j & d) == 0) {
+                        const int a = v[j], b = v[j | d];
                         v[j] = min(a, b);
-                        v[j + dj] = max(a, b);
+                        v[j | d] = max(a, b);
                     }
                 }
             } else {
+                const int m = d / NR;
+                const bool lower = (lane & m) == 0;
 #pragma unroll
                 for (int j = 0; j < NR; ++j) {
-                    const int other = __shfl_xor_sync(kFull, v[j], d);
-                    const bool lower = (lane & d) == 0;
-                    v[j] = lower ? min(v[j], other) : max(v[j], other);
+                    const int o = __shfl_xor_sync(kFull, v[j], m);
+                    v[j] = lower ? min(v[j], o) : max(v[j], o);
                 }
             }
         }
@@ -380,18 +389,18 @@ __device__ __forceinline__ void sort_list_regs(int *src, int len)
     int v[NR];
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
-        const int e = j * 32 + lane;
+        const int e = lane * NR + j;
         v[j] = e < len ? src[e] : 0x7fffffff;
     }
     warp_sort<NR>(v);
 #pragma unroll
     for (int j = 0; j < NR; ++j) {
-        const int e = j * 32 + lane;
+        const int e = lane * NR + j;
         if (e < len) src[e] = v[j];
     }
 }
 
-// One warp per receiver list; lists up to 256 sort in registers, up to
+// One warp per receiver list; lists up to 512 sort in registers, up to
 // SEG_WARP_MAX in shared memory, longer ones go to a second pass.
 __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__ nctr, int cap, long long chunk_work,
                                                  int max_chunks, uint8_t *nchunks,
@@ -441,6 +450,7 @@ __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__
         if (len <= 64) { sort_list_regs<2>(src, len); continue; }
         if (len <= 128) { sort_list_regs<4>(src, len); continue; }
         if (len <= 256) { sort_list_regs<8>(src, len); continue; }
+        if (len <= 512) { sort_list_regs<16>(src, len); continue; }
         if (len > SEG_WARP_MAX) {
             if (lane == 0) long_seg[atomicAdd(&ctr->n_long, 1)] = job;
             continue;
