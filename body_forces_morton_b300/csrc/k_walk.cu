@@ -284,7 +284,23 @@ __global__ __launch_bounds__(CS_THREADS) void k_csr_scan(const DevCounters *__re
     }
 }
 
-// Scatter the unordered pairs into their receivers' segments. The counts are
+// One directed entry per lane (receiver r >= 0; r < 0: none) into the
+// receiver's segment: the lanes of a warp with the same receiver take their
+// places with one atomic, the leader's, in lane order.
+__device__ __forceinline__ void fill_entry(int r, int v, int *cnt, const int *__restrict__ off, int *__restrict__ src)
+{
+    const unsigned peers = __match_any_sync(kFull, r);
+    const int leader = __ffs(peers) - 1;
+    const int lane = threadIdx.x & 31;
+    int top = 0;
+    if (lane == leader && r >= 0) top = atomicSub(&cnt[r], __popc(peers));
+    top = __shfl_sync(kFull, top, leader);
+    if (r >= 0) src[off[r] + top - 1 - __popc(peers & lanemask_lt())] = v;
+}
+
+// Scatter the unordered pairs into their receivers' segments, both directions,
+// one warp-aggregated atomic per receiver and warp (pairs of one receiver come
+// in runs: the children of a split against the same partner). The counts are
 // used as countdown cursors and end at zero, ready for the next evaluation.
 __global__ void k_csr_fill(const int2 *__restrict__ m2l_pairs, int capm_s, const int2 *__restrict__ p2p_pairs,
                            int capp_s, int *m2l_cnt, int *p2p_cnt, const int *__restrict__ m2l_off,
@@ -295,16 +311,19 @@ __global__ void k_csr_fill(const int2 *__restrict__ m2l_pairs, int capm_s, const
     shard_prefix(ctr->n_m2l_pairs, capm_s, pm);
     shard_prefix(ctr->n_p2p_pairs, capp_s, pp);
     const int nm = pm[kShards], np = pp[kShards];
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nm + np; i += gridDim.x * blockDim.x) {
-        if (i < nm) {
-            const int2 pr = m2l_pairs[shard_addr(pm, i, capm_s)];
-            m2l_src[m2l_off[pr.x] + atomicSub(&m2l_cnt[pr.x], 1) - 1] = pr.y;
-            m2l_src[m2l_off[pr.y] + atomicSub(&m2l_cnt[pr.y], 1) - 1] = pr.x;
-        } else {
-            const int2 pr = p2p_pairs[shard_addr(pp, i - nm, capp_s)];
-            p2p_src[p2p_off[pr.x] + atomicSub(&p2p_cnt[pr.x], 1) - 1] = pr.y;
-            if (pr.x != pr.y) p2p_src[p2p_off[pr.y] + atomicSub(&p2p_cnt[pr.y], 1) - 1] = pr.x;
-        }
+    const int lane = threadIdx.x & 31;
+    const int stride = gridDim.x * blockDim.x;
+    for (int b = blockIdx.x * blockDim.x + (threadIdx.x & ~31); b < nm + np; b += stride) {
+        const int i = b + lane;
+        int2 pr = make_int2(-1, -1);
+        if (i < nm) pr = m2l_pairs[shard_addr(pm, i, capm_s)];
+        const bool p = i >= nm && i < nm + np;
+        if (p) pr = p2p_pairs[shard_addr(pp, i - nm, capp_s)];
+        // a warp straddling the two lists handles each lane under its own list
+        fill_entry(p ? -1 : pr.x, pr.y, m2l_cnt, m2l_off, m2l_src);
+        fill_entry(p ? -1 : pr.y, pr.x, m2l_cnt, m2l_off, m2l_src);
+        fill_entry(p ? pr.x : -1, pr.y, p2p_cnt, p2p_off, p2p_src);
+        fill_entry(p && pr.x != pr.y ? pr.y : -1, pr.x, p2p_cnt, p2p_off, p2p_src);
     }
 }
 
