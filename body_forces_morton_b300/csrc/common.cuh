@@ -13,10 +13,17 @@ constexpr int kMaxLevel = 21;        // Morton keys carry 21 bits per axis
 constexpr int kMaxP = 8;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kShards = 64;          // the walk's outputs are split into this many independently counted shards
-// P2P work of one receiver leaf above kChunkWork interactions (or above the
-// total over the node capacity, if larger) is split into up to kMaxChunks
-// chunks of its source list, taken by different warps.
-constexpr long long kChunkWork = 1ll << 20;
+// P2P work of one receiver leaf is split into up to kMaxChunks chunks of its
+// source list, taken by different warps, when it is above the largest of
+// kChunkWork interactions, the total over the node capacity (which bounds the
+// number of chunks) and the total over kShareDiv per SM (about a third of an
+// even share of the resident warps, so that no single receiver's warp is left
+// running alone at the end of the near field).
+// fp64 plans keep a floor of 2^20: a double-float pair costs several fp32 pairs,
+// and their chunk waits cost more than the tail they would cut.
+constexpr long long kChunkWork = 1ll << 16;
+constexpr long long kChunkWorkF64 = 1ll << 20;
+constexpr int kShareDiv = 64;
 constexpr int kMaxChunks = 64;
 constexpr unsigned kSpinLimit = 1u << 22;  // iterations of any bounded wait
 // polls of a chunk-turn wait (wait_turn), the first 4096 64 ns apart and the rest 1 us apart: about

@@ -43,9 +43,9 @@ namespace {
 constexpr int VJP_WARPS = 4;                                                // warps per block of k_vjp_near
 template <class T> struct VjpChunk { static constexpr int value = 128; };  // staged sources per warp
 template <> struct VjpChunk<double> { static constexpr int value = 64; };
-// receivers per lane of k_vjp_near: four in the scalar (fp64) path, two in the packed fp32 path
+// receivers per lane of k_vjp_near, in both paths: four (the packed fp32 path also fills the lanes of
+// partly filled leaves better than with two)
 template <class T> struct VjpK { static constexpr int value = 4; };
-template <> struct VjpK<float> { static constexpr int value = 2; };
 
 template <class T>
 __global__ __launch_bounds__(256) void k_vjp_sources(int n, const uint32_t *__restrict__ perm,

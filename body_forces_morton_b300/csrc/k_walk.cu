@@ -422,7 +422,7 @@ __device__ __forceinline__ void sort_list_regs(int *src, int len)
 // One warp per receiver list; lists up to 512 sort in registers, up to
 // SEG_WARP_MAX in shared memory, longer ones go to a second pass.
 __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__ nctr, int cap, long long chunk_work,
-                                                 int max_chunks, uint8_t *nchunks,
+                                                 long long share_div, int max_chunks, uint8_t *nchunks,
                                                  const int *__restrict__ m2l_off, int *m2l_src,
                                                  const int *__restrict__ p2p_off, int *p2p_src, int *long_seg,
                                                  const int *__restrict__ count, uint8_t *__restrict__ key,
@@ -440,9 +440,10 @@ __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__
         const int len = (isp ? p2p_off[a + 1] : m2l_off[a + 1]) - beg;
         int *src = (isp ? p2p_src : m2l_src) + beg;
         // work bucket of this receiver (see k_order_scatter): P2P work = count * sum of the
-        // source leaves' counts, split into chunks of at most max(chunk_work, total / cap) (at most
-        // max_chunks <= 255; so the chunks of all receivers number at most 2 cap), bucketed by the work of
-        // one chunk; M2L work = list length; bucket floor(log2(work)) + 1, 0 for none
+        // source leaves' counts, split into chunks of at most max(chunk_work, total / cap, total /
+        // share_div) (at most max_chunks <= 255; so the chunks of all receivers number at most 2 cap),
+        // bucketed by the work of one chunk; M2L work = list length; bucket floor(log2(work)) + 1, 0 for
+        // none
         {
             int k, nch = 1;
             if (isp) {
@@ -450,7 +451,8 @@ __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__
                 for (int e = lane; e < len; e += 32) s += count[src[e]];
                 for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
                 const long long work = s * count[a];
-                const long long wmax = max(chunk_work, ctr->p2p_interactions / cap + 1);
+                const long long tot = ctr->p2p_interactions;
+                const long long wmax = max(chunk_work, max(tot / cap + 1, tot / share_div + 1));
                 nch = (int)min((long long)max_chunks, (work + wmax - 1) / wmax);
                 nch = max(nch, 1);
                 const long long wc = work / nch;
@@ -642,9 +644,10 @@ int launch_lists(Plan &P, cudaStream_t s)
     // in dependent steps of one pair per lane, so one warp on a receiver with a long list would be the
     // tail (the fp32 mutual kernel has the forward near field's lane layout and its chunks)
     const bool fine = P.mutual && P.dtype != 0;
-    const long long chunk_work = fine ? kChunkWorkMutual : kChunkWork;
+    const long long chunk_work = fine ? kChunkWorkMutual : (P.dtype == 0 ? kChunkWork : kChunkWorkF64);
     const int max_chunks = fine ? kMaxChunksMutual : kMaxChunks;
-    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, cap, chunk_work, max_chunks, P.p2p_nch, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
+    const long long share_div = (long long)P.num_sms * kShareDiv;
+    k_segsort<<<P.num_sms * 8, 256, 0, s>>>(P.ctr, cap, chunk_work, share_div, max_chunks, P.p2p_nch, P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg,
                                             P.node_count, P.order_key, P.ctr);
     k_segsort_long<<<P.num_sms, 1024, 0, s>>>(P.m2l_off, P.m2l_src, P.p2p_off, P.p2p_src, P.long_seg, P.ctr);
     k_order_scatter<<<P.num_sms * 4, 256, 0, s>>>(P.ctr, cap, P.order_key, P.p2p_nch, P.p2p_items, P.order, P.ctr);
