@@ -249,7 +249,7 @@ void destroy_plan(Plan &P)
     free_nodes(P);
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
-    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.vwin); dfree(P.tree_cc); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar);
+    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.vwin); dfree(P.tree_cc); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar); dfree(P.sort_cnt);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     dfree(P.vjp_acc); dfree(P.vjp_src); dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
     free_mutual(P);
@@ -326,7 +326,7 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         // ---- phase 1: box, keys, sort, tree (the tree kernel records the node count and depth)
         record(P, 0, s);
         CUDA_TRY(cudaMemsetAsync(P.ctr, 0, sizeof(DevCounters), s));
-        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 2 * sizeof(GridBarrier), s));
+        CUDA_TRY(cudaMemsetAsync(P.gbar, 0, 3 * sizeof(GridBarrier), s));
         P.launches += launch_keys(P, pos, s);
         record(P, 1, s);
         P.launches += launch_sort(P, pos, mass, s);
@@ -494,6 +494,11 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         // syncs faster between the small generations of small trees)
         const int wb = n >= (1 << 19) ? 8 : 4;
         P.coop_blocks_walk = std::min(2048, P.num_sms * std::max(1, std::min(wb, walk_max_blocks_per_sm(P.dtype))));
+        // the cooperative radix sort runs when all its tiles are co-resident (grid barriers take up to 2048)
+        sort_coop_capacity(P.num_sms, P.coop_tiles_sort);
+        P.coop_tiles_sort[0] = std::min(2048, P.coop_tiles_sort[0]);
+        P.coop_tiles_sort[1] = std::min(2048, P.coop_tiles_sort[1]);
+        P.sort_cnt_cap = (size_t)256 * std::max(1, std::max(P.coop_tiles_sort[0], P.coop_tiles_sort[1]));
     }
     const size_t nn = (size_t)n, e = (size_t)P.esize;
     if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
@@ -502,7 +507,8 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         !ok(dalloc(P.vwin, nn), "tree windows") || !ok(dalloc(P.tree_cc, tree_cc_ints(n)), "tree counts") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
-        !ok(dalloc(P.gbar, 2), "grid barriers") ||
+        !ok(dalloc(P.gbar, 3), "grid barriers") ||
+        !ok(dalloc(P.sort_cnt, P.sort_cnt_cap), "sort counts") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);
     for (int i = 0; i < kNumEvents; ++i)

@@ -7,13 +7,16 @@
 // is evaluated step by step in the plan's precision without contraction, so the
 // keys are exactly those of any other implementation doing the same steps.
 //
-// Radix sort: 8 passes of 8 bits. Each pass is one kernel: a block takes a
-// 4096-key tile from a ticket counter, ranks its keys per digit with warp
-// match_any (stable within the tile), finds the tile's output offset per digit
-// with a decoupled look-back over the earlier tiles, reorders the tile by digit
-// in shared memory and writes it out in runs of consecutive positions (one
-// digit's keys of a tile are contiguous in the output). The last pass also
-// gathers (x, y, z, m) into sorted order.
+// Radix sort: 8 passes of 8 bits. A block ranks a 4096-key tile's keys per
+// digit with warp match_any (stable within the tile), finds the tile's output
+// offset per digit, reorders the tile by digit in shared memory and writes it
+// out in runs of consecutive positions (one digit's keys of a tile are
+// contiguous in the output). When every tile fits on the GPU at once, all 8
+// passes run in one cooperative launch, the offsets from a scan of the tiles'
+// counts between grid barriers (k_radix_coop), and a second kernel gathers
+// (x, y, z, m) into sorted order; otherwise each pass is one kernel that takes
+// tiles from a ticket counter and finds the offsets with a decoupled look-back
+// over the earlier tiles, the last pass gathering the particles.
 #include "plan.h"
 
 namespace bfm {
@@ -287,6 +290,187 @@ __global__ void k_diverge(const uint64_t *__restrict__ keys, int n, uint8_t *__r
     }
 }
 
+// All 8 passes in one cooperative launch, one tile of RS_THREADS * ITEMS keys
+// per block with every tile resident (N up to the co-resident tiles). Per
+// pass: each tile ranks its keys per digit as k_radix_pass does, publishes its
+// 256 digit counts and reorders itself by digit in shared memory; after a grid
+// barrier the blocks scan each digit's counts over the tiles (a column per
+// block, in place, into exclusive offsets); after a second barrier each tile
+// writes its runs to the pass's global digit start plus its offset; a third
+// barrier ends the pass. Three barriers replace the look-back chain, which
+// with every tile starting at once runs through the tiles one after another.
+template <int ITEMS>
+__global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_t *v0, uint64_t *k1, uint32_t *v1,
+                                                           int n, unsigned *cnt, GridBarrier *gb, DevCounters *ctr)
+{
+    constexpr int TILE = RS_THREADS * ITEMS;
+    extern __shared__ __align__(16) unsigned char rs_smem[];
+    uint64_t *const s_k = reinterpret_cast<uint64_t *>(rs_smem);
+    uint32_t *const s_v = reinterpret_cast<uint32_t *>(s_k + TILE);
+    __shared__ unsigned s_hist[RS_WARPS][256];
+    __shared__ unsigned s_lstart[256];
+    __shared__ unsigned s_base[256];
+    __shared__ unsigned s_wsum[2][RS_WARPS];
+    __shared__ unsigned s_col[RS_WARPS + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tile = blockIdx.x, ntiles = gridDim.x;
+    const int64_t start = (int64_t)tile * TILE + warp * (32 * ITEMS);
+    const int64_t left = (int64_t)n - (int64_t)tile * TILE;
+    const int tile_n = left < TILE ? (int)left : TILE;
+    unsigned bar = 0;
+    for (int pass = 0; pass < 8; ++pass) {
+        const uint64_t *kin = (pass & 1) ? k1 : k0;
+        const uint32_t *vin = (pass & 1) ? v1 : v0;
+        uint64_t *kout = (pass & 1) ? k0 : k1;
+        uint32_t *vout = (pass & 1) ? v0 : v1;
+        const int shift = 8 * pass;
+        for (int i = tid; i < RS_WARPS * 256; i += RS_THREADS) (&s_hist[0][0])[i] = 0;
+        __syncthreads();
+        uint64_t k[ITEMS];
+        uint32_t v[ITEMS];
+        unsigned rank[ITEMS];
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j) {
+            const int64_t i = start + j * 32 + lane;
+            const bool valid = i < n;
+            k[j] = valid ? ld_cg(kin + i) : ~0ull;  // written by other blocks in the previous pass
+            v[j] = valid ? (pass == 0 ? (uint32_t)i : ld_cg(vin + i)) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j) {
+            const bool valid = start + j * 32 + lane < n;
+            const unsigned d = valid ? (unsigned)((k[j] >> shift) & 255u) : 256u;
+            const unsigned peers = __match_any_sync(kFull, d);
+            const int leader = __ffs(peers) - 1;
+            unsigned mine = (lane == leader && valid) ? s_hist[warp][d] : 0u;
+            const unsigned b = __shfl_sync(kFull, mine, leader);
+            rank[j] = b + __popc(peers & lanemask_lt());
+            __syncwarp();
+            if (lane == leader && valid) s_hist[warp][d] = b + __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        // per digit d: warp offsets within the tile, the tile's count (published), the tile-local start
+        // and the pass's global start (from the key kernel's histogram)
+        const int d = tid;
+        unsigned tot = 0;
+#pragma unroll
+        for (int w = 0; w < RS_WARPS; ++w) {
+            const unsigned c = s_hist[w][d];
+            s_hist[w][d] = tot;
+            tot += c;
+        }
+        cnt[(size_t)tile * 256 + d] = tot;
+        unsigned gpart;
+        {
+            const unsigned g = ctr->hist[pass][d];
+            unsigned incl = g, inct = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned t = __shfl_up_sync(kFull, incl, o);
+                const unsigned u = __shfl_up_sync(kFull, inct, o);
+                if (lane >= o) {
+                    incl += t;
+                    inct += u;
+                }
+            }
+            if (lane == 31) {
+                s_wsum[0][warp] = incl;
+                s_wsum[1][warp] = inct;
+            }
+            __syncthreads();
+            unsigned wbase = 0, wbase_t = 0;
+            for (int w = 0; w < warp; ++w) {
+                wbase += s_wsum[0][w];
+                wbase_t += s_wsum[1][w];
+            }
+            const unsigned lstart = wbase_t + inct - tot;
+            s_lstart[d] = lstart;
+            gpart = wbase + incl - g - lstart;  // unsigned: wraps back once the tile offset is added
+        }
+        __syncthreads();
+        // the tile into shared memory in digit order (stable: warps, then items, then lanes)
+#pragma unroll
+        for (int j = 0; j < ITEMS; ++j) {
+            if (start + j * 32 + lane < n) {
+                const unsigned dj = (unsigned)((k[j] >> shift) & 255u);
+                const unsigned local = s_lstart[dj] + s_hist[warp][dj] + rank[j];
+                s_k[local] = k[j];
+                s_v[local] = v[j];
+            }
+        }
+        if (!grid_barrier(gb, bar++, ctr)) return;
+        // each digit's counts over the tiles into exclusive offsets, a column per block
+        for (int dd = blockIdx.x; dd < 256; dd += ntiles) {
+            unsigned carry = 0;
+            for (int t0 = 0; t0 < ntiles; t0 += RS_THREADS) {
+                const int t = t0 + tid;
+                const unsigned c = t < ntiles ? ld_cg(cnt + (size_t)t * 256 + dd) : 0u;
+                const unsigned incl = (unsigned)warp_incl_scan((int)c);
+                if (lane == 31) s_col[warp] = incl;
+                __syncthreads();
+                if (tid == 0) {
+                    unsigned run = 0;
+                    for (int w = 0; w < RS_WARPS; ++w) {
+                        const unsigned x = s_col[w];
+                        s_col[w] = run;
+                        run += x;
+                    }
+                    s_col[RS_WARPS] = run;
+                }
+                __syncthreads();
+                if (t < ntiles) cnt[(size_t)t * 256 + dd] = carry + s_col[warp] + incl - c;
+                carry += s_col[RS_WARPS];
+                __syncthreads();
+            }
+        }
+        if (!grid_barrier(gb, bar++, ctr)) return;
+        s_base[d] = gpart + ld_cg(cnt + (size_t)tile * 256 + d);
+        __syncthreads();
+        for (int i = tid; i < tile_n; i += RS_THREADS) {
+            const uint64_t key = s_k[i];
+            const unsigned dk = (unsigned)((key >> shift) & 255u);
+            const unsigned out = s_base[dk] + (unsigned)i;
+            if (out < (unsigned)n) {
+                kout[out] = key;
+                vout[out] = s_v[i];
+            } else {
+                set_error(ctr, ERR_BOUNDS);
+            }
+        }
+        if (pass < 7 && !grid_barrier(gb, bar++, ctr)) return;
+    }
+}
+
+// After the cooperative sort: the sorted particles (x, y, z, m) gathered through
+// the permutation, and the divergence levels and root node as k_diverge sets
+// them.
+template <class T>
+__global__ void k_gather_diverge(const uint64_t *__restrict__ keys, const uint32_t *__restrict__ perm, int n,
+                                 const T *__restrict__ pos, const T *__restrict__ mass, vec4<T> *__restrict__ xyzm,
+                                 uint8_t *__restrict__ div, int *first, int *count, int *child0, int *nchild,
+                                 int *parent, int *level, DevCounters *ctr)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const uint32_t o = perm[i];
+        if (o < (uint32_t)n) {
+            const T *q = pos + 3 * (int64_t)o;
+            xyzm[i] = make4<T>(q[0], q[1], q[2], mass[o]);
+        } else {
+            set_error(ctr, ERR_BOUNDS);
+        }
+        if (i == 0) {
+            div[0] = 0;
+            first[0] = 0; count[0] = n; child0[0] = -1; nchild[0] = 0; parent[0] = -1; level[0] = 0;
+            ctr->level_off[0] = 0;
+            ctr->level_off[1] = 1;
+        } else {
+            const uint64_t x = keys[i - 1] ^ keys[i];
+            div[i] = x ? (uint8_t)(21 - (63 - __clzll((long long)x)) / 3) : (uint8_t)22;
+        }
+    }
+}
+
 template <class T>
 int launch_keys_t(Plan &P, const void *pos, cudaStream_t s)
 {
@@ -326,9 +510,45 @@ int radix_passes(Plan &P, const void *pos, const void *mass, cudaStream_t s)
     return 8;
 }
 
+template <int ITEMS>
+int coop_tiles_max(int num_sms)
+{
+    const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
+    cudaFuncSetAttribute(k_radix_coop<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int b = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_radix_coop<ITEMS>, RS_THREADS, smem);
+    return b * num_sms;
+}
+
+// The cooperative sort when every tile fits on the GPU at once; false otherwise.
+template <class T, int ITEMS>
+bool radix_coop(Plan &P, const void *pos, const void *mass, cudaStream_t s)
+{
+    const int n = (int)P.n;
+    const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
+    if (tiles > P.coop_tiles_sort[ITEMS == RS_ITEMS_LARGE ? 1 : 0] || (size_t)tiles * 256 > P.sort_cnt_cap) return false;
+    const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
+    GridBarrier *gb = P.gbar + 2;
+    void *args[] = {&P.keys[0], &P.idx[0], &P.keys[1], &P.idx[1], (void *)&n, &P.sort_cnt, &gb, &P.ctr};
+    if (cudaLaunchCooperativeKernel((const void *)k_radix_coop<ITEMS>, dim3(tiles), dim3(RS_THREADS), args, smem, s) !=
+        cudaSuccess) {
+        cudaGetLastError();  // a refused launch (not expected: the tiles were counted against the capacity)
+        return false;
+    }
+    // after 8 passes the sorted data is back in buffer 0
+    if (P.mass_wait) cudaStreamWaitEvent(s, P.mass_wait, 0);  // masses still arriving on a side stream
+    k_gather_diverge<T><<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], n, (const T *)pos, (const T *)mass,
+                                                     (vec4<T> *)P.xyzm, P.div, P.node_first, P.node_count,
+                                                     P.node_child0, P.node_nchild, P.node_parent, P.node_level,
+                                                     P.ctr);
+    return true;
+}
+
 template <class T>
 int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
 {
+    if (P.n >= (1 << 19) ? radix_coop<T, RS_ITEMS_LARGE>(P, pos, mass, s) : radix_coop<T, RS_ITEMS_SMALL>(P, pos, mass, s))
+        return 2;
     const int launches = P.n >= (1 << 19) ? radix_passes<T, RS_ITEMS_LARGE>(P, pos, mass, s)
                                           : radix_passes<T, RS_ITEMS_SMALL>(P, pos, mass, s);
     // after 8 passes the sorted data is back in buffer 0
@@ -347,6 +567,12 @@ int launch_keys(Plan &P, const void *pos, cudaStream_t s)
 int launch_sort(Plan &P, const void *pos, const void *mass, cudaStream_t s)
 {
     return P.dtype == 0 ? launch_sort_t<float>(P, pos, mass, s) : launch_sort_t<double>(P, pos, mass, s);
+}
+
+void sort_coop_capacity(int num_sms, int tiles[2])
+{
+    tiles[0] = coop_tiles_max<RS_ITEMS_SMALL>(num_sms);
+    tiles[1] = coop_tiles_max<RS_ITEMS_LARGE>(num_sms);
 }
 
 }  // namespace bfm

@@ -30,6 +30,7 @@ struct Plan {
     int num_sms = 148;
     int coop_blocks_tree = 148;   // grids of the cooperative launches (co-resident blocks)
     int coop_blocks_walk = 148;
+    int coop_tiles_sort[2] = {0, 0};  // co-resident tiles of the cooperative radix sort (small, large tiles)
 
     // capacities
     int64_t cap_nodes = 0, cap_frontier = 0, cap_m2l = 0, cap_p2p = 0, cap_flags = 0;
@@ -79,7 +80,9 @@ struct Plan {
 
     // status
     DevCounters *ctr = nullptr;      // device
-    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0] and walk [1]
+    GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0], walk [1] and sort [2]
+    unsigned *sort_cnt = nullptr;    // device: per tile and digit, the cooperative sort's counts and offsets
+    size_t sort_cnt_cap = 0;         // its entries
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
@@ -136,6 +139,7 @@ int launch_keys(Plan &P, const void *pos, cudaStream_t s);
 int launch_sort(Plan &P, const void *pos, const void *mass, cudaStream_t s);
 int launch_tree(Plan &P, cudaStream_t s);
 size_t tree_cc_ints(int64_t n);  // size of Plan::tree_cc for n particles
+void sort_coop_capacity(int num_sms, int tiles[2]);  // co-resident tiles of the cooperative sort
 int tree_max_blocks_per_sm();
 int walk_max_blocks_per_sm(int dtype);
 int launch_upward(Plan &P, cudaStream_t s);
