@@ -59,18 +59,18 @@ P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r
 # 1e5 fp64, p 4), keyed by the hash of the kernel sources they were counted on;
 # a changed kernel reports null until it is counted again.
 DF_FMA_OPS_PER_PAIR = {
-    # k_p2p_df: 9,097,899,392 FMA-pipe thread instructions (all scalar) over 48,823,340 pairs
-    ("k_p2p_df", "ced2e98ffaa7e256"): 186.34,
-    # k_m2l_df<4>: 6,073,018,112 over 1,833,964 pairs (the moments' conversion kernel is not counted)
-    ("k_m2l_df", "61a2aad5e1163c40"): 3311.4,
+    # k_p2p_df: 9,097,920,864 FMA-pipe thread instructions (all scalar) over 48,823,340 pairs
+    ("k_p2p_df", "4905586f2eef129a"): 186.34,
+    # k_m2l_df<4>: 6,075,552,672 over 1,833,964 pairs (the moments' conversion kernel is not counted)
+    ("k_m2l_df", "24ba5cc236d86c00"): 3312.8,
 }
 
 # DRAM traffic of the P2P kernel per launch (dram__bytes_read.sum +
 # dram__bytes_write.sum, one warm launch of clustered N = 2^20 fp32), keyed by
 # the hash of the kernel sources it was taken on; null once they change.
 TRAFFIC = {
-    # k_p2p<float>: 52,506,624 B read + 3,641,088 B written
-    ("clustered_2p20_f32", "4ee36c430f265157"): 56147712,
+    # k_p2p<float>: 52,613,632 B read + 3,910,912 B written
+    ("clustered_2p20_f32", "79e69f34e661b67d"): 56524544,
 }
 
 

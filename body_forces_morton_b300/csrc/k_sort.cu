@@ -294,8 +294,8 @@ __global__ void k_diverge(const uint64_t *__restrict__ keys, int n, uint8_t *__r
 // per block with every tile resident (N up to the co-resident tiles). Per
 // pass: each tile ranks its keys per digit as k_radix_pass does, publishes its
 // 256 digit counts and reorders itself by digit in shared memory; after a grid
-// barrier the blocks scan each digit's counts over the tiles (a column per
-// block, in place, into exclusive offsets); after a second barrier each tile
+// barrier the warps scan each digit's counts over the tiles (a column per
+// warp, in place, into exclusive offsets); after a second barrier each tile
 // writes its runs to the pass's global digit start plus its offset; a third
 // barrier ends the pass. Three barriers replace the look-back chain, which
 // with every tile starting at once runs through the tiles one after another.
@@ -311,7 +311,6 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_
     __shared__ unsigned s_lstart[256];
     __shared__ unsigned s_base[256];
     __shared__ unsigned s_wsum[2][RS_WARPS];
-    __shared__ unsigned s_col[RS_WARPS + 1];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int tile = blockIdx.x, ntiles = gridDim.x;
     const int64_t start = (int64_t)tile * TILE + warp * (32 * ITEMS);
@@ -400,28 +399,25 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_
             }
         }
         if (!grid_barrier(gb, bar++, ctr)) return;
-        // each digit's counts over the tiles into exclusive offsets, a column per block
-        for (int dd = blockIdx.x; dd < 256; dd += ntiles) {
+        // each digit's counts over the tiles into exclusive offsets, a column per warp (lanes over
+        // tiles), so that small grids need no block barriers for it; columns go to the blocks in turn,
+        // then to their warps, which spreads the column loads over the SMs
+        for (int dd = blockIdx.x + ntiles * warp; dd < 256; dd += ntiles * RS_WARPS) {
             unsigned carry = 0;
-            for (int t0 = 0; t0 < ntiles; t0 += RS_THREADS) {
-                const int t = t0 + tid;
-                const unsigned c = t < ntiles ? ld_cg(cnt + (size_t)t * 256 + dd) : 0u;
-                const unsigned incl = (unsigned)warp_incl_scan((int)c);
-                if (lane == 31) s_col[warp] = incl;
-                __syncthreads();
-                if (tid == 0) {
-                    unsigned run = 0;
-                    for (int w = 0; w < RS_WARPS; ++w) {
-                        const unsigned x = s_col[w];
-                        s_col[w] = run;
-                        run += x;
-                    }
-                    s_col[RS_WARPS] = run;
+            for (int t0 = 0; t0 < ntiles; t0 += 32 * 8) {
+                unsigned c[8];  // eight chunks of 32 tiles loaded at once
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = t0 + 32 * u + lane;
+                    c[u] = t < ntiles ? ld_cg(cnt + (size_t)t * 256 + dd) : 0u;
                 }
-                __syncthreads();
-                if (t < ntiles) cnt[(size_t)t * 256 + dd] = carry + s_col[warp] + incl - c;
-                carry += s_col[RS_WARPS];
-                __syncthreads();
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int t = t0 + 32 * u + lane;
+                    const unsigned incl = (unsigned)warp_incl_scan((int)c[u]);
+                    if (t < ntiles) cnt[(size_t)t * 256 + dd] = carry + incl - c[u];
+                    carry += __shfl_sync(kFull, incl, 31);
+                }
             }
         }
         if (!grid_barrier(gb, bar++, ctr)) return;
@@ -526,7 +522,10 @@ bool radix_coop(Plan &P, const void *pos, const void *mass, cudaStream_t s)
 {
     const int n = (int)P.n;
     const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
-    if (tiles > P.coop_tiles_sort[ITEMS == RS_ITEMS_LARGE ? 1 : 0] || (size_t)tiles * 256 > P.sort_cnt_cap) return false;
+    // below 16 tiles the per-pass kernels win (their look-backs are short and the launches cost less than
+    // the cooperative kernel's 23 grid barriers); above the co-resident tiles they are the only choice
+    if (tiles < 16 || tiles > P.coop_tiles_sort[ITEMS == RS_ITEMS_LARGE ? 1 : 0] || (size_t)tiles * 256 > P.sort_cnt_cap)
+        return false;
     const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
     GridBarrier *gb = P.gbar + 2;
     void *args[] = {&P.keys[0], &P.idx[0], &P.keys[1], &P.idx[1], (void *)&n, &P.sort_cnt, &gb, &P.ctr};
