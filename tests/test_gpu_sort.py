@@ -1,0 +1,33 @@
+"""The radix sort's dispatch edges against the oracle's keys and a stable sort.
+
+The evaluation sorts (key, index) pairs with one cooperative launch for all 8
+passes when the tiles number at least 16 and all fit on the GPU at once, and
+with one kernel per pass otherwise; 2^19 switches the tile from 2048 to 4096
+keys. Each case checks the sorted keys and the permutation bit for bit against
+the oracle's keys sorted by (key, index), with a run of coincident particles
+so that equal keys must keep their index order.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from body_forces_morton_b300 import workloads as W
+from gpu_helpers import gpu_eval
+
+pytestmark = pytest.mark.gpu
+
+# 15 tiles of 2048 (per pass), 16 (cooperative), 256 tiles of 2048 and 128 of 4096 (cooperative),
+# about 500 tiles of 4096 (more than fit at once: per pass)
+SIZES = [15 * 2048, 15 * 2048 + 1, (1 << 19) - 1, 1 << 19, 2_100_000]
+
+
+@pytest.mark.parametrize("n", SIZES)
+def test_sort_dispatch_edges(n):
+    g = W.generate(W.WORKLOADS[4], n=n)
+    pos = np.array(g["pos"])
+    pos[100:300] = pos[100]  # 200 equal keys
+    k, _ = oracle.keys(pos)
+    perm = np.lexsort((np.arange(n), k))
+    _, _, ex, _ = gpu_eval(pos, g["mass"], 0, 0.7, 64, want_pot=False, exports=("keys", "perm"))
+    assert np.array_equal(ex["keys"], k[perm]), "sorted keys differ"
+    assert np.array_equal(ex["perm"].astype(np.int64), perm), "sort permutation differs"
