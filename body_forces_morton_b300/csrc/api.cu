@@ -249,7 +249,7 @@ void destroy_plan(Plan &P)
     free_nodes(P);
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
-    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.vwin); dfree(P.tree_cc); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar); dfree(P.sort_cnt);
+    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.vwin); dfree(P.tree_cc); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar); dfree(P.sort_cnt); dfree(P.sort_big);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     dfree(P.vjp_acc); dfree(P.vjp_src); dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
     free_mutual(P);
@@ -501,6 +501,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         P.sort_cnt_cap = (size_t)256 * std::max(1, std::max(P.coop_tiles_sort[0], P.coop_tiles_sort[1]));
     }
     const size_t nn = (size_t)n, e = (size_t)P.esize;
+    P.sort_big_cap = nn / 33 + 1;  // runs of over 32 keys
     if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
         !ok(dalloc(P.idx[0], nn), "perm") || !ok(dalloc(P.idx[1], nn), "perm") ||
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
@@ -509,6 +510,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
         !ok(dalloc(P.gbar, 3), "grid barriers") ||
         !ok(dalloc(P.sort_cnt, P.sort_cnt_cap), "sort counts") ||
+        !ok(dalloc(P.sort_big, P.sort_big_cap), "sort runs") ||
         !ok(cudaMallocHost((void **)&P.ctr_host, sizeof(DevCounters)), "pinned counters"))
         return fail(FMM_ERR_OOM);
     for (int i = 0; i < kNumEvents; ++i)

@@ -7,16 +7,19 @@
 // is evaluated step by step in the plan's precision without contraction, so the
 // keys are exactly those of any other implementation doing the same steps.
 //
-// Radix sort: 8 passes of 8 bits. A block ranks a 4096-key tile's keys per
-// digit with warp match_any (stable within the tile), finds the tile's output
-// offset per digit, reorders the tile by digit in shared memory and writes it
-// out in runs of consecutive positions (one digit's keys of a tile are
-// contiguous in the output). When every tile fits on the GPU at once, all 8
-// passes run in one cooperative launch, the offsets from a scan of the tiles'
-// counts between grid barriers (k_radix_coop), and a second kernel gathers
-// (x, y, z, m) into sorted order; otherwise each pass is one kernel that takes
-// tiles from a ticket counter and finds the offsets with a decoupled look-back
-// over the earlier tiles, the last pass gathering the particles.
+// Radix sort of (key, index) pairs: 4 passes of 8 bits over the high word
+// (bits 32..63), then each run of keys with equal high words sorted by its low
+// word and index (k_sort_groups, k_sort_big): the same order as sorting the
+// whole key, since the passes are stable. At 2^20 clustered keys the runs
+// number about 9e4 and hold at most a dozen keys. A pass ranks a 4096-key
+// tile's keys per digit with warp match_any (stable within the tile), reorders
+// the tile by digit in shared memory and writes it out in runs of consecutive
+// positions (one digit's keys of a tile are contiguous in the output). When
+// every tile fits on the GPU at once, the passes run in one cooperative launch,
+// the offsets from a scan of the tiles' counts between grid barriers
+// (k_radix_coop); otherwise each pass is one kernel that takes tiles from a
+// ticket counter and finds the offsets with a decoupled look-back over the
+// earlier tiles. A last kernel gathers (x, y, z, m) into sorted order.
 #include "plan.h"
 
 namespace bfm {
@@ -29,6 +32,13 @@ constexpr int RS_WARPS = RS_THREADS / 32;
 // keys per thread: 16 (4096-key tiles) from N = 2^19 on, 8 (2048-key tiles, twice the
 // blocks) below, where the sort has too few tiles to fill the GPU (both measured)
 constexpr int RS_ITEMS_LARGE = 16, RS_ITEMS_SMALL = 8;
+// The radix passes sort by the high word (digits 4..7, bits 32..63); runs of
+// keys with equal high words are then sorted by their low words: up to
+// kGroupMax keys by one thread, longer runs by a block (in shared memory up to
+// kBigSmem keys, else four stable passes over the low word).
+constexpr int kSortPass0 = 4;
+constexpr int kGroupMax = 32;
+constexpr int kBigSmem = 4096;
 
 __device__ __forceinline__ uint64_t spread3(uint32_t v)
 {
@@ -128,7 +138,8 @@ template <class T> __device__ __forceinline__ uint32_t quantise(T x, T lo, T sid
     return q > 2097151u ? 2097151u : q;
 }
 
-// Keys in the caller's order plus the digit histograms of all 8 passes.
+// Keys in the caller's order plus the digit histograms of the radix passes
+// (the digits of the high word).
 template <class T>
 __global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, uint64_t *__restrict__ keys,
                                               DevCounters *ctr)
@@ -143,7 +154,7 @@ __global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, 
                      spread3(quantise(q[2], lo2, side));
         keys[i] = k;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) atomicAdd(&h[r][(k >> (8 * r)) & 255u], 1u);
+        for (int r = kSortPass0; r < 8; ++r) atomicAdd(&h[r][(k >> (8 * r)) & 255u], 1u);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) {
@@ -152,13 +163,12 @@ __global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, 
     }
 }
 
-template <class T, bool FIRST, bool LAST, int RS_ITEMS>
+template <bool FIRST, int RS_ITEMS>
 __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__restrict__ kin,
                                                            const uint32_t *__restrict__ vin,
                                                            uint64_t *__restrict__ kout, uint32_t *__restrict__ vout,
                                                            int n, int pass, unsigned long long *flags, unsigned epoch,
-                                                           int slot, DevCounters *ctr, const T *__restrict__ pos,
-                                                           const T *__restrict__ mass, vec4<T> *__restrict__ xyzm)
+                                                           int slot, DevCounters *ctr)
 {
     constexpr int TILE = RS_THREADS * RS_ITEMS;
     extern __shared__ __align__(16) unsigned char rs_smem[];
@@ -261,36 +271,13 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
         if (out < (unsigned)n) {
             kout[out] = key;
             vout[out] = val;
-            if (LAST) {
-                const T *q = pos + 3 * (int64_t)val;
-                xyzm[out] = make4<T>(q[0], q[1], q[2], mass[val]);
-            }
         } else {
             set_error(ctr, ERR_BOUNDS);
         }
     }
 }
 
-// Divergence level of consecutive sorted keys: the first tree level at which
-// keys[i-1] and keys[i] fall in different cells (22 when equal). Also sets up
-// the root node.
-__global__ void k_diverge(const uint64_t *__restrict__ keys, int n, uint8_t *__restrict__ div, int *first,
-                          int *count, int *child0, int *nchild, int *parent, int *level, DevCounters *ctr)
-{
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        if (i == 0) {
-            div[0] = 0;
-            first[0] = 0; count[0] = n; child0[0] = -1; nchild[0] = 0; parent[0] = -1; level[0] = 0;
-            ctr->level_off[0] = 0;
-            ctr->level_off[1] = 1;
-        } else {
-            uint64_t x = keys[i - 1] ^ keys[i];
-            div[i] = x ? (uint8_t)(21 - (63 - __clzll((long long)x)) / 3) : (uint8_t)22;
-        }
-    }
-}
-
-// All 8 passes in one cooperative launch, one tile of RS_THREADS * ITEMS keys
+// All radix passes in one cooperative launch, one tile of RS_THREADS * ITEMS keys
 // per block with every tile resident (N up to the co-resident tiles). Per
 // pass: each tile ranks its keys per digit as k_radix_pass does, publishes its
 // 256 digit counts and reorders itself by digit in shared memory; after a grid
@@ -317,7 +304,7 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_
     const int64_t left = (int64_t)n - (int64_t)tile * TILE;
     const int tile_n = left < TILE ? (int)left : TILE;
     unsigned bar = 0;
-    for (int pass = 0; pass < 8; ++pass) {
+    for (int pass = kSortPass0; pass < 8; ++pass) {
         const uint64_t *kin = (pass & 1) ? k1 : k0;
         const uint32_t *vin = (pass & 1) ? v1 : v0;
         uint64_t *kout = (pass & 1) ? k0 : k1;
@@ -333,7 +320,7 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_
             const int64_t i = start + j * 32 + lane;
             const bool valid = i < n;
             k[j] = valid ? ld_cg(kin + i) : ~0ull;  // written by other blocks in the previous pass
-            v[j] = valid ? (pass == 0 ? (uint32_t)i : ld_cg(vin + i)) : 0u;
+            v[j] = valid ? (pass == kSortPass0 ? (uint32_t)i : ld_cg(vin + i)) : 0u;
         }
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
@@ -438,9 +425,10 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_
     }
 }
 
-// After the cooperative sort: the sorted particles (x, y, z, m) gathered through
-// the permutation, and the divergence levels and root node as k_diverge sets
-// them.
+// After the sort: the sorted particles (x, y, z, m) gathered through the
+// permutation, the divergence levels of consecutive sorted keys (the first tree
+// level at which keys[i-1] and keys[i] fall in different cells, 22 when equal)
+// and the root node.
 template <class T>
 __global__ void k_gather_diverge(const uint64_t *__restrict__ keys, const uint32_t *__restrict__ perm, int n,
                                  const T *__restrict__ pos, const T *__restrict__ mass, vec4<T> *__restrict__ xyzm,
@@ -467,6 +455,168 @@ __global__ void k_gather_diverge(const uint64_t *__restrict__ keys, const uint32
     }
 }
 
+// Runs of equal high words after the radix passes are in index order; each is
+// sorted by (key, index). The thread at a run's head sorts a run of up to
+// kGroupMax keys in place (insertion sort, stable, so equal keys keep their
+// index order); longer runs are listed for k_sort_big. A run's writes permute
+// keys that share one high word, so the neighbours' run tests are unaffected.
+__global__ void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int *big, int cap_big, DevCounters *ctr)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const uint32_t hi = (uint32_t)(keys[i] >> 32);
+        if (i > 0 && (uint32_t)(keys[i - 1] >> 32) == hi) continue;       // not the head of a run
+        if (i + 1 >= n || (uint32_t)(keys[i + 1] >> 32) != hi) continue;  // a run of one
+        int len = 2;
+        while (len <= kGroupMax && i + len < n && (uint32_t)(keys[i + len] >> 32) == hi) ++len;
+        if (len > kGroupMax) {
+            const int slot = atomicAdd(&ctr->n_sort_groups, 1);
+            if (slot < cap_big) big[slot] = i;
+            else set_error(ctr, ERR_BOUNDS);
+            continue;
+        }
+        uint64_t k[kGroupMax];
+        uint32_t v[kGroupMax];
+        for (int j = 0; j < len; ++j) {
+            k[j] = keys[i + j];
+            v[j] = idx[i + j];
+        }
+        for (int j = 1; j < len; ++j) {
+            const uint64_t kj = k[j];
+            const uint32_t vj = v[j];
+            int m = j - 1;
+            while (m >= 0 && k[m] > kj) {
+                k[m + 1] = k[m];
+                v[m + 1] = v[m];
+                --m;
+            }
+            k[m + 1] = kj;
+            v[m + 1] = vj;
+        }
+        for (int j = 0; j < len; ++j) {
+            keys[i + j] = k[j];
+            idx[i + j] = v[j];
+        }
+    }
+}
+
+// The listed long runs, a block each: up to kBigSmem keys sorted in shared
+// memory by (low word, index) with the bitonic network of cmpswap_u64 below;
+// longer runs by four stable passes of 8 bits over the low word, between the
+// run's place in buffers 0 and 1 (tiles of 256 keys in order; within a tile,
+// warp match_any ranks and per-warp digit counts keep the order).
+__device__ __forceinline__ void cmpswap_u64(uint64_t *v, int i, int j)
+{
+    const uint64_t a = v[i], b = v[j];
+    if (b < a) {
+        v[i] = b;
+        v[j] = a;
+    }
+}
+
+__global__ __launch_bounds__(256) void k_sort_big(uint64_t *k0, uint32_t *v0, uint64_t *k1, uint32_t *v1, int n,
+                                                  const int *__restrict__ big, int cap_big, const DevCounters *cst,
+                                                  DevCounters *ctr)
+{
+    __shared__ uint64_t s_c[kBigSmem];
+    __shared__ unsigned s_wcnt[8][256];
+    __shared__ unsigned s_base[256];
+    __shared__ unsigned s_wsum[8];
+    __shared__ int s_end;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nb = min(cst->n_sort_groups, cap_big);
+    for (int b = blockIdx.x; b < nb; b += gridDim.x) {
+        const int s = big[b];
+        const uint32_t hw = (uint32_t)(k0[s] >> 32);
+        if (tid == 0) {  // the run's end: the keys are ordered by high word
+            int lo = s, hi = n;
+            while (lo < hi) {
+                const int mid = lo + (hi - lo) / 2;
+                if ((uint32_t)(k0[mid] >> 32) <= hw) lo = mid + 1;
+                else hi = mid;
+            }
+            s_end = lo;
+        }
+        __syncthreads();
+        const int e = s_end, G = e - s;
+        if (G <= kBigSmem) {
+            int S = 2;
+            while (S < G) S <<= 1;
+            for (int i = tid; i < S; i += 256)
+                s_c[i] = i < G ? ((k0[s + i] & 0xffffffffull) << 32) | (uint64_t)v0[s + i] : ~0ull;
+            __syncthreads();
+            for (int lk = 1; (1 << lk) <= S; ++lk) {
+                const int k = 1 << lk;
+                for (int i = tid; i < S / 2; i += 256) {
+                    const int blk = i >> (lk - 1), pos = i & ((k >> 1) - 1);
+                    cmpswap_u64(s_c, blk * k + pos, blk * k + k - 1 - pos);
+                }
+                __syncthreads();
+                for (int lj = lk - 2; lj >= 0; --lj) {
+                    const int j = 1 << lj;
+                    for (int i = tid; i < S / 2; i += 256) {
+                        const int blk = i >> lj, pos = i & (j - 1);
+                        cmpswap_u64(s_c, (blk << (lj + 1)) + pos, (blk << (lj + 1)) + pos + j);
+                    }
+                    __syncthreads();
+                }
+            }
+            for (int i = tid; i < G; i += 256) {
+                const uint64_t c = s_c[i];
+                k0[s + i] = ((uint64_t)hw << 32) | (c >> 32);
+                v0[s + i] = (uint32_t)c;
+            }
+            __syncthreads();
+            continue;
+        }
+        for (int pass = 0; pass < 4; ++pass) {
+            const uint64_t *ki = (pass & 1) ? k1 : k0;
+            const uint32_t *vi = (pass & 1) ? v1 : v0;
+            uint64_t *ko = (pass & 1) ? k0 : k1;
+            uint32_t *vo = (pass & 1) ? v0 : v1;
+            const int shift = 8 * pass;
+            for (int i = tid; i < 8 * 256; i += 256) (&s_wcnt[0][0])[i] = 0;
+            __syncthreads();
+            for (int j = s + tid; j < e; j += 256) atomicAdd(&s_wcnt[0][(ki[j] >> shift) & 255u], 1u);
+            __syncthreads();
+            {  // exclusive scan of the run's digit counts into the digits' starts
+                const unsigned c = s_wcnt[0][tid];
+                const unsigned incl = (unsigned)warp_incl_scan((int)c);
+                if (lane == 31) s_wsum[warp] = incl;
+                __syncthreads();
+                unsigned wb = 0;
+                for (int w = 0; w < warp; ++w) wb += s_wsum[w];
+                s_base[tid] = (unsigned)s + wb + incl - c;
+                s_wcnt[0][tid] = 0;
+            }
+            __syncthreads();
+            for (int t0 = s; t0 < e; t0 += 256) {
+                const int j = t0 + tid;
+                const bool valid = j < e;
+                const unsigned d = valid ? (unsigned)((ki[j] >> shift) & 255u) : 256u;
+                const unsigned peers = __match_any_sync(kFull, d);
+                const int leader = __ffs(peers) - 1;
+                if (lane == leader && valid) s_wcnt[warp][d] = __popc(peers);
+                __syncthreads();
+                if (valid) {
+                    unsigned off = s_base[d] + __popc(peers & lanemask_lt());
+                    for (int w = 0; w < warp; ++w) off += s_wcnt[w][d];
+                    ko[off] = ki[j];
+                    vo[off] = vi[j];
+                }
+                __syncthreads();
+                unsigned add = 0;
+                for (int w = 0; w < 8; ++w) {
+                    add += s_wcnt[w][tid];
+                    s_wcnt[w][tid] = 0;
+                }
+                s_base[tid] += add;
+                __syncthreads();
+            }
+        }
+    }
+    (void)ctr;
+}
+
 template <class T>
 int launch_keys_t(Plan &P, const void *pos, cudaStream_t s)
 {
@@ -476,34 +626,26 @@ int launch_keys_t(Plan &P, const void *pos, cudaStream_t s)
     return 2;
 }
 
-template <class T, int ITEMS>
-int radix_passes(Plan &P, const void *pos, const void *mass, cudaStream_t s)
+template <int ITEMS>
+int radix_passes(Plan &P, cudaStream_t s)
 {
     const int n = (int)P.n;
     const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
     const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
-    cudaFuncSetAttribute(k_radix_pass<T, true, false, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(k_radix_pass<T, false, false, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(k_radix_pass<T, false, true, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    for (int pass = 0; pass < 8; ++pass) {
+    cudaFuncSetAttribute(k_radix_pass<true, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(k_radix_pass<false, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    for (int pass = kSortPass0; pass < 8; ++pass) {
         const int src = pass & 1, dst = src ^ 1;
         const int slot = P.next_slot();
         const unsigned ep = P.next_epoch();
-        if (pass == 0)
-            k_radix_pass<T, true, false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
-                P.keys[src], nullptr, P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
-                nullptr);
-        else if (pass == 7) {
-            if (P.mass_wait) cudaStreamWaitEvent(s, P.mass_wait, 0);  // masses still arriving on a side stream
-            k_radix_pass<T, false, true, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
-                P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, (const T *)pos,
-                (const T *)mass, (vec4<T> *)P.xyzm);
-        } else
-            k_radix_pass<T, false, false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(
-                P.keys[src], P.idx[src], P.keys[dst], P.idx[dst], n, pass, P.flags, ep, slot, P.ctr, nullptr, nullptr,
-                nullptr);
+        if (pass == kSortPass0)
+            k_radix_pass<true, ITEMS><<<tiles, RS_THREADS, smem, s>>>(P.keys[src], nullptr, P.keys[dst], P.idx[dst], n,
+                                                                      pass, P.flags, ep, slot, P.ctr);
+        else
+            k_radix_pass<false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(P.keys[src], P.idx[src], P.keys[dst], P.idx[dst],
+                                                                       n, pass, P.flags, ep, slot, P.ctr);
     }
-    return 8;
+    return 8 - kSortPass0;
 }
 
 template <int ITEMS>
@@ -517,13 +659,13 @@ int coop_tiles_max(int num_sms)
 }
 
 // The cooperative sort when every tile fits on the GPU at once; false otherwise.
-template <class T, int ITEMS>
-bool radix_coop(Plan &P, const void *pos, const void *mass, cudaStream_t s)
+template <int ITEMS>
+bool radix_coop(Plan &P, cudaStream_t s)
 {
     const int n = (int)P.n;
     const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
     // below 16 tiles the per-pass kernels win (their look-backs are short and the launches cost less than
-    // the cooperative kernel's 23 grid barriers); above the co-resident tiles they are the only choice
+    // the cooperative kernel's 11 grid barriers); above the co-resident tiles they are the only choice
     if (tiles < 16 || tiles > P.coop_tiles_sort[ITEMS == RS_ITEMS_LARGE ? 1 : 0] || (size_t)tiles * 256 > P.sort_cnt_cap)
         return false;
     const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
@@ -534,26 +676,30 @@ bool radix_coop(Plan &P, const void *pos, const void *mass, cudaStream_t s)
         cudaGetLastError();  // a refused launch (not expected: the tiles were counted against the capacity)
         return false;
     }
-    // after 8 passes the sorted data is back in buffer 0
-    if (P.mass_wait) cudaStreamWaitEvent(s, P.mass_wait, 0);  // masses still arriving on a side stream
-    k_gather_diverge<T><<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], n, (const T *)pos, (const T *)mass,
-                                                     (vec4<T> *)P.xyzm, P.div, P.node_first, P.node_count,
-                                                     P.node_child0, P.node_nchild, P.node_parent, P.node_level,
-                                                     P.ctr);
     return true;
 }
 
 template <class T>
 int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
 {
-    if (P.n >= (1 << 19) ? radix_coop<T, RS_ITEMS_LARGE>(P, pos, mass, s) : radix_coop<T, RS_ITEMS_SMALL>(P, pos, mass, s))
-        return 2;
-    const int launches = P.n >= (1 << 19) ? radix_passes<T, RS_ITEMS_LARGE>(P, pos, mass, s)
-                                          : radix_passes<T, RS_ITEMS_SMALL>(P, pos, mass, s);
-    // after 8 passes the sorted data is back in buffer 0
-    k_diverge<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], (int)P.n, P.div, P.node_first, P.node_count, P.node_child0,
-                                           P.node_nchild, P.node_parent, P.node_level, P.ctr);
-    return launches + 1;
+    const int n = (int)P.n;
+    int launches;
+    if (P.n >= (1 << 19) ? radix_coop<RS_ITEMS_LARGE>(P, s) : radix_coop<RS_ITEMS_SMALL>(P, s))
+        launches = 1;
+    else
+        launches = P.n >= (1 << 19) ? radix_passes<RS_ITEMS_LARGE>(P, s) : radix_passes<RS_ITEMS_SMALL>(P, s);
+    // an even number of passes: the data is back in buffer 0, ordered by high word; then the runs of equal
+    // high words by low word and index
+    const int cap_big = (int)P.sort_big_cap;
+    k_sort_groups<<<P.num_sms * 8, 256, 0, s>>>(P.keys[0], P.idx[0], n, P.sort_big, cap_big, P.ctr);
+    k_sort_big<<<P.num_sms, 256, 0, s>>>(P.keys[0], P.idx[0], P.keys[1], P.idx[1], n, P.sort_big, cap_big, P.ctr,
+                                         P.ctr);
+    if (P.mass_wait) cudaStreamWaitEvent(s, P.mass_wait, 0);  // masses still arriving on a side stream
+    k_gather_diverge<T><<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], n, (const T *)pos, (const T *)mass,
+                                                     (vec4<T> *)P.xyzm, P.div, P.node_first, P.node_count,
+                                                     P.node_child0, P.node_nchild, P.node_parent, P.node_level,
+                                                     P.ctr);
+    return launches + 3;
 }
 
 }  // namespace
