@@ -367,6 +367,8 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
             P.retries++;
             continue;
         }
+        // the next evaluation's sort: all 8 digits when long runs of equal high words held many keys here
+        P.sort_full = P.sort_full || (int64_t)h.sort_long_keys * 64 > P.n;
         P.depth = h.depth;
         P.n_nodes = h.n_nodes;
         const unsigned cap_bits = ERR_FRONTIER | ERR_M2L_CAP | ERR_P2P_CAP;

@@ -62,6 +62,7 @@ struct DevCounters {
     long long p2p_interactions;
     int n_long;                    // list segments too long for the warp sort
     int n_sort_groups;             // runs of equal high key words too long for one thread
+    int sort_long_keys;            // the keys in those runs
     long long mut_need[3];         // mutual buffers needed (set with ERR_MUT_CAP): P2P share slots, M2L
                                    // list entries, P2P list entries
     int order_cnt[2][64];          // work buckets (0: P2P receivers, 1: M2L receivers)

@@ -9,17 +9,20 @@
 //
 // Radix sort of (key, index) pairs: 4 passes of 8 bits over the high word
 // (bits 32..63), then each run of keys with equal high words sorted by its low
-// word and index (k_sort_groups, k_sort_big): the same order as sorting the
-// whole key, since the passes are stable. At 2^20 clustered keys the runs
-// number about 9e4 and hold at most a dozen keys. A pass ranks a 4096-key
-// tile's keys per digit with warp match_any (stable within the tile), reorders
-// the tile by digit in shared memory and writes it out in runs of consecutive
-// positions (one digit's keys of a tile are contiguous in the output). When
-// every tile fits on the GPU at once, the passes run in one cooperative launch,
-// the offsets from a scan of the tiles' counts between grid barriers
-// (k_radix_coop); otherwise each pass is one kernel that takes tiles from a
-// ticket counter and finds the offsets with a decoupled look-back over the
-// earlier tiles. A last kernel gathers (x, y, z, m) into sorted order.
+// word and index (k_sort_groups, k_sort_runs_warp, k_sort_big): the same order
+// as sorting the whole key, since the passes are stable. At 2^20 clustered
+// keys the runs number about 9e4 and hold at most a dozen keys; strongly
+// clustered states (collapsed halo cores) put a large share of the keys into
+// long runs, and after such an evaluation the plan sorts all 8 digits instead.
+// A pass ranks a 4096-key tile's keys per digit with warp match_any (stable
+// within the tile), reorders the tile by digit in shared memory and writes it
+// out in runs of consecutive positions (one digit's keys of a tile are
+// contiguous in the output). When every tile fits on the GPU at once, the
+// passes run in one cooperative launch, the offsets from a scan of the tiles'
+// counts between grid barriers (k_radix_coop); otherwise each pass is one
+// kernel that takes tiles from a ticket counter and finds the offsets with a
+// decoupled look-back over the earlier tiles. A last kernel gathers
+// (x, y, z, m) into sorted order.
 #include "plan.h"
 
 namespace bfm {
@@ -34,11 +37,17 @@ constexpr int RS_WARPS = RS_THREADS / 32;
 constexpr int RS_ITEMS_LARGE = 16, RS_ITEMS_SMALL = 8;
 // The radix passes sort by the high word (digits 4..7, bits 32..63); runs of
 // keys with equal high words are then sorted by their low words: up to
-// kGroupMax keys by one thread, longer runs by a block (in shared memory up to
-// kBigSmem keys, else four stable passes over the low word).
-constexpr int kSortPass0 = 4;
+// kGroupMax keys by one thread, up to kWarpRun by a warp in registers, longer
+// runs by a block (in shared memory up to kBigSmem keys, else four stable
+// passes over the low word). When the previous evaluation found more than
+// N / kLongRunsDiv keys in runs longer than kGroupMax (strongly clustered or
+// coincident particles), all 8 digits are sorted instead and the runs need no
+// second step.
+constexpr int kSortHighPass0 = 4;
 constexpr int kGroupMax = 32;
+constexpr int kWarpRun = 512;
 constexpr int kBigSmem = 4096;
+constexpr int kLongRunsDiv = 64;
 
 __device__ __forceinline__ uint64_t spread3(uint32_t v)
 {
@@ -142,7 +151,7 @@ template <class T> __device__ __forceinline__ uint32_t quantise(T x, T lo, T sid
 // (the digits of the high word).
 template <class T>
 __global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, uint64_t *__restrict__ keys,
-                                              DevCounters *ctr)
+                                              int p0, DevCounters *ctr)
 {
     __shared__ unsigned h[8][256];
     for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) (&h[0][0])[i] = 0;
@@ -154,7 +163,8 @@ __global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, 
                      spread3(quantise(q[2], lo2, side));
         keys[i] = k;
 #pragma unroll
-        for (int r = kSortPass0; r < 8; ++r) atomicAdd(&h[r][(k >> (8 * r)) & 255u], 1u);
+        for (int r = 0; r < 8; ++r)
+            if (r >= p0) atomicAdd(&h[r][(k >> (8 * r)) & 255u], 1u);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) {
@@ -288,7 +298,8 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_pass(const uint64_t *__res
 // with every tile starting at once runs through the tiles one after another.
 template <int ITEMS>
 __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_t *v0, uint64_t *k1, uint32_t *v1,
-                                                           int n, unsigned *cnt, GridBarrier *gb, DevCounters *ctr)
+                                                           int n, int p0, unsigned *cnt, GridBarrier *gb,
+                                                           DevCounters *ctr)
 {
     constexpr int TILE = RS_THREADS * ITEMS;
     extern __shared__ __align__(16) unsigned char rs_smem[];
@@ -304,7 +315,7 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_
     const int64_t left = (int64_t)n - (int64_t)tile * TILE;
     const int tile_n = left < TILE ? (int)left : TILE;
     unsigned bar = 0;
-    for (int pass = kSortPass0; pass < 8; ++pass) {
+    for (int pass = p0; pass < 8; ++pass) {
         const uint64_t *kin = (pass & 1) ? k1 : k0;
         const uint32_t *vin = (pass & 1) ? v1 : v0;
         uint64_t *kout = (pass & 1) ? k0 : k1;
@@ -320,7 +331,7 @@ __global__ __launch_bounds__(RS_THREADS) void k_radix_coop(uint64_t *k0, uint32_
             const int64_t i = start + j * 32 + lane;
             const bool valid = i < n;
             k[j] = valid ? ld_cg(kin + i) : ~0ull;  // written by other blocks in the previous pass
-            v[j] = valid ? (pass == kSortPass0 ? (uint32_t)i : ld_cg(vin + i)) : 0u;
+            v[j] = valid ? (pass == p0 ? (uint32_t)i : ld_cg(vin + i)) : 0u;
         }
 #pragma unroll
         for (int j = 0; j < ITEMS; ++j) {
@@ -458,9 +469,11 @@ __global__ void k_gather_diverge(const uint64_t *__restrict__ keys, const uint32
 // Runs of equal high words after the radix passes are in index order; each is
 // sorted by (key, index). The thread at a run's head sorts a run of up to
 // kGroupMax keys in place (insertion sort, stable, so equal keys keep their
-// index order); longer runs are listed for k_sort_big. A run's writes permute
+// index order); for a longer run it finds the run's end (galloping over the
+// high words, which ascend) and lists (start, length) for the warp and block
+// kernels, adding its length to the long-run key count. A run's writes permute
 // keys that share one high word, so the neighbours' run tests are unaffected.
-__global__ void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int *big, int cap_big, DevCounters *ctr)
+__global__ void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int2 *big, int cap_big, DevCounters *ctr)
 {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const uint32_t hi = (uint32_t)(keys[i] >> 32);
@@ -469,9 +482,22 @@ __global__ void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int *big, in
         int len = 2;
         while (len <= kGroupMax && i + len < n && (uint32_t)(keys[i + len] >> 32) == hi) ++len;
         if (len > kGroupMax) {
+            int a = i + kGroupMax, span = kGroupMax;  // keys[a] is in the run
+            while (a + span < n && (uint32_t)(keys[a + span] >> 32) == hi) {
+                a += span;
+                span *= 2;
+            }
+            int b = min(n, a + span);  // the run ends in (a, b]
+            while (b - a > 1) {
+                const int m = a + (b - a) / 2;
+                if ((uint32_t)(keys[m] >> 32) == hi) a = m;
+                else b = m;
+            }
+            len = b - i;
             const int slot = atomicAdd(&ctr->n_sort_groups, 1);
-            if (slot < cap_big) big[slot] = i;
+            if (slot < cap_big) big[slot] = make_int2(i, len);
             else set_error(ctr, ERR_BOUNDS);
+            atomicAdd(&ctr->sort_long_keys, len);
             continue;
         }
         uint64_t k[kGroupMax];
@@ -499,6 +525,100 @@ __global__ void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int *big, in
     }
 }
 
+// Warp-wide ascending bitonic sort of 32 NR unsigned 64-bit values in the
+// blocked layout (value e = NR lane + j in v[j]): the network of the lists'
+// warp sort, on the composites (low key word << 32 | index) of one run.
+template <int NR>
+__device__ __forceinline__ void warp_sort_u64(uint64_t (&v)[NR])
+{
+    constexpr int N = 32 * NR;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= N; k <<= 1) {
+        if (k <= NR) {
+#pragma unroll
+            for (int j = 0; j < NR; ++j) {
+                const int pj = j ^ (k - 1);
+                if ((j & (k >> 1)) == 0) {
+                    const uint64_t a = v[j], b = v[pj];
+                    v[j] = a < b ? a : b;
+                    v[pj] = a < b ? b : a;
+                }
+            }
+        } else {
+            const int m = k / NR - 1;
+            const bool lower = (lane & ((k >> 1) / NR)) == 0;
+#pragma unroll
+            for (int j = 0; j < NR / 2; ++j) {
+                const uint64_t oa = __shfl_xor_sync(kFull, v[NR - 1 - j], m);
+                const uint64_t ob = __shfl_xor_sync(kFull, v[j], m);
+                const uint64_t a = v[j], b = v[NR - 1 - j];
+                v[j] = lower ? (a < oa ? a : oa) : (a < oa ? oa : a);
+                v[NR - 1 - j] = lower ? (b < ob ? b : ob) : (b < ob ? ob : b);
+            }
+        }
+#pragma unroll
+        for (int d = k >> 2; d >= 1; d >>= 1) {
+            if (d < NR) {
+#pragma unroll
+                for (int j = 0; j < NR; ++j) {
+                    if ((j & d) == 0) {
+                        const uint64_t a = v[j], b = v[j | d];
+                        v[j] = a < b ? a : b;
+                        v[j | d] = a < b ? b : a;
+                    }
+                }
+            } else {
+                const int m = d / NR;
+                const bool lower = (lane & m) == 0;
+#pragma unroll
+                for (int j = 0; j < NR; ++j) {
+                    const uint64_t o = __shfl_xor_sync(kFull, v[j], m);
+                    v[j] = lower ? (v[j] < o ? v[j] : o) : (v[j] < o ? o : v[j]);
+                }
+            }
+        }
+    }
+}
+
+template <int NR>
+__device__ __forceinline__ void sort_run_warp(uint64_t *keys, uint32_t *idx, int s, int len)
+{
+    const int lane = threadIdx.x & 31;
+    const uint64_t hw = keys[s] & 0xffffffff00000000ull;
+    uint64_t c[NR];
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        const int e = lane * NR + j;
+        c[j] = e < len ? ((keys[s + e] & 0xffffffffull) << 32) | (uint64_t)idx[s + e] : ~0ull;
+    }
+    warp_sort_u64<NR>(c);
+#pragma unroll
+    for (int j = 0; j < NR; ++j) {
+        const int e = lane * NR + j;
+        if (e < len) {
+            keys[s + e] = hw | (c[j] >> 32);
+            idx[s + e] = (uint32_t)c[j];
+        }
+    }
+}
+
+// The listed runs of kGroupMax + 1 .. kWarpRun keys, a warp each: the
+// composites (low key word, index) sorted in registers.
+__global__ __launch_bounds__(256) void k_sort_runs_warp(uint64_t *keys, uint32_t *idx, const int2 *__restrict__ big,
+                                                        int cap_big, const DevCounters *cst)
+{
+    const int nb = min(cst->n_sort_groups, cap_big);
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nb; b += nwarps) {
+        const int2 r = big[b];
+        if (r.y <= 64) sort_run_warp<2>(keys, idx, r.x, r.y);
+        else if (r.y <= 128) sort_run_warp<4>(keys, idx, r.x, r.y);
+        else if (r.y <= 256) sort_run_warp<8>(keys, idx, r.x, r.y);
+        else if (r.y <= kWarpRun) sort_run_warp<16>(keys, idx, r.x, r.y);
+    }
+}
+
 // The listed long runs, a block each: up to kBigSmem keys sorted in shared
 // memory by (low word, index) with the bitonic network of cmpswap_u64 below;
 // longer runs by four stable passes of 8 bits over the low word, between the
@@ -513,31 +633,20 @@ __device__ __forceinline__ void cmpswap_u64(uint64_t *v, int i, int j)
     }
 }
 
-__global__ __launch_bounds__(256) void k_sort_big(uint64_t *k0, uint32_t *v0, uint64_t *k1, uint32_t *v1, int n,
-                                                  const int *__restrict__ big, int cap_big, const DevCounters *cst,
-                                                  DevCounters *ctr)
+__global__ __launch_bounds__(256) void k_sort_big(uint64_t *k0, uint32_t *v0, uint64_t *k1, uint32_t *v1,
+                                                  const int2 *__restrict__ big, int cap_big, const DevCounters *cst)
 {
     __shared__ uint64_t s_c[kBigSmem];
     __shared__ unsigned s_wcnt[8][256];
     __shared__ unsigned s_base[256];
     __shared__ unsigned s_wsum[8];
-    __shared__ int s_end;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nb = min(cst->n_sort_groups, cap_big);
     for (int b = blockIdx.x; b < nb; b += gridDim.x) {
-        const int s = big[b];
+        const int2 r = big[b];
+        if (r.y <= kWarpRun) continue;  // block-uniform: the warp kernel's runs
+        const int s = r.x, G = r.y, e = s + G;
         const uint32_t hw = (uint32_t)(k0[s] >> 32);
-        if (tid == 0) {  // the run's end: the keys are ordered by high word
-            int lo = s, hi = n;
-            while (lo < hi) {
-                const int mid = lo + (hi - lo) / 2;
-                if ((uint32_t)(k0[mid] >> 32) <= hw) lo = mid + 1;
-                else hi = mid;
-            }
-            s_end = lo;
-        }
-        __syncthreads();
-        const int e = s_end, G = e - s;
         if (G <= kBigSmem) {
             int S = 2;
             while (S < G) S <<= 1;
@@ -614,7 +723,6 @@ __global__ __launch_bounds__(256) void k_sort_big(uint64_t *k0, uint32_t *v0, ui
             }
         }
     }
-    (void)ctr;
 }
 
 template <class T>
@@ -622,30 +730,31 @@ int launch_keys_t(Plan &P, const void *pos, cudaStream_t s)
 {
     const int nb = P.num_sms * 4;
     k_bbox<T><<<nb, kBoxThreads, 0, s>>>((const T *)pos, (int)P.n, (T *)P.scratch, P.ctr);
-    k_keys<T><<<P.num_sms * 8, 256, 0, s>>>((const T *)pos, (int)P.n, P.keys[0], P.ctr);
+    k_keys<T><<<P.num_sms * 8, 256, 0, s>>>((const T *)pos, (int)P.n, P.keys[0], P.sort_full ? 0 : kSortHighPass0,
+                                            P.ctr);
     return 2;
 }
 
 template <int ITEMS>
-int radix_passes(Plan &P, cudaStream_t s)
+int radix_passes(Plan &P, int p0, cudaStream_t s)
 {
     const int n = (int)P.n;
     const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
     const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
     cudaFuncSetAttribute(k_radix_pass<true, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaFuncSetAttribute(k_radix_pass<false, ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    for (int pass = kSortPass0; pass < 8; ++pass) {
+    for (int pass = p0; pass < 8; ++pass) {
         const int src = pass & 1, dst = src ^ 1;
         const int slot = P.next_slot();
         const unsigned ep = P.next_epoch();
-        if (pass == kSortPass0)
+        if (pass == p0)
             k_radix_pass<true, ITEMS><<<tiles, RS_THREADS, smem, s>>>(P.keys[src], nullptr, P.keys[dst], P.idx[dst], n,
                                                                       pass, P.flags, ep, slot, P.ctr);
         else
             k_radix_pass<false, ITEMS><<<tiles, RS_THREADS, smem, s>>>(P.keys[src], P.idx[src], P.keys[dst], P.idx[dst],
                                                                        n, pass, P.flags, ep, slot, P.ctr);
     }
-    return 8 - kSortPass0;
+    return 8 - p0;
 }
 
 template <int ITEMS>
@@ -660,17 +769,17 @@ int coop_tiles_max(int num_sms)
 
 // The cooperative sort when every tile fits on the GPU at once; false otherwise.
 template <int ITEMS>
-bool radix_coop(Plan &P, cudaStream_t s)
+bool radix_coop(Plan &P, int p0, cudaStream_t s)
 {
     const int n = (int)P.n;
     const int tiles = (n + RS_THREADS * ITEMS - 1) / (RS_THREADS * ITEMS);
     // below 16 tiles the per-pass kernels win (their look-backs are short and the launches cost less than
-    // the cooperative kernel's 11 grid barriers); above the co-resident tiles they are the only choice
+    // the cooperative kernel's grid barriers); above the co-resident tiles they are the only choice
     if (tiles < 16 || tiles > P.coop_tiles_sort[ITEMS == RS_ITEMS_LARGE ? 1 : 0] || (size_t)tiles * 256 > P.sort_cnt_cap)
         return false;
     const int smem = RS_THREADS * ITEMS * (int)(sizeof(uint64_t) + sizeof(uint32_t));
     GridBarrier *gb = P.gbar + 2;
-    void *args[] = {&P.keys[0], &P.idx[0], &P.keys[1], &P.idx[1], (void *)&n, &P.sort_cnt, &gb, &P.ctr};
+    void *args[] = {&P.keys[0], &P.idx[0], &P.keys[1], &P.idx[1], (void *)&n, &p0, &P.sort_cnt, &gb, &P.ctr};
     if (cudaLaunchCooperativeKernel((const void *)k_radix_coop<ITEMS>, dim3(tiles), dim3(RS_THREADS), args, smem, s) !=
         cudaSuccess) {
         cudaGetLastError();  // a refused launch (not expected: the tiles were counted against the capacity)
@@ -683,23 +792,26 @@ template <class T>
 int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
 {
     const int n = (int)P.n;
+    const int p0 = P.sort_full ? 0 : kSortHighPass0;  // an even number of passes: the data ends in buffer 0
     int launches;
-    if (P.n >= (1 << 19) ? radix_coop<RS_ITEMS_LARGE>(P, s) : radix_coop<RS_ITEMS_SMALL>(P, s))
+    if (P.n >= (1 << 19) ? radix_coop<RS_ITEMS_LARGE>(P, p0, s) : radix_coop<RS_ITEMS_SMALL>(P, p0, s))
         launches = 1;
     else
-        launches = P.n >= (1 << 19) ? radix_passes<RS_ITEMS_LARGE>(P, s) : radix_passes<RS_ITEMS_SMALL>(P, s);
-    // an even number of passes: the data is back in buffer 0, ordered by high word; then the runs of equal
-    // high words by low word and index
-    const int cap_big = (int)P.sort_big_cap;
-    k_sort_groups<<<P.num_sms * 8, 256, 0, s>>>(P.keys[0], P.idx[0], n, P.sort_big, cap_big, P.ctr);
-    k_sort_big<<<P.num_sms, 256, 0, s>>>(P.keys[0], P.idx[0], P.keys[1], P.idx[1], n, P.sort_big, cap_big, P.ctr,
-                                         P.ctr);
+        launches = P.n >= (1 << 19) ? radix_passes<RS_ITEMS_LARGE>(P, p0, s) : radix_passes<RS_ITEMS_SMALL>(P, p0, s);
+    if (!P.sort_full) {
+        // ordered by high word; then the runs of equal high words by low word and index
+        const int cap_big = (int)P.sort_big_cap;
+        k_sort_groups<<<P.num_sms * 8, 256, 0, s>>>(P.keys[0], P.idx[0], n, P.sort_big, cap_big, P.ctr);
+        k_sort_runs_warp<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], P.sort_big, cap_big, P.ctr);
+        k_sort_big<<<P.num_sms, 256, 0, s>>>(P.keys[0], P.idx[0], P.keys[1], P.idx[1], P.sort_big, cap_big, P.ctr);
+        launches += 3;
+    }
     if (P.mass_wait) cudaStreamWaitEvent(s, P.mass_wait, 0);  // masses still arriving on a side stream
     k_gather_diverge<T><<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], n, (const T *)pos, (const T *)mass,
                                                      (vec4<T> *)P.xyzm, P.div, P.node_first, P.node_count,
                                                      P.node_child0, P.node_nchild, P.node_parent, P.node_level,
                                                      P.ctr);
-    return launches + 3;
+    return launches + 1;
 }
 
 }  // namespace

@@ -83,8 +83,10 @@ struct Plan {
     GridBarrier *gbar = nullptr;     // device: barriers of the cooperative tree [0], walk [1] and sort [2]
     unsigned *sort_cnt = nullptr;    // device: per tile and digit, the cooperative sort's counts and offsets
     size_t sort_cnt_cap = 0;         // its entries
-    int *sort_big = nullptr;         // device: starts of the runs of equal high key words longer than one thread sorts
+    int2 *sort_big = nullptr;        // device: (start, length) of the runs of equal high key words longer than one
+                                     // thread sorts
     size_t sort_big_cap = 0;         // its entries (such runs hold over 32 keys each)
+    bool sort_full = false;          // sort all 8 key digits: the last evaluation found many keys in long runs
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
