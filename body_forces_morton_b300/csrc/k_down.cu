@@ -507,10 +507,52 @@ __global__ __launch_bounds__(256) void k_l2l_flags(DevCounters *ctr, const int *
     }
 }
 
+// fp32 plans, p <= 4: every node's complete local at once, its own M2L local
+// plus each ancestor's M2L local translated straight to the node's centre
+// (nearest ancestor first). A degree-p local shifts exactly, so this is the
+// level-by-level translation through the intermediate centres up to rounding,
+// and no node waits for another: a thread per node walks its parent chain.
+template <class T, int P>
+__global__ __launch_bounds__(256) void k_l2l_direct(const DevCounters *__restrict__ ctr,
+                                                    const int *__restrict__ parent, const vec4<T> *__restrict__ nc,
+                                                    const T *__restrict__ Lm2l, T *__restrict__ L, int ncp)
+{
+    constexpr int NC = Exp<P>::NC;
+    const int n = phase2_nodes(ctr);
+    for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n; a += gridDim.x * blockDim.x) {
+        T out[NC];
+        const T *own = Lm2l + (size_t)a * ncp;
+#pragma unroll
+        for (int k = 0; k < NC; ++k) out[k] = own[k];
+        const vec4<T> c = nc[a];
+        int b = parent[a];
+        for (int up = 0; b >= 0 && up <= kMaxLevel; ++up) {
+            T lb[NC];
+            const T *src = Lm2l + (size_t)b * ncp;
+#pragma unroll
+            for (int k = 0; k < NC; ++k) lb[k] = src[k];
+            const vec4<T> cb = nc[b];
+            Exp<P>::template l2l<T>(lb, c.x - cb.x, c.y - cb.y, c.z - cb.z, out);
+            b = parent[b];
+        }
+        T *dst = L + (size_t)a * ncp;
+#pragma unroll
+        for (int k = 0; k < NC; ++k) dst[k] = out[k];
+    }
+}
+
 template <class T, int P>
 int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 {
     (void)depth;  // read on the device
+    if constexpr (sizeof(T) == 4 && P <= 4) {
+        // (under the injected spin fault the level-ordered kernel below runs, whose waits it exercises)
+        if (!P_.fault_spin) {
+            k_l2l_direct<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, P_.node_parent, (const vec4<T> *)P_.node_c,
+                                                              (const T *)P_.Lm2l, (T *)P_.L, P_.ncp);
+            return 1;
+        }
+    }
     const unsigned seq = P_.next_flag_seq(s);
     // a parent is complete when its flag holds seq; the injected fault waits for a value no pass stores
     // (pass numbers stay below 2^31)

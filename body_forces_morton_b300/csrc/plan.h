@@ -35,7 +35,8 @@ struct Plan {
     // capacities
     int64_t cap_nodes = 0, cap_frontier = 0, cap_m2l = 0, cap_p2p = 0, cap_flags = 0;
     bool minimal_caps = false;     // BFM_FMM_FAULT=capacity: buffers start at their minimum
-    bool fault_spin = false;       // BFM_FMM_FAULT=spin: L2L waits for a flag value that no pass stores
+    bool fault_spin = false;       // BFM_FMM_FAULT=spin: the level-ordered L2L kernel (also in fp32 plans)
+                                   // waits for a flag value that no pass stores
 
     // particle buffers
     uint64_t *keys[2] = {nullptr, nullptr};
