@@ -249,7 +249,7 @@ void destroy_plan(Plan &P)
     free_nodes(P);
     free_lists(P);
     dfree(P.keys[0]); dfree(P.keys[1]); dfree(P.idx[0]); dfree(P.idx[1]);
-    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.vwin); dfree(P.tree_cc); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar); dfree(P.sort_cnt); dfree(P.sort_big);
+    dfree(P.xyzm); dfree(P.far); dfree(P.div); dfree(P.vwin); dfree(P.leaf_of); dfree(P.tree_cc); dfree(P.rel); dfree(P.scratch); dfree(P.ctr); dfree(P.gbar); dfree(P.sort_cnt); dfree(P.sort_big);
     dfree(P.h_pos); dfree(P.h_mass); dfree(P.h_acc); dfree(P.h_pot); dfree(P.acc_cache);
     dfree(P.vjp_acc); dfree(P.vjp_src); dfree(P.Ms); dfree(P.Lsm); dfree(P.Ls);
     free_mutual(P);
@@ -507,7 +507,7 @@ fmm_plan *fmm_plan_create(int64_t n, int p, double theta, int leaf, fmm_dtype dt
     if (!ok(dalloc(P.keys[0], nn), "keys") || !ok(dalloc(P.keys[1], nn), "keys") ||
         !ok(dalloc(P.idx[0], nn), "perm") || !ok(dalloc(P.idx[1], nn), "perm") ||
         !ok(cudaMalloc(&P.xyzm, 4 * nn * e), "particles") || !ok(cudaMalloc(&P.far, 4 * nn * e), "far field") || !ok(dalloc(P.div, nn), "divergence") ||
-        !ok(dalloc(P.vwin, nn), "tree windows") || !ok(dalloc(P.tree_cc, tree_cc_ints(n)), "tree counts") ||
+        !ok(dalloc(P.vwin, nn), "tree windows") || !ok(dalloc(P.leaf_of, nn), "particle leaves") || !ok(dalloc(P.tree_cc, tree_cc_ints(n)), "tree counts") ||
         (P.dtype == 1 && !ok(cudaMalloc(&P.rel, 2 * nn * sizeof(float4)), "leaf-relative particles")) ||
         !ok(cudaMalloc(&P.scratch, 65536), "scratch") || !ok(dalloc(P.ctr, 1), "counters") ||
         !ok(dalloc(P.gbar, 3), "grid barriers") ||

@@ -515,7 +515,9 @@ __global__ __launch_bounds__(256) void k_l2l_flags(DevCounters *ctr, const int *
 template <class T, int P>
 __global__ __launch_bounds__(256) void k_l2l_direct(const DevCounters *__restrict__ ctr,
                                                     const int *__restrict__ parent, const vec4<T> *__restrict__ nc,
-                                                    const T *__restrict__ Lm2l, T *__restrict__ L, int ncp)
+                                                    const T *__restrict__ Lm2l, T *__restrict__ L, int ncp,
+                                                    const int *__restrict__ nchild, const int *__restrict__ first,
+                                                    const int *__restrict__ count, int *__restrict__ leaf_of)
 {
     constexpr int NC = Exp<P>::NC;
     const int n = phase2_nodes(ctr);
@@ -538,6 +540,33 @@ __global__ __launch_bounds__(256) void k_l2l_direct(const DevCounters *__restric
         T *dst = L + (size_t)a * ncp;
 #pragma unroll
         for (int k = 0; k < NC; ++k) dst[k] = out[k];
+        if (nchild[a] == 0) {  // a leaf: its particles' leaf, for the L2P by particle
+            const int f = first[a], c = count[a];
+            for (int i = f; i < f + c; ++i) leaf_of[i] = a;
+        }
+    }
+}
+
+// L2P by particle, after k_l2l_direct: thread i evaluates its leaf's complete
+// local (the same arithmetic as k_l2p, so the same bits) at particle i.
+template <class T, int P>
+__global__ __launch_bounds__(256) void k_l2p_part(const DevCounters *__restrict__ nctr, int n,
+                                                  const int *__restrict__ leaf_of, const vec4<T> *__restrict__ xyzm,
+                                                  const vec4<T> *__restrict__ nc, const T *__restrict__ L, int ncp,
+                                                  vec4<T> *__restrict__ far, DevCounters *ctr)
+{
+    const int n_nodes = phase2_nodes(nctr);
+    if (n_nodes == 0) return;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const int a = leaf_of[i];
+        if (a < 0 || a >= n_nodes) {
+            set_error(ctr, ERR_BOUNDS);
+            continue;
+        }
+        const vec4<T> ca = nc[a], q = xyzm[i];
+        T phi = T(0), ax = T(0), ay = T(0), az = T(0);
+        Exp<P>::template l2p<T>(L + (size_t)a * ncp, q.x - ca.x, q.y - ca.y, q.z - ca.z, phi, ax, ay, az);
+        far[i] = make4<T>(phi, ax, ay, az);
     }
 }
 
@@ -549,7 +578,8 @@ int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
         // (under the injected spin fault the level-ordered kernel below runs, whose waits it exercises)
         if (!P_.fault_spin) {
             k_l2l_direct<T, P><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, P_.node_parent, (const vec4<T> *)P_.node_c,
-                                                              (const T *)P_.Lm2l, (T *)P_.L, P_.ncp);
+                                                              (const T *)P_.Lm2l, (T *)P_.L, P_.ncp, P_.node_nchild,
+                                                              P_.node_first, P_.node_count, P_.leaf_of);
             return 1;
         }
     }
@@ -566,6 +596,14 @@ int launch_l2l_tp(Plan &P_, int depth, cudaStream_t s)
 template <class T, int P>
 int launch_l2p_tp(Plan &P_, cudaStream_t s)
 {
+    if constexpr (sizeof(T) == 4 && P <= 4) {
+        if (!P_.fault_spin) {  // the direct L2L ran and recorded each particle's leaf
+            k_l2p_part<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, (int)P_.n, P_.leaf_of, (const vec4<T> *)P_.xyzm,
+                                                            (const vec4<T> *)P_.node_c, (const T *)P_.L, P_.ncp,
+                                                            (vec4<T> *)P_.far, P_.ctr);
+            return 1;
+        }
+    }
     k_l2p<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.node_first, P_.node_count, P_.node_nchild,
                                                (const vec4<T> *)P_.xyzm, (const vec4<T> *)P_.node_c,
                                                (const T *)P_.L, P_.ncp, (vec4<T> *)P_.far);

@@ -45,6 +45,7 @@ struct Plan {
     void *far = nullptr;           // far field at the sorted particles, vec4<T> (phi, ax, ay, az)
     uint8_t *div = nullptr;        // divergence level of consecutive sorted keys
     uint8_t *vwin = nullptr;       // per sorted position: the deepest level whose run around it holds > leaf keys
+    int *leaf_of = nullptr;        // per sorted particle: its leaf (written by the direct L2L)
     int *tree_cc = nullptr;        // per level and chunk of positions: node counts, then their offsets
     void *rel = nullptr;           // fp64 plans: leaf-relative particles as double-float float4 [2][N]
 
