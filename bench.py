@@ -59,19 +59,19 @@ P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r
 # 1e5 fp64, p 4), keyed by the hash of the kernel sources they were counted on;
 # a changed kernel reports null until it is counted again.
 DF_FMA_OPS_PER_PAIR = {
-    # k_p2p_df: 9,097,920,864 FMA-pipe thread instructions (all scalar) over the 48,723,340 pairs the
+    # k_p2p_df: 9,097,988,608 FMA-pipe thread instructions (all scalar) over the 48,723,340 pairs the
     # roofline counts (the interactions less the 1e5 zero-separation self pairs)
-    ("k_p2p_df", "4905586f2eef129a"): 186.73,
-    # k_m2l_df<4>: 6,075,552,672 over 1,833,964 pairs (the moments' conversion kernel is not counted)
-    ("k_m2l_df", "24ba5cc236d86c00"): 3312.8,
+    ("k_p2p_df", "a71b96b0dadb26fe"): 186.73,
+    # k_m2l_df<4>: 6,072,086,944 over 1,833,964 pairs (the moments' conversion kernel is not counted)
+    ("k_m2l_df", "159774f6b7e517df"): 3310.9,
 }
 
 # DRAM traffic of the P2P kernel per launch (dram__bytes_read.sum +
 # dram__bytes_write.sum, one warm launch of clustered N = 2^20 fp32), keyed by
 # the hash of the kernel sources it was taken on; null once they change.
 TRAFFIC = {
-    # k_p2p<float>: 52,613,632 B read + 3,910,912 B written
-    ("clustered_2p20_f32", "79e69f34e661b67d"): 56524544,
+    # k_p2p<float>: 52,625,152 B read + 4,587,520 B written
+    ("clustered_2p20_f32", "7a6f7f106e0b3105"): 57212672,
 }
 
 
