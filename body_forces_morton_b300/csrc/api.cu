@@ -336,9 +336,6 @@ fmm_status eval_device(Plan &P, const void *pos, const void *mass, void *acc, vo
         // ---- phase 2, launched without waiting: every kernel reads the node count (and the walk
         // and L2L their extent) on the device, and skips the tree if its build failed
         record(P, 4, s);
-        CUDA_TRY(cudaMemsetAsync(P.m2l_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
-        CUDA_TRY(cudaMemsetAsync(P.p2p_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s));
-        CUDA_TRY(cudaMemsetAsync(P.p2p_done, 0, (size_t)P.cap_nodes * sizeof(int), s));
         P.launches += launch_upward(P, s);
         record(P, 5, s);
         P.launches += launch_walk(P, 0, s);

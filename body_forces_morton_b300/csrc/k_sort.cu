@@ -9,7 +9,7 @@
 //
 // Radix sort of (key, index) pairs: 4 passes of 8 bits over the high word
 // (bits 32..63), then each run of keys with equal high words sorted by its low
-// word and index (k_sort_groups, k_sort_runs_warp, k_sort_big): the same order
+// word and index (k_sort_groups, k_sort_runs): the same order
 // as sorting the whole key, since the passes are stable. At 2^20 clustered
 // keys the runs number about 9e4 and hold at most a dozen keys; strongly
 // clustered states (collapsed halo cores) put a large share of the keys into
@@ -471,7 +471,7 @@ __global__ void k_gather_diverge(const uint64_t *__restrict__ keys, const uint32
 // kGroupMax keys in place (insertion sort, stable, so equal keys keep their
 // index order); for a longer run it finds the run's end (galloping over the
 // high words, which ascend) and lists (start, length) for the warp and block
-// kernels, adding its length to the long-run key count. A run's writes permute
+// kernel, adding its length to the long-run key count. A run's writes permute
 // keys that share one high word, so the neighbours' run tests are unaffected.
 __global__ void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int2 *big, int cap_big, DevCounters *ctr)
 {
@@ -603,27 +603,14 @@ __device__ __forceinline__ void sort_run_warp(uint64_t *keys, uint32_t *idx, int
     }
 }
 
-// The listed runs of kGroupMax + 1 .. kWarpRun keys, a warp each: the
-// composites (low key word, index) sorted in registers.
-__global__ __launch_bounds__(256) void k_sort_runs_warp(uint64_t *keys, uint32_t *idx, const int2 *__restrict__ big,
-                                                        int cap_big, const DevCounters *cst)
-{
-    const int nb = min(cst->n_sort_groups, cap_big);
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nb; b += nwarps) {
-        const int2 r = big[b];
-        if (r.y <= 64) sort_run_warp<2>(keys, idx, r.x, r.y);
-        else if (r.y <= 128) sort_run_warp<4>(keys, idx, r.x, r.y);
-        else if (r.y <= 256) sort_run_warp<8>(keys, idx, r.x, r.y);
-        else if (r.y <= kWarpRun) sort_run_warp<16>(keys, idx, r.x, r.y);
-    }
-}
-
-// The listed long runs, a block each: up to kBigSmem keys sorted in shared
-// memory by (low word, index) with the bitonic network of cmpswap_u64 below;
-// longer runs by four stable passes of 8 bits over the low word, between the
-// run's place in buffers 0 and 1 (tiles of 256 keys in order; within a tile,
-// warp match_any ranks and per-warp digit counts keep the order).
+// The listed runs: first those over kWarpRun keys, a block each (up to
+// kBigSmem keys sorted in shared memory by (low word, index) with the bitonic
+// network of cmpswap_u64 below; longer runs by four stable passes of 8 bits
+// over the low word, between the run's place in buffers 0 and 1: tiles of 256
+// keys in order, within a tile warp match_any ranks and per-warp digit counts
+// keep the order); then the others, a warp each, the composites sorted in
+// registers. The two groups of runs are disjoint, so the phases need no barrier
+// between them.
 __device__ __forceinline__ void cmpswap_u64(uint64_t *v, int i, int j)
 {
     const uint64_t a = v[i], b = v[j];
@@ -633,8 +620,8 @@ __device__ __forceinline__ void cmpswap_u64(uint64_t *v, int i, int j)
     }
 }
 
-__global__ __launch_bounds__(256) void k_sort_big(uint64_t *k0, uint32_t *v0, uint64_t *k1, uint32_t *v1,
-                                                  const int2 *__restrict__ big, int cap_big, const DevCounters *cst)
+__global__ __launch_bounds__(256) void k_sort_runs(uint64_t *k0, uint32_t *v0, uint64_t *k1, uint32_t *v1,
+                                                   const int2 *__restrict__ big, int cap_big, const DevCounters *cst)
 {
     __shared__ uint64_t s_c[kBigSmem];
     __shared__ unsigned s_wcnt[8][256];
@@ -723,6 +710,14 @@ __global__ __launch_bounds__(256) void k_sort_big(uint64_t *k0, uint32_t *v0, ui
             }
         }
     }
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; b < nb; b += nwarps) {
+        const int2 r = big[b];
+        if (r.y <= 64) sort_run_warp<2>(k0, v0, r.x, r.y);
+        else if (r.y <= 128) sort_run_warp<4>(k0, v0, r.x, r.y);
+        else if (r.y <= 256) sort_run_warp<8>(k0, v0, r.x, r.y);
+        else if (r.y <= kWarpRun) sort_run_warp<16>(k0, v0, r.x, r.y);
+    }
 }
 
 template <class T>
@@ -802,9 +797,9 @@ int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
         // ordered by high word; then the runs of equal high words by low word and index
         const int cap_big = (int)P.sort_big_cap;
         k_sort_groups<<<P.num_sms * 8, 256, 0, s>>>(P.keys[0], P.idx[0], n, P.sort_big, cap_big, P.ctr);
-        k_sort_runs_warp<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], P.sort_big, cap_big, P.ctr);
-        k_sort_big<<<P.num_sms, 256, 0, s>>>(P.keys[0], P.idx[0], P.keys[1], P.idx[1], P.sort_big, cap_big, P.ctr);
-        launches += 3;
+        k_sort_runs<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], P.keys[1], P.idx[1], P.sort_big, cap_big,
+                                                  P.ctr);
+        launches += 2;
     }
     if (P.mass_wait) cudaStreamWaitEvent(s, P.mass_wait, 0);  // masses still arriving on a side stream
     k_gather_diverge<T><<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], n, (const T *)pos, (const T *)mass,

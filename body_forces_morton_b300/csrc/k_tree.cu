@@ -181,11 +181,12 @@ __device__ __forceinline__ uint8_t *slide(uint8_t *a, uint8_t *b, int len, int w
 
 // Per block, TB_TILE positions: V(k) for its positions (stored), and per warp
 // chunk and level the number of nodes starting in the chunk. Also clears the
-// count and nchild arrays, which the node kernel assembles by additions.
+// count and nchild arrays, which the node kernel assembles by additions, and
+// the later stages' per-node counters (list lengths, chunk turns).
 __global__ __launch_bounds__(TB_THREADS) void k_tree_windows(const uint8_t *__restrict__ div, int n, int leaf,
                                                              int cap_nodes, int *count, int *nchild,
                                                              uint8_t *__restrict__ vwin, int *__restrict__ cc,
-                                                             int nchunks)
+                                                             int nchunks, int *m2l_cnt, int *p2p_cnt, int *p2p_done)
 {
     extern __shared__ __align__(16) uint8_t tw_smem[];
     const int span = TB_TILE + 2 * leaf;  // div[t0 - leaf .. t0 + TB_TILE + leaf)
@@ -194,6 +195,9 @@ __global__ __launch_bounds__(TB_THREADS) void k_tree_windows(const uint8_t *__re
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < cap_nodes; i += gridDim.x * blockDim.x) {
         count[i] = 0;
         nchild[i] = 0;
+        m2l_cnt[i] = 0;  // the walk's per-receiver list lengths and the P2P chunk turns, for this evaluation
+        p2p_cnt[i] = 0;
+        p2p_done[i] = 0;
     }
     for (int i = threadIdx.x; i < span; i += blockDim.x) {
         const long long g = (long long)t0 - leaf + i;
@@ -372,7 +376,8 @@ int launch_tree(Plan &P, cudaStream_t s)
         const int ntiles = (n + TB_TILE - 1) / TB_TILE, nchunks = (n + TB_CHUNK - 1) / TB_CHUNK;
         k_tree_windows<<<ntiles, TB_THREADS, 3 * (TB_TILE + 2 * leaf), s>>>(P.div, n, leaf, cap, P.node_count,
                                                                             P.node_nchild, P.vwin, P.tree_cc,
-                                                                            nchunks);
+                                                                            nchunks, P.m2l_cnt, P.p2p_cnt,
+                                                                            P.p2p_done);
         k_tree_scan<<<TB_LV, 1024, 0, s>>>(P.tree_cc, nchunks);
         k_tree_nodes<<<ntiles, TB_THREADS, 0, s>>>(P.div, P.vwin, P.tree_cc, nchunks, n, cap, P.node_first,
                                                    P.node_count, P.node_child0, P.node_nchild, P.node_parent,
@@ -389,6 +394,10 @@ int launch_tree(Plan &P, cudaStream_t s)
     void *args[] = {&leaf, &cap, &keys, &P.node_first, &P.node_count, &P.node_child0, &P.node_nchild,
                     &P.node_parent, &P.node_level, &P.flags, (void *)&epoch0, (void *)&slot0, &gb, &P.ctr};
     cudaLaunchCooperativeKernel((const void *)k_tree_all, dim3(P.coop_blocks_tree), dim3(TR_THREADS), args, 0, s);
+    // the later stages' per-node counters (the window build clears them itself)
+    cudaMemsetAsync(P.m2l_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s);
+    cudaMemsetAsync(P.p2p_cnt, 0, (size_t)P.cap_nodes * sizeof(int), s);
+    cudaMemsetAsync(P.p2p_done, 0, (size_t)P.cap_nodes * sizeof(int), s);
     return 1;
 }
 
