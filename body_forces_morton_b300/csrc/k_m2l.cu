@@ -29,6 +29,8 @@
 // sums the lanes, so the result is reproducible.
 #include "expansions_gen.cuh"
 #include "plan.h"
+
+#include <type_traits>
 #include "rotation_gen.cuh"
 
 namespace bfm {
@@ -375,7 +377,8 @@ int launch_m2l_mutual_tp(Plan &P_, cudaStream_t s)
 {
     const int launches = launch_mutual_index(P_, s);
     const long long rows = P_.mut_cap_em;
-    k_moments_r<T, P, OpReduced<P>><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)P_.M, (T *)P_.Mr);
+    const bool fresh = P_.mr_fresh;
+    if (!fresh) k_moments_r<T, P, OpReduced<P>><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)P_.M, (T *)P_.Mr);
     using MS = MutShape<T, P>;
     static_assert(MS::smem <= 227 * 1024, "mutual M2L staging exceeds shared memory");
     cudaFuncSetAttribute(k_m2l_mut1<T, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MS::smem);
@@ -384,7 +387,7 @@ int launch_m2l_mutual_tp(Plan &P_, cudaStream_t s)
         (const vec4<T> *)P_.node_c, (const T *)P_.Mr, (T *)P_.mut_rm2l, rows, (T *)P_.mut_lpart, P_.ctr);
     k_m2l_mut2<T, P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.m2l_off, P_.mut_lo, (const T *)P_.mut_rm2l, rows,
                                                     (const T *)P_.mut_lpart, (T *)P_.Lm2l, P_.ctr);
-    return launches + 3;
+    return launches + (fresh ? 2 : 3);
 }
 
 template <class T>
@@ -409,12 +412,14 @@ int launch_m2l_op(Plan &P_, const void *M, void *Lout, cudaStream_t s)
     using S = M2LShape<T, P>;
     static_assert(S::NRP % S::V == 0, "row stride must be a whole number of 16-byte loads");
     static_assert(S::smem <= 227 * 1024, "M2L staging exceeds shared memory");
-    k_moments_r<T, P, Op><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)M, (T *)P_.Mr);
+    // the forward moments' reduced rows come from the upward pass when it wrote them
+    const bool fresh = std::is_same_v<Op, OpReduced<P>> && M == P_.M && P_.mr_fresh;
+    if (!fresh) k_moments_r<T, P, Op><<<P_.num_sms * 4, 256, 0, s>>>(P_.ctr, (const T *)M, (T *)P_.Mr);
     cudaFuncSetAttribute(k_m2l<T, P, Op>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::smem);
     k_m2l<T, P, Op><<<P_.num_sms * 16, M2L_WARPS * 32, S::smem, s>>>(
         P_.ctr, P_.order + P_.cap_nodes, P_.m2l_off, P_.m2l_src, (const vec4<T> *)P_.node_c,
         (const T *)P_.Mr, (T *)Lout, P_.ctr);
-    return 2;
+    return fresh ? 1 : 2;
 }
 
 template <class T, int P>

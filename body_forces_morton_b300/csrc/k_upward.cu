@@ -63,7 +63,7 @@ __global__ __launch_bounds__(256) void k_upward_flags(DevCounters *ctr, const ve
                                                       const int *__restrict__ first, const int *__restrict__ count,
                                                       const int *__restrict__ child0, const int *__restrict__ nchild,
                                                       T *node_lo, T *node_hi, vec4<T> *nc, vec4<T> *nl, T *M, int ncp,
-                                                      unsigned *flag, unsigned seq)
+                                                      unsigned *flag, unsigned seq, T *Mr)
 {
     constexpr int NC = Exp<P>::NC;
     constexpr int NR = Padded<NC>::value;
@@ -148,8 +148,20 @@ __global__ __launch_bounds__(256) void k_upward_flags(DevCounters *ctr, const ve
         // publish the group's box and moments, then the node's flag
         __threadfence();
         __syncwarp();
-        if (valid && j == 0)
+        if (valid && j == 0) {
             cuda::atomic_ref<unsigned, cuda::thread_scope_device>(flag[a]).store(seq, cuda::memory_order_release);
+            if (Mr != nullptr) {  // the reduced row the M2L reads, off the parents' wait
+                constexpr int NRC = Exp<P>::NRC, NRP = (NRC + 3) / 4 * 4;
+                T mk[NC], r[NRP];
+#pragma unroll
+                for (int k = 0; k < NC; ++k) mk[k] = dst[k];
+#pragma unroll
+                for (int k = NRC; k < NRP; ++k) r[k] = T(0);
+                Exp<P>::template reduce_m<T>(mk, r);
+#pragma unroll
+                for (int k = 0; k < NRP; ++k) Mr[(size_t)a * NRP + k] = r[k];
+            }
+        }
     }
 }
 
@@ -274,13 +286,15 @@ int launch_upward_tp(Plan &P_, cudaStream_t s)
             P_.ctr, (const vec4<T> *)P_.xyzm, P_.node_first, P_.node_count, P_.node_child0, P_.node_nchild,
             P_.node_parent, P_.node_done, (T *)P_.node_lo, (T *)P_.node_hi, (vec4<T> *)P_.node_c,
             (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp, !P_.f64_ieee);
+        P_.mr_fresh = false;
         return 1;
     } else {
         const unsigned seq = P_.next_flag_seq(s);
         k_upward_flags<T, P><<<P_.num_sms * 4, 256, 0, s>>>(
             P_.ctr, (const vec4<T> *)P_.xyzm, P_.node_first, P_.node_count, P_.node_child0, P_.node_nchild,
             (T *)P_.node_lo, (T *)P_.node_hi, (vec4<T> *)P_.node_c, (vec4<T> *)P_.node_l, (T *)P_.M, P_.ncp,
-            P_.node_flag, seq);
+            P_.node_flag, seq, P_.m2l_rotation ? (T *)nullptr : (T *)P_.Mr);
+        P_.mr_fresh = !P_.m2l_rotation;  // the reduced rows of this evaluation's moments are written
         return 1;
     }
 }

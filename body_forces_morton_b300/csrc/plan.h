@@ -89,6 +89,7 @@ struct Plan {
                                      // thread sorts
     size_t sort_big_cap = 0;         // its entries (such runs hold over 32 keys each)
     bool sort_full = false;          // sort all 8 key digits: the last evaluation found many keys in long runs
+    bool mr_fresh = false;           // the upward pass wrote the reduced rows of this evaluation's moments
     DevCounters *ctr_host = nullptr; // pinned mirror
 
     // host-buffer staging (fmm_eval_host), allocated on first use
