@@ -168,14 +168,21 @@ __global__ __launch_bounds__(M2L_WARPS * 32, M2LMinBlocks<T, P, Op>::value) void
         cp_async_commit();
         return cb;
     };
+    // the next receiver's ticket and node are taken while the current one computes
+    auto ticket = [&]() {
+        int tk = 0;
+        if (lane == 0) tk = atomicAdd(&ctr->work_ctr[1], 1);
+        return __shfl_sync(kFull, tk, 0);
+    };
+    int t = ticket();
+    int a_n = t < n_nodes ? order[t] : 0;
     for (;;) {
-        int t = 0;
-        if (lane == 0) t = atomicAdd(&ctr->work_ctr[1], 1);
-        t = __shfl_sync(kFull, t, 0);
         if (t >= n_nodes) break;
-        const int a = order[t];
+        const int a = a_n;
         const int beg = off[a], end = off[a + 1];
         const vec4<T> ca = nc[a];
+        t = ticket();
+        a_n = t < n_nodes ? order[t] : 0;
         T L[S::NR];
 #pragma unroll
         for (int k = 0; k < S::NR; ++k) L[k] = T(0);
