@@ -473,13 +473,67 @@ __global__ void k_gather_diverge(const uint64_t *__restrict__ keys, const uint32
 // high words, which ascend) and lists (start, length) for the warp and block
 // kernel, adding its length to the long-run key count. A run's writes permute
 // keys that share one high word, so the neighbours' run tests are unaffected.
-__global__ void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int2 *big, int cap_big, DevCounters *ctr)
+// One comparator of a sorting network on (key, index) pairs: the lower pair to a.
+__device__ __forceinline__ void ce_key_idx(uint64_t &ka, uint32_t &va, uint64_t &kb, uint32_t &vb)
+{
+    const bool sw = kb < ka || (kb == ka && vb < va);
+    const uint64_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
+    const uint32_t v0 = sw ? vb : va, v1 = sw ? va : vb;
+    ka = k0;
+    kb = k1;
+    va = v0;
+    vb = v1;
+}
+
+__global__ __launch_bounds__(256) void k_sort_groups(uint64_t *keys, uint32_t *idx, int n, int2 *big, int cap_big,
+                                                     DevCounters *ctr)
 {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        const uint32_t hi = (uint32_t)(keys[i] >> 32);
-        if (i > 0 && (uint32_t)(keys[i - 1] >> 32) == hi) continue;       // not the head of a run
-        if (i + 1 >= n || (uint32_t)(keys[i + 1] >> 32) != hi) continue;  // a run of one
-        int len = 2;
+        // the key, its neighbours, and for the head of a run the next six keys and eight indices, each
+        // group loaded at once
+        const uint64_t kc = keys[i];
+        const uint64_t kp = i > 0 ? keys[i - 1] : 0;
+        const uint64_t kn = i + 1 < n ? keys[i + 1] : 0;
+        const uint32_t hi = (uint32_t)(kc >> 32);
+        if (i > 0 && (uint32_t)(kp >> 32) == hi) continue;       // not the head of a run
+        if (i + 1 >= n || (uint32_t)(kn >> 32) != hi) continue;  // a run of one
+        {
+            uint64_t k[8];
+            uint32_t v[8];
+            k[0] = kc;
+            k[1] = kn;
+#pragma unroll
+            for (int j = 2; j < 8; ++j) k[j] = i + j < n ? keys[i + j] : ~0ull;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = i + j < n ? idx[i + j] : ~0u;
+            int len = 2;
+#pragma unroll
+            for (int j = 2; j < 8; ++j) len += (len == j && (uint32_t)(k[j] >> 32) == hi) ? 1 : 0;
+            if (len < 8 || i + 8 >= n || (uint32_t)(keys[i + 8] >> 32) != hi) {
+                // a run of at most 8: Batcher's odd-even merge network in registers, padded with pairs
+                // above every key (keys have 63 bits); the (key, index) order is the stable order by key,
+                // since the passes before left each run in index order
+#pragma unroll
+                for (int j = 2; j < 8; ++j)
+                    if (j >= len) {
+                        k[j] = ~0ull;
+                        v[j] = ~0u;
+                    }
+                constexpr int net[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                                            {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                                            {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+                for (int c = 0; c < 19; ++c) ce_key_idx(k[net[c][0]], v[net[c][0]], k[net[c][1]], v[net[c][1]]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < len) {
+                        keys[i + j] = k[j];
+                        idx[i + j] = v[j];
+                    }
+                continue;
+            }
+        }
+        int len = 9;
         while (len <= kGroupMax && i + len < n && (uint32_t)(keys[i + len] >> 32) == hi) ++len;
         if (len > kGroupMax) {
             int a = i + kGroupMax, span = kGroupMax;  // keys[a] is in the run
@@ -796,7 +850,13 @@ int launch_sort_t(Plan &P, const void *pos, const void *mass, cudaStream_t s)
     if (!P.sort_full) {
         // ordered by high word; then the runs of equal high words by low word and index
         const int cap_big = (int)P.sort_big_cap;
-        k_sort_groups<<<P.num_sms * 8, 256, 0, s>>>(P.keys[0], P.idx[0], n, P.sort_big, cap_big, P.ctr);
+        // one wave of blocks: a partial second wave would wait for the first's latency-bound loads
+        static int groups_per_sm = 0;
+        if (!groups_per_sm) {
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&groups_per_sm, k_sort_groups, 256, 0);
+            groups_per_sm = std::max(groups_per_sm, 1);
+        }
+        k_sort_groups<<<P.num_sms * groups_per_sm, 256, 0, s>>>(P.keys[0], P.idx[0], n, P.sort_big, cap_big, P.ctr);
         k_sort_runs<<<P.num_sms * 4, 256, 0, s>>>(P.keys[0], P.idx[0], P.keys[1], P.idx[1], P.sort_big, cap_big,
                                                   P.ctr);
         launches += 2;
