@@ -72,13 +72,24 @@ __global__ __launch_bounds__(kBoxThreads) void k_bbox(const T *__restrict__ pos,
     T lo[3], hi[3];
     for (int a = 0; a < 3; ++a) { lo[a] = pos_inf<T>(); hi[a] = -pos_inf<T>(); }
     bool bad = false;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-        for (int a = 0; a < 3; ++a) {
-            T v = pos[3 * (int64_t)i + a];
-            bad |= !finite_t(v);
-            lo[a] = tmin(lo[a], v);
-            hi[a] = tmax(hi[a], v);
+    // four positions a stride apart per thread and round, their loads issued together
+    const int stride = gridDim.x * blockDim.x;
+    for (int i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 4 * stride) {
+        T v[4][3];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * stride;
+#pragma unroll
+            for (int a = 0; a < 3; ++a) v[u][a] = i < n ? pos[3 * (int64_t)i + a] : pos[a];
         }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int a = 0; a < 3; ++a) {
+                bad |= !finite_t(v[u][a]);
+                lo[a] = tmin(lo[a], v[u][a]);
+                hi[a] = tmax(hi[a], v[u][a]);
+            }
     }
     if (__any_sync(kFull, bad) && (threadIdx.x & 31) == 0) set_error(ctr, ERR_NONFINITE);
     for (int o = 16; o > 0; o >>= 1)
@@ -150,8 +161,8 @@ template <class T> __device__ __forceinline__ uint32_t quantise(T x, T lo, T sid
 // Keys in the caller's order plus the digit histograms of the radix passes
 // (the digits of the high word).
 template <class T>
-__global__ __launch_bounds__(256) void k_keys(const T *__restrict__ pos, int n, uint64_t *__restrict__ keys,
-                                              int p0, DevCounters *ctr)
+__global__ __launch_bounds__(1024) void k_keys(const T *__restrict__ pos, int n, uint64_t *__restrict__ keys,
+                                               int p0, DevCounters *ctr)
 {
     __shared__ unsigned h[8][256];
     for (int i = threadIdx.x; i < 8 * 256; i += blockDim.x) (&h[0][0])[i] = 0;
@@ -779,8 +790,10 @@ int launch_keys_t(Plan &P, const void *pos, cudaStream_t s)
 {
     const int nb = P.num_sms * 4;
     k_bbox<T><<<nb, kBoxThreads, 0, s>>>((const T *)pos, (int)P.n, (T *)P.scratch, P.ctr);
-    k_keys<T><<<P.num_sms * 8, 256, 0, s>>>((const T *)pos, (int)P.n, P.keys[0], P.sort_full ? 0 : kSortHighPass0,
-                                            P.ctr);
+    // blocks of 1024 threads: each block adds its digit counts to the global histograms once, so fewer,
+    // larger blocks put fewer atomics on the same counters
+    k_keys<T><<<P.num_sms * 2, 1024, 0, s>>>((const T *)pos, (int)P.n, P.keys[0], P.sort_full ? 0 : kSortHighPass0,
+                                             P.ctr);
     return 2;
 }
 
