@@ -152,7 +152,7 @@ __global__ __launch_bounds__(TR_THREADS) void k_tree_all(int leaf, int cap_nodes
 
 // ---- every level at once ----
 constexpr int TB_THREADS = 256;
-constexpr int TB_ROWS = 16;                              // rows of 32 positions per warp
+constexpr int TB_ROWS = 4;                               // rows of 32 positions per warp
 constexpr int TB_CHUNK = 32 * TB_ROWS;                   // positions per warp (one chunk)
 constexpr int TB_TILE = TB_CHUNK * (TB_THREADS / 32);    // positions per block
 constexpr int TB_LEAF_MAX = 4096;                        // shared memory 3 (TB_TILE + 2 leaf) bytes
