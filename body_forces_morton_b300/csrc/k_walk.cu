@@ -313,17 +313,18 @@ __global__ void k_csr_fill(const int2 *__restrict__ m2l_pairs, int capm_s, const
     const int nm = pm[kShards], np = pp[kShards];
     const int lane = threadIdx.x & 31;
     const int stride = gridDim.x * blockDim.x;
-    for (int b = blockIdx.x * blockDim.x + (threadIdx.x & ~31); b < nm + np; b += stride) {
+    // the M2L pairs, then the P2P pairs: a warp's lanes are all in one list, two entries each
+    for (int b = blockIdx.x * blockDim.x + (threadIdx.x & ~31); b < nm; b += stride) {
         const int i = b + lane;
-        int2 pr = make_int2(-1, -1);
-        if (i < nm) pr = m2l_pairs[shard_addr(pm, i, capm_s)];
-        const bool p = i >= nm && i < nm + np;
-        if (p) pr = p2p_pairs[shard_addr(pp, i - nm, capp_s)];
-        // a warp straddling the two lists handles each lane under its own list
-        fill_entry(p ? -1 : pr.x, pr.y, m2l_cnt, m2l_off, m2l_src);
-        fill_entry(p ? -1 : pr.y, pr.x, m2l_cnt, m2l_off, m2l_src);
-        fill_entry(p ? pr.x : -1, pr.y, p2p_cnt, p2p_off, p2p_src);
-        fill_entry(p && pr.x != pr.y ? pr.y : -1, pr.x, p2p_cnt, p2p_off, p2p_src);
+        const int2 pr = i < nm ? m2l_pairs[shard_addr(pm, i, capm_s)] : make_int2(-1, -1);
+        fill_entry(pr.x, pr.y, m2l_cnt, m2l_off, m2l_src);
+        fill_entry(pr.y, pr.x, m2l_cnt, m2l_off, m2l_src);
+    }
+    for (int b = blockIdx.x * blockDim.x + (threadIdx.x & ~31); b < np; b += stride) {
+        const int i = b + lane;
+        const int2 pr = i < np ? p2p_pairs[shard_addr(pp, i, capp_s)] : make_int2(-1, -1);
+        fill_entry(pr.x, pr.y, p2p_cnt, p2p_off, p2p_src);
+        fill_entry(pr.x != pr.y ? pr.y : -1, pr.x, p2p_cnt, p2p_off, p2p_src);
     }
 }
 
