@@ -520,26 +520,42 @@ __global__ __launch_bounds__(256) void k_l2l_direct(const DevCounters *__restric
                                                     const int *__restrict__ count, int *__restrict__ leaf_of)
 {
     constexpr int NC = Exp<P>::NC;
+    static_assert(sizeof(T) == 4, "rows move as float4: fp32 plans only");
+    constexpr int NV = (NC + 3) / 4;  // 16-byte pieces of a row (rows are padded to a multiple of 4)
+    // a row into registers in 16-byte loads (one thread per node touches its own rows, so scalar loads
+    // would each be a separate request)
+    auto load_row = [](const T *row, T (&r)[NC]) {
+        const float4 *v = reinterpret_cast<const float4 *>(row);
+#pragma unroll
+        for (int q = 0; q < NV; ++q) {
+            const float4 x = v[q];
+            const float e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                if (4 * q + h < NC) r[4 * q + h] = e[h];
+        }
+    };
     const int n = phase2_nodes(ctr);
     for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n; a += gridDim.x * blockDim.x) {
         T out[NC];
-        const T *own = Lm2l + (size_t)a * ncp;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) out[k] = own[k];
+        load_row(Lm2l + (size_t)a * ncp, out);
         const vec4<T> c = nc[a];
         int b = parent[a];
         for (int up = 0; b >= 0 && up <= kMaxLevel; ++up) {
             T lb[NC];
-            const T *src = Lm2l + (size_t)b * ncp;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) lb[k] = src[k];
+            load_row(Lm2l + (size_t)b * ncp, lb);
             const vec4<T> cb = nc[b];
             Exp<P>::template l2l<T>(lb, c.x - cb.x, c.y - cb.y, c.z - cb.z, out);
             b = parent[b];
         }
-        T *dst = L + (size_t)a * ncp;
+        float4 *dst = reinterpret_cast<float4 *>(L + (size_t)a * ncp);
 #pragma unroll
-        for (int k = 0; k < NC; ++k) dst[k] = out[k];
+        for (int q = 0; q < NV; ++q) {
+            float e[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) e[h] = 4 * q + h < NC ? out[4 * q + h] : 0.0f;
+            dst[q] = make_float4(e[0], e[1], e[2], e[3]);
+        }
         if (nchild[a] == 0) {  // a leaf: its particles' leaf, for the L2P by particle
             const int f = first[a], c = count[a];
             for (int i = f; i < f + c; ++i) leaf_of[i] = a;
