@@ -136,8 +136,21 @@ __global__ __launch_bounds__(256) void k_upward_flags(DevCounters *ctr, const ve
             }
         } else if (has) {
             T mc[NC];
+            if constexpr (sizeof(T) == 4) {
+                // the child's row in 16-byte pieces through L2 (rows are padded to a multiple of 4)
+                const float4 *v = reinterpret_cast<const float4 *>(M + (size_t)ch * ncp);
 #pragma unroll
-            for (int k = 0; k < NC; ++k) mc[k] = ld_cg(M + (size_t)ch * ncp + k);
+                for (int q = 0; q < (NC + 3) / 4; ++q) {
+                    const float4 x = __ldcg(v + q);
+                    const float e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+                        if (4 * q + h < NC) mc[4 * q + h] = e[h];
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < NC; ++k) mc[k] = ld_cg(M + (size_t)ch * ncp + k);
+            }
             const vec4<T> cc = ld_cg(nc + ch);
             Exp<P>::template m2m<T>(mc, cc.x - cen[0], cc.y - cen[1], cc.z - cen[2], m);
         }
@@ -158,8 +171,14 @@ __global__ __launch_bounds__(256) void k_upward_flags(DevCounters *ctr, const ve
 #pragma unroll
                 for (int k = NRC; k < NRP; ++k) r[k] = T(0);
                 Exp<P>::template reduce_m<T>(mk, r);
+                if constexpr (sizeof(T) == 4) {
+                    float4 *v = reinterpret_cast<float4 *>(Mr + (size_t)a * NRP);
 #pragma unroll
-                for (int k = 0; k < NRP; ++k) Mr[(size_t)a * NRP + k] = r[k];
+                    for (int q = 0; q < NRP / 4; ++q) v[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NRP; ++k) Mr[(size_t)a * NRP + k] = r[k];
+                }
             }
         }
     }
