@@ -166,8 +166,20 @@ __global__ __launch_bounds__(256) void k_upward_flags(DevCounters *ctr, const ve
             if (Mr != nullptr) {  // the reduced row the M2L reads, off the parents' wait
                 constexpr int NRC = Exp<P>::NRC, NRP = (NRC + 3) / 4 * 4;
                 T mk[NC], r[NRP];
+                if constexpr (sizeof(T) == 4) {
+                    const float4 *v = reinterpret_cast<const float4 *>(dst);
 #pragma unroll
-                for (int k = 0; k < NC; ++k) mk[k] = dst[k];
+                    for (int q = 0; q < (NC + 3) / 4; ++q) {
+                        const float4 x = v[q];
+                        const float e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h)
+                            if (4 * q + h < NC) mk[4 * q + h] = e[h];
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) mk[k] = dst[k];
+                }
 #pragma unroll
                 for (int k = NRC; k < NRP; ++k) r[k] = T(0);
                 Exp<P>::template reduce_m<T>(mk, r);
