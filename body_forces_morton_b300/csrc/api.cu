@@ -87,7 +87,7 @@ void free_nodes(Plan &P)
                     &P.node_level, &P.node_done,  &P.m2l_cnt,     &P.p2p_cnt,     &P.m2l_off,
                     &P.p2p_off,    &P.long_seg,    &P.order,       &P.p2p_done};
     for (int **q : ints) { dfree(*q); *q = nullptr; }
-    void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.M, &P.Lm2l, &P.L, &P.Mr};
+    void **vs[] = {&P.node_lo, &P.node_hi, &P.node_c, &P.node_l, &P.node_w, &P.M, &P.Lm2l, &P.L, &P.Mr};
     for (void **q : vs) { dfree(*q); *q = nullptr; }
     dfree(P.flags);
     P.flags = nullptr;
@@ -147,6 +147,7 @@ fmm_status alloc_nodes(Plan &P, int64_t cap)
     CUDA_TRY(cudaMalloc(&P.node_hi, 3 * c * e));
     CUDA_TRY(cudaMalloc(&P.node_c, 4 * c * e));
     CUDA_TRY(cudaMalloc(&P.node_l, 4 * c * e));
+    CUDA_TRY(cudaMalloc(&P.node_w, 8 * c * e));
     CUDA_TRY(cudaMalloc(&P.M, (size_t)P.ncp * c * e));
     CUDA_TRY(cudaMalloc(&P.Lm2l, (size_t)P.ncp * c * e));
     CUDA_TRY(cudaMalloc(&P.L, (size_t)P.ncp * c * e));

@@ -29,11 +29,33 @@ constexpr int WK_THREADS = 256;
 constexpr int SEG_WARP_MAX = 1024;     // segments up to this length sort in a warp
 constexpr int CS_THREADS = 256, CS_ITEMS = 4, CS_TILE = CS_THREADS * CS_ITEMS;
 
-__global__ void k_walk_init(int2 *f0, DevCounters *ctr)
+// Integer bits in a floating-point slot of a node record (stored and loaded,
+// never computed with).
+__device__ __forceinline__ float int_slot(int v, float) { return __int_as_float(v); }
+__device__ __forceinline__ double int_slot(int v, double) { return __longlong_as_double((long long)v); }
+__device__ __forceinline__ int slot_int(float v) { return __float_as_int(v); }
+__device__ __forceinline__ int slot_int(double v) { return (int)__double_as_longlong(v); }
+
+// The walk's first frontier, and every node's record for the walk: what it
+// reads of a node (centre, half-widths, child count and first child) in one
+// 2 x vec4<T> record, so a node costs two loads from one sector (fp32) instead
+// of four loads from four arrays.
+template <class T>
+__global__ void k_walk_init(int2 *f0, const DevCounters *__restrict__ nctr, const vec4<T> *__restrict__ nc,
+                            const vec4<T> *__restrict__ nl, const int *__restrict__ nchild,
+                            const int *__restrict__ child0, vec4<T> *__restrict__ wrec, DevCounters *ctr)
 {
-    f0[0] = make_int2(0, 0);
-    ctr->frontier_cnt[0][0] = 1;
-    ctr->frontier_max = 1;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        f0[0] = make_int2(0, 0);
+        ctr->frontier_cnt[0][0] = 1;
+        ctr->frontier_max = 1;
+    }
+    const int n = phase2_nodes(nctr);
+    for (int a = blockIdx.x * blockDim.x + threadIdx.x; a < n; a += gridDim.x * blockDim.x) {
+        const vec4<T> c = nc[a], l = nl[a];
+        wrec[2 * a] = make4<T>(c.x, c.y, c.z, int_slot(nchild[a], T(0)));
+        wrec[2 * a + 1] = make4<T>(l.x, l.y, l.z, int_slot(child0[a], T(0)));
+    }
 }
 
 // Prefix over the shards of a sharded list (each shard's count clamped to its
@@ -79,11 +101,8 @@ __device__ __forceinline__ size_t shard_addr(const int *s_pre, int g, int cap_s)
 // written by other blocks of this launch, so they are read through L2.
 template <class T>
 __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0, int2 *f1, int capf_s,
-                                                         const int *__restrict__ nchild,
-                                                         const int *__restrict__ child0,
                                                          const int *__restrict__ count,
-                                                         const vec4<T> *__restrict__ nc,
-                                                         const vec4<T> *__restrict__ nl, T th2, int2 *m2l_pairs,
+                                                         const vec4<T> *__restrict__ wrec, T th2, int2 *m2l_pairs,
                                                          int capm_s, int2 *p2p_pairs, int capp_s, int *m2l_cnt,
                                                          int *p2p_cnt, GridBarrier *gb, DevCounters *ctr)
 {
@@ -123,7 +142,8 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0
                 A = pr.x;
                 B = pr.y;
                 ++visited;
-                const int nA = nchild[A], c0A = child0[A];
+                const vec4<T> cA = wrec[2 * A], lA = wrec[2 * A + 1];
+                const int nA = slot_int(cA.w), c0A = slot_int(lA.w);
                 if (A == B) {
                     if (nA == 0) {
                         p2p = 1;
@@ -131,10 +151,11 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0
                     } else {
                         kids = nA * (nA + 1) / 2;
                         c0 = c0A;
+                        other = nA;  // a self pair: the child count
                     }
                 } else {
-                    const int nB = nchild[B], c0B = child0[B];
-                    const vec4<T> cA = nc[A], cB = nc[B], lA = nl[A], lB = nl[B];
+                    const vec4<T> cB = wrec[2 * B], lB = wrec[2 * B + 1];
+                    const int nB = slot_int(cB.w), c0B = slot_int(lB.w);
                     const T s2 = norm2_rn(add_rn(lA.x, lB.x), add_rn(lA.y, lB.y), add_rn(lA.z, lB.z));
                     const T r2 = norm2_rn(sub_rn(cA.x, cB.x), sub_rn(cA.y, cB.y), sub_rn(cA.z, cB.z));
                     if (s2 < mul_rn(th2, r2)) {
@@ -143,7 +164,10 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0
                         p2p = 1;
                         inter_sum += 2ll * count[A] * count[B];
                     } else {
-                        const bool splitA = (nB == 0) ? true : ((nA == 0) ? false : (cA.w >= cB.w));
+                        // |l|^2 as the upward pass computed it for the node centres' records
+                        const bool splitA = (nB == 0) ? true
+                                          : ((nA == 0) ? false
+                                                       : (norm2_rn(lA.x, lA.y, lA.z) >= norm2_rn(lB.x, lB.y, lB.z)));
                         other = splitA ? B : A;
                         kids = splitA ? nA : nB;
                         c0 = splitA ? c0A : c0B;
@@ -196,7 +220,7 @@ __global__ __launch_bounds__(WK_THREADS) void k_walk_all(int max_iters, int2 *f0
                 int o = s_base[2] + s_wtot[2][warp] + ik - kids;
                 int2 *dst = fout + (size_t)bshard * capf_s;
                 if (A == B) {
-                    const int nA = nchild[A];
+                    const int nA = other;
                     for (int x = 0; x < nA; ++x)
                         for (int y = x; y < nA; ++y, ++o) {
                             if (o < capf_s) dst[o] = make_int2(c0 + x, c0 + y);
@@ -599,16 +623,17 @@ template <class T>
 int launch_walk_t(Plan &P, int depth, cudaStream_t s)
 {
     T th2 = (T)(P.theta * P.theta);
-    k_walk_init<<<1, 1, 0, s>>>(P.frontier[0], P.ctr);
+    k_walk_init<T><<<P.num_sms * 4, 256, 0, s>>>(P.frontier[0], P.ctr, (const vec4<T> *)P.node_c,
+                                                  (const vec4<T> *)P.node_l, P.node_nchild, P.node_child0,
+                                                  (vec4<T> *)P.node_w, P.ctr);
     int iters = 2 * kMaxLevel + 2;
     (void)depth;
     int capf_s = (int)(P.cap_frontier / kShards), capm_s = (int)(P.cap_m2l / kShards);
     int capp_s = (int)(P.cap_p2p / kShards);
-    const vec4<T> *nc = (const vec4<T> *)P.node_c, *nl = (const vec4<T> *)P.node_l;
+    const vec4<T> *wrec = (const vec4<T> *)P.node_w;
     GridBarrier *gb = P.gbar + 1;
-    void *args[] = {&iters, &P.frontier[0], &P.frontier[1], &capf_s, &P.node_nchild, &P.node_child0, &P.node_count,
-                    (void *)&nc, (void *)&nl, &th2, &P.m2l_pairs, &capm_s, &P.p2p_pairs, &capp_s, &P.m2l_cnt,
-                    &P.p2p_cnt, &gb, &P.ctr};
+    void *args[] = {&iters, &P.frontier[0], &P.frontier[1], &capf_s, &P.node_count, (void *)&wrec, &th2,
+                    &P.m2l_pairs, &capm_s, &P.p2p_pairs, &capp_s, &P.m2l_cnt, &P.p2p_cnt, &gb, &P.ctr};
     cudaLaunchCooperativeKernel((const void *)k_walk_all<T>, dim3(P.coop_blocks_walk), dim3(WK_THREADS), args, 0, s);
     return 2;
 }

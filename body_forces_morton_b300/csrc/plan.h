@@ -54,6 +54,7 @@ struct Plan {
     int *node_parent = nullptr, *node_level = nullptr, *node_done = nullptr;
     void *node_lo = nullptr, *node_hi = nullptr;  // T[3] per node
     void *node_c = nullptr, *node_l = nullptr;    // vec4<T>: (cx, cy, cz, |l|^2), (lx, ly, lz, 0)
+    void *node_w = nullptr;  // the walk's node records, 2 vec4<T>: (cx, cy, cz, nchild), (lx, ly, lz, child0), ints as bits
     void *M = nullptr, *Lm2l = nullptr, *L = nullptr;  // T[ncp] per node
     void *Mr = nullptr;            // reduced (n_z <= 1) moments for M2L, [nrp] 8-byte slots per node: T for
                                    // fp32 and fp64 p >= 5, double-float pairs in level units for fp64 p <= 4
