@@ -426,21 +426,57 @@ __device__ __forceinline__ void warp_sort(int (&v)[NR])
     }
 }
 
+// A list of up to 32 NR entries sorted in registers; for NR > 1 it moves
+// between global memory and the blocked layout through the warp's shared
+// buffer sv (coalesced global accesses, vector shared accesses).
 template <int NR>
-__device__ __forceinline__ void sort_list_regs(int *src, int len)
+__device__ __forceinline__ void sort_list_regs(int *src, int len, int *sv)
 {
     const int lane = threadIdx.x & 31;
     int v[NR];
+    if constexpr (NR == 1) {
+        v[0] = lane < len ? src[lane] : 0x7fffffff;
+    } else {
 #pragma unroll
-    for (int j = 0; j < NR; ++j) {
-        const int e = lane * NR + j;
-        v[j] = e < len ? src[e] : 0x7fffffff;
+        for (int j = 0; j < NR; ++j) {
+            const int e = j * 32 + lane;
+            sv[e] = e < len ? src[e] : 0x7fffffff;
+        }
+        __syncwarp();
+        if constexpr (NR % 4 == 0) {
+#pragma unroll
+            for (int j = 0; j < NR; j += 4) {
+                const int4 x = *reinterpret_cast<const int4 *>(sv + lane * NR + j);
+                v[j] = x.x;
+                v[j + 1] = x.y;
+                v[j + 2] = x.z;
+                v[j + 3] = x.w;
+            }
+        } else {
+            const int2 x = *reinterpret_cast<const int2 *>(sv + lane * NR);
+            v[0] = x.x;
+            v[1] = x.y;
+        }
     }
     warp_sort<NR>(v);
+    if constexpr (NR == 1) {
+        if (lane < len) src[lane] = v[0];
+    } else {
+        __syncwarp();
+        if constexpr (NR % 4 == 0) {
 #pragma unroll
-    for (int j = 0; j < NR; ++j) {
-        const int e = lane * NR + j;
-        if (e < len) src[e] = v[j];
+            for (int j = 0; j < NR; j += 4)
+                *reinterpret_cast<int4 *>(sv + lane * NR + j) = make_int4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        } else {
+            *reinterpret_cast<int2 *>(sv + lane * NR) = make_int2(v[0], v[1]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+            const int e = j * 32 + lane;
+            if (e < len) src[e] = sv[e];
+        }
+        __syncwarp();
     }
 }
 
@@ -454,7 +490,7 @@ __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__
                                                  DevCounters *ctr)
 {
     const int n_nodes = phase2_nodes(nctr);
-    __shared__ int buf[8][SEG_WARP_MAX];
+    __shared__ __align__(16) int buf[8][SEG_WARP_MAX];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int *sv = buf[w];
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -492,11 +528,11 @@ __global__ __launch_bounds__(256) void k_segsort(const DevCounters *__restrict__
             }
         }
         if (len <= 1) continue;
-        if (len <= 32) { sort_list_regs<1>(src, len); continue; }
-        if (len <= 64) { sort_list_regs<2>(src, len); continue; }
-        if (len <= 128) { sort_list_regs<4>(src, len); continue; }
-        if (len <= 256) { sort_list_regs<8>(src, len); continue; }
-        if (len <= 512) { sort_list_regs<16>(src, len); continue; }
+        if (len <= 32) { sort_list_regs<1>(src, len, sv); continue; }
+        if (len <= 64) { sort_list_regs<2>(src, len, sv); continue; }
+        if (len <= 128) { sort_list_regs<4>(src, len, sv); continue; }
+        if (len <= 256) { sort_list_regs<8>(src, len, sv); continue; }
+        if (len <= 512) { sort_list_regs<16>(src, len, sv); continue; }
         if (len > SEG_WARP_MAX) {
             if (lane == 0) long_seg[atomicAdd(&ctr->n_long, 1)] = job;
             continue;
