@@ -436,6 +436,53 @@ __global__ __launch_bounds__(LF_WARPS * 32) void k_p2p(const DevCounters *__rest
     }
 }
 
+// A node's row of NC coefficients moved in 16-byte pieces (rows are padded to
+// a multiple of 4 elements, so every piece lies inside the row): loads plain
+// or through L2 (CG, for rows other blocks of the launch wrote), stores with
+// the padding zeroed.
+template <class T, int NC, bool CG>
+__device__ __forceinline__ void row_load16(const T *row, T (&r)[NC])
+{
+    if constexpr (sizeof(T) == 4) {
+        const float4 *v = reinterpret_cast<const float4 *>(row);
+#pragma unroll
+        for (int q = 0; q < (NC + 3) / 4; ++q) {
+            const float4 x = CG ? __ldcg(v + q) : v[q];
+            const float e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                if (4 * q + h < NC) r[4 * q + h] = e[h];
+        }
+    } else {
+        const double2 *v = reinterpret_cast<const double2 *>(row);
+#pragma unroll
+        for (int q = 0; q < (NC + 1) / 2; ++q) {
+            const double2 x = CG ? __ldcg(v + q) : v[q];
+            r[2 * q] = x.x;
+            if (2 * q + 1 < NC) r[2 * q + 1] = x.y;
+        }
+    }
+}
+
+template <class T, int NC>
+__device__ __forceinline__ void row_store16(T *row, const T (&r)[NC])
+{
+    if constexpr (sizeof(T) == 4) {
+        float4 *v = reinterpret_cast<float4 *>(row);
+#pragma unroll
+        for (int q = 0; q < (NC + 3) / 4; ++q) {
+            float e[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) e[h] = 4 * q + h < NC ? r[4 * q + h] : 0.0f;
+            v[q] = make_float4(e[0], e[1], e[2], e[3]);
+        }
+    } else {
+        double2 *v = reinterpret_cast<double2 *>(row);
+#pragma unroll
+        for (int q = 0; q < (NC + 1) / 2; ++q) v[q] = make_double2(r[2 * q], 2 * q + 1 < NC ? r[2 * q + 1] : 0.0);
+    }
+}
+
 // L2L in one launch, without grid barriers: warps take chunks of up to 32
 // nodes of one level from a shared counter, in level order (root first). A
 // node's thread waits, bounded, until its parent's flag holds this pass's
@@ -479,9 +526,7 @@ __global__ __launch_bounds__(256) void k_l2l_flags(DevCounters *ctr, const int *
         const int a = lo + lane;
         if (a >= hi) continue;
         T out[NC];
-        const T *own = Lm2l + (size_t)a * ncp;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) out[k] = own[k];
+        row_load16<T, NC, false>(Lm2l + (size_t)a * ncp, out);
         if (level > 0) {
             const int par = parent[a];
             cuda::atomic_ref<unsigned, cuda::thread_scope_device> f(flag[par]);
@@ -494,15 +539,11 @@ __global__ __launch_bounds__(256) void k_l2l_flags(DevCounters *ctr, const int *
                 __nanosleep(32);
             }
             T lp[NC];
-            const T *pr = L + (size_t)par * ncp;
-#pragma unroll
-            for (int k = 0; k < NC; ++k) lp[k] = ld_cg(pr + k);
+            row_load16<T, NC, true>(L + (size_t)par * ncp, lp);
             const vec4<T> c = nc[a], cp = nc[par];
             Exp<P>::template l2l<T>(lp, c.x - cp.x, c.y - cp.y, c.z - cp.z, out);
         }
-        T *dst = L + (size_t)a * ncp;
-#pragma unroll
-        for (int k = 0; k < NC; ++k) dst[k] = out[k];
+        row_store16<T, NC>(L + (size_t)a * ncp, out);
         cuda::atomic_ref<unsigned, cuda::thread_scope_device>(flag[a]).store(seq, cuda::memory_order_release);
     }
 }
