@@ -622,7 +622,9 @@ __global__ __launch_bounds__(256) void k_l2p_part(const DevCounters *__restrict_
         }
         const vec4<T> ca = nc[a], q = xyzm[i];
         T phi = T(0), ax = T(0), ay = T(0), az = T(0);
-        Exp<P>::template l2p<T>(L + (size_t)a * ncp, q.x - ca.x, q.y - ca.y, q.z - ca.z, phi, ax, ay, az);
+        T la[Exp<P>::NC];
+        row_load16<T, Exp<P>::NC, false>(L + (size_t)a * ncp, la);  // the leaf's local in 16-byte pieces
+        Exp<P>::template l2p<T>(la, q.x - ca.x, q.y - ca.y, q.z - ca.z, phi, ax, ay, az);
         far[i] = make4<T>(phi, ax, ay, az);
     }
 }
