@@ -72,7 +72,7 @@ __global__ __launch_bounds__(kBoxThreads) void k_bbox(const T *__restrict__ pos,
     T lo[3], hi[3];
     for (int a = 0; a < 3; ++a) { lo[a] = pos_inf<T>(); hi[a] = -pos_inf<T>(); }
     bool bad = false;
-    // four positions a stride apart per thread and round, their loads issued together
+    // four positions a stride apart per thread and loop iteration, their loads issued together
     const int stride = gridDim.x * blockDim.x;
     for (int i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < n; i0 += 4 * stride) {
         T v[4][3];
