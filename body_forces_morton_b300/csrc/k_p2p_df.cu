@@ -89,8 +89,10 @@ __global__ __launch_bounds__(256) void k_leaf_offsets(const DevCounters *__restr
     if (n_nodes <= 0) return;
     const int lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    int ex, em;
-    df_units(nl, M, ex, em);
+    __shared__ int s_units[2];  // the unit exponents, found once per block
+    if (threadIdx.x == 0) df_units(nl, M, s_units[0], s_units[1]);
+    __syncthreads();
+    const int ex = s_units[0], em = s_units[1];
     for (int a = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; a < n_nodes; a += nwarps) {
         if (nchild[a] != 0) continue;
         const dbl4 c = nc[a];
@@ -412,7 +414,7 @@ template <int P>
 int launch_l2p_df_p(Plan &P_, cudaStream_t s)
 {
     // leaf-relative offsets first (they serve this kernel and the near field)
-    k_leaf_offsets<<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, (int)P_.n, P_.node_first, P_.node_count, P_.node_nchild,
+    k_leaf_offsets<<<P_.num_sms * 2, 256, 0, s>>>(P_.ctr, (int)P_.n, P_.node_first, P_.node_count, P_.node_nchild,
                                                   (const dbl4 *)P_.xyzm, (const dbl4 *)P_.node_c,
                                                   (const dbl4 *)P_.node_l, (const double *)P_.M, (float4 *)P_.rel);
     k_l2p_df<P><<<P_.num_sms * 8, 256, 0, s>>>(P_.ctr, P_.node_first, P_.node_count, P_.node_nchild, P_.node_level,
