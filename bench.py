@@ -59,9 +59,9 @@ P2P_FLOPS_PER_PAIR = 20  # 3 sub, 3 mul + 2 add (r^2), rsqrt (1), 3 mul (m/r, /r
 # 1e5 fp64, p 4), keyed by the hash of the kernel sources they were counted on;
 # a changed kernel reports null until it is counted again.
 DF_FMA_OPS_PER_PAIR = {
-    # k_p2p_df: 9,097,988,608 FMA-pipe thread instructions (all scalar) over the 48,723,340 pairs the
+    # k_p2p_df: 9,098,613,344 FMA-pipe thread instructions (all scalar) over the 48,723,340 pairs the
     # roofline counts (the interactions less the 1e5 zero-separation self pairs)
-    ("k_p2p_df", "a71b96b0dadb26fe"): 186.73,
+    ("k_p2p_df", "453998eb2c42ecbf"): 186.74,
     # k_m2l_df<4>: 6,072,086,944 over 1,833,964 pairs (the moments' conversion kernel is not counted)
     ("k_m2l_df", "159774f6b7e517df"): 3310.9,
 }
